@@ -1,0 +1,483 @@
+"""Throughput of server-side FedAvg aggregation on GB300.
+
+One step = one aggregation round of the whole path: reset, every client's
+update streamed in flat chunks through fa_accumulate (weighted fp32 running
+sum in HBM), fa_finalize (divide by the per-key weight total, RNE to bf16).
+
+  value  client-update GB/s with every client's update already resident in HBM
+         (the chunks a NIC or copy engine would have landed there)
+  e2e    the same metric through the same C ABI calls with pinned HOST buffers:
+         every step copies the client updates host->device through the library's
+         staging ring and the aggregate back device->host
+  roofline  the accumulate kernel (the dominant one): algorithmic bytes per launch
+         (bf16 input read + fp32 sum read + fp32 sum write; the first client's
+         launches skip the sum read) over its CUDA-event-timed duration
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (the path has no exchange
+step): value = all ranks' client bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "client-update GB/s aggregated (1×GB300) and % of HBM peak; oracle host GB/s"
+DEFAULT_WORKLOAD = "llama7b"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------- round drivers
+def stream_client(fa, ctx, w, k, base_ptr, stream):
+    """Client k's whole update (flat layout at base_ptr, device or host) in chunk_elems pieces."""
+    P, ce = w.P, w.chunk_elems or w.P
+    es = 2 if w.dtype_in == "bf16" else 4
+    calls = 0
+    for c0 in range(0, P, ce):
+        n = min(ce, P - c0)
+        fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base_ptr + c0 * es, n, stream)
+        calls += 1
+    return calls
+
+
+def run_streamed_round(w, resident=False):
+    """One full round on the device, inputs from the device generator, streamed
+    client by client exactly as the bench does; returns the flat bf16 output."""
+    import torch
+
+    import server_side_fedavg_gb300 as fa
+    import synth
+
+    tdt = torch.int16 if w.dtype_in == "bf16" else torch.float32
+    s = torch.cuda.current_stream()
+    ctx = fa.fa_open([(n, m) for (n, _), m in zip(w.keys, w.numels)], w.dtype_in, w.dtype_out,
+                     w.K, flags=fa.FA_FLAT_OUT)
+    try:
+        if resident:
+            bufs = [torch.empty(w.P, dtype=tdt, device="cuda") for _ in range(w.K)]
+            for k in range(w.K):
+                synth.client_fill_device(w, k, 0, w.P, bufs[k].data_ptr(), s.cuda_stream)
+        else:
+            buf = torch.empty(w.P, dtype=tdt, device="cuda")
+        for k in range(w.K):
+            if resident:
+                ptr = bufs[k].data_ptr()
+            else:
+                synth.client_fill_device(w, k, 0, w.P, buf.data_ptr(), s.cuda_stream)
+                ptr = buf.data_ptr()
+            stream_client(fa, ctx, w, k, ptr, s.cuda_stream)
+        out = torch.empty(w.P, dtype=torch.int16 if w.dtype_out == "bf16" else torch.float32,
+                          device="cuda")
+        fa.fa_finalize(ctx, [out], s.cuda_stream)
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+        return out
+    finally:
+        fa.fa_close(ctx)
+
+
+def algorithmic_bytes(w):
+    """Per round, streaming path: first client s_in+4, later clients s_in+8,
+    finalize 4+s_out bytes per element (all clients send every key here)."""
+    si = 2 if w.dtype_in == "bf16" else 4
+    so = 2 if w.dtype_out == "bf16" else 4
+    acc_first = w.P * (si + 4)
+    acc_later = (w.K - 1) * w.P * (si + 8)
+    fin = w.P * (4 + so)
+    return acc_first, acc_later, fin
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- CPU oracle baseline
+def cpu_sample(w, elems):
+    """Inputs of the CPU sample: the first `elems` flat elements of every client."""
+    import synth
+    return [synth.client_flat(w, k, 0, elems) for k in range(w.K)]
+
+
+def cpu_pass(w, xs, threads):
+    """One timed pass of the fp64 oracle (as it stands) over the sample, split
+    into contiguous slices over `threads` host threads (ctypes drops the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    elems = xs[0].size
+    per = -(-elems // threads)
+    reps = [True] * w.K
+
+    def part(i):
+        a, b = i * per, min(elems, (i + 1) * per)
+        if b > a:
+            oracle.fedavg_key(w.weights, reps, [x[a:b] for x in xs], w.dtype_in, w.dtype_out)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(part, range(threads)))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, elems, min_seconds=10.0, threads=None):
+    """Oracle throughput on the host cores: passes over a bounded sample until
+    at least `min_seconds` of wall time; inputs are made before timing."""
+    threads = threads or (os.cpu_count() or 1)
+    xs = cpu_sample(w, elems)
+    si = 2 if w.dtype_in == "bf16" else 4
+    passes, dt = 0, 0.0
+    while dt < min_seconds:
+        dt += cpu_pass(w, xs, threads)
+        passes += 1
+    gbs = passes * w.K * elems * si / dt / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{w.name}: first {elems} flat elements x {w.K} clients "
+                      f"({w.K * elems * si / 1e9:.2f} GB of client bytes), fp64 C oracle, "
+                      f"{passes} passes in {dt:.1f} s on {threads} threads"}
+
+
+# --------------------------------------------------------------------------- distributed bits
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, v: float) -> float:
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args, world, rank, pg):
+    from synth import workloads as W
+
+    if rank != 0:
+        return 0
+    w = W.make(args.workload)
+    elems = args.ref_elems
+    threads = os.cpu_count() or 1
+    si = 2 if w.dtype_in == "bf16" else 4
+    xs = cpu_sample(w, elems)
+    for _ in range(args.warmup):
+        cpu_pass(w, xs, threads)
+    times = [cpu_pass(w, xs, threads) for _ in range(args.steps)]
+    v = round(w.K * elems * si * args.steps / sum(times) / 1e9, 3)
+    sample = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+              "sample": f"{w.name}: first {elems} flat elements x {w.K} clients "
+                        f"({w.K * elems * si / 1e9:.2f} GB of client bytes) per step, "
+                        f"fp64 C oracle on {threads} threads"}
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sum(times) / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "K": w.K, "P": w.P, "sample_elems": elems},
+        "cpu_baseline": sample,
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local, pg):
+    import torch
+
+    import server_side_fedavg_gb300 as fa
+    import synth
+    from synth import workloads as W
+
+    torch.cuda.set_device(local)
+    w = W.make(args.workload)
+    si = 2 if w.dtype_in == "bf16" else 4
+    so = 2 if w.dtype_out == "bf16" else 4
+    tin = torch.int16 if si == 2 else torch.float32
+    tout = torch.int16 if so == 2 else torch.float32
+    layout = [(n, m) for (n, _), m in zip(w.keys, w.numels)]
+    s = torch.cuda.Stream()
+    sh = s.cuda_stream
+    client_bytes = w.K * w.P * si
+    peak, peak_kind = _peaks()
+
+    # ---- regime A: every client's update resident in HBM
+    free, _ = torch.cuda.mem_get_info()
+    per_client = w.P * si
+    fixed = w.P * 4 + w.P * so + (6 << 30)
+    resident = max(1, min(w.K, int((free - fixed) // per_client)))
+    bufs = [torch.empty(w.P, dtype=tin, device="cuda") for _ in range(resident)]
+    for k in range(resident):
+        synth.client_fill_device(w, k, 0, w.P, bufs[k].data_ptr(), sh)
+    out = torch.empty(w.P, dtype=tout, device="cuda")
+    ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
+    torch.cuda.synchronize()
+
+    nchunk = -(-w.P // (w.chunk_elems or w.P))
+
+    def step(evs=None):
+        fa.fa_reset(ctx)
+        i = 0
+        if evs is not None:
+            evs[0].record(s)
+        for k in range(w.K):
+            base = bufs[k % resident].data_ptr()
+            P, ce = w.P, w.chunk_elems or w.P
+            for c0 in range(0, P, ce):
+                fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base + c0 * si,
+                                 min(ce, P - c0), sh)
+                i += 1
+                if evs is not None:
+                    evs[i].record(s)
+        fa.fa_finalize(ctx, [out], sh)
+        if evs is not None:
+            evs[i + 1].record(s)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+
+    n_calls = w.K * nchunk
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 2)] for _ in range(args.steps)]
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = fa.fa_get_stats(ctx)["kernel_launches"]
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0e.record(s)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        step(ev_sets[i])
+    t1e.record(s)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    launches = fa.fa_get_stats(ctx)["kernel_launches"] - launches0
+    barrier(pg)
+    ms_total = t0e.elapsed_time(t1e)
+    ms_total = max_over_ranks(pg, ms_total)
+
+    # per-launch kernel times (events bracket each accumulate launch on its stream)
+    acc_first_b, acc_later_b, fin_b = algorithmic_bytes(w)
+    acc_ms = 0.0
+    fin_ms = 0.0
+    for evs in ev_sets:
+        for j in range(n_calls):
+            acc_ms += evs[j].elapsed_time(evs[j + 1])
+        fin_ms += evs[n_calls].elapsed_time(evs[n_calls + 1])
+    acc_launch_ms = acc_ms / (args.steps * n_calls)
+    acc_bytes_per_launch = (acc_first_b + acc_later_b) / n_calls
+    achieved = acc_bytes_per_launch / (acc_launch_ms * 1e-3) / 1e9
+    fin_gbs = fin_b / (fin_ms / args.steps * 1e-3) / 1e9
+    step_bytes = acc_first_b + acc_later_b + fin_b
+    ms_per_step = ms_total / args.steps
+    value = world * client_bytes / (ms_per_step * 1e-3) / 1e9
+
+    fa.fa_close(ctx)
+    del bufs, out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # ---- e2e: pinned host buffers through the same calls
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(args, w, layout, s, pg, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "P": w.P, "K": w.K, "n_keys": w.n_keys,
+                   "dtype_in": w.dtype_in, "dtype_out": w.dtype_out,
+                   "chunk_bytes": (w.chunk_elems or w.P) * si, "resident_clients": resident,
+                   "l2": "inputs (client updates, running sum) far larger than L2; no flush",
+                   "hbm_frac_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4),
+                   "finalize_gbs": round(fin_gbs, 1),
+                   "wall_s": round(wall, 3)},
+        "roofline": {"bound": "hbm", "kernel": "accumulate_kernel<bf16,1>",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "bytes_per_launch": int(acc_bytes_per_launch),
+                     "launch_ms": round(acc_launch_ms, 4), "traffic": None},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.ref_elems)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(args, w, layout, s, pg, world):
+    """Client chunks from pinned host memory (a pool of distinct chunks, reused),
+    aggregate written to a pinned host buffer; copies inside the timed region."""
+    import torch
+
+    import server_side_fedavg_gb300 as fa
+    import synth
+
+    si = 2 if w.dtype_in == "bf16" else 4
+    so = 2 if w.dtype_out == "bf16" else 4
+    ce = w.chunk_elems or w.P
+    nchunk = -(-w.P // ce)
+    pool_n = min(args.e2e_pool, w.K * nchunk)
+    pool = []
+    for i in range(pool_n):
+        k, c = divmod(i, nchunk)
+        c0 = c * ce
+        n = min(ce, w.P - c0)
+        t = torch.empty(ce, dtype=torch.int16 if si == 2 else torch.float32).pin_memory()
+        a = synth.client_flat(w, k, c0, n)
+        t[:n].numpy().view(a.dtype)[:] = a
+        pool.append(t)
+    out = torch.empty(w.P, dtype=torch.int16 if so == 2 else torch.float32).pin_memory()
+    ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
+    sh = s.cuda_stream
+
+    def step():
+        fa.fa_reset(ctx)
+        i = 0
+        for k in range(w.K):
+            for c0 in range(0, w.P, ce):
+                n = min(ce, w.P - c0)
+                fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0,
+                                 pool[i % pool_n].data_ptr(), n, sh)
+                i += 1
+        fa.fa_finalize(ctx, [out], sh)
+        fa.fa_sync(ctx)
+
+    try:
+        for _ in range(max(1, args.warmup // 2)):
+            step()
+        torch.cuda.synchronize()
+        barrier(pg)
+        st0 = fa.fa_get_stats(ctx)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            step()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        st1 = fa.fa_get_stats(ctx)
+        dt = max_over_ranks(pg, dt)
+    finally:
+        fa.fa_close(ctx)
+    h2d = (st1["h2d_bytes"] - st0["h2d_bytes"]) // args.e2e_steps
+    d2h = (st1["d2h_bytes"] - st0["d2h_bytes"]) // args.e2e_steps
+    v = world * w.K * w.P * si * args.e2e_steps / dt / 1e9
+    return {"value": round(v, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
+            "ms_per_step": round(dt / args.e2e_steps * 1e3, 2),
+            "host_pool": f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-pool", type=int, default=24)
+    ap.add_argument("--ref-elems", type=int, default=64 << 20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local, pg = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank, pg)
+        return run_ours(args, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,199 @@
+/*
+ * fedavg.h -- server-side FedAvg aggregation on one GPU (C ABI).
+ *
+ * Computes, for every key p (one tensor of a model state dict),
+ *
+ *     global[p][i] = sum_{k in S_p} n_k * w_k[p][i]  /  N_p,     N_p = sum_{k in S_p} n_k
+ *
+ * where S_p is the set of clients that sent key p in this round and n_k is
+ * client k's weight (its sample count).  Client updates arrive as chunks,
+ * in any order, from host or device memory; a fp32 running sum lives in
+ * device memory, so memory does not grow with the number of clients.
+ *
+ * Passages the operations follow:
+ *  [Clara]  "Federated learning implemented by NVIDIA Clara" (epnc.co.kr):
+ *           opening section -- the server aggregates the clients' models as a
+ *           simple average or weighted by each client's contribution, and
+ *           clients share only part of the weights; "Server-side workflow" --
+ *           after all updates arrive the server runs a weighted aggregation,
+ *           updates the global model and starts the next round.
+ *  [FLARE]  "Building Federated Multimodal AI Workflows with NVIDIA FLARE":
+ *           "Coordinating training across clients" -- the client update
+ *           contract fixes which components each client may update and how
+ *           component-level updates are combined; "Moving and aggregating
+ *           large model updates efficiently" -- the two memory pressures
+ *           (one update in flight; many updates held during aggregation), the
+ *           Tensor Downloader's tunable chunk size, and aggregation offloaded
+ *           so server memory does not grow with the client count;
+ *           "Federating small adapters on a frozen VLM with FedUMM" -- only
+ *           adapter updates are aggregated.
+ *  [Part]   "Technical Summary: Adaptive Data Partitioning for Energy-
+ *           Efficient Federated and Distributed Learning in Heterogeneous
+ *           Systems", section 2, "The adaptive controller", Measurement --
+ *           each participant reports its sample count n_i for the round.
+ *  [NVFP4]  "Accelerating LLM training with NVFP4 on NVIDIA Blackwell",
+ *           list of ingredients, stochastic-rounding item -- weights are
+ *           rounded to nearest even; "Applying NVFP4 in Transformer layers"
+ *           -- low-precision results fold into fp32 master weights.
+ *
+ * Conventions for every call:
+ *  - No call aborts, traps or waits without bound.  Errors come back as a
+ *    negative fa_status; fa_last_error() gives a one-line detail.
+ *  - Calls on one context are serialised by a mutex inside the context.
+ *  - Device work is issued on the caller's `stream` (a cudaStream_t passed as
+ *    void*, NULL = the legacy default stream).  Work on one context is
+ *    chained across streams with events, so contributions apply in call
+ *    order and two streams never race on the running sum.
+ *  - Sizes and offsets are in ELEMENTS of the input dtype.
+ */
+#ifndef FEDAVG_H
+#define FEDAVG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t fa_status;
+
+#define FA_OK              0
+#define FA_ERR_ARG        -1   /* null/invalid argument, unknown key, client id >= max_clients */
+#define FA_ERR_RANGE      -2   /* offset+len past the key (or the flat layout), or more elements
+                                  than numel sent by one client for one key */
+#define FA_ERR_DTYPE      -3   /* unsupported dtype combination */
+#define FA_ERR_WEIGHT     -4   /* weight not finite, < 0, > 2^24, or unlike this client's earlier chunks */
+#define FA_ERR_INCOMPLETE -5   /* finalize: some client sent only part of a key */
+#define FA_ERR_STATE      -6   /* accumulate after finalize (call fa_reset first) */
+#define FA_ERR_NOMEM      -7   /* device or pinned host allocation failed */
+#define FA_ERR_CUDA       -8   /* a CUDA runtime call failed (detail in fa_last_error) */
+#define FA_ERR_TIMEOUT    -9   /* a bounded host wait ran out (opts.timeout_ms) */
+#define FA_ERR_INTERNAL  -10   /* broken invariant inside the library */
+
+typedef enum { FA_F32 = 0, FA_BF16 = 1 } fa_dtype;
+
+/* One entry of the layout: key id = index in the layout array.  `name` is
+ * informational (may be NULL); `numel` >= 1. */
+typedef struct {
+    const char* name;
+    uint64_t numel;
+} fa_key;
+
+typedef struct fa_ctx fa_ctx;   /* opaque; owned by the library */
+
+/* Pass as `key` to address the flat layout: the keys concatenated in layout
+ * order without padding.  A flat chunk may span several keys. */
+#define FA_KEY_FLAT (-1)
+
+/* fa_opts.flags */
+#define FA_FLAT_OUT 1u   /* fa_finalize takes ONE output pointer to the flat layout */
+
+typedef struct {
+    uint32_t size;        /* sizeof(fa_opts): lets the struct grow */
+    uint32_t ring_slots;  /* device staging slots for host-memory chunks (0 = default 4) */
+    uint64_t slot_bytes;  /* bytes per staging slot (0 = default 64 MiB; rounded up to 256 B) --
+                             the chunk-size knob of [FLARE]'s Tensor Downloader, here a
+                             trade of pinned/device staging memory against per-copy overhead */
+    uint32_t timeout_ms;  /* bound on every host-side wait (0 = default 60000) */
+    uint32_t flags;       /* FA_FLAT_OUT */
+} fa_opts;
+
+typedef struct {
+    uint64_t kernel_launches;   /* kernels this context has launched since fa_open */
+    uint64_t client_bytes;      /* bytes of client updates accumulated */
+    uint64_t h2d_bytes;         /* bytes copied host -> device by the staging ring */
+    uint64_t d2h_bytes;         /* bytes copied device -> host by fa_finalize */
+    uint64_t chunks;            /* accepted fa_accumulate / fa_accumulate_batch calls */
+} fa_stats;
+
+/* Create an aggregation context on the current CUDA device.
+ *   layout[0..n_keys)  the state dict's keys (copied; caller keeps ownership)
+ *   dtype_in           element type of client updates (FA_F32 or FA_BF16)
+ *   dtype_out          element type of the aggregate (FA_F32 or FA_BF16); rounding to
+ *                      nearest even per [NVFP4]
+ *   max_clients        client ids are 0..max_clients-1 (>= 1)
+ *   opts               NULL for defaults
+ * Allocates the fp32 running sum (sum of numel rounded up to 32 per key, x 4 bytes)
+ * in device memory, the staging ring lazily on first host-memory chunk.
+ * Errors: FA_ERR_ARG, FA_ERR_DTYPE, FA_ERR_NOMEM, FA_ERR_CUDA.  *out is NULL on error. */
+fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_dtype dtype_out,
+                  uint32_t max_clients, const fa_opts* opts, fa_ctx** out);
+
+/* Add one chunk of client `client_id`'s update, weighted by `weight_nk`
+ * ([Part]: the client's sample count; [Clara]: weighted aggregation).
+ *   key            a key id, or FA_KEY_FLAT
+ *   offset_elems   first element of the chunk within the key (or the flat layout)
+ *   chunk_ptr      len_elems contiguous values of dtype_in, in device memory or host
+ *                  memory (pinned or pageable; detected per call)
+ *   stream         cudaStream_t (as void*) ordering the read of chunk_ptr
+ * The first chunk of a client in a round fixes its weight: later chunks must pass the
+ * same value (else FA_ERR_WEIGHT).  weight_nk must be finite, >= 0 and <= 2^24 (the
+ * device multiplies by (float)weight_nk, exact for integers in that range).
+ * A client that sends a key must send all of it before fa_finalize (chunks of one
+ * client and key must not overlap; the library counts elements).
+ * Ownership: device and pinned-host chunks are read in order on `stream`: the caller
+ * must not overwrite them until the work this call queued on `stream` has completed.
+ * Pageable-host chunks have been copied into library staging when the call returns.
+ * len_elems == 0 is a no-op.  Nothing is changed when an error is returned.
+ * Errors: FA_ERR_ARG, FA_ERR_RANGE, FA_ERR_WEIGHT, FA_ERR_STATE, FA_ERR_CUDA,
+ * FA_ERR_TIMEOUT, FA_ERR_NOMEM. */
+fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64_t key,
+                        uint64_t offset_elems, const void* chunk_ptr, uint64_t len_elems,
+                        void* stream);
+
+/* K-resident form of fa_accumulate: n_clients updates of the SAME element range,
+ * all in device memory, reduced in one pass over the running sum.  Equivalent
+ * to calling fa_accumulate for client_ids[0], client_ids[1], ... in that order,
+ * and bit-identical to it.  Client ids within one call must be distinct.
+ * [FLARE]: the second memory pressure -- many client updates held at once --
+ * turned into one read of each update and one write of the sum.
+ * Errors: as fa_accumulate; FA_ERR_ARG if any chunk_ptrs[j] is not device memory. */
+fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
+                              const double* weights, int64_t key, uint64_t offset_elems,
+                              const void* const* chunk_ptrs, uint64_t len_elems, void* stream);
+
+/* Write the aggregate: for every key with N_p > 0,
+ *     out[p][i] = round_to_dtype_out( sum[p][i] / (float)N_p )      (IEEE division, RNE)
+ * Keys no client sent (or whose reporters all have weight 0) are NOT written, so the
+ * caller's previous global values survive (the frozen-backbone / adapter case of [FLARE]).
+ *   out_ptrs  n_keys pointers (one per key, numel elements of dtype_out each), or, with
+ *             FA_FLAT_OUT, one pointer to the flat layout.  Device or host memory.
+ * Returns FA_ERR_INCOMPLETE, writing nothing, if a client sent part of a key.
+ * Non-destructive: calling it again gives the same result.  After it, fa_accumulate
+ * returns FA_ERR_STATE until fa_reset.  Output is complete once the work queued on
+ * `stream` has completed (host outputs: once the call's copies on `stream` complete).
+ * Errors: FA_ERR_ARG, FA_ERR_INCOMPLETE, FA_ERR_CUDA, FA_ERR_NOMEM, FA_ERR_TIMEOUT. */
+fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream);
+
+/* Start a new round ([Clara] "Server-side workflow": the loop repeats per round):
+ * forget weights, per-key totals, reporter masks and element counts.  The running sum
+ * is not cleared (the first contribution of the next round overwrites it).  Waits
+ * (bounded) for the context's queued work first.  Errors: FA_ERR_TIMEOUT, FA_ERR_CUDA. */
+fa_status fa_reset(fa_ctx* ctx);
+
+/* Wait (bounded by opts.timeout_ms) for the context's queued work, then free it.
+ * NULL is accepted.  Errors: FA_ERR_TIMEOUT (the context is then still freed). */
+fa_status fa_close(fa_ctx* ctx);
+
+/* Per-key weight total N_p (fp64, summed in ascending client id) and the number of
+ * clients that sent key p, from the host bookkeeping -- exact, no device access. */
+fa_status fa_key_total(const fa_ctx* ctx, uint32_t key, double* sum_nk, uint32_t* n_clients);
+
+/* Wait, bounded by opts.timeout_ms, until all work the context queued has completed.
+ * Returns FA_ERR_TIMEOUT (never hangs) or FA_ERR_CUDA if that work failed. */
+fa_status fa_sync(fa_ctx* ctx);
+
+/* Counters since fa_open (host-side, exact). */
+fa_status fa_get_stats(const fa_ctx* ctx, fa_stats* out);
+
+/* Static text for a status code. */
+const char* fa_strerror(fa_status status);
+
+/* Detail of the last error on this context ("" if none); valid until the next call. */
+const char* fa_last_error(const fa_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FEDAVG_H */

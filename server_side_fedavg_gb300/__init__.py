@@ -1,0 +1,194 @@
+"""Server-side FedAvg aggregation on one GB300: Python binding of libfedavg.so.
+
+Thin ctypes marshalling over the C ABI in include/fedavg.h; every function
+has the C name and raises FedAvgError on a negative status.  All device work
+happens in the library's CUDA kernels: there is no Python or CPU compute path,
+and importing the binding without the built library fails loudly.
+
+Pointers may be given as ints, as objects with .data_ptr() (torch tensors) or
+as numpy arrays (host memory); streams as ints or objects with .cuda_stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfedavg.so")
+
+FA_OK = 0
+FA_ERR_ARG = -1
+FA_ERR_RANGE = -2
+FA_ERR_DTYPE = -3
+FA_ERR_WEIGHT = -4
+FA_ERR_INCOMPLETE = -5
+FA_ERR_STATE = -6
+FA_ERR_NOMEM = -7
+FA_ERR_CUDA = -8
+FA_ERR_TIMEOUT = -9
+FA_ERR_INTERNAL = -10
+
+FA_F32 = 0
+FA_BF16 = 1
+FA_KEY_FLAT = -1
+FA_FLAT_OUT = 1
+
+DTYPES = {"f32": FA_F32, "bf16": FA_BF16, FA_F32: FA_F32, FA_BF16: FA_BF16}
+
+
+class fa_key(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("numel", ctypes.c_uint64)]
+
+
+class fa_opts(ctypes.Structure):
+    _fields_ = [("size", ctypes.c_uint32), ("ring_slots", ctypes.c_uint32),
+                ("slot_bytes", ctypes.c_uint64), ("timeout_ms", ctypes.c_uint32),
+                ("flags", ctypes.c_uint32)]
+
+
+class fa_stats(ctypes.Structure):
+    _fields_ = [("kernel_launches", ctypes.c_uint64), ("client_bytes", ctypes.c_uint64),
+                ("h2d_bytes", ctypes.c_uint64), ("d2h_bytes", ctypes.c_uint64),
+                ("chunks", ctypes.c_uint64)]
+
+
+class FedAvgError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        self.detail = detail
+        super().__init__(f"{status} ({fa_strerror(status)}): {detail}")
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libfedavg.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, u32, u64, i64, f64, vp = (ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint64,
+                                       ctypes.c_int64, ctypes.c_double, ctypes.c_void_p)
+        L.fa_open.argtypes = [ctypes.POINTER(fa_key), u32, i32, i32, u32, ctypes.POINTER(fa_opts),
+                              ctypes.POINTER(vp)]
+        L.fa_accumulate.argtypes = [vp, u32, f64, i64, u64, vp, u64, vp]
+        L.fa_accumulate_batch.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64), i64,
+                                          u64, ctypes.POINTER(vp), u64, vp]
+        L.fa_finalize.argtypes = [vp, ctypes.POINTER(vp), vp]
+        L.fa_reset.argtypes = [vp]
+        L.fa_close.argtypes = [vp]
+        L.fa_key_total.argtypes = [vp, u32, ctypes.POINTER(f64), ctypes.POINTER(u32)]
+        L.fa_sync.argtypes = [vp]
+        L.fa_get_stats.argtypes = [vp, ctypes.POINTER(fa_stats)]
+        L.fa_strerror.argtypes = [i32]
+        L.fa_strerror.restype = ctypes.c_char_p
+        L.fa_last_error.argtypes = [vp]
+        L.fa_last_error.restype = ctypes.c_char_p
+        for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_finalize", "fa_reset",
+                     "fa_close", "fa_key_total", "fa_sync", "fa_get_stats"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    if hasattr(x, "ctypes"):
+        return int(x.ctypes.data)
+    raise TypeError(f"cannot take a pointer of {type(x)!r}")
+
+
+def _stream(s) -> int:
+    if s is None:
+        return 0
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(status: int, ctx=None):
+    if status != FA_OK:
+        detail = fa_last_error(ctx) if ctx is not None else ""
+        raise FedAvgError(status, detail)
+
+
+def fa_strerror(status: int) -> str:
+    return lib().fa_strerror(status).decode()
+
+
+def fa_last_error(ctx) -> str:
+    r = lib().fa_last_error(ctx)
+    return r.decode() if r else ""
+
+
+def fa_open(layout, dtype_in, dtype_out, max_clients, ring_slots=0, slot_bytes=0,
+            timeout_ms=0, flags=0):
+    """layout: list of (name, numel).  Returns an opaque context handle."""
+    n = len(layout)
+    keys = (fa_key * max(n, 1))()
+    names = []
+    for i, (name, numel) in enumerate(layout):
+        b = name.encode() if isinstance(name, str) else name
+        names.append(b)
+        keys[i].name = b
+        keys[i].numel = int(numel)
+    opts = fa_opts(ctypes.sizeof(fa_opts), ring_slots, slot_bytes, timeout_ms, flags)
+    ctx = ctypes.c_void_p()
+    _check(lib().fa_open(keys, n, DTYPES[dtype_in], DTYPES[dtype_out], max_clients,
+                         ctypes.byref(opts), ctypes.byref(ctx)))
+    return ctx
+
+
+def fa_accumulate(ctx, client_id, weight_nk, key, offset_elems, chunk, len_elems, stream=None):
+    _check(lib().fa_accumulate(ctx, client_id, float(weight_nk), key, offset_elems, _ptr(chunk),
+                               len_elems, _stream(stream)), ctx)
+
+
+def fa_accumulate_batch(ctx, client_ids, weights, key, offset_elems, chunks, len_elems,
+                        stream=None):
+    J = len(client_ids)
+    ids = (ctypes.c_uint32 * J)(*client_ids)
+    ws = (ctypes.c_double * J)(*[float(w) for w in weights])
+    ps = (ctypes.c_void_p * J)(*[_ptr(c) for c in chunks])
+    _check(lib().fa_accumulate_batch(ctx, J, ids, ws, key, offset_elems, ps, len_elems,
+                                     _stream(stream)), ctx)
+
+
+def fa_finalize(ctx, outs, stream=None):
+    """outs: list of per-key outputs (None allowed for keys that will not be written),
+    or a one-element list with the flat output when opened with FA_FLAT_OUT."""
+    ps = (ctypes.c_void_p * max(len(outs), 1))(*[_ptr(o) for o in outs])
+    _check(lib().fa_finalize(ctx, ps, _stream(stream)), ctx)
+
+
+def fa_reset(ctx):
+    _check(lib().fa_reset(ctx), ctx)
+
+
+def fa_close(ctx):
+    _check(lib().fa_close(ctx))
+
+
+def fa_key_total(ctx, key):
+    s = ctypes.c_double()
+    n = ctypes.c_uint32()
+    _check(lib().fa_key_total(ctx, key, ctypes.byref(s), ctypes.byref(n)), ctx)
+    return s.value, n.value
+
+
+def fa_sync(ctx):
+    _check(lib().fa_sync(ctx), ctx)
+
+
+def fa_get_stats(ctx) -> dict:
+    st = fa_stats()
+    _check(lib().fa_get_stats(ctx, ctypes.byref(st)), ctx)
+    return {f: getattr(st, f) for f, _ in fa_stats._fields_}

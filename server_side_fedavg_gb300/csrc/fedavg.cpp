@@ -1,0 +1,614 @@
+// Runtime and C ABI of the aggregation library (declared in include/fedavg.h).
+//
+// One context = one round's state on one GPU:
+//  - the fp32 running sum in device memory (padded layout, see ledger.hpp);
+//  - the host ledger (weights, reporter masks, element counts, per-key totals);
+//  - a staging ring for chunks that arrive in host memory: R device slots fed by
+//    cudaMemcpyAsync on a copy stream, overlapped with the kernels on the caller's
+//    stream, plus R pinned host slots used only for pageable sources.  This is the
+//    chunked, memory-bounded ingest that "Building Federated Multimodal AI Workflows
+//    with NVIDIA FLARE" motivates ("Moving and aggregating large model updates
+//    efficiently": the Tensor Downloader's chunk size trades per-request overhead
+//    against per-chunk memory);
+//  - an event chain: after every launch an event is recorded on the stream used and
+//    the next launch (on any stream) waits for it, so contributions land in call
+//    order and streams never race on the running sum.
+// Every host wait polls with a deadline (opts.timeout_ms) and returns
+// FA_ERR_TIMEOUT instead of blocking forever.
+#include <fedavg.h>
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "kernels.cuh"
+#include "ledger.hpp"
+
+namespace {
+
+constexpr uint64_t kDefaultSlotBytes = 64ull << 20;
+constexpr uint32_t kDefaultSlots = 4;
+constexpr uint32_t kDefaultTimeoutMs = 60000;
+
+enum class Mem { kDevice, kPinned, kPageable };
+
+}  // namespace
+
+struct fa_ctx {
+    std::mutex mu;
+    fa::Ledger ledger;
+    int device = 0;
+    int din = 0, dout = 0;        // 0 fp32, 1 bf16
+    uint32_t s_in = 4, s_out = 4;
+    uint32_t flags = 0;
+    uint32_t timeout_ms = kDefaultTimeoutMs;
+    uint32_t slots = kDefaultSlots;
+    uint64_t slot_bytes = kDefaultSlotBytes;
+    float* acc = nullptr;
+    fa::LaunchShape shape;
+
+    cudaEvent_t chain = nullptr;  // recorded after the last queued operation
+    bool chain_valid = false;
+    cudaEvent_t user_ev = nullptr;
+
+    cudaStream_t copy_stream = nullptr;
+    std::vector<void*> dev_slot, host_slot;
+    std::vector<cudaEvent_t> ev_copied, ev_free;
+    std::vector<uint8_t> slot_used;
+    uint32_t next_slot = 0;
+
+    fa::FinSeg* fin_dev = nullptr;
+    fa::FinSeg* fin_host = nullptr;
+    cudaEvent_t fin_ev = nullptr;
+    bool fin_pending = false;
+    void* out_stage = nullptr;
+
+    bool broken = false;          // a CUDA call failed after the ledger was updated
+    fa_stats stats{};
+    std::string err;
+    std::vector<fa::Piece> pieces;
+    std::vector<fa::FinItem> items;
+};
+
+namespace {
+
+// Switches to the context's device for the duration of a call.
+class DeviceGuard {
+public:
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev_) == cudaSuccess && prev_ != dev) {
+            if (cudaSetDevice(dev) == cudaSuccess) restore_ = true;
+        }
+    }
+    ~DeviceGuard() {
+        if (restore_) cudaSetDevice(prev_);
+    }
+
+private:
+    int prev_ = 0;
+    bool restore_ = false;
+};
+
+fa_status fail(fa_ctx* c, fa_status s, const std::string& what) {
+    c->err = what;
+    return s;
+}
+
+fa_status cuda_fail(fa_ctx* c, cudaError_t e, const char* where) {
+    c->err = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return e == cudaErrorMemoryAllocation ? FA_ERR_NOMEM : FA_ERR_CUDA;
+}
+
+#define FA_CUDA(ctx, call)                                   \
+    do {                                                     \
+        cudaError_t e_ = (call);                             \
+        if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
+    } while (0)
+
+// Poll an event until it completes or the deadline passes.
+fa_status wait_event(fa_ctx* c, cudaEvent_t ev, const char* what) {
+    auto t0 = std::chrono::steady_clock::now();
+    uint32_t spins = 0;
+    for (;;) {
+        cudaError_t e = cudaEventQuery(ev);
+        if (e == cudaSuccess) return FA_OK;
+        if (e != cudaErrorNotReady) return cuda_fail(c, e, what);
+        auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                      std::chrono::steady_clock::now() - t0)
+                      .count();
+        if (ms > static_cast<long long>(c->timeout_ms)) {
+            c->err = std::string(what) + ": no completion within timeout_ms";
+            return FA_ERR_TIMEOUT;
+        }
+        if (++spins < 64)
+            std::this_thread::yield();
+        else
+            std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+}
+
+Mem classify(const void* p, int device, bool* other_device) {
+    *other_device = false;
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return Mem::kPageable;
+    }
+    switch (at.type) {
+        case cudaMemoryTypeDevice:
+            *other_device = at.device != device;
+            return Mem::kDevice;
+        case cudaMemoryTypeManaged:
+            return Mem::kDevice;
+        case cudaMemoryTypeHost:
+            return Mem::kPinned;
+        default:
+            return Mem::kPageable;
+    }
+}
+
+// Make `s` wait for everything queued on the context so far.
+fa_status chain_in(fa_ctx* c, cudaStream_t s) {
+    if (c->chain_valid) FA_CUDA(c, cudaStreamWaitEvent(s, c->chain, 0));
+    return FA_OK;
+}
+
+fa_status chain_out(fa_ctx* c, cudaStream_t s) {
+    FA_CUDA(c, cudaEventRecord(c->chain, s));
+    c->chain_valid = true;
+    return FA_OK;
+}
+
+fa_status ensure_ring(fa_ctx* c, bool need_host) {
+    if (c->dev_slot.empty()) {
+        FA_CUDA(c, cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking));
+        c->dev_slot.assign(c->slots, nullptr);
+        c->host_slot.assign(c->slots, nullptr);
+        c->ev_copied.assign(c->slots, nullptr);
+        c->ev_free.assign(c->slots, nullptr);
+        c->slot_used.assign(c->slots, 0);
+        for (uint32_t i = 0; i < c->slots; ++i) {
+            FA_CUDA(c, cudaMalloc(&c->dev_slot[i], c->slot_bytes));
+            FA_CUDA(c, cudaEventCreateWithFlags(&c->ev_copied[i], cudaEventDisableTiming));
+            FA_CUDA(c, cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming));
+        }
+    }
+    if (need_host && c->host_slot[0] == nullptr) {
+        for (uint32_t i = 0; i < c->slots; ++i)
+            FA_CUDA(c, cudaHostAlloc(&c->host_slot[i], c->slot_bytes, cudaHostAllocDefault));
+    }
+    return FA_OK;
+}
+
+// Launch the accumulate kernel(s) for the pieces that fall in chunk elements
+// [c0, c0 + n), reading inputs xs[0..J) whose element 0 is chunk element c0.
+fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_t c0,
+                        uint64_t n, const void* const* xs, const float* ws, uint32_t J,
+                        cudaStream_t s) {
+    // greedy split of J into launches of 16, 8, 4, 2, 1 clients; after the first
+    // launch the sum is started everywhere
+    uint32_t done = 0;
+    while (done < J) {
+        uint32_t left = J - done, jb = 16;
+        while (jb > left) jb >>= 1;
+        fa::AccArgs a;
+        std::memset(&a, 0, sizeof a);
+        for (uint32_t j = 0; j < jb; ++j) {
+            a.x[j] = xs[done + j];
+            a.w[j] = ws[done + j];
+        }
+        a.acc = c->acc;
+        a.J = jb;
+        auto flush = [&]() -> fa_status {
+            if (a.nseg == 0) return FA_OK;
+            FA_CUDA(c, fa::launch_accumulate(a, c->din, c->shape, s));
+            c->stats.kernel_launches++;
+            a.nseg = 0;
+            a.ntiles = 0;
+            a.vec_ok = 0;
+            return FA_OK;
+        };
+        for (const auto& p : pieces) {
+            uint64_t b = std::max(p.chunk_off, c0);
+            uint64_t e = std::min(p.chunk_off + p.len, c0 + n);
+            if (b >= e) continue;
+            if (a.nseg == static_cast<uint32_t>(fa::kMaxSegs)) {
+                fa_status st = flush();
+                if (st != FA_OK) return st;
+            }
+            fa::AccSeg& g = a.seg[a.nseg];
+            g.x_off = b - c0;
+            g.acc_idx = p.acc_idx + (b - p.chunk_off);
+            g.len = e - b;
+            g.first = (p.first && done == 0) ? 1u : 0u;
+            g.tile0 = a.ntiles;
+            bool ok = (reinterpret_cast<uintptr_t>(c->acc + g.acc_idx) & 15u) == 0;
+            for (uint32_t j = 0; j < jb && ok; ++j) {
+                uintptr_t xa = reinterpret_cast<uintptr_t>(a.x[j]) + g.x_off * c->s_in;
+                ok = (xa & 15u) == 0;
+            }
+            if (ok) a.vec_ok |= 1ull << a.nseg;
+            uint64_t tiles = (g.len + fa::kTile - 1) / fa::kTile;
+            if (tiles > 0xFFFFFFFFull - a.ntiles) return fail(c, FA_ERR_RANGE, "chunk too large for one launch");
+            a.ntiles += static_cast<uint32_t>(tiles);
+            a.nseg++;
+        }
+        fa_status st = flush();
+        if (st != FA_OK) return st;
+        done += jb;
+    }
+    return FA_OK;
+}
+
+fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const double* weights,
+                          int64_t key, uint64_t offset, const void* const* ptrs, uint64_t len,
+                          cudaStream_t s, bool batch) {
+    if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
+    if (len > 0) {
+        for (uint32_t j = 0; j < J; ++j)
+            if (ptrs == nullptr || ptrs[j] == nullptr) return fail(c, FA_ERR_ARG, "chunk pointer is NULL");
+    }
+    Mem kind = Mem::kDevice;
+    if (len > 0) {
+        for (uint32_t j = 0; j < J; ++j) {
+            bool other = false;
+            Mem m = classify(ptrs[j], c->device, &other);
+            if (other) return fail(c, FA_ERR_ARG, "chunk is in another GPU's memory");
+            if (batch && m != Mem::kDevice)
+                return fail(c, FA_ERR_ARG, "fa_accumulate_batch takes device memory only");
+            kind = m;
+        }
+    }
+    std::string e;
+    int32_t st = c->ledger.plan_accumulate(ids, weights, J, key, offset, len, &c->pieces, &e);
+    if (st != fa::kOk) return fail(c, st, e);
+    if (len == 0) return FA_OK;
+
+    std::vector<float> wv(J);
+    for (uint32_t j = 0; j < J; ++j) wv[j] = static_cast<float>(weights[j]);
+    const float* wp = wv.data();
+
+    fa_status r = FA_OK;
+    if (kind == Mem::kDevice) {
+        r = chain_in(c, s);
+        if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, J, s);
+        if (r == FA_OK) r = chain_out(c, s);
+    } else {
+        // host memory: through the staging ring, slot-sized pieces
+        r = ensure_ring(c, kind == Mem::kPageable);
+        const uint64_t per = c->slot_bytes / c->s_in;
+        const char* src0 = static_cast<const char*>(ptrs[0]);
+        if (r == FA_OK && kind == Mem::kPinned) {
+            // the copy must follow the caller's earlier work on `s`
+            cudaError_t ce = cudaEventRecord(c->user_ev, s);
+            if (ce == cudaSuccess) ce = cudaStreamWaitEvent(c->copy_stream, c->user_ev, 0);
+            if (ce != cudaSuccess) r = cuda_fail(c, ce, "order copy after caller stream");
+        }
+        for (uint64_t c0 = 0; r == FA_OK && c0 < len; c0 += per) {
+            const uint64_t n = std::min(per, len - c0);
+            const uint32_t k = c->next_slot;
+            c->next_slot = (k + 1) % c->slots;
+            const void* src = src0 + c0 * c->s_in;
+            if (kind == Mem::kPageable) {
+                if (c->slot_used[k]) {
+                    r = wait_event(c, c->ev_copied[k], "staging slot reuse");
+                    if (r != FA_OK) break;
+                }
+                std::memcpy(c->host_slot[k], src, n * c->s_in);
+                src = c->host_slot[k];
+            }
+            cudaError_t ce = cudaSuccess;
+            if (c->slot_used[k]) ce = cudaStreamWaitEvent(c->copy_stream, c->ev_free[k], 0);
+            if (ce == cudaSuccess)
+                ce = cudaMemcpyAsync(c->dev_slot[k], src, n * c->s_in, cudaMemcpyHostToDevice,
+                                     c->copy_stream);
+            if (ce == cudaSuccess) ce = cudaEventRecord(c->ev_copied[k], c->copy_stream);
+            if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, c->ev_copied[k], 0);
+            if (ce != cudaSuccess) {
+                r = cuda_fail(c, ce, "staging copy");
+                break;
+            }
+            c->slot_used[k] = 1;
+            c->stats.h2d_bytes += n * c->s_in;
+            r = chain_in(c, s);
+            const void* xs[1] = {c->dev_slot[k]};
+            if (r == FA_OK) r = launch_pieces(c, c->pieces, c0, n, xs, wp, 1, s);
+            if (r == FA_OK) r = chain_out(c, s);
+            if (r == FA_OK) {
+                ce = cudaEventRecord(c->ev_free[k], s);
+                if (ce != cudaSuccess) r = cuda_fail(c, ce, "slot release");
+            }
+        }
+    }
+    if (r != FA_OK) {
+        c->broken = true;
+        return r;
+    }
+    c->stats.chunks++;
+    c->stats.client_bytes += static_cast<uint64_t>(J) * len * c->s_in;
+    return FA_OK;
+}
+
+void free_ctx(fa_ctx* c) {
+    if (c->acc) cudaFree(c->acc);
+    for (void* p : c->dev_slot)
+        if (p) cudaFree(p);
+    for (void* p : c->host_slot)
+        if (p) cudaFreeHost(p);
+    for (auto ev : c->ev_copied)
+        if (ev) cudaEventDestroy(ev);
+    for (auto ev : c->ev_free)
+        if (ev) cudaEventDestroy(ev);
+    if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+    if (c->chain) cudaEventDestroy(c->chain);
+    if (c->user_ev) cudaEventDestroy(c->user_ev);
+    if (c->fin_ev) cudaEventDestroy(c->fin_ev);
+    if (c->fin_dev) cudaFree(c->fin_dev);
+    if (c->fin_host) cudaFreeHost(c->fin_host);
+    if (c->out_stage) cudaFree(c->out_stage);
+    delete c;
+}
+
+fa_status sync_impl(fa_ctx* c) {
+    if (c->chain_valid) {
+        fa_status r = wait_event(c, c->chain, "fa_sync");
+        if (r != FA_OK) return r;
+    }
+    for (size_t k = 0; k < c->ev_copied.size(); ++k) {
+        if (!c->slot_used[k]) continue;
+        fa_status r = wait_event(c, c->ev_copied[k], "fa_sync (copy)");
+        if (r != FA_OK) return r;
+    }
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_strerror(fa_status s) {
+    switch (s) {
+        case FA_OK: return "ok";
+        case FA_ERR_ARG: return "invalid argument";
+        case FA_ERR_RANGE: return "offset or length out of range";
+        case FA_ERR_DTYPE: return "unsupported dtype";
+        case FA_ERR_WEIGHT: return "invalid or inconsistent client weight";
+        case FA_ERR_INCOMPLETE: return "a client sent only part of a key";
+        case FA_ERR_STATE: return "call not allowed in the current state";
+        case FA_ERR_NOMEM: return "out of memory";
+        case FA_ERR_CUDA: return "CUDA error";
+        case FA_ERR_TIMEOUT: return "timed out waiting for the GPU";
+        case FA_ERR_INTERNAL: return "internal error";
+        default: return "unknown status";
+    }
+}
+
+const char* fa_last_error(const fa_ctx* ctx) { return ctx ? ctx->err.c_str() : ""; }
+
+fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_dtype dtype_out,
+                  uint32_t max_clients, const fa_opts* opts, fa_ctx** out) {
+    if (out == nullptr) return FA_ERR_ARG;
+    *out = nullptr;
+    if (layout == nullptr || n_keys == 0 || max_clients == 0) return FA_ERR_ARG;
+    if ((dtype_in != FA_F32 && dtype_in != FA_BF16) || (dtype_out != FA_F32 && dtype_out != FA_BF16))
+        return FA_ERR_DTYPE;
+    fa_opts o{};
+    if (opts) {
+        if (opts->size < sizeof(uint32_t) * 2) return FA_ERR_ARG;
+        std::memcpy(&o, opts, std::min<size_t>(opts->size, sizeof o));
+    }
+    fa_ctx* c = new (std::nothrow) fa_ctx;
+    if (!c) return FA_ERR_NOMEM;
+    c->din = dtype_in == FA_F32 ? 0 : 1;
+    c->dout = dtype_out == FA_F32 ? 0 : 1;
+    c->s_in = c->din == 0 ? 4 : 2;
+    c->s_out = c->dout == 0 ? 4 : 2;
+    c->flags = o.flags;
+    if (o.timeout_ms) c->timeout_ms = o.timeout_ms;
+    if (o.ring_slots) c->slots = o.ring_slots;
+    if (o.slot_bytes) c->slot_bytes = (o.slot_bytes + 255) / 256 * 256;
+    if (c->slots > 64) {
+        delete c;
+        return FA_ERR_ARG;
+    }
+    std::vector<uint64_t> numels(n_keys);
+    for (uint32_t p = 0; p < n_keys; ++p) numels[p] = layout[p].numel;
+    std::string e;
+    if (c->ledger.init(numels.data(), n_keys, max_clients, &e) != fa::kOk) {
+        delete c;
+        return FA_ERR_ARG;
+    }
+    cudaError_t ce = cudaGetDevice(&c->device);
+    if (ce == cudaSuccess) ce = fa::query_launch_shape(&c->shape);
+    if (ce == cudaSuccess) ce = cudaMalloc(&c->acc, c->ledger.padded_elems() * sizeof(float));
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->chain, cudaEventDisableTiming);
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->user_ev, cudaEventDisableTiming);
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->fin_ev, cudaEventDisableTiming);
+    if (ce == cudaSuccess) ce = cudaMalloc(&c->fin_dev, sizeof(fa::FinSeg) * n_keys);
+    if (ce == cudaSuccess) ce = cudaHostAlloc(&c->fin_host, sizeof(fa::FinSeg) * n_keys, cudaHostAllocDefault);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        free_ctx(c);
+        return ce == cudaErrorMemoryAllocation ? FA_ERR_NOMEM : FA_ERR_CUDA;
+    }
+    *out = c;
+    return FA_OK;
+}
+
+fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64_t key,
+                        uint64_t offset_elems, const void* chunk_ptr, uint64_t len_elems,
+                        void* stream) {
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    ctx->err.clear();
+    const void* ptrs[1] = {chunk_ptr};
+    return accumulate_impl(ctx, 1, &client_id, &weight_nk, key, offset_elems, ptrs, len_elems,
+                           static_cast<cudaStream_t>(stream), false);
+}
+
+fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
+                              const double* weights, int64_t key, uint64_t offset_elems,
+                              const void* const* chunk_ptrs, uint64_t len_elems, void* stream) {
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    ctx->err.clear();
+    if (n_clients == 0 || client_ids == nullptr || weights == nullptr || chunk_ptrs == nullptr)
+        return fail(ctx, FA_ERR_ARG, "empty batch");
+    return accumulate_impl(ctx, n_clients, client_ids, weights, key, offset_elems, chunk_ptrs,
+                           len_elems, static_cast<cudaStream_t>(stream), true);
+}
+
+fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    fa_ctx* c = ctx;
+    c->err.clear();
+    if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
+    if (out_ptrs == nullptr) return fail(c, FA_ERR_ARG, "out_ptrs is NULL");
+    const bool flat = (c->flags & FA_FLAT_OUT) != 0;
+    std::string e;
+    {
+        int32_t st = c->ledger.plan_finalize(&c->items, &e);
+        if (st != fa::kOk) return fail(c, st, e);
+    }
+    std::vector<Mem> kind(c->items.size());
+    bool any_host = false;
+    for (size_t i = 0; i < c->items.size(); ++i) {
+        const auto& it = c->items[i];
+        void* dst = flat ? out_ptrs[0] : out_ptrs[it.key];
+        if (dst == nullptr) return fail(c, FA_ERR_ARG, "output pointer is NULL for a key to be written");
+        bool other = false;
+        kind[i] = classify(dst, c->device, &other);
+        if (other) return fail(c, FA_ERR_ARG, "output is in another GPU's memory");
+        any_host = any_host || kind[i] != Mem::kDevice;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (any_host && c->out_stage == nullptr)
+        FA_CUDA(c, cudaMalloc(&c->out_stage, c->ledger.total_elems() * c->s_out));
+    if (c->fin_pending) {
+        fa_status r = wait_event(c, c->fin_ev, "finalize table reuse");
+        if (r != FA_OK) return r;
+        c->fin_pending = false;
+    }
+    uint32_t ntiles = 0;
+    for (size_t i = 0; i < c->items.size(); ++i) {
+        const auto& it = c->items[i];
+        char* dst = static_cast<char*>(flat ? out_ptrs[0] : out_ptrs[it.key]);
+        if (flat) dst += it.flat_off * c->s_out;
+        if (kind[i] != Mem::kDevice)
+            dst = static_cast<char*>(c->out_stage) + it.flat_off * c->s_out;
+        fa::FinSeg& g = c->fin_host[i];
+        g.acc_idx = it.acc_idx;
+        g.len = it.numel;
+        g.out = dst;
+        g.divisor = static_cast<float>(it.total);
+        g.tile0 = ntiles;
+        uint64_t t = (it.numel + fa::kTile - 1) / fa::kTile;
+        if (t > 0xFFFFFFFFull - ntiles) return fail(c, FA_ERR_RANGE, "layout too large for one finalize");
+        ntiles += static_cast<uint32_t>(t);
+    }
+    // the round is closed from here on
+    c->ledger.close();
+    const uint32_t nseg = static_cast<uint32_t>(c->items.size());
+    fa_status r = chain_in(c, s);
+    if (r != FA_OK) return r;
+    if (nseg > 0) {
+        FA_CUDA(c, cudaMemcpyAsync(c->fin_dev, c->fin_host, sizeof(fa::FinSeg) * nseg,
+                                   cudaMemcpyHostToDevice, s));
+        FA_CUDA(c, cudaEventRecord(c->fin_ev, s));
+        c->fin_pending = true;
+        FA_CUDA(c, fa::launch_finalize(c->fin_dev, nseg, ntiles, c->dout, c->acc, c->shape, s));
+        c->stats.kernel_launches++;
+        // host outputs: copy the staged keys back, merging neighbours in the flat layout
+        for (size_t i = 0; i < c->items.size();) {
+            if (kind[i] == Mem::kDevice) {
+                ++i;
+                continue;
+            }
+            const auto& it = c->items[i];
+            if (flat) {
+                size_t j = i + 1;
+                uint64_t end = it.flat_off + it.numel;
+                while (j < c->items.size() && kind[j] != Mem::kDevice && c->items[j].flat_off == end) {
+                    end += c->items[j].numel;
+                    ++j;
+                }
+                char* dst = static_cast<char*>(out_ptrs[0]) + it.flat_off * c->s_out;
+                const char* src = static_cast<const char*>(c->out_stage) + it.flat_off * c->s_out;
+                uint64_t bytes = (end - it.flat_off) * c->s_out;
+                FA_CUDA(c, cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s));
+                c->stats.d2h_bytes += bytes;
+                i = j;
+            } else {
+                const char* src = static_cast<const char*>(c->out_stage) + it.flat_off * c->s_out;
+                uint64_t bytes = it.numel * c->s_out;
+                FA_CUDA(c, cudaMemcpyAsync(out_ptrs[it.key], src, bytes, cudaMemcpyDeviceToHost, s));
+                c->stats.d2h_bytes += bytes;
+                ++i;
+            }
+        }
+    }
+    return chain_out(c, s);
+}
+
+fa_status fa_reset(fa_ctx* ctx) {
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    ctx->err.clear();
+    fa_status r = sync_impl(ctx);
+    if (r != FA_OK) return r;
+    ctx->ledger.reset();
+    ctx->broken = false;
+    return FA_OK;
+}
+
+fa_status fa_close(fa_ctx* ctx) {
+    if (!ctx) return FA_OK;
+    DeviceGuard dg(ctx->device);
+    fa_status r;
+    {
+        // wait for callers still inside the context, then for its GPU work
+        std::lock_guard<std::mutex> lk(ctx->mu);
+        r = sync_impl(ctx);
+    }
+    // the mutex is released before the context (and the mutex) is freed
+    free_ctx(ctx);
+    return r;
+}
+
+fa_status fa_key_total(const fa_ctx* ctx, uint32_t key, double* sum_nk, uint32_t* n_clients) {
+    if (!ctx) return FA_ERR_ARG;
+    fa_ctx* c = const_cast<fa_ctx*>(ctx);
+    std::lock_guard<std::mutex> lk(c->mu);
+    return c->ledger.key_total(key, sum_nk, n_clients) == fa::kOk ? FA_OK : FA_ERR_ARG;
+}
+
+fa_status fa_sync(fa_ctx* ctx) {
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    ctx->err.clear();
+    return sync_impl(ctx);
+}
+
+fa_status fa_get_stats(const fa_ctx* ctx, fa_stats* out) {
+    if (!ctx || !out) return FA_ERR_ARG;
+    fa_ctx* c = const_cast<fa_ctx*>(ctx);
+    std::lock_guard<std::mutex> lk(c->mu);
+    *out = c->stats;
+    return FA_OK;
+}
+
+}  // extern "C"

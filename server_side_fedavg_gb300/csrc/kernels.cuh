@@ -1,0 +1,71 @@
+// Device kernels of the aggregation path and their launch interface.
+//
+//   accumulate  sum[i] = n_k * x[i]                (first contribution to element i)
+//               sum[i] = fma(n_k, x[i], sum[i])    (every later one)
+//               J >= 1 resident clients per launch: the same operation sequence,
+//               applied in client order with the partial sum kept in registers, so
+//               a batch is bit-identical to J single launches.
+//   finalize    out[i] = round_rne(sum[i] / N_p)   (IEEE division, then RNE to bf16
+//                                                   or a plain fp32 store)
+//
+// All three are HBM-bandwidth bound streaming passes (about 0.1 flop per byte):
+// no tensor cores.  Layout: the fp32 running sum is padded per key to 32
+// elements, so each key starts 128-byte aligned.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+constexpr int kBlock = 256;           // threads per CTA
+constexpr int kVec = 8;               // elements per vector (16 B of bf16, 2 x 16 B of fp32 sum)
+constexpr int kTile = 4096;           // elements per CTA work unit
+constexpr int kMaxSegs = 48;          // segments per accumulate launch
+constexpr int kMaxBatch = 16;         // resident clients per accumulate launch
+
+struct AccSeg {
+    uint64_t x_off;     // element offset into every input chunk
+    uint64_t acc_idx;   // element index into the running sum
+    uint64_t len;       // elements (>= 1)
+    uint32_t first;     // 1: the first client of the launch starts the sum here
+    uint32_t tile0;     // first tile of this segment in the launch's tile numbering
+};
+
+struct AccArgs {
+    const void* x[kMaxBatch];   // J input chunk bases (device), dtype_in
+    float w[kMaxBatch];         // (float) n_k per input
+    float* acc;
+    uint32_t J;
+    uint32_t nseg;
+    uint32_t ntiles;
+    uint64_t vec_ok;            // bit s: segment s is 16-byte aligned for x and sum
+    AccSeg seg[kMaxSegs];
+};
+
+struct FinSeg {
+    uint64_t acc_idx;   // start in the running sum
+    uint64_t len;       // elements
+    void* out;          // destination of element 0 (device), dtype_out
+    float divisor;      // (float) N_p
+    uint32_t tile0;     // first tile of this segment
+};
+
+struct LaunchShape {
+    int sms = 0;
+    int acc_ctas_per_sm[2][5] = {};   // [dtype_in][log2 J]
+    int fin_ctas_per_sm[2] = {};      // [dtype_out]
+};
+
+// Fills the occupancy table for the current device.
+cudaError_t query_launch_shape(LaunchShape* s);
+
+// dtype codes: 0 = fp32, 1 = bf16.  J must be 1, 2, 4, 8 or 16.
+cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,
+                              cudaStream_t stream);
+
+// segs: device array of nseg FinSeg sorted by tile0.
+cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_out,
+                            const float* acc, const LaunchShape& s, cudaStream_t stream);
+
+}  // namespace fa

@@ -19,6 +19,7 @@ adaptive-partitioning summary's per-participant sample counts n_i):
   llama7b   K=16, 7B-parameter decoder bf16 state dict, N(0,0.02) except one
             seeded client at 0.02*Student-t(3); n_k Zipf(1.2)-skewed;
             streamed in 256 MiB flat chunks
+  decoder1l K=4, one layer of the 7B decoder (profiling size)
 """
 from __future__ import annotations
 
@@ -231,9 +232,19 @@ def make(name: str) -> Workload:
         dists[_rng.below(seed, 6000, K)] = DIST_STUDENT3
         w = Workload(name, i, keys, K, BF16, BF16, 0.02, zipf_weights(seed, K),
                      [list(range(len(keys)))] * K, dists, (256 << 20) // 2, seed)
+    elif name == "decoder1l":
+        # one decoder layer of the 7B shape, K=4: the same kernels and chunking as
+        # llama7b at about 3 GB of device memory, still far larger than L2
+        i = 5
+        seed = BASE_SEED + i
+        keys = llama7b_layout(layers=1)[1:10]
+        K = 4
+        w = Workload(name, i, keys, K, BF16, BF16, 0.02, uniform_int_weights(seed, K),
+                     [list(range(len(keys)))] * K, [DIST_NORMAL] * K, (256 << 20) // 2, seed)
     else:
         raise ValueError(f"unknown workload {name!r}")
     return _finish(w)
 
 
 NAMES = ("tiny", "unet3d", "lora", "vlm2b", "llama7b")
+EXTRA = ("decoder1l",)

@@ -1,0 +1,96 @@
+"""The C ABI library loads and exports every entry point include/fedavg.h
+declares, its constants agree with the binding, and argument errors that need
+no device come back as status codes (CPU; no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import server_side_fedavg_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fedavg.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def _defines():
+    out = {}
+    for m in re.finditer(r"#define\s+(FA_\w+)\s+\(?(-?\w+)\)?", open(HEADER).read()):
+        try:
+            out[m.group(1)] = int(m.group(2).rstrip("uU"), 0)
+        except ValueError:
+            pass
+    return out
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return fa.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 11, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in fedavg.h but not exported"
+
+
+def test_constants_match_binding():
+    d = _defines()
+    for k, v in d.items():
+        if hasattr(fa, k):
+            assert getattr(fa, k) == v, k
+    assert d["FA_KEY_FLAT"] == -1 and d["FA_FLAT_OUT"] == 1
+
+
+def test_strerror_covers_all_codes(lib):
+    codes = [v for k, v in _defines().items() if k.startswith("FA_ERR_") or k == "FA_OK"]
+    texts = [fa.fa_strerror(c) for c in codes]
+    assert all(texts) and len(set(texts)) == len(texts)
+    assert fa.fa_strerror(-999) == "unknown status"
+
+
+def test_argument_errors_need_no_device(lib):
+    ctx = ctypes.c_void_p()
+    keys = (fa.fa_key * 1)(fa.fa_key(b"w", 4))
+    assert lib.fa_open(keys, 1, 0, 0, 1, None, None) == fa.FA_ERR_ARG
+    assert lib.fa_open(None, 1, 0, 0, 1, None, ctypes.byref(ctx)) == fa.FA_ERR_ARG
+    assert lib.fa_open(keys, 0, 0, 0, 1, None, ctypes.byref(ctx)) == fa.FA_ERR_ARG
+    assert lib.fa_open(keys, 1, 0, 0, 0, None, ctypes.byref(ctx)) == fa.FA_ERR_ARG
+    assert lib.fa_open(keys, 1, 7, 0, 1, None, ctypes.byref(ctx)) == fa.FA_ERR_DTYPE
+    assert lib.fa_open(keys, 1, 0, 2, 1, None, ctypes.byref(ctx)) == fa.FA_ERR_DTYPE
+    zero = (fa.fa_key * 1)(fa.fa_key(b"w", 0))
+    assert lib.fa_open(zero, 1, 0, 0, 1, None, ctypes.byref(ctx)) == fa.FA_ERR_ARG
+    assert ctx.value is None
+    assert lib.fa_close(None) == fa.FA_OK
+    assert lib.fa_sync(None) == fa.FA_ERR_ARG
+    assert lib.fa_reset(None) == fa.FA_ERR_ARG
+    assert lib.fa_accumulate(None, 0, 1.0, 0, 0, None, 0, None) == fa.FA_ERR_ARG
+    assert lib.fa_finalize(None, None, None) == fa.FA_ERR_ARG
+    assert fa.fa_last_error(None) == ""
+
+
+def test_open_without_a_device_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    ctx = ctypes.c_void_p()
+    keys = (fa.fa_key * 1)(fa.fa_key(b"w", 4))
+    st = lib.fa_open(keys, 1, 0, 0, 1, None, ctypes.byref(ctx))
+    assert st in (fa.FA_ERR_CUDA, fa.FA_ERR_NOMEM) and ctx.value is None
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(fa, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        fa.lib()

@@ -1,0 +1,210 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small workloads (tiny CNN, 3-D U-Net, LoRA adapters with partial participation)
+are compared element by element on every key; the two full-size streamed
+workloads (2.2B VLM, 7B decoder) run exactly as bench.py streams them and are
+compared on sampled elements the oracle recomputes one by one.
+Tolerances: tests/compare.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import server_side_fedavg_gb300 as fa
+import synth
+from synth import workloads as W
+from tests.compare import Bf16Tally, check_bf16, check_f32
+from tests.gpu_helpers import (ragged_splits, sentinel, sentinel_np, to_dev, to_np, to_pinned,
+                               torch_dtype)
+
+pytestmark = pytest.mark.gpu
+
+
+def _layout(w):
+    return [(name, n) for (name, _), n in zip(w.keys, w.numels)]
+
+
+def _host_inputs(w):
+    return {(k, p): synth.client_key(w, k, p) for k in range(w.K) for p in w.reports[k]}
+
+
+def run_per_key(w, host, mode="device", pieces=1, seed=0, **opts):
+    """Feed every (client, key) as `pieces` ragged chunks; returns outputs (numpy)."""
+    rng = np.random.default_rng(seed)
+    ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, **opts)
+    keep = []
+    try:
+        s = torch.cuda.current_stream()
+        for k in range(w.K):
+            for p in w.reports[k]:
+                x = host[(k, p)]
+                if mode == "device":
+                    t = to_dev(x)
+                elif mode == "pinned":
+                    t = to_pinned(x)
+                else:
+                    t = x
+                keep.append(t)
+                es = x.itemsize
+                base = fa._ptr(t)
+                for a, b in ragged_splits(w.numels[p], pieces, rng):
+                    fa.fa_accumulate(ctx, k, w.weights[k], p, a, base + a * es, b - a, s)
+        outs = [sentinel(n, w.dtype_out) for n in w.numels]
+        fa.fa_finalize(ctx, outs, s)
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+        totals = [fa.fa_key_total(ctx, p) for p in range(w.n_keys)]
+        return [to_np(o, w.dtype_out) for o in outs], totals
+    finally:
+        fa.fa_close(ctx)
+
+
+def check_against_oracle(w, host, outs, totals):
+    tally = Bf16Tally()
+    for p in range(w.n_keys):
+        rep = [p in set(w.reports[k]) for k in range(w.K)]
+        xs = [host.get((k, p)) for k in range(w.K)]
+        want, N, cnt = oracle.fedavg_key(w.weights, rep, xs, w.dtype_in, w.dtype_out)
+        assert totals[p] == (N, cnt), f"key {p}: totals {totals[p]} != oracle {(N, cnt)}"
+        if want is None:
+            assert np.array_equal(outs[p], sentinel_np(w.numels[p], w.dtype_out)), f"key {p} written"
+            continue
+        if w.dtype_out == "f32":
+            maxw = max(float(np.abs(synth.to_f64(xs[k], w.dtype_in)).max()) for k in range(w.K) if rep[k])
+            check_f32(outs[p], want, maxw, cnt, f"key {p}")
+        else:
+            tally.add(outs[p], want, f"key {p}")
+    if w.dtype_out == "bf16":
+        frac = tally.check(w.name)
+        print(f"{w.name}: {tally.total} elements, {frac:.6%} bf16 bit-identical")
+
+
+@pytest.fixture(scope="module")
+def small():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            w = W.make(name)
+            cache[name] = (w, _host_inputs(w))
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("name", ["tiny", "unet3d", "lora"])
+def test_small_workloads_full_compare(small, name):
+    w, host = small(name)
+    outs, totals = run_per_key(w, host)
+    check_against_oracle(w, host, outs, totals)
+
+
+def test_lora_has_unreported_modules(small):
+    w, _ = small("lora")
+    sent = set(p for r in w.reports for p in r)
+    # partial participation is exercised: some clients skip modules
+    assert any(len(r) < w.n_keys for r in w.reports)
+    assert len(sent) <= w.n_keys
+
+
+@pytest.mark.parametrize("mode", ["device", "pinned", "pageable"])
+@pytest.mark.parametrize("pieces", [1, 5])
+def test_ingest_modes_bit_identical(small, mode, pieces):
+    """Host (pinned / pageable) and device ingest, whole or ragged chunks: same bits."""
+    w, host = small("lora")
+    ref, _ = run_per_key(w, host, "device", 1)
+    got, _ = run_per_key(w, host, mode, pieces, seed=3, ring_slots=2, slot_bytes=1 << 20)
+    for p in range(w.n_keys):
+        assert np.array_equal(got[p], ref[p]), f"key {p}"
+
+
+def test_ring_geometry_bit_identical(small):
+    w, host = small("unet3d")
+    a, _ = run_per_key(w, host, "pageable", 3, seed=5, ring_slots=2, slot_bytes=4096)
+    b, _ = run_per_key(w, host, "pinned", 1, ring_slots=6, slot_bytes=1 << 24)
+    for p in range(w.n_keys):
+        assert np.array_equal(a[p], b[p]), f"key {p}"
+
+
+@pytest.mark.parametrize("J", [2, 3, 8, 11, 16])
+def test_batch_bit_identical_to_sequential(J):
+    """fa_accumulate_batch == the same clients through fa_accumulate, bit for bit."""
+    rng = np.random.default_rng(J)
+    numels = [5, 4096 * 3 + 17, 777, 65536]
+    layout = [(f"k{i}", n) for i, n in enumerate(numels)]
+    weights = [float(v) for v in rng.integers(1, 5000, J)]
+    xs = [[to_dev((rng.standard_normal(n) * 0.02).astype(np.float32).view(np.uint32).__rshift__(16).astype(np.uint16))
+           for n in numels] for _ in range(J)]
+    outs = []
+    for batched in (False, True):
+        ctx = fa.fa_open(layout, "bf16", "f32", J)
+        try:
+            for p, n in enumerate(numels):
+                if batched:
+                    fa.fa_accumulate_batch(ctx, list(range(J)), weights, p, 0, [xs[j][p] for j in range(J)], n)
+                else:
+                    for j in range(J):
+                        fa.fa_accumulate(ctx, j, weights[j], p, 0, xs[j][p], n)
+            o = [torch.empty(n, dtype=torch.float32, device="cuda") for n in numels]
+            fa.fa_finalize(ctx, o)
+            torch.cuda.synchronize()
+            outs.append([t.cpu().numpy() for t in o])
+        finally:
+            fa.fa_close(ctx)
+    for p in range(len(numels)):
+        assert np.array_equal(outs[0][p].view(np.uint32), outs[1][p].view(np.uint32)), f"key {p}"
+
+
+def test_flat_chunks_spanning_keys_match_per_key(small):
+    """Ragged FLAT chunks across key boundaries == per-key chunks, bit for bit."""
+    w, host = small("tiny")
+    ref, _ = run_per_key(w, host)
+    rng = np.random.default_rng(9)
+    ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
+    try:
+        for k in range(w.K):
+            flat = to_dev(synth.client_flat(w, k, 0, w.P))
+            for a, b in ragged_splits(w.P, 13, rng):
+                fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, a, flat.data_ptr() + a * 4, b - a)
+        out = sentinel(w.P, w.dtype_out)
+        fa.fa_finalize(ctx, [out])
+        torch.cuda.synchronize()
+        got = to_np(out, w.dtype_out)
+    finally:
+        fa.fa_close(ctx)
+    offs = w.flat_offsets()
+    for p in range(w.n_keys):
+        assert np.array_equal(got[offs[p]:offs[p] + w.numels[p]], ref[p]), f"key {p}"
+
+
+# ------------------------------------------------------------------ full-size streamed
+def _sample_indices(w, n_random=200_000, seed=1):
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(0, w.P, n_random, dtype=np.int64)]
+    for off, n in zip(w.flat_offsets(), w.numels):
+        idx.append(np.arange(off, off + min(n, 64)))
+        idx.append(np.arange(off + n - min(n, 64), off + n))
+    ce = w.chunk_elems
+    for c in range(ce, w.P, ce):
+        idx.append(np.arange(max(0, c - 64), min(w.P, c + 64)))
+    idx.append(np.arange(w.P - 256, w.P))
+    return np.unique(np.concatenate(idx)).astype(np.uint64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["vlm2b", "llama7b"])
+def test_full_size_streamed_sampled(name):
+    import bench
+    w = W.make(name)
+    free, _ = torch.cuda.mem_get_info()
+    need = w.P * 2 * 2 + w.P * 4 + (8 << 30)
+    assert free > need, f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}"
+    idx = _sample_indices(w)
+    out = bench.run_streamed_round(w, resident=False)
+    got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+    assert bool(torch.isfinite(out.view(torch.bfloat16)).all())
+    del out
+    torch.cuda.empty_cache()
+    xs = [synth.client_gather(w, k, idx) for k in range(w.K)]
+    want, N, cnt = oracle.fedavg_key(w.weights, [True] * w.K, xs, w.dtype_in, w.dtype_out)
+    frac = check_bf16(got, want, name)
+    print(f"{name}: {idx.size} sampled elements, {frac:.6%} bit-identical")

@@ -1,0 +1,200 @@
+"""Host bookkeeping of a round (CPU, via the host-only ledger shim): argument
+validation, flat chunks split at key boundaries, which elements take their
+first contribution, per-client element counts, per-key weight totals N_p and
+reporter counts (bit-exact against the oracle's totals), round state."""
+import random
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.ledger import Ledger
+
+OK, ARG, RANGE, WEIGHT, INCOMPLETE, STATE = 0, -1, -2, -4, -5, -6
+
+
+def test_padding_is_32_elements():
+    lg = Ledger([1, 33, 64, 7], 2)
+    assert [lg.acc_off(p) for p in range(4)] == [0, 32, 96, 160]
+    assert lg.padded() == 192
+
+
+def test_bad_layouts():
+    assert Ledger([], 1).status == ARG
+    assert Ledger([3, 0], 1).status == ARG
+    assert Ledger([3], 0).status == ARG
+
+
+def test_weight_validation():
+    lg = Ledger([10], 3)
+    for w in (-1.0, float("nan"), float("inf"), 2.0 ** 24 + 1):
+        assert lg.accumulate([0], [w], 0, 0, 5)[0] == WEIGHT
+    assert lg.accumulate([0], [2.0 ** 24], 0, 0, 5)[0] == OK
+    assert lg.accumulate([0], [7.0], 0, 5, 5)[0] == WEIGHT        # unlike its first chunk
+    assert lg.accumulate([0], [2.0 ** 24], 0, 5, 5)[0] == OK
+    assert lg.accumulate([1], [0.0], 0, 0, 10)[0] == OK           # zero weight is allowed
+
+
+def test_empty_chunk_registers_nothing():
+    lg = Ledger([10], 2)
+    assert lg.accumulate([0], [5.0], 0, 3, 0) == (OK, [])
+    assert lg.accumulate([0], [6.0], 0, 0, 10)[0] == OK           # weight not fixed by the empty call
+    assert lg.key_total(0) == (OK, 6.0, 1)
+
+
+def test_ids_keys_ranges():
+    lg = Ledger([10, 20], 2)
+    assert lg.accumulate([2], [1.0], 0, 0, 1)[0] == ARG
+    assert lg.accumulate([0, 0], [1.0, 1.0], 0, 0, 1)[0] == ARG
+    assert lg.accumulate([0], [1.0], 2, 0, 1)[0] == ARG
+    assert lg.accumulate([0], [1.0], -2, 0, 1)[0] == ARG
+    assert lg.accumulate([0], [1.0], 0, 0, 11)[0] == RANGE
+    assert lg.accumulate([0], [1.0], 0, 11, 0)[0] == RANGE
+    assert lg.accumulate([0], [1.0], 0, 2 ** 64 - 1, 2)[0] == RANGE   # no wrap-around
+    assert lg.accumulate([0], [1.0], -1, 25, 6)[0] == RANGE
+    assert lg.accumulate([0], [1.0], -1, 25, 5)[0] == OK
+
+
+def test_flat_chunk_splits_at_keys():
+    lg = Ledger([10, 20, 5], 1)
+    st, pieces = lg.accumulate([0], [1.0], -1, 8, 24)
+    assert st == OK
+    # (key, chunk_off, acc_idx, len, first)
+    assert pieces == [(0, 0, 8, 2, 1), (1, 2, 32, 20, 1), (2, 22, 64, 2, 1)]
+
+
+def test_first_contribution_tracking():
+    lg = Ledger([5, 20], 2)
+    assert lg.accumulate([0], [1.0], 1, 0, 10)[1] == [(1, 0, 32, 10, 1)]
+    assert lg.accumulate([1], [1.0], 1, 5, 10)[1] == [(1, 0, 37, 5, 0), (1, 5, 42, 5, 1)]
+    assert lg.accumulate([0], [1.0], 1, 10, 10)[1] == [(1, 0, 42, 5, 0), (1, 5, 47, 5, 1)]
+    assert lg.accumulate([1], [1.0], 1, 0, 5)[1] == [(1, 0, 32, 5, 0)]
+    assert lg.accumulate([1], [1.0], 1, 15, 5)[1] == [(1, 0, 47, 5, 0)]
+
+
+def test_over_coverage_and_incomplete():
+    lg = Ledger([10], 2)
+    assert lg.accumulate([0], [1.0], 0, 0, 6)[0] == OK
+    assert lg.accumulate([0], [1.0], 0, 0, 5)[0] == RANGE         # 6 + 5 > 10
+    st, items = lg.finalize()
+    assert st == INCOMPLETE
+    assert lg.accumulate([0], [1.0], 0, 6, 4)[0] == OK
+    st, items = lg.finalize()
+    assert st == OK and items == [(0, 0, 0, 10, 1, 1.0)]
+
+
+def test_finalize_skips_unsent_and_zero_weight_keys_then_closes():
+    lg = Ledger([4, 4, 4], 3)
+    lg.accumulate([0], [0.0], 1, 0, 4)
+    lg.accumulate([1], [0.0], 1, 0, 4)
+    lg.accumulate([2], [3.0], 2, 0, 4)
+    st, items = lg.finalize()
+    assert st == OK
+    assert items == [(2, 64, 8, 4, 1, 3.0)]
+    assert lg.key_total(1) == (OK, 0.0, 2)
+    assert lg.accumulate([2], [3.0], 0, 0, 1)[0] == STATE
+    lg.reset()
+    assert lg.key_total(2) == (OK, 0.0, 0)
+    assert lg.accumulate([2], [9.0], 0, 0, 4)[1] == [(0, 0, 0, 4, 1)]
+
+
+def test_batch_starts_sum_once():
+    lg = Ledger([8, 8], 4)
+    st, pieces = lg.accumulate([3, 1, 2], [1.0, 2.0, 3.0], -1, 4, 8)
+    assert st == OK and pieces == [(0, 0, 4, 4, 1), (1, 4, 32, 4, 1)]
+    assert lg.key_total(0) == (OK, 6.0, 3)
+
+
+def test_totals_bit_exact_with_oracle():
+    """Random partial participation: N_p and |S_p| equal the oracle's, bit for bit."""
+    rng = np.random.default_rng(5)
+    numels = [int(v) for v in rng.integers(1, 50, 30)]
+    K = 9
+    weights = [float(v) for v in rng.integers(0, 5000, K)] 
+    weights[3] = 0.1            # non-integer weights sum in client order too
+    weights[5] = 1e-3
+    lg = Ledger(numels, K)
+    reports = [[p for p in range(len(numels)) if rng.random() < 0.6] for _ in range(K)]
+    order = [(k, p) for k in range(K) for p in reports[k]]
+    random.Random(1).shuffle(order)
+    for k, p in order:
+        assert lg.accumulate([k], [weights[k]], p, 0, numels[p])[0] == OK
+    st, items = lg.finalize()
+    assert st == OK
+    by_key = {it[0]: it for it in items}
+    for p, n in enumerate(numels):
+        rep = [p in reports[k] for k in range(K)]
+        xs = [np.zeros(n, np.float32)] * K
+        _, N, cnt = oracle.fedavg_key(weights, rep, xs, "f32", "f32")
+        assert lg.key_total(p) == (OK, N, cnt)
+        if cnt and N > 0:
+            assert by_key[p][4] == cnt and by_key[p][5] == N
+        else:
+            assert p not in by_key
+
+
+def test_random_operations_against_model():
+    """Random chunked traffic against a plain per-element model of the bookkeeping."""
+    rng = random.Random(11)
+    for trial in range(30):
+        numels = [rng.randint(1, 40) for _ in range(rng.randint(1, 6))]
+        K = rng.randint(1, 5)
+        lg = Ledger(numels, K)
+        offs = np.cumsum([0] + numels)
+        started = [np.zeros(n, bool) for n in numels]
+        recv = np.zeros((K, len(numels)), np.int64)
+        weight = {}
+        for _ in range(60):
+            J = rng.randint(1, K)
+            clients = rng.sample(range(K), J)
+            ws = [weight.get(c, float(rng.randint(0, 9))) for c in clients]
+            if rng.random() < 0.5:
+                key = -1
+                off = rng.randint(0, int(offs[-1]))
+                ln = rng.randint(0, int(offs[-1]) - off)
+            else:
+                key = rng.randrange(len(numels))
+                off = rng.randint(0, numels[key])
+                ln = rng.randint(0, numels[key] - off)
+            # expected status
+            spans = []
+            if key == -1:
+                pos = off
+                while pos < off + ln:
+                    p = int(np.searchsorted(offs, pos, side="right") - 1)
+                    e = min(off + ln, int(offs[p + 1]))
+                    spans.append((p, pos - int(offs[p]), e - pos, pos - off))
+                    pos = e
+            elif ln:
+                spans.append((key, off, ln, 0))
+            over = any(recv[c, p] + n > numels[p] for c in clients for (p, _, n, _) in spans)
+            st, pieces = lg.accumulate(clients, ws, key, off, ln)
+            if over:
+                assert st == RANGE
+                continue
+            assert st == OK
+            if ln == 0:
+                assert pieces == []
+                continue
+            for c, w in zip(clients, ws):
+                weight[c] = w
+                for (p, _, n, _) in spans:
+                    recv[c, p] += n
+            # element-wise first flags
+            got = {}
+            for (p, coff, acc, n, first) in pieces:
+                for i in range(n):
+                    got[(p, acc - lg.acc_off(p) + i)] = (first, coff + i)
+            for (p, koff, n, coff) in spans:
+                for i in range(n):
+                    f, ci = got.pop((p, koff + i))
+                    assert ci == coff + i
+                    assert f == (0 if started[p][koff + i] else 1)
+                    started[p][koff + i] = True
+            assert not got
+        for p in range(len(numels)):
+            rep = [k for k in range(K) if recv[k, p] > 0]
+            assert lg.key_total(p) == (OK, sum(weight[k] for k in rep), len(rep))
+        st, items = lg.finalize()
+        complete = all(recv[k, p] in (0, numels[p]) for k in range(K) for p in range(len(numels)))
+        assert st == (OK if complete else INCOMPLETE)
