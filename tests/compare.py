@@ -51,6 +51,27 @@ def check_bf16(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "") -> f
     return t.check(what)
 
 
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_f32_to_bf16(got_bits, want_bits, max_abs_in: float, K: int, what: str = "") -> int:
+    """fp32 inputs, bf16 output: the fp32 running-sum bound plus one bf16 ulp of the
+    result.  (With fp32 inputs the products n_k*x round inside the sum, so near-total
+    cancellation can move a small result by several bf16 ulps; the bf16 rule above
+    is for bf16 inputs, whose products are exact.)  Returns the number of elements
+    that are not bit-identical."""
+    g = bf16_values(got_bits.view(np.uint16))
+    w = bf16_values(want_bits)
+    mag = np.maximum(np.abs(w), 2.0 ** -126)
+    ulp = np.exp2(np.floor(np.log2(mag)) - 7)
+    tol = 1e-6 * max_abs_in * K + ulp
+    d = np.abs(g - w)
+    bad = d > tol
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond fp32 bound + 1 bf16 ulp"
+    return int(np.count_nonzero(g != w))
+
+
 def check_f32(got: np.ndarray, want: np.ndarray, max_abs_in: float, K: int, what: str = "") -> float:
     tol = 1e-6 * max_abs_in * K
     d = np.abs(got.astype(np.float64) - want.astype(np.float64))

@@ -43,3 +43,15 @@ def test_tally_judges_the_total():
     t.add(big.copy(), big)
     assert t.frac() > 0.9999
     t.check()
+
+
+def test_f32_to_bf16_bound():
+    from tests.compare import check_f32_to_bf16
+    a = np.array([0x3F80, 0x0001, 0xBC00], np.uint16)
+    b = a.copy()
+    b[0] += 1                         # one ulp at 1.0: inside
+    assert check_f32_to_bf16(b, a, 0.05, 4) == 1
+    c = a.copy()
+    c[0] += 3                         # three ulps at 1.0 (0.023) > 2e-7 + 0.0078
+    with pytest.raises(AssertionError):
+        check_f32_to_bf16(c, a, 0.05, 4)
