@@ -186,6 +186,35 @@ fa_status fa_sync(fa_ctx* ctx);
 /* Counters since fa_open (host-side, exact). */
 fa_status fa_get_stats(const fa_ctx* ctx, fa_stats* out);
 
+/* Largest tensor fa_aggregate_noalloc takes (elements): 2^22, i.e. a 16 MiB fp32 sum. */
+#define FA_NOALLOC_MAX_ELEMS 4194304ull
+
+/* Aggregate ONE tensor of n_clients resident updates without allocating anything.
+ * The pages have no counterpart: this is for callers that cannot let a library call
+ * cudaMalloc -- a process whose device memory belongs to another allocator (a
+ * framework's caching pool, a server that reserves its memory at start-up) or that
+ * forbids allocation on its request path.  It computes what fa_open + fa_accumulate
+ * (client 0, 1, ... in order) + fa_finalize + fa_close compute for a one-key layout,
+ * with the same kernels, but keeps the fp32 running sum in a fixed array inside the
+ * library's device image instead of allocated memory: FA_NOALLOC_MAX_ELEMS floats
+ * (16 MiB), held on every GPU that loads the library until the process exits.
+ *   weights[j]       n_j: finite, >= 0, <= 2^24
+ *   client_ptrs[j]   numel values of dtype_in in this device's memory
+ *   out              numel values of dtype_out in this device's memory; left untouched
+ *                    if sum(weights) == 0
+ *   stream           cudaStream_t (as void*) the work is queued on; the call does not wait
+ * The first call on each device looks up the array's device address (set-up); make that
+ * first call before any stream capture.  Every call uses the same array and it keeps the
+ * previous call's contents: each call overwrites what it uses before reading it, and
+ * calls that overlap on the GPU (different streams, or different host threads without
+ * ordering) race on it.  Calls no cudaMalloc, cudaFree or other allocating routine.
+ * Errors: FA_ERR_RANGE if numel > FA_NOALLOC_MAX_ELEMS (nothing is launched),
+ * FA_ERR_ARG, FA_ERR_WEIGHT, FA_ERR_DTYPE, FA_ERR_CUDA.  numel == 0 or n_clients == 0
+ * is a no-op. */
+fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weights,
+                               const void* const* client_ptrs, uint64_t numel, fa_dtype dtype_in,
+                               fa_dtype dtype_out, void* out, void* stream);
+
 /* Static text for a status code. */
 const char* fa_strerror(fa_status status);
 

@@ -32,6 +32,7 @@ FA_F32 = 0
 FA_BF16 = 1
 FA_KEY_FLAT = -1
 FA_FLAT_OUT = 1
+FA_NOALLOC_MAX_ELEMS = 1 << 22
 
 DTYPES = {"f32": FA_F32, "bf16": FA_BF16, FA_F32: FA_F32, FA_BF16: FA_BF16}
 
@@ -83,6 +84,9 @@ def lib():
         L.fa_key_total.argtypes = [vp, u32, ctypes.POINTER(f64), ctypes.POINTER(u32)]
         L.fa_sync.argtypes = [vp]
         L.fa_get_stats.argtypes = [vp, ctypes.POINTER(fa_stats)]
+        L.fa_aggregate_noalloc.argtypes = [u32, ctypes.POINTER(f64), ctypes.POINTER(vp), u64, i32, i32,
+                                           vp, vp]
+        L.fa_aggregate_noalloc.restype = i32
         L.fa_strerror.argtypes = [i32]
         L.fa_strerror.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = [vp]
@@ -192,3 +196,14 @@ def fa_get_stats(ctx) -> dict:
     st = fa_stats()
     _check(lib().fa_get_stats(ctx, ctypes.byref(st)), ctx)
     return {f: getattr(st, f) for f, _ in fa_stats._fields_}
+
+
+def fa_aggregate_noalloc(weights, chunks, numel, dtype_in, dtype_out, out, stream=None):
+    """One tensor, all clients resident, no allocation: the running sum lives in a
+    fixed 16 MiB array of the library (see include/fedavg.h).  For callers that must
+    not have a library allocate device memory."""
+    J = len(chunks)
+    ws = (ctypes.c_double * max(J, 1))(*[float(w) for w in weights])
+    ps = (ctypes.c_void_p * max(J, 1))(*[_ptr(c) for c in chunks])
+    _check(lib().fa_aggregate_noalloc(J, ws, ps, numel, DTYPES[dtype_in], DTYPES[dtype_out],
+                                      _ptr(out), _stream(stream)))

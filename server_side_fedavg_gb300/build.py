@@ -16,7 +16,7 @@ BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(BUILD, "libfedavg.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["kernels.cu", "fedavg.cpp", "ledger.cpp"]
+SOURCES = ["kernels.cu", "noalloc.cu", "fedavg.cpp", "ledger.cpp"]
 
 
 def _common():
