@@ -107,6 +107,38 @@ def algorithmic_bytes(w):
     return acc_first, acc_later, fin
 
 
+def kernel_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kernels.cu", "kernels.cuh"):
+        with open(os.path.join(ROOT, "server_side_fedavg_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(bytes_per_launch):
+    """DRAM bytes per accumulate launch from the committed ncu summary, scaled from the
+    captured launch to the average launch by algorithmic bytes; None once the kernel
+    source differs from the one the counters were taken on."""
+    path = os.path.join(ROOT, "profiles", "accumulate_decoder1l.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ": " in line:
+                k, v = line[2:].split(": ", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    try:
+        if fields.get("kernel source digest") != kernel_source_digest():
+            return None
+        dram = float(fields["dram bytes per launch"])
+        algo = float(fields["algorithmic bytes of the captured launch"])
+    except (KeyError, ValueError):
+        return None
+    return int(dram / algo * bytes_per_launch)
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -297,8 +329,8 @@ def run_ours(args, world, rank, local, pg):
     nchunk = -(-w.P // (w.chunk_elems or w.P))
 
     def step(evs=None):
+        # evs: (start, after the accumulate launches, after finalize) on the launching stream
         fa.fa_reset(ctx)
-        i = 0
         if evs is not None:
             evs[0].record(s)
         for k in range(w.K):
@@ -307,12 +339,11 @@ def run_ours(args, world, rank, local, pg):
             for c0 in range(0, P, ce):
                 fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base + c0 * si,
                                  min(ce, P - c0), sh)
-                i += 1
-                if evs is not None:
-                    evs[i].record(s)
+        if evs is not None:
+            evs[1].record(s)
         fa.fa_finalize(ctx, [out], sh)
         if evs is not None:
-            evs[i + 1].record(s)
+            evs[2].record(s)
 
     for _ in range(args.warmup):
         step()
@@ -321,7 +352,7 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize()
 
     n_calls = w.K * nchunk
-    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 2)] for _ in range(args.steps)]
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = fa.fa_get_stats(ctx)["kernel_launches"]
     clocks = ClockSampler(local)
@@ -339,14 +370,14 @@ def run_ours(args, world, rank, local, pg):
     ms_total = t0e.elapsed_time(t1e)
     ms_total = max_over_ranks(pg, ms_total)
 
-    # per-launch kernel times (events bracket each accumulate launch on its stream)
+    # kernel times: events bracket each step's run of accumulate launches (one launch
+    # per call here) and its finalize launch, on the stream they are launched on
     acc_first_b, acc_later_b, fin_b = algorithmic_bytes(w)
     acc_ms = 0.0
     fin_ms = 0.0
     for evs in ev_sets:
-        for j in range(n_calls):
-            acc_ms += evs[j].elapsed_time(evs[j + 1])
-        fin_ms += evs[n_calls].elapsed_time(evs[n_calls + 1])
+        acc_ms += evs[0].elapsed_time(evs[1])
+        fin_ms += evs[1].elapsed_time(evs[2])
     acc_launch_ms = acc_ms / (args.steps * n_calls)
     acc_bytes_per_launch = (acc_first_b + acc_later_b) / n_calls
     achieved = acc_bytes_per_launch / (acc_launch_ms * 1e-3) / 1e9
@@ -381,7 +412,8 @@ def run_ours(args, world, rank, local, pg):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": int(acc_bytes_per_launch),
-                     "launch_ms": round(acc_launch_ms, 4), "traffic": None},
+                     "launch_ms": round(acc_launch_ms, 4),
+                     "traffic": profiled_traffic(acc_bytes_per_launch)},
         "gpu_launches": int(launches),
         "clocks": clk,
         "e2e": e2e,

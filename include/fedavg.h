@@ -165,6 +165,19 @@ fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* c
  * Errors: FA_ERR_ARG, FA_ERR_INCOMPLETE, FA_ERR_CUDA, FA_ERR_NOMEM, FA_ERR_TIMEOUT. */
 fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream);
 
+/* Finalize a round of DELTA updates into the global model ([Clara] "Server-side workflow":
+ * after aggregating, the server updates the existing global model as a whole):
+ *     out[p][i] = round_to_dtype_out( base[p][i] + server_lr * sum[p][i] / N_p )
+ * computed as q = sum / (float)N_p (IEEE division), fma((float)server_lr, q, base) (one
+ * rounding), then the RNE cast.  server_lr = 1 is plain FedAvg on deltas; the pages fix no
+ * other value.  base_ptrs / out_ptrs: n_keys pointers each (or one flat pointer with
+ * FA_FLAT_OUT), dtype_out values in this GPU's memory; out may equal base (in place).
+ * Keys with N_p == 0 are not written (out keeps its contents; in place, the model is
+ * unchanged).  Otherwise as fa_finalize (closes the round, non-destructive, may repeat).
+ * Errors: as fa_finalize; FA_ERR_ARG for host memory or a non-finite server_lr. */
+fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* const* out_ptrs,
+                            double server_lr, void* stream);
+
 /* Start a new round ([Clara] "Server-side workflow": the loop repeats per round):
  * forget weights, per-key totals, reporter masks and element counts.  The running sum
  * is not cleared (the first contribution of the next round overwrites it).  Waits

@@ -57,6 +57,8 @@ def lib():
         L.fo_fedavg_key.restype = i32
         L.fo_fedavg_key_f64.argtypes = [u32, vp, vp, vp, i32, u64, vp]
         L.fo_fedavg_key_f64.restype = i32
+        L.fo_fedavg_apply_key.argtypes = [u32, vp, vp, vp, i32, u64, vp, f64, i32, vp, vp, vp]
+        L.fo_fedavg_apply_key.restype = i32
         L.fo_bf16_rne_n.argtypes = [vp, u64, vp]
         L.fo_bf16_rne_n.restype = None
         L.fo_f32_rn_n.argtypes = [vp, u64, vp]
@@ -130,3 +132,20 @@ def fedavg_key_f64(weights, reported, xs, dtype_in):
     wrote = lib().fo_fedavg_key_f64(K, n.ctypes.data, rep.ctypes.data, ptrs, _CODES[dtype_in],
                                     numel, y.ctypes.data)
     return y if wrote else None
+
+
+def fedavg_apply_key(weights, reported, xs, dtype_in, base, server_lr, dtype_out, out=None):
+    """Delta round for one key: round(base + server_lr * weighted mean of xs).
+    Returns (out_or_None, N_p, cnt_p); `base` holds dtype_out values."""
+    K, n, rep, ptrs, arrs, numel = _prep(weights, reported, xs, dtype_in)
+    b = np.ascontiguousarray(base)
+    want = np.float32 if dtype_out == F32 else np.uint16
+    if b.dtype != want or b.size != numel:
+        raise TypeError("base must hold numel values of dtype_out")
+    res = out if out is not None else np.empty(numel, _np_out(dtype_out))
+    N = ctypes.c_double()
+    cnt = ctypes.c_uint32()
+    wrote = lib().fo_fedavg_apply_key(K, n.ctypes.data, rep.ctypes.data, ptrs, _CODES[dtype_in], numel,
+                                      b.ctypes.data, float(server_lr), _CODES[dtype_out], res.ctypes.data,
+                                      ctypes.byref(N), ctypes.byref(cnt))
+    return (res if wrote else None), N.value, cnt.value

@@ -146,3 +146,39 @@ void fo_bf16_rne_n(const double* y, uint64_t m, uint16_t* out) {
 void fo_f32_rn_n(const double* y, uint64_t m, float* out) {
     for (uint64_t i = 0; i < m; ++i) out[i] = fo_f32_rn(y[i]);
 }
+
+/* Delta rounds: clients send updates relative to the current global model and
+ * the server applies their weighted mean to it -- "Federated learning
+ * implemented by NVIDIA Clara", "Server-side workflow": after aggregation the
+ * server updates the existing global model as a whole and serves it in the
+ * next round.  With server_lr = 1 this is plain FedAvg on deltas; other values
+ * scale the mean update (a server step size; the pages fix none).
+ *   base    numel values of dtype_out: the current global model for this key
+ *   out[i] = round_out( base[i] + server_lr * (sum_k n_k * x_k[i]) / N_p )   (fp64)
+ * Keys with no weight are left untouched, as in fo_fedavg_key. */
+int fo_fedavg_apply_key(uint32_t K, const double* n, const uint8_t* reported,
+                        const void* const* x, int dtype_in, uint64_t numel, const void* base,
+                        double server_lr, int dtype_out, void* out, double* N_out,
+                        uint32_t* cnt_out) {
+    double N = 0.0;
+    uint32_t cnt = 0;
+    for (uint32_t k = 0; k < K; ++k) {
+        if (reported[k]) {
+            N += n[k];
+            cnt += 1;
+        }
+    }
+    if (N_out) *N_out = N;
+    if (cnt_out) *cnt_out = cnt;
+    if (cnt == 0 || N == 0.0) return 0;
+    for (uint64_t i = 0; i < numel; ++i) {
+        double s = 0.0;
+        for (uint32_t k = 0; k < K; ++k) {
+            if (reported[k]) s += n[k] * fo_load(x[k], dtype_in, i);
+        }
+        double y = fo_load(base, dtype_out, i) + server_lr * (s / N);
+        if (dtype_out == FO_F32) ((float*)out)[i] = fo_f32_rn(y);
+        else ((uint16_t*)out)[i] = fo_bf16_rne(y);
+    }
+    return 1;
+}

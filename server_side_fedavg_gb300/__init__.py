@@ -79,6 +79,7 @@ def lib():
         L.fa_accumulate_batch.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64), i64,
                                           u64, ctypes.POINTER(vp), u64, vp]
         L.fa_finalize.argtypes = [vp, ctypes.POINTER(vp), vp]
+        L.fa_finalize_apply.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), f64, vp]
         L.fa_reset.argtypes = [vp]
         L.fa_close.argtypes = [vp]
         L.fa_key_total.argtypes = [vp, u32, ctypes.POINTER(f64), ctypes.POINTER(u32)]
@@ -91,7 +92,8 @@ def lib():
         L.fa_strerror.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = [vp]
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_finalize", "fa_reset",
+        for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_finalize",
+                     "fa_finalize_apply", "fa_reset",
                      "fa_close", "fa_key_total", "fa_sync", "fa_get_stats"):
             getattr(L, name).restype = i32
         _lib = L
@@ -171,6 +173,13 @@ def fa_finalize(ctx, outs, stream=None):
     or a one-element list with the flat output when opened with FA_FLAT_OUT."""
     ps = (ctypes.c_void_p * max(len(outs), 1))(*[_ptr(o) for o in outs])
     _check(lib().fa_finalize(ctx, ps, _stream(stream)), ctx)
+
+
+def fa_finalize_apply(ctx, bases, outs, server_lr=1.0, stream=None):
+    """Delta rounds: outs = round(bases + server_lr * weighted mean); outs may be bases."""
+    bs = (ctypes.c_void_p * max(len(bases), 1))(*[_ptr(b) for b in bases])
+    ps = (ctypes.c_void_p * max(len(outs), 1))(*[_ptr(o) for o in outs])
+    _check(lib().fa_finalize_apply(ctx, bs, ps, float(server_lr), _stream(stream)), ctx)
 
 
 def fa_reset(ctx):

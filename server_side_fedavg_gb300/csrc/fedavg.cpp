@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <chrono>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -56,6 +57,7 @@ struct fa_ctx {
 
     cudaEvent_t chain = nullptr;  // recorded after the last queued operation
     bool chain_valid = false;
+    unsigned long long chain_stream_id = 0;   // stream the chain event was last recorded on
     cudaEvent_t user_ev = nullptr;
 
     cudaStream_t copy_stream = nullptr;
@@ -155,14 +157,21 @@ Mem classify(const void* p, int device, bool* other_device) {
     }
 }
 
-// Make `s` wait for everything queued on the context so far.
+// Make `s` wait for everything queued on the context so far.  Work on the same
+// stream as the last record is already ordered after it (stream ids are unique
+// for the life of the context, unlike handles), so the wait is only issued when
+// the stream changes -- a cross-stream wait costs a full launch latency.
 fa_status chain_in(fa_ctx* c, cudaStream_t s) {
-    if (c->chain_valid) FA_CUDA(c, cudaStreamWaitEvent(s, c->chain, 0));
+    if (!c->chain_valid) return FA_OK;
+    unsigned long long id = 0;
+    FA_CUDA(c, cudaStreamGetId(s, &id));
+    if (id != c->chain_stream_id) FA_CUDA(c, cudaStreamWaitEvent(s, c->chain, 0));
     return FA_OK;
 }
 
 fa_status chain_out(fa_ctx* c, cudaStream_t s) {
     FA_CUDA(c, cudaEventRecord(c->chain, s));
+    FA_CUDA(c, cudaStreamGetId(s, &c->chain_stream_id));
     c->chain_valid = true;
     return FA_OK;
 }
@@ -212,7 +221,6 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
             FA_CUDA(c, fa::launch_accumulate(a, c->din, c->shape, s));
             c->stats.kernel_launches++;
             a.nseg = 0;
-            a.ntiles = 0;
             a.vec_ok = 0;
             return FA_OK;
         };
@@ -229,16 +237,12 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
             g.acc_idx = p.acc_idx + (b - p.chunk_off);
             g.len = e - b;
             g.first = (p.first && done == 0) ? 1u : 0u;
-            g.tile0 = a.ntiles;
             bool ok = (reinterpret_cast<uintptr_t>(c->acc + g.acc_idx) & 15u) == 0;
             for (uint32_t j = 0; j < jb && ok; ++j) {
                 uintptr_t xa = reinterpret_cast<uintptr_t>(a.x[j]) + g.x_off * c->s_in;
                 ok = (xa & 15u) == 0;
             }
             if (ok) a.vec_ok |= 1ull << a.nseg;
-            uint64_t tiles = (g.len + fa::kTile - 1) / fa::kTile;
-            if (tiles > 0xFFFFFFFFull - a.ntiles) return fail(c, FA_ERR_RANGE, "chunk too large for one launch");
-            a.ntiles += static_cast<uint32_t>(tiles);
             a.nseg++;
         }
         fa_status st = flush();
@@ -367,6 +371,12 @@ fa_status sync_impl(fa_ctx* c) {
         fa_status r = wait_event(c, c->ev_copied[k], "fa_sync (copy)");
         if (r != FA_OK) return r;
     }
+    unsigned int code = 0;
+    FA_CUDA(c, fa::take_device_error(&code));
+    if (code != 0) {
+        c->broken = true;
+        return fail(c, FA_ERR_INTERNAL, "a device-side wait gave up (bounded mbarrier wait): results of this round are invalid");
+    }
     return FA_OK;
 }
 
@@ -468,12 +478,14 @@ fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* c
                            len_elems, static_cast<cudaStream_t>(stream), true);
 }
 
-fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
-    if (!ctx) return FA_ERR_ARG;
-    std::lock_guard<std::mutex> lk(ctx->mu);
-    DeviceGuard dg(ctx->device);
-    fa_ctx* c = ctx;
-    c->err.clear();
+}  // extern "C"
+
+namespace {
+
+// Shared driver of fa_finalize and fa_finalize_apply (base_ptrs != NULL).
+fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* out_ptrs,
+                        double server_lr, void* stream) {
+    const bool apply = base_ptrs != nullptr;
     if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
     if (out_ptrs == nullptr) return fail(c, FA_ERR_ARG, "out_ptrs is NULL");
     const bool flat = (c->flags & FA_FLAT_OUT) != 0;
@@ -491,6 +503,14 @@ fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
         bool other = false;
         kind[i] = classify(dst, c->device, &other);
         if (other) return fail(c, FA_ERR_ARG, "output is in another GPU's memory");
+        if (apply) {
+            const void* b = flat ? base_ptrs[0] : base_ptrs[it.key];
+            bool bo = false;
+            if (b == nullptr || classify(b, c->device, &bo) != Mem::kDevice || bo)
+                return fail(c, FA_ERR_ARG, "fa_finalize_apply: base values must be in this GPU's memory");
+            if (kind[i] != Mem::kDevice)
+                return fail(c, FA_ERR_ARG, "fa_finalize_apply: outputs must be in this GPU's memory");
+        }
         any_host = any_host || kind[i] != Mem::kDevice;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -512,6 +532,11 @@ fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
         g.acc_idx = it.acc_idx;
         g.len = it.numel;
         g.out = dst;
+        g.base = nullptr;
+        if (apply) {
+            const char* b = static_cast<const char*>(flat ? base_ptrs[0] : base_ptrs[it.key]);
+            g.base = flat ? b + it.flat_off * c->s_out : b;
+        }
         g.divisor = static_cast<float>(it.total);
         g.tile0 = ntiles;
         uint64_t t = (it.numel + fa::kTile - 1) / fa::kTile;
@@ -528,7 +553,8 @@ fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
                                    cudaMemcpyHostToDevice, s));
         FA_CUDA(c, cudaEventRecord(c->fin_ev, s));
         c->fin_pending = true;
-        FA_CUDA(c, fa::launch_finalize(c->fin_dev, nseg, ntiles, c->dout, c->acc, c->shape, s));
+        FA_CUDA(c, fa::launch_finalize(c->fin_dev, nseg, ntiles, c->dout, c->acc, apply,
+                                       static_cast<float>(server_lr), c->shape, s));
         c->stats.kernel_launches++;
         // host outputs: copy the staged keys back, merging neighbours in the flat layout
         for (size_t i = 0; i < c->items.size();) {
@@ -560,6 +586,29 @@ fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
         }
     }
     return chain_out(c, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    ctx->err.clear();
+    return finalize_impl(ctx, nullptr, out_ptrs, 1.0, stream);
+}
+
+fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* const* out_ptrs,
+                            double server_lr, void* stream) {
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    ctx->err.clear();
+    if (base_ptrs == nullptr) return fail(ctx, FA_ERR_ARG, "base_ptrs is NULL");
+    if (!std::isfinite(server_lr)) return fail(ctx, FA_ERR_ARG, "server_lr must be finite");
+    return finalize_impl(ctx, base_ptrs, out_ptrs, server_lr, stream);
 }
 
 fa_status fa_reset(fa_ctx* ctx) {

@@ -20,7 +20,8 @@ namespace fa {
 
 constexpr int kBlock = 256;           // threads per CTA
 constexpr int kVec = 8;               // elements per vector (16 B of bf16, 2 x 16 B of fp32 sum)
-constexpr int kTile = 4096;           // elements per CTA work unit
+constexpr int kTile = 4096;           // elements per CTA work unit (direct-load kernels)
+constexpr int kBulkTile = 8192;       // elements per pipeline stage (bulk-copy kernel)
 constexpr int kMaxSegs = 48;          // segments per accumulate launch
 constexpr int kMaxBatch = 16;         // resident clients per accumulate launch
 
@@ -29,7 +30,7 @@ struct AccSeg {
     uint64_t acc_idx;   // element index into the running sum
     uint64_t len;       // elements (>= 1)
     uint32_t first;     // 1: the first client of the launch starts the sum here
-    uint32_t tile0;     // first tile of this segment in the launch's tile numbering
+    uint32_t tile0;     // first tile of this segment (set by launch_accumulate)
 };
 
 struct AccArgs {
@@ -38,7 +39,7 @@ struct AccArgs {
     float* acc;
     uint32_t J;
     uint32_t nseg;
-    uint32_t ntiles;
+    uint32_t ntiles;            // set by launch_accumulate
     uint64_t vec_ok;            // bit s: segment s is 16-byte aligned for x and sum
     AccSeg seg[kMaxSegs];
 };
@@ -47,25 +48,40 @@ struct FinSeg {
     uint64_t acc_idx;   // start in the running sum
     uint64_t len;       // elements
     void* out;          // destination of element 0 (device), dtype_out
+    const void* base;   // delta rounds: current global model (dtype_out), else unused
     float divisor;      // (float) N_p
     uint32_t tile0;     // first tile of this segment
 };
 
 struct LaunchShape {
     int sms = 0;
+    int bulk_ctas_per_sm[2] = {};     // [dtype_in], streaming (J = 1) bulk-copy kernel
     int acc_ctas_per_sm[2][5] = {};   // [dtype_in][log2 J]
-    int fin_ctas_per_sm[2] = {};      // [dtype_out]
+    int fin_ctas_per_sm[2][2] = {};   // [apply][dtype_out]
 };
 
-// Fills the occupancy table for the current device.
+// Device-side error bits (file-scope word shared by every launch on a device).
+constexpr unsigned int kErrWaitTimeout = 1u;   // a bounded mbarrier wait gave up
+
+// Reads and clears the device error word of the current device.
+cudaError_t take_device_error(unsigned int* code);
+
+// Fills the occupancy table for the current device (and sets the kernels'
+// shared-memory limits).
 cudaError_t query_launch_shape(LaunchShape* s);
 
-// dtype codes: 0 = fp32, 1 = bf16.  J must be 1, 2, 4, 8 or 16.
+// dtype codes: 0 = fp32, 1 = bf16.  J must be 1, 2, 4, 8 or 16.  The caller fills
+// x, w, acc, J, nseg, vec_ok and each segment's x_off / acc_idx / len / first; the
+// launcher numbers the tiles for the kernel it picks (J = 1: the bulk-copy kernel).
+// Returns cudaErrorInvalidValue if the tiles do not fit 32-bit numbering.
 cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,
                               cudaStream_t stream);
 
 // segs: device array of nseg FinSeg sorted by tile0.
+//   apply == false: out = RNE(sum / N)
+//   apply == true:  out = RNE(fma(server_lr, sum / N, base))   (delta rounds)
 cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_out,
-                            const float* acc, const LaunchShape& s, cudaStream_t stream);
+                            const float* acc, bool apply, float server_lr, const LaunchShape& s,
+                            cudaStream_t stream);
 
 }  // namespace fa

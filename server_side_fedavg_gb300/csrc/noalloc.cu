@@ -109,7 +109,6 @@ extern "C" fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weig
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int din = dtype_in == FA_F32 ? 0 : 1;
-    const uint32_t ntiles = static_cast<uint32_t>((numel + fa::kTile - 1) / fa::kTile);
     // clients in batches of 16, 8, 4, 2, 1, in index order; the first batch
     // starts the sum (stores its first product), so no clearing is needed
     uint32_t done = 0;
@@ -127,18 +126,16 @@ extern "C" fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weig
         a.acc = d->sum;
         a.J = jb;
         a.nseg = 1;
-        a.ntiles = ntiles;
         a.vec_ok = aligned ? 1ull : 0ull;
         a.seg[0].x_off = 0;
         a.seg[0].acc_idx = 0;
         a.seg[0].len = numel;
         a.seg[0].first = done == 0 ? 1u : 0u;
-        a.seg[0].tile0 = 0;
         if (fa::launch_accumulate(a, din, d->shape, s) != cudaSuccess) return FA_ERR_CUDA;
         done += jb;
     }
     const float divisor = static_cast<float>(total);
-    const int per = d->shape.fin_ctas_per_sm[dtype_out == FA_F32 ? 0 : 1];
+    const int per = d->shape.fin_ctas_per_sm[0][dtype_out == FA_F32 ? 0 : 1];
     uint64_t want = (numel + fa::kBlock - 1) / fa::kBlock;
     uint64_t cap = static_cast<uint64_t>(d->shape.sms > 0 ? d->shape.sms : 1) * (per > 0 ? per : 1);
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);

@@ -28,6 +28,15 @@ MUTANTS = {
     "truncating_cast": ("if (frac > 0.5) k = fl + 1.0;", "if (frac > 2.0) k = fl + 1.0;"),
 }
 
+APPLY_MUTANTS = {
+    "apply_drops_base": ("double y = fo_load(base, dtype_out, i) + server_lr * (s / N);",
+                         "double y = server_lr * (s / N);"),
+    "apply_drops_lr": ("double y = fo_load(base, dtype_out, i) + server_lr * (s / N);",
+                       "double y = fo_load(base, dtype_out, i) + (s / N);"),
+    "apply_sign": ("double y = fo_load(base, dtype_out, i) + server_lr * (s / N);",
+                   "double y = fo_load(base, dtype_out, i) - server_lr * (s / N);"),
+}
+
 
 def _build(tmp, name, a, b):
     src = open(SRC).read()
@@ -42,6 +51,8 @@ def _build(tmp, name, a, b):
     u32, u64, i32, f64, vp = ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
     L.fo_fedavg_key.argtypes = [u32, vp, vp, vp, i32, u64, i32, vp, vp, vp]
     L.fo_fedavg_key.restype = i32
+    L.fo_fedavg_apply_key.argtypes = [u32, vp, vp, vp, i32, u64, vp, f64, i32, vp, vp, vp]
+    L.fo_fedavg_apply_key.restype = i32
     return L
 
 
@@ -84,10 +95,40 @@ def _pins_pass(L) -> bool:
     return True
 
 
+def _apply_pins_pass(L) -> bool:
+    """A compact replay of the delta-round exact-rational pin."""
+    rng = np.random.default_rng(98)
+    for trial in range(20):
+        K, m = int(rng.integers(1, 5)), 8
+        weights = [float(v) for v in rng.integers(1, 3000, K)]
+        xs = [(rng.standard_normal(m) * 1e-3).astype(np.float32) for _ in range(K)]
+        base = (rng.standard_normal(m) * 0.02).astype(np.float32)
+        lr = float(rng.choice([0.5, 2.0]))
+        ptrs = (ctypes.c_void_p * K)(*[x.ctypes.data for x in xs])
+        n = np.asarray(weights, np.float64)
+        rep = np.ones(K, np.uint8)
+        out = np.zeros(m, np.float32)
+        L.fo_fedavg_apply_key(K, n.ctypes.data, rep.ctypes.data, ptrs, 0, m, base.ctypes.data, lr, 0,
+                              out.ctypes.data, None, None)
+        mean = exact.exact_fedavg(weights, [True] * K, [x.astype(np.float64).tolist() for x in xs])
+        want = [exact.nearest_f32(Fraction(float(base[i])) + Fraction(lr) * mean[i]) for i in range(m)]
+        if out.view(np.uint32).tolist() != want:
+            return False
+    return True
+
+
 def test_unmutated_copy_passes(tmp_path):
     src = open(SRC).read()
     L = _build(str(tmp_path), "identity", src[:10], src[:10])
     assert _pins_pass(L)
+    assert _apply_pins_pass(L)
+
+
+@pytest.mark.parametrize("name", sorted(APPLY_MUTANTS))
+def test_apply_mutant_is_caught(tmp_path, name):
+    a, b = APPLY_MUTANTS[name]
+    L = _build(str(tmp_path), name, a, b)
+    assert not _apply_pins_pass(L), f"pins did not catch mutant {name}"
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
