@@ -13,6 +13,8 @@ sum in HBM), fa_finalize (divide by the per-key weight total, RNE to bf16).
          (bf16 input read + fp32 sum read + fp32 sum write; the first client's
          launches skip the sum read) over its CUDA-event-timed duration
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
+  resident  the same round when every update is resident, reduced in one pass by
+         fa_reduce_resident (K*s_in + s_out bytes per element), for comparison
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs an independent replica (the path has no exchange
@@ -386,6 +388,36 @@ def run_ours(args, world, rank, local, pg):
     ms_per_step = ms_total / args.steps
     value = world * client_bytes / (ms_per_step * 1e-3) / 1e9
 
+    # ---- the same round with every update resident, reduced in one pass (fa_reduce_resident)
+    resident_line = None
+    if resident == w.K and not args.no_resident:
+        ids = list(range(w.K))
+        ptrs = [b.data_ptr() for b in bufs]
+
+        def round_resident():
+            fa.fa_reset(ctx)
+            fa.fa_reduce_resident(ctx, ids, w.weights, ptrs, [out], sh)
+
+        for _ in range(args.warmup):
+            round_resident()
+        torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0 = fa.fa_get_stats(ctx)["kernel_launches"]
+        r0.record(s)
+        for _ in range(args.steps):
+            round_resident()
+        r1.record(s)
+        torch.cuda.synchronize()
+        rms = r0.elapsed_time(r1) / args.steps
+        rbytes = w.P * (w.K * si + so)
+        resident_line = {"value": round(client_bytes / (rms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                         "ms_per_round": round(rms, 3),
+                         "hbm_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1),
+                         "hbm_frac": round(rbytes / (rms * 1e-3) / 1e9 / peak, 4),
+                         "bytes_per_round": int(rbytes),
+                         "launches_per_round": int((fa.fa_get_stats(ctx)["kernel_launches"] - l0) // args.steps),
+                         "kernel": "reduce_bulk_kernel<bf16,bf16,final>"}
+
     fa.fa_close(ctx)
     del bufs, out
     torch.cuda.synchronize()
@@ -415,6 +447,7 @@ def run_ours(args, world, rank, local, pg):
                      "launch_ms": round(acc_launch_ms, 4),
                      "traffic": profiled_traffic(acc_bytes_per_launch)},
         "gpu_launches": int(launches),
+        "resident": resident_line,
         "clocks": clk,
         "e2e": e2e,
     }
@@ -498,6 +531,7 @@ def main(argv=None):
     ap.add_argument("--e2e-pool", type=int, default=24)
     ap.add_argument("--ref-elems", type=int, default=64 << 20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-resident", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -178,6 +178,27 @@ fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream);
 fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* const* out_ptrs,
                             double server_lr, void* stream);
 
+/* A whole round in one pass when every client's FULL update is resident in device
+ * memory ([FLARE] "Moving and aggregating large model updates efficiently": the second
+ * memory pressure is holding many clients' updates during aggregation -- once they are
+ * all in HBM, the weighted mean is one read of each update and one write of the output,
+ * K*s_in + s_out bytes per element instead of streaming's ~10 per client-element).
+ *   client_ids[j], weights[j]  as fa_accumulate; contributions apply in this order
+ *   flat_ptrs[j]  client j's update over the whole flat layout (total numel values of
+ *                 dtype_in, in this GPU's memory)
+ *   out_ptrs      as fa_finalize (n_keys pointers, or one with FA_FLAT_OUT), in this
+ *                 GPU's memory
+ * Every client counts as having sent every key.  The result is bit-identical to
+ * fa_accumulate of each update (in the same order) followed by fa_finalize; up to 16
+ * clients take one pass, more take ceil(K/16) passes (the earlier ones through the
+ * running sum).  Needs a round with no contributions yet; closes it (fa_key_total works,
+ * fa_finalize then returns FA_ERR_STATE because the outputs are already written).
+ * If all weights are 0 nothing is written.
+ * Errors: FA_ERR_ARG, FA_ERR_WEIGHT, FA_ERR_STATE, FA_ERR_CUDA. */
+fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
+                             const double* weights, const void* const* flat_ptrs,
+                             void* const* out_ptrs, void* stream);
+
 /* Start a new round ([Clara] "Server-side workflow": the loop repeats per round):
  * forget weights, per-key totals, reporter masks and element counts.  The running sum
  * is not cleared (the first contribution of the next round overwrites it).  Waits
@@ -198,6 +219,33 @@ fa_status fa_sync(fa_ctx* ctx);
 
 /* Counters since fa_open (host-side, exact). */
 fa_status fa_get_stats(const fa_ctx* ctx, fa_stats* out);
+
+/* Options of fa_partition_plan (NULL = {1, 0, 0.5, 0.05}: the "time only" policy). */
+typedef struct {
+    double w_time;      /* w_t >= 0: weight of the per-sample time cost */
+    double w_energy;    /* w_e >= 0: weight of the per-sample energy cost (w_t + w_e > 0) */
+    double ema_alpha;   /* 0 < alpha <= 1: weight of the newest measurement in the moving average */
+    double deadband;    /* >= 0: keep the allocation if no share would move by more than this
+                           fraction of its current value */
+} fa_partition_opts;
+
+/* Next round's sample counts n_i (the FedAvg weights) from this round's measurements:
+ * the adaptive controller of [Part] section 2, "The adaptive controller" -- per-sample
+ * costs tau_i = t_i / n_i and eps_i = e_i / n_i, smoothed by an exponential moving
+ * average; combined cost c_i = w_t * tau^_i / median(tau^) + w_e * eps^_i / median(eps^);
+ * the fixed budget sum(n_i) split inversely proportional to c_i (every participant keeps
+ * at least one sample, remainders by largest fraction, ties to the lower index) unless
+ * no share would move by more than the deadband.  The page fixes neither alpha nor the
+ * deadband (defaults 0.5 and 5 %).  A zero median falls back to the mean (all zero: that
+ * cost is left out); a zero combined cost is floored at 1e-12 of the largest.
+ *   m           participants
+ *   time_s, energy_j, samples   this round's t_i >= 0, e_i >= 0, n_i >= 1
+ *   ema_tau, ema_eps            in/out moving-average state (negative or NaN = no history)
+ *   new_samples out: next round's n_i (sums to the same budget)
+ * Host code only; needs no GPU.  Errors: FA_ERR_ARG, FA_ERR_RANGE (budget overflow). */
+fa_status fa_partition_plan(uint32_t m, const double* time_s, const double* energy_j,
+                            const uint64_t* samples, double* ema_tau, double* ema_eps,
+                            const fa_partition_opts* opts, uint64_t* new_samples);
 
 /* Largest tensor fa_aggregate_noalloc takes (elements): 2^22, i.e. a 16 MiB fp32 sum. */
 #define FA_NOALLOC_MAX_ELEMS 4194304ull

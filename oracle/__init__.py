@@ -22,8 +22,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 SO = os.path.join(_BUILD, "libfedavg_oracle.so")
 
-F32, BF16 = "f32", "bf16"
-_CODES = {F32: 0, BF16: 1}
+F32, BF16, F64 = "f32", "bf16", "f64"
+_CODES = {F32: 0, BF16: 1, F64: 2}
 
 
 def build_commands():
@@ -90,7 +90,7 @@ def _prep(weights, reported, xs, dtype_in):
     K = len(weights)
     n = np.ascontiguousarray(weights, dtype=np.float64)
     rep = np.ascontiguousarray([1 if r else 0 for r in reported], dtype=np.uint8)
-    want = np.float32 if dtype_in == F32 else np.uint16
+    want = {F32: np.float32, BF16: np.uint16, F64: np.float64}[dtype_in]
     numel = None
     arrs = []
     for k in range(K):
@@ -149,3 +149,17 @@ def fedavg_apply_key(weights, reported, xs, dtype_in, base, server_lr, dtype_out
                                       b.ctypes.data, float(server_lr), _CODES[dtype_out], res.ctypes.data,
                                       ctypes.byref(N), ctypes.byref(cnt))
     return (res if wrote else None), N.value, cnt.value
+
+
+def hierarchical_f64(silos, weights, reported, xs, dtype_in):
+    """Two-level weighted mean (silo means, then a mean of silo means weighted by each
+    silo's total), all in fp64.  silos: list of client-index lists."""
+    means, totals = [], []
+    for members in silos:
+        y = fedavg_key_f64([weights[k] for k in members], [reported[k] for k in members],
+                           [xs[k] for k in members], dtype_in)
+        n = sum(weights[k] for k in members if reported[k])
+        means.append(y if y is not None else np.zeros(1))
+        totals.append(n if y is not None else 0.0)
+    rep = [t > 0 for t in totals]
+    return fedavg_key_f64(totals, rep, means, F64)

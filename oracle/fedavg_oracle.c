@@ -36,10 +36,12 @@
 #include <string.h>
 #include <math.h>
 
-enum { FO_F32 = 0, FO_BF16 = 1 };
+enum { FO_F32 = 0, FO_BF16 = 1, FO_F64 = 2 };
 
-/* Decode input element i of a client tensor to fp64 (exact). */
+/* Decode input element i of a client tensor to fp64 (exact).  FO_F64 inputs are
+ * already fp64: they let the oracle nest (a mean of means, for silos). */
 static double fo_load(const void* x, int dtype, uint64_t i) {
+    if (dtype == FO_F64) return ((const double*)x)[i];
     if (dtype == FO_F32) return (double)((const float*)x)[i];
     uint32_t u = (uint32_t)((const uint16_t*)x)[i] << 16; /* bf16 = top half of a binary32 */
     float f;

@@ -53,6 +53,11 @@ class fa_stats(ctypes.Structure):
                 ("chunks", ctypes.c_uint64)]
 
 
+class fa_partition_opts(ctypes.Structure):
+    _fields_ = [("w_time", ctypes.c_double), ("w_energy", ctypes.c_double),
+                ("ema_alpha", ctypes.c_double), ("deadband", ctypes.c_double)]
+
+
 class FedAvgError(RuntimeError):
     def __init__(self, status: int, detail: str):
         self.status = status
@@ -79,6 +84,8 @@ def lib():
         L.fa_accumulate_batch.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64), i64,
                                           u64, ctypes.POINTER(vp), u64, vp]
         L.fa_finalize.argtypes = [vp, ctypes.POINTER(vp), vp]
+        L.fa_reduce_resident.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64),
+                                         ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
         L.fa_finalize_apply.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), f64, vp]
         L.fa_reset.argtypes = [vp]
         L.fa_close.argtypes = [vp]
@@ -88,12 +95,14 @@ def lib():
         L.fa_aggregate_noalloc.argtypes = [u32, ctypes.POINTER(f64), ctypes.POINTER(vp), u64, i32, i32,
                                            vp, vp]
         L.fa_aggregate_noalloc.restype = i32
+        L.fa_partition_plan.argtypes = [u32, vp, vp, vp, vp, vp, ctypes.POINTER(fa_partition_opts), vp]
+        L.fa_partition_plan.restype = i32
         L.fa_strerror.argtypes = [i32]
         L.fa_strerror.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = [vp]
         L.fa_last_error.restype = ctypes.c_char_p
         for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_finalize",
-                     "fa_finalize_apply", "fa_reset",
+                     "fa_finalize_apply", "fa_reduce_resident", "fa_reset",
                      "fa_close", "fa_key_total", "fa_sync", "fa_get_stats"):
             getattr(L, name).restype = i32
         _lib = L
@@ -182,6 +191,16 @@ def fa_finalize_apply(ctx, bases, outs, server_lr=1.0, stream=None):
     _check(lib().fa_finalize_apply(ctx, bs, ps, float(server_lr), _stream(stream)), ctx)
 
 
+def fa_reduce_resident(ctx, client_ids, weights, flat_updates, outs, stream=None):
+    """Whole round from resident full updates (one flat buffer per client) straight to outs."""
+    J = len(client_ids)
+    ids = (ctypes.c_uint32 * J)(*client_ids)
+    ws = (ctypes.c_double * J)(*[float(w) for w in weights])
+    ps = (ctypes.c_void_p * J)(*[_ptr(x) for x in flat_updates])
+    os_ = (ctypes.c_void_p * max(len(outs), 1))(*[_ptr(o) for o in outs])
+    _check(lib().fa_reduce_resident(ctx, J, ids, ws, ps, os_, _stream(stream)), ctx)
+
+
 def fa_reset(ctx):
     _check(lib().fa_reset(ctx), ctx)
 
@@ -216,3 +235,20 @@ def fa_aggregate_noalloc(weights, chunks, numel, dtype_in, dtype_out, out, strea
     ps = (ctypes.c_void_p * max(J, 1))(*[_ptr(c) for c in chunks])
     _check(lib().fa_aggregate_noalloc(J, ws, ps, numel, DTYPES[dtype_in], DTYPES[dtype_out],
                                       _ptr(out), _stream(stream)))
+
+
+def fa_partition_plan(time_s, energy_j, samples, ema_tau=None, ema_eps=None, w_time=1.0,
+                      w_energy=0.0, ema_alpha=0.5, deadband=0.05):
+    """Next round's sample counts; returns (new_samples, ema_tau, ema_eps) as lists."""
+    import numpy as np
+    m = len(samples)
+    t = np.ascontiguousarray(time_s, dtype=np.float64)
+    e = np.ascontiguousarray(energy_j, dtype=np.float64)
+    n = np.ascontiguousarray(samples, dtype=np.uint64)
+    tau = np.full(m, np.nan) if ema_tau is None else np.array(ema_tau, dtype=np.float64)
+    eps = np.full(m, np.nan) if ema_eps is None else np.array(ema_eps, dtype=np.float64)
+    out = np.zeros(m, dtype=np.uint64)
+    o = fa_partition_opts(w_time, w_energy, ema_alpha, deadband)
+    _check(lib().fa_partition_plan(m, t.ctypes.data, e.ctypes.data, n.ctypes.data, tau.ctypes.data,
+                                   eps.ctypes.data, ctypes.byref(o), out.ctypes.data))
+    return [int(v) for v in out], tau.tolist(), eps.tolist()

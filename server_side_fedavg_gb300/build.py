@@ -16,7 +16,7 @@ BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(BUILD, "libfedavg.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["kernels.cu", "noalloc.cu", "fedavg.cpp", "ledger.cpp"]
+SOURCES = ["kernels.cu", "noalloc.cu", "fedavg.cpp", "ledger.cpp", "partition.cpp"]
 
 
 def _common():
@@ -33,7 +33,7 @@ def compile_commands(extra=None):
         if src.endswith(".cu"):
             cmd += ARCH + ["-lineinfo", "-Xptxas", "-v"]
         else:
-            cmd += ["-x", "c++"]
+            cmd += ["-x", "c++", "-Xcompiler", "-ffp-contract=off"]
         cmd += ["-c", os.path.join(CSRC, src), "-o", obj]
         cmds.append((obj, cmd))
     return cmds

@@ -73,6 +73,7 @@ struct fa_ctx {
     void* out_stage = nullptr;
 
     bool broken = false;          // a CUDA call failed after the ledger was updated
+    bool reduced = false;         // this round was written by fa_reduce_resident
     fa_stats stats{};
     std::string err;
     std::vector<fa::Piece> pieces;
@@ -202,12 +203,11 @@ fa_status ensure_ring(fa_ctx* c, bool need_host) {
 fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_t c0,
                         uint64_t n, const void* const* xs, const float* ws, uint32_t J,
                         cudaStream_t s) {
-    // greedy split of J into launches of 16, 8, 4, 2, 1 clients; after the first
-    // launch the sum is started everywhere
+    // launches of up to 16 clients; after the first launch the sum is started everywhere
     uint32_t done = 0;
     while (done < J) {
-        uint32_t left = J - done, jb = 16;
-        while (jb > left) jb >>= 1;
+        const uint32_t left = J - done;
+        const uint32_t jb = left < static_cast<uint32_t>(fa::kMaxBatch) ? left : fa::kMaxBatch;
         fa::AccArgs a;
         std::memset(&a, 0, sizeof a);
         for (uint32_t j = 0; j < jb; ++j) {
@@ -486,6 +486,8 @@ namespace {
 fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* out_ptrs,
                         double server_lr, void* stream) {
     const bool apply = base_ptrs != nullptr;
+    if (c->reduced)
+        return fail(c, FA_ERR_STATE, "this round was reduced by fa_reduce_resident: its outputs are already written");
     if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
     if (out_ptrs == nullptr) return fail(c, FA_ERR_ARG, "out_ptrs is NULL");
     const bool flat = (c->flags & FA_FLAT_OUT) != 0;
@@ -611,6 +613,120 @@ fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* con
     return finalize_impl(ctx, base_ptrs, out_ptrs, server_lr, stream);
 }
 
+fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
+                             const double* weights, const void* const* flat_ptrs,
+                             void* const* out_ptrs, void* stream) {
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    fa_ctx* c = ctx;
+    c->err.clear();
+    if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
+    if (n_clients == 0 || client_ids == nullptr || weights == nullptr || flat_ptrs == nullptr ||
+        out_ptrs == nullptr)
+        return fail(c, FA_ERR_ARG, "empty client list or NULL argument");
+    if (c->ledger.closed() || c->ledger.has_contributions())
+        return fail(c, FA_ERR_STATE, "fa_reduce_resident needs a round with no contributions yet (fa_reset)");
+    for (uint32_t j = 0; j < n_clients; ++j) {
+        bool other = false;
+        if (flat_ptrs[j] == nullptr || classify(flat_ptrs[j], c->device, &other) != Mem::kDevice || other)
+            return fail(c, FA_ERR_ARG, "every client update must be in this GPU's memory");
+    }
+    const bool flat = (c->flags & FA_FLAT_OUT) != 0;
+    const uint32_t nk = c->ledger.n_keys();
+    double total = 0.0;
+    for (uint32_t j = 0; j < n_clients; ++j) total += std::isfinite(weights[j]) ? weights[j] : 0.0;
+    if (total > 0.0) {
+        for (uint32_t p = 0; p < (flat ? 1u : nk); ++p) {
+            bool other = false;
+            if (out_ptrs[p] == nullptr || classify(out_ptrs[p], c->device, &other) != Mem::kDevice || other)
+                return fail(c, FA_ERR_ARG, "fa_reduce_resident: outputs must be in this GPU's memory");
+        }
+    }
+    // bookkeeping: every client sends every key (validates ids and weights first)
+    std::string e;
+    int32_t st = c->ledger.plan_accumulate(client_ids, weights, n_clients, -1, 0,
+                                           c->ledger.total_elems(), &c->pieces, &e);
+    if (st != fa::kOk) return fail(c, st, e);
+    st = c->ledger.plan_finalize(&c->items, &e);
+    if (st != fa::kOk) return fail(c, FA_ERR_INTERNAL, e);
+    c->ledger.close();
+    c->reduced = true;
+    c->stats.chunks++;
+    c->stats.client_bytes += static_cast<uint64_t>(n_clients) * c->ledger.total_elems() * c->s_in;
+    if (c->items.empty()) return FA_OK;   // no weight anywhere: nothing is written
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    fa_status r = chain_in(c, s);
+    if (r != FA_OK) return r;
+    const uint32_t K = n_clients;
+    const uint32_t last = K - (K - 1) / fa::kMaxBatch * fa::kMaxBatch;   // 1..16 clients in the last pass
+    const uint32_t head = K - last;                                       // earlier passes write the sum
+    std::vector<float> w(K);
+    for (uint32_t j = 0; j < K; ++j) w[j] = static_cast<float>(weights[j]);
+    auto aligned = [&](const void* p, uint64_t off_bytes) {
+        return ((reinterpret_cast<uintptr_t>(p) + off_bytes) & 15u) == 0;
+    };
+    for (uint32_t g = 0; g < head; g += fa::kMaxBatch) {
+        fa::AccArgs a;
+        std::memset(&a, 0, sizeof a);
+        a.J = fa::kMaxBatch;
+        for (uint32_t j = 0; j < a.J; ++j) {
+            a.x[j] = flat_ptrs[g + j];
+            a.w[j] = w[g + j];
+        }
+        a.acc = c->acc;
+        for (uint32_t p = 0; p < nk;) {
+            a.nseg = 0;
+            a.vec_ok = 0;
+            for (; p < nk && a.nseg < static_cast<uint32_t>(fa::kMaxSegs); ++p) {
+                fa::AccSeg& sg = a.seg[a.nseg];
+                sg.x_off = c->ledger.flat_off(p);
+                sg.acc_idx = c->ledger.acc_off(p);
+                sg.len = c->ledger.numel(p);
+                sg.first = g == 0 ? 1u : 0u;
+                bool ok = true;
+                for (uint32_t j = 0; j < a.J; ++j) ok = ok && aligned(a.x[j], sg.x_off * c->s_in);
+                if (ok) a.vec_ok |= 1ull << a.nseg;
+                a.nseg++;
+            }
+            FA_CUDA(c, fa::launch_accumulate(a, c->din, c->shape, s));
+            c->stats.kernel_launches++;
+        }
+    }
+    fa::RedArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    ra.J = last;
+    for (uint32_t j = 0; j < last; ++j) {
+        ra.x[j] = flat_ptrs[head + j];
+        ra.w[j] = w[head + j];
+    }
+    ra.acc = c->acc;
+    for (size_t i = 0; i < c->items.size();) {
+        ra.nseg = 0;
+        ra.vec_ok = 0;
+        for (; i < c->items.size() && ra.nseg < static_cast<uint32_t>(fa::kMaxSegs); ++i) {
+            const fa::FinItem& it = c->items[i];
+            fa::RedSeg& sg = ra.seg[ra.nseg];
+            sg.x_off = it.flat_off;
+            sg.acc_idx = it.acc_idx;
+            sg.len = it.numel;
+            char* dst = static_cast<char*>(flat ? out_ptrs[0] : out_ptrs[it.key]);
+            if (flat) dst += it.flat_off * c->s_out;
+            sg.out = dst;
+            sg.divisor = static_cast<float>(it.total);
+            sg.read_sum = head > 0 ? 1u : 0u;
+            bool ok = aligned(dst, 0);
+            for (uint32_t j = 0; j < last; ++j) ok = ok && aligned(ra.x[j], sg.x_off * c->s_in);
+            if (ok) ra.vec_ok |= 1ull << ra.nseg;
+            ra.nseg++;
+        }
+        FA_CUDA(c, fa::launch_reduce_final(ra, c->din, c->dout, c->shape, s));
+        c->stats.kernel_launches++;
+    }
+    return chain_out(c, s);
+}
+
 fa_status fa_reset(fa_ctx* ctx) {
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
@@ -620,6 +736,7 @@ fa_status fa_reset(fa_ctx* ctx) {
     if (r != FA_OK) return r;
     ctx->ledger.reset();
     ctx->broken = false;
+    ctx->reduced = false;
     return FA_OK;
 }
 

@@ -1,23 +1,28 @@
 // Aggregation kernels for sm_103a (see kernels.cuh).
 //
-// Design (GB300: 152 SMs, HBM3e):
-//  - persistent CTAs, grid = SMs x resident CTAs per SM, striding over 4096-element
-//    tiles; a tile never crosses a segment (one key's run), so each CTA takes one
-//    uniform branch per tile;
-//  - 128-bit loads and stores, 8 elements per vector: one 16-byte load of bf16
-//    input (or two of fp32) and two 16-byte loads / stores of the fp32 sum; a warp
-//    touches 512 contiguous bytes of the sum per vector step;
-//  - client input is read once: non-coherent loads that skip L1; the sum keeps the
-//    default policy so small layouts (adapters) stay resident in the 129 MB L2
-//    between clients;
-//  - ragged tails (len % 8) and segments whose pointers are not 16-byte aligned
-//    take a scalar path, one element per thread.
-// Arithmetic: __fmul_rn / __fmaf_rn / __fdiv_rn so the compiler never fuses or
-// reorders: the first contribution is a rounded product, every later one one
-// fused multiply-add, in client order.
+// GB300: 152 SMs, HBM3e.  Every kernel is a bandwidth-bound streaming pass:
+//  - accumulate_bulk_kernel (one client per launch, the streaming hot path) and
+//    reduce_bulk_kernel (J resident clients per launch) move their tiles with bulk
+//    copies (cp.async.bulk, the 1-D form of TMA) through a three-stage shared-memory
+//    pipeline: one elected thread arms a stage's mbarrier with the byte count and
+//    issues the loads, all threads compute in shared memory, the elected thread
+//    writes the result tile back with one bulk store, and a stage is refilled once
+//    that store has read it.  Persistent grids, one or two CTAs per SM, keep about
+//    150-200 KB of copies in flight per SM -- a timed sweep of tile sizes, stage
+//    counts and direct-load variants on GB300 chose these shapes;
+//  - finalize_kernel reads the sum with 128-bit loads and writes 128-bit stores;
+//  - ragged tails (< 8 elements) and segments whose pointers are not 16-byte
+//    aligned use direct per-element loads and stores.
+// Arithmetic: __fmul_rn / __fmaf_rn / __fdiv_rn so the compiler never contracts or
+// reorders: the first contribution is a rounded product, every later one one fused
+// multiply-add, in client order -- so every path yields the same bits.
+// Every mbarrier wait is bounded; a timeout sets g_device_error (read by fa_sync),
+// makes the CTA wait (bounded) for its own loads in flight, and return.
 #include "kernels.cuh"
 
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 namespace fa {
 
@@ -26,7 +31,9 @@ __device__ unsigned int g_device_error;
 namespace {
 
 constexpr uint32_t kMaxWaitSpins = 1u << 24;   // bound on every mbarrier wait
+constexpr int kStages = 3;
 
+// ----------------------------------------------------------------- memory helpers
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -59,100 +66,67 @@ __device__ __forceinline__ void st_v4u(void* p, uint4 v) {
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+}
+
+// One element of dtype Tin from global memory, read-only path.
 template <typename Tin>
-struct Load8;
+__device__ __forceinline__ float load_one(const Tin* p);
 
 template <>
-struct Load8<uint16_t> {   // bf16
-    static __device__ __forceinline__ void vec(const uint16_t* p, float (&v)[8]) {
-        uint4 r = ld_stream_v4(p);
-        v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x);
-        v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
-        v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z);
-        v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
-    }
-    static __device__ __forceinline__ float one(const uint16_t* p) {
-        uint16_t u;
-        asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(u) : "l"(p));
-        return __uint_as_float(static_cast<uint32_t>(u) << 16);
-    }
-};
+__device__ __forceinline__ float load_one<uint16_t>(const uint16_t* p) {
+    uint16_t u;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(u) : "l"(p));
+    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
 
 template <>
-struct Load8<float> {
-    static __device__ __forceinline__ void vec(const float* p, float (&v)[8]) {
-        uint4 a = ld_stream_v4(p);
-        uint4 b = ld_stream_v4(p + 4);
-        v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
-        v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
-        v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
-        v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
-    }
-    static __device__ __forceinline__ float one(const float* p) {
-        float f;
-        asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(f) : "l"(p));
-        return f;
-    }
-};
+__device__ __forceinline__ float load_one<float>(const float* p) {
+    float f;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(f) : "l"(p));
+    return f;
+}
 
-// One vector of 8 elements: r = first ? w0*x0 : sum;  r = fma(wj, xj, r) for j >= 1
-// (j >= 0 when not first).
-template <typename Tin, int J>
-__device__ __forceinline__ void acc_vec(const AccArgs& a, uint64_t xe, float* s, bool first) {
-    float x[J][8];
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-        Load8<Tin>::vec(static_cast<const Tin*>(a.x[j]) + xe, x[j]);
-    float r[8];
-    if (first) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) r[e] = __fmul_rn(a.w[0], x[0][e]);
+// Eight elements of dtype Tin from a 16-byte aligned shared-memory vector slot.
+template <typename Tin>
+__device__ __forceinline__ void smem_vec8(const uint8_t* base, uint32_t v, float (&x)[8]) {
+    if constexpr (sizeof(Tin) == 2) {
+        const uint4 q = reinterpret_cast<const uint4*>(base)[v];
+        x[0] = bf16_lo(q.x); x[1] = bf16_hi(q.x);
+        x[2] = bf16_lo(q.y); x[3] = bf16_hi(q.y);
+        x[4] = bf16_lo(q.z); x[5] = bf16_hi(q.z);
+        x[6] = bf16_lo(q.w); x[7] = bf16_hi(q.w);
     } else {
-        float4 lo = ld_v4f(s), hi = ld_v4f(s + 4);
-        r[0] = lo.x; r[1] = lo.y; r[2] = lo.z; r[3] = lo.w;
-        r[4] = hi.x; r[5] = hi.y; r[6] = hi.z; r[7] = hi.w;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) r[e] = __fmaf_rn(a.w[0], x[0][e], r[e]);
+        const float4 p = reinterpret_cast<const float4*>(base)[2 * v];
+        const float4 q = reinterpret_cast<const float4*>(base)[2 * v + 1];
+        x[0] = p.x; x[1] = p.y; x[2] = p.z; x[3] = p.w;
+        x[4] = q.x; x[5] = q.y; x[6] = q.z; x[7] = q.w;
     }
-#pragma unroll
-    for (int j = 1; j < J; ++j) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) r[e] = __fmaf_rn(a.w[j], x[j][e], r[e]);
-    }
-    st_v4f(s, make_float4(r[0], r[1], r[2], r[3]));
-    st_v4f(s + 4, make_float4(r[4], r[5], r[6], r[7]));
 }
 
-template <typename Tin, int J>
-__device__ __forceinline__ void acc_one(const AccArgs& a, uint64_t xe, float* s, bool first) {
-    float r = first ? __fmul_rn(a.w[0], Load8<Tin>::one(static_cast<const Tin*>(a.x[0]) + xe))
-                    : __fmaf_rn(a.w[0], Load8<Tin>::one(static_cast<const Tin*>(a.x[0]) + xe), *s);
-#pragma unroll
-    for (int j = 1; j < J; ++j)
-        r = __fmaf_rn(a.w[j], Load8<Tin>::one(static_cast<const Tin*>(a.x[j]) + xe), r);
-    *s = r;
+// Store eight results of dtype Tout (RNE for bf16) to shared memory vector slot v.
+template <typename Tout>
+__device__ __forceinline__ void smem_store8(uint8_t* base, uint32_t v, const float (&q)[8]) {
+    if constexpr (sizeof(Tout) == 2) {
+        reinterpret_cast<uint4*>(base)[v] = make_uint4(pack_bf16(q[0], q[1]), pack_bf16(q[2], q[3]),
+                                                       pack_bf16(q[4], q[5]), pack_bf16(q[6], q[7]));
+    } else {
+        reinterpret_cast<float4*>(base)[2 * v] = make_float4(q[0], q[1], q[2], q[3]);
+        reinterpret_cast<float4*>(base)[2 * v + 1] = make_float4(q[4], q[5], q[6], q[7]);
+    }
 }
 
-// ---------------------------------------------------------------------------
-// Streaming accumulate (one client per launch) through a shared-memory pipeline
-// fed by bulk copies (cp.async.bulk, the 1-D form of TMA):
-//   thread 0 keeps S-1 tiles in flight: for each tile it arms the stage's
-//   mbarrier with the byte count and issues one bulk load of the input tile and,
-//   unless this is the first contribution, one of the sum tile;
-//   all 256 threads wait on the stage's mbarrier, compute in shared memory, and
-//   thread 0 writes the sum tile back with one bulk store;
-//   a stage is refilled once the bulk store that drained it has read it.
-// A tile's vector part (multiple of 8 elements) moves by bulk copies; its ragged
-// tail and any segment whose pointers are not 16-byte aligned use direct loads.
-// Every mbarrier wait is bounded; a timeout sets g_device_error (read by
-// fa_sync), makes the CTA wait (bounded) for its own loads in flight, and return.
-template <typename Tin>
-struct BulkStages;
-template <>
-struct BulkStages<uint16_t> { static constexpr int kS = 3; };   // 3 x 48 KB = 144 KB: 1 CTA per SM
-template <>
-struct BulkStages<float> { static constexpr int kS = 3; };      // 3 x 64 KB = 192 KB: 1 CTA per SM
+template <typename Tout>
+__device__ __forceinline__ void store_one(void* out, uint64_t e, float q) {
+    if constexpr (sizeof(Tout) == 2)
+        static_cast<uint16_t*>(out)[e] = __bfloat16_as_ushort(__float2bfloat16_rn(q));
+    else
+        static_cast<float*>(out)[e] = q;
+}
 
+// ----------------------------------------------------------------- pipeline helpers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -169,39 +143,100 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
+__device__ __forceinline__ void mbar_init(uint64_t* bars, int n) {
+    for (int s = 0; s < n; ++s)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[s])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst_smem)), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(smem_addr(src_smem)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
 struct TileAt {
     uint32_t si;
     uint64_t e0;
     uint32_t cnt;
 };
 
-__device__ __forceinline__ TileAt tile_at(const AccArgs& a, uint32_t t, uint32_t& cursor) {
-    while (cursor + 1 < a.nseg && t >= a.seg[cursor + 1].tile0) ++cursor;
-    const AccSeg& sg = a.seg[cursor];
+// Tile t (numbered across segments by tile0) with `tile` elements per tile; the cursor
+// only moves forward because each CTA visits its tiles in increasing order.
+template <typename Seg>
+__device__ __forceinline__ TileAt tile_at(const Seg* segs, uint32_t nseg, uint32_t t,
+                                          uint32_t tile, uint32_t& cursor) {
+    while (cursor + 1 < nseg && t >= segs[cursor + 1].tile0) ++cursor;
+    const Seg& sg = segs[cursor];
     TileAt r;
     r.si = cursor;
-    r.e0 = static_cast<uint64_t>(t - sg.tile0) * kBulkTile;
+    r.e0 = static_cast<uint64_t>(t - sg.tile0) * tile;
     const uint64_t rem = sg.len - r.e0;
-    r.cnt = rem < kBulkTile ? static_cast<uint32_t>(rem) : kBulkTile;
+    r.cnt = rem < tile ? static_cast<uint32_t>(rem) : tile;
     return r;
 }
 
+// The bounded end of a pipelined kernel: after an early exit (a wait gave up) the
+// elected thread flags the error and waits for the loads it still has in flight;
+// in every case it waits for its bulk stores before the CTA leaves.
+__device__ __forceinline__ void pipeline_drain(uint64_t* bars, uint32_t consumed,
+                                               uint32_t issued, uint32_t count) {
+    if (consumed < count) {
+        atomicOr(&g_device_error, kErrWaitTimeout);
+        for (uint32_t j = consumed; j < issued; ++j)
+            mbar_wait(smem_addr(&bars[j % kStages]), (j / kStages) & 1u);
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- streaming accumulate
+// One element through global memory (ragged tails, unaligned segments).
+template <typename Tin>
+__device__ __forceinline__ void acc_one(const Tin* x, float w, float* s, bool first) {
+    const float xv = load_one<Tin>(x);
+    *s = first ? __fmul_rn(w, xv) : __fmaf_rn(w, xv, *s);
+}
+
+template <typename Tin>
+constexpr size_t bulk_smem_bytes() {
+    return static_cast<size_t>(kStages) * kBulkTile * (sizeof(Tin) + sizeof(float)) +
+           static_cast<size_t>(kStages) * sizeof(uint64_t);
+}
+
+// Stage = input tile (kBulkTile x Tin) + sum tile (kBulkTile x fp32): 48 KB for bf16,
+// 64 KB for fp32 input; one CTA per SM.
 template <typename Tin>
 __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid_constant__ AccArgs a) {
-    constexpr int S = BulkStages<Tin>::kS;
     constexpr uint32_t XB = kBulkTile * sizeof(Tin);
     constexpr uint32_t SB = kBulkTile * sizeof(float);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* xs = smem;
-    uint8_t* ss = smem + S * XB;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * (XB + SB));
+    uint8_t* ss = smem + kStages * XB;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * (XB + SB));
     const uint32_t count =
         blockIdx.x < a.ntiles ? (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[s])) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    if (threadIdx.x == 0) mbar_init(bars, kStages);
     __syncthreads();
     const Tin* x0 = static_cast<const Tin*>(a.x[0]);
     const float w = a.w[0];
@@ -209,40 +244,31 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
     uint32_t issued = 0;
 
     auto issue = [&](uint32_t i) {    // thread 0 only
-        const int s = static_cast<int>(i % S);
-        const TileAt ta = tile_at(a, blockIdx.x + i * gridDim.x, pcur);
+        const int s = static_cast<int>(i % kStages);
+        const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + i * gridDim.x, kBulkTile, pcur);
         const AccSeg& sg = a.seg[ta.si];
         const uint32_t bar = smem_addr(&bars[s]);
         const uint32_t n8 = ta.cnt / kVec;
         if (((a.vec_ok >> ta.si) & 1ull) && n8 > 0) {
             const uint32_t xb = n8 * kVec * sizeof(Tin);
             const uint32_t sb = sg.first ? 0u : n8 * kVec * sizeof(float);
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                         ::"r"(bar), "r"(xb + sb) : "memory");
-            asm volatile(
-                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                ::"r"(smem_addr(xs + s * XB)), "l"(x0 + sg.x_off + ta.e0), "r"(xb), "r"(bar)
-                : "memory");
-            if (sb)
-                asm volatile(
-                    "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                    ::"r"(smem_addr(ss + s * SB)), "l"(a.acc + sg.acc_idx + ta.e0), "r"(sb), "r"(bar)
-                    : "memory");
+            mbar_expect(bar, xb + sb);
+            bulk_load(xs + s * XB, x0 + sg.x_off + ta.e0, xb, bar);
+            if (sb) bulk_load(ss + s * SB, a.acc + sg.acc_idx + ta.e0, sb, bar);
         } else {
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+            mbar_arrive(bar);
         }
     };
 
     if (threadIdx.x == 0) {
-        for (uint32_t i = 0; i < count && i < static_cast<uint32_t>(S); ++i) issue(i);
-        issued = count < static_cast<uint32_t>(S) ? count : static_cast<uint32_t>(S);
+        for (uint32_t i = 0; i < count && i < static_cast<uint32_t>(kStages); ++i) issue(i);
+        issued = count < static_cast<uint32_t>(kStages) ? count : static_cast<uint32_t>(kStages);
     }
     uint32_t consumed = 0;
-    bool ok = true;
     for (uint32_t i = 0; i < count; ++i) {
-        const int s = static_cast<int>(i % S);
-        ok = mbar_wait(smem_addr(&bars[s]), (i / S) & 1u);
-        const TileAt ta = tile_at(a, blockIdx.x + i * gridDim.x, ccur);
+        const int s = static_cast<int>(i % kStages);
+        const bool ok = mbar_wait(smem_addr(&bars[s]), (i / kStages) & 1u);
+        const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + i * gridDim.x, kBulkTile, ccur);
         const AccSeg& sg = a.seg[ta.si];
         const bool first = sg.first != 0;
         const uint64_t xe0 = sg.x_off + ta.e0;
@@ -250,23 +276,11 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
         const bool bulk = ((a.vec_ok >> ta.si) & 1ull) && ta.cnt >= static_cast<uint32_t>(kVec);
         const uint32_t n8 = bulk ? ta.cnt / kVec : 0;
         if (ok && bulk) {
-            const Tin* xt = reinterpret_cast<const Tin*>(xs + s * XB);
-            float* st = reinterpret_cast<float*>(ss + s * SB);
+            const uint8_t* xt = xs + s * XB;
+            float4* st = reinterpret_cast<float4*>(ss + s * SB);
             for (uint32_t v = threadIdx.x; v < n8; v += kBlock) {
                 float xv[8];
-                if constexpr (sizeof(Tin) == 2) {
-                    const uint4 q = reinterpret_cast<const uint4*>(xt)[v];
-                    xv[0] = bf16_lo(q.x); xv[1] = bf16_hi(q.x);
-                    xv[2] = bf16_lo(q.y); xv[3] = bf16_hi(q.y);
-                    xv[4] = bf16_lo(q.z); xv[5] = bf16_hi(q.z);
-                    xv[6] = bf16_lo(q.w); xv[7] = bf16_hi(q.w);
-                } else {
-                    const float4 p = reinterpret_cast<const float4*>(xt)[2 * v];
-                    const float4 q = reinterpret_cast<const float4*>(xt)[2 * v + 1];
-                    xv[0] = p.x; xv[1] = p.y; xv[2] = p.z; xv[3] = p.w;
-                    xv[4] = q.x; xv[5] = q.y; xv[6] = q.z; xv[7] = q.w;
-                }
-                float4* sv = reinterpret_cast<float4*>(st) + 2 * v;
+                smem_vec8<Tin>(xt, v, xv);
                 float4 lo, hi;
                 if (first) {
                     lo = make_float4(__fmul_rn(w, xv[0]), __fmul_rn(w, xv[1]), __fmul_rn(w, xv[2]),
@@ -274,122 +288,194 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
                     hi = make_float4(__fmul_rn(w, xv[4]), __fmul_rn(w, xv[5]), __fmul_rn(w, xv[6]),
                                      __fmul_rn(w, xv[7]));
                 } else {
-                    lo = sv[0];
-                    hi = sv[1];
+                    lo = st[2 * v];
+                    hi = st[2 * v + 1];
                     lo.x = __fmaf_rn(w, xv[0], lo.x); lo.y = __fmaf_rn(w, xv[1], lo.y);
                     lo.z = __fmaf_rn(w, xv[2], lo.z); lo.w = __fmaf_rn(w, xv[3], lo.w);
                     hi.x = __fmaf_rn(w, xv[4], hi.x); hi.y = __fmaf_rn(w, xv[5], hi.y);
                     hi.z = __fmaf_rn(w, xv[6], hi.z); hi.w = __fmaf_rn(w, xv[7], hi.w);
                 }
-                sv[0] = lo;
-                sv[1] = hi;
+                st[2 * v] = lo;
+                st[2 * v + 1] = hi;
             }
             const uint32_t tail = ta.cnt - n8 * kVec;
             if (threadIdx.x < tail) {
                 const uint32_t e = n8 * kVec + threadIdx.x;
-                acc_one<Tin, 1>(a, xe0 + e, g0 + e, first);
+                acc_one<Tin>(x0 + xe0 + e, w, g0 + e, first);
             }
         } else if (ok) {
-            for (uint32_t e = threadIdx.x; e < ta.cnt; e += kBlock) acc_one<Tin, 1>(a, xe0 + e, g0 + e, first);
+            for (uint32_t e = threadIdx.x; e < ta.cnt; e += kBlock)
+                acc_one<Tin>(x0 + xe0 + e, w, g0 + e, first);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (!__syncthreads_and(ok)) break;
         consumed = i + 1;
         if (threadIdx.x == 0) {
-            if (n8 > 0)
-                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                             ::"l"(g0), "r"(smem_addr(ss + s * SB)), "r"(n8 * kVec * 4u) : "memory");
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            if (n8 > 0) bulk_store(g0, ss + s * SB, n8 * kVec * 4u);
+            bulk_commit();
             // refill the stage drained one iteration ago once its store has read it
-            if (i >= 1 && i - 1 + S < count) {
+            if (i >= 1 && i - 1 + kStages < count) {
                 asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                issue(i - 1 + S);
-                issued = i + S;
+                issue(i - 1 + kStages);
+                issued = i + kStages;
             }
         }
     }
-    if (threadIdx.x == 0) {
-        if (consumed < count) {
-            atomicOr(&g_device_error, kErrWaitTimeout);
-            for (uint32_t j = consumed; j < issued; ++j)
-                mbar_wait(smem_addr(&bars[j % S]), (j / S) & 1u);
-        }
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    }
+    if (threadIdx.x == 0) pipeline_drain(bars, consumed, issued, count);
     __syncthreads();
 }
 
-template <typename Tin, int J>
-__global__ void __launch_bounds__(kBlock) accumulate_kernel(const __grid_constant__ AccArgs a) {
-    constexpr int kVecPerTile = kTile / kVec;                  // 512
-    constexpr int kUnroll = kVecPerTile / kBlock;              // 2
-    uint32_t si = 0;
-    for (uint32_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
-        while (si + 1 < a.nseg && t >= a.seg[si + 1].tile0) ++si;
-        const AccSeg& sg = a.seg[si];
-        const uint64_t e0 = static_cast<uint64_t>(t - sg.tile0) * kTile;
-        const uint64_t rem = sg.len - e0;
-        const uint32_t cnt = rem < kTile ? static_cast<uint32_t>(rem) : kTile;
-        const bool first = sg.first != 0;
-        const uint64_t xe0 = sg.x_off + e0;
-        float* s0 = a.acc + sg.acc_idx + e0;
-        if ((a.vec_ok >> si) & 1ull) {
-            if (cnt == kTile) {
+// ----------------------------------------------------------------- J-client reduce
+// Stage = J input tiles (T x Tin each) [+ sum tile (T x fp32): sum mode, or final mode
+// reading earlier contributions] [+ output tile (T x Tout): final mode]; T is chosen on
+// the host so a stage fits kReduceStageBytes (one CTA per SM, three stages: about
+// 200 KB of copies in flight).  Sum mode writes the running sum back; final mode
+// divides by the segment's divisor and rounds to Tout.  kJ > 0 fixes the client count
+// at compile time so the per-client loop unrolls (J = 16 and 8); kJ = 0 reads it from
+// the arguments.
+template <bool kFinal, typename Tin, typename Tout>
+__host__ __device__ constexpr uint32_t reduce_elem_bytes(uint32_t J, bool has_sum) {
+    return J * static_cast<uint32_t>(sizeof(Tin)) + (has_sum ? 4u : 0u) +
+           (kFinal ? static_cast<uint32_t>(sizeof(Tout)) : 0u);
+}
+
+template <typename Tin, typename Tout, bool kFinal>
+__device__ __forceinline__ void red_one(const RedArgs& a, const RedSeg& sg, uint64_t e, uint32_t J) {
+    // element e of the segment, through global memory
+    const uint64_t xe = sg.x_off + e;
+    float r;
+    uint32_t j0 = 0;
+    if (sg.read_sum) {
+        r = a.acc[sg.acc_idx + e];
+    } else {
+        r = __fmul_rn(a.w[0], load_one<Tin>(static_cast<const Tin*>(a.x[0]) + xe));
+        j0 = 1;
+    }
+    for (uint32_t j = j0; j < J; ++j)
+        r = __fmaf_rn(a.w[j], load_one<Tin>(static_cast<const Tin*>(a.x[j]) + xe), r);
+    if constexpr (kFinal)
+        store_one<Tout>(sg.out, e, __fdiv_rn(r, sg.divisor));
+    else
+        a.acc[sg.acc_idx + e] = r;
+}
+
+template <typename Tin, typename Tout, bool kFinal, int kJ>
+__global__ void __launch_bounds__(kBlock, 1) reduce_bulk_kernel(const __grid_constant__ RedArgs a) {
+    const uint32_t T = a.tile;
+    const uint32_t J = kJ > 0 ? static_cast<uint32_t>(kJ) : a.J;
+    const uint32_t XB = T * sizeof(Tin);
+    const uint32_t SB = a.has_sum ? T * static_cast<uint32_t>(sizeof(float)) : 0u;
+    const uint32_t stage = T * reduce_elem_bytes<kFinal, Tin, Tout>(J, a.has_sum != 0);
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * stage);
+    const uint32_t count =
+        blockIdx.x < a.ntiles ? (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    if (threadIdx.x == 0) mbar_init(bars, kStages);
+    __syncthreads();
+    uint32_t pcur = 0, ccur = 0, issued = 0;
+
+    auto issue = [&](uint32_t i) {    // thread 0 only
+        const uint32_t s = i % kStages;
+        const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + i * gridDim.x, T, pcur);
+        const RedSeg& sg = a.seg[ta.si];
+        const uint32_t bar = smem_addr(&bars[s]);
+        const uint32_t n8 = ta.cnt / kVec;
+        if (((a.vec_ok >> ta.si) & 1ull) && n8 > 0) {
+            const uint32_t xb = n8 * kVec * sizeof(Tin);
+            const uint32_t sb = sg.read_sum ? n8 * kVec * 4u : 0u;
+            mbar_expect(bar, J * xb + sb);
+            uint8_t* st = smem + s * stage;
+            for (uint32_t j = 0; j < J; ++j)
+                bulk_load(st + j * XB, static_cast<const Tin*>(a.x[j]) + sg.x_off + ta.e0, xb, bar);
+            if (sb) bulk_load(st + J * XB, a.acc + sg.acc_idx + ta.e0, sb, bar);
+        } else {
+            mbar_arrive(bar);
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < count && i < static_cast<uint32_t>(kStages); ++i) issue(i);
+        issued = count < static_cast<uint32_t>(kStages) ? count : static_cast<uint32_t>(kStages);
+    }
+    uint32_t consumed = 0;
+    for (uint32_t i = 0; i < count; ++i) {
+        const uint32_t s = i % kStages;
+        const bool ok = mbar_wait(smem_addr(&bars[s]), (i / kStages) & 1u);
+        const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + i * gridDim.x, T, ccur);
+        const RedSeg& sg = a.seg[ta.si];
+        const bool bulk = ((a.vec_ok >> ta.si) & 1ull) && ta.cnt >= static_cast<uint32_t>(kVec);
+        const uint32_t n8 = bulk ? ta.cnt / kVec : 0;
+        uint8_t* st = smem + s * stage;
+        float4* sum = reinterpret_cast<float4*>(st + J * XB);
+        uint8_t* res = st + J * XB + SB;                      // final mode output tile
+        if (ok && bulk) {
+            for (uint32_t v = threadIdx.x; v < n8; v += kBlock) {
+                float r[8];
+                {
+                    float xv[8];
+                    smem_vec8<Tin>(st, v, xv);
+                    if (sg.read_sum) {          // client 0 joins the earlier contributions
+                        const float4 lo = sum[2 * v], hi = sum[2 * v + 1];
+                        r[0] = lo.x; r[1] = lo.y; r[2] = lo.z; r[3] = lo.w;
+                        r[4] = hi.x; r[5] = hi.y; r[6] = hi.z; r[7] = hi.w;
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const uint32_t v = threadIdx.x + u * kBlock;
-                    acc_vec<Tin, J>(a, xe0 + v * kVec, s0 + v * kVec, first);
+                        for (int e = 0; e < 8; ++e) r[e] = __fmaf_rn(a.w[0], xv[e], r[e]);
+                    } else {                    // client 0 starts the sum
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) r[e] = __fmul_rn(a.w[0], xv[e]);
+                    }
                 }
-            } else {
-                const uint32_t nv = cnt / kVec;
-                for (uint32_t v = threadIdx.x; v < nv; v += kBlock)
-                    acc_vec<Tin, J>(a, xe0 + v * kVec, s0 + v * kVec, first);
-                const uint32_t tail = cnt - nv * kVec;
-                if (threadIdx.x < tail) {
-                    const uint32_t e = nv * kVec + threadIdx.x;
-                    acc_one<Tin, J>(a, xe0 + e, s0 + e, first);
+#pragma unroll
+                for (uint32_t j = 1; j < (kJ > 0 ? static_cast<uint32_t>(kJ) : static_cast<uint32_t>(kMaxBatch)); ++j) {
+                    if (kJ == 0 && j >= J) break;
+                    float xv[8];
+                    smem_vec8<Tin>(st + j * XB, v, xv);
+                    const float wj = a.w[j];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) r[e] = __fmaf_rn(wj, xv[e], r[e]);
+                }
+                if constexpr (kFinal) {
+                    const float d = sg.divisor;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) r[e] = __fdiv_rn(r[e], d);
+                    smem_store8<Tout>(res, v, r);
+                } else {
+                    sum[2 * v] = make_float4(r[0], r[1], r[2], r[3]);
+                    sum[2 * v + 1] = make_float4(r[4], r[5], r[6], r[7]);
                 }
             }
-        } else {
-            for (uint32_t e = threadIdx.x; e < cnt; e += kBlock)
-                acc_one<Tin, J>(a, xe0 + e, s0 + e, first);
+            const uint32_t tail = ta.cnt - n8 * kVec;
+            if (threadIdx.x < tail) red_one<Tin, Tout, kFinal>(a, sg, ta.e0 + n8 * kVec + threadIdx.x, J);
+        } else if (ok) {
+            for (uint32_t e = threadIdx.x; e < ta.cnt; e += kBlock)
+                red_one<Tin, Tout, kFinal>(a, sg, ta.e0 + e, J);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (!__syncthreads_and(ok)) break;
+        consumed = i + 1;
+        if (threadIdx.x == 0) {
+            if (n8 > 0) {
+                if constexpr (kFinal)
+                    bulk_store(static_cast<Tout*>(sg.out) + ta.e0, res, n8 * kVec * sizeof(Tout));
+                else
+                    bulk_store(a.acc + sg.acc_idx + ta.e0, sum, n8 * kVec * 4u);
+            }
+            bulk_commit();
+            if (i >= 1 && i - 1 + kStages < count) {
+                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                issue(i - 1 + kStages);
+                issued = i + kStages;
+            }
         }
     }
+    if (threadIdx.x == 0) pipeline_drain(bars, consumed, issued, count);
+    __syncthreads();
 }
 
-template <typename Tout>
-struct Store;
+constexpr size_t kReduceSmemBytes =
+    static_cast<size_t>(kStages) * kReduceStageBytes + kStages * sizeof(uint64_t);
 
-template <>
-struct Store<float> {
-    static __device__ __forceinline__ void vec(void* out, uint64_t e, const float (&q)[8]) {
-        float* p = static_cast<float*>(out) + e;
-        st_v4f(p, make_float4(q[0], q[1], q[2], q[3]));
-        st_v4f(p + 4, make_float4(q[4], q[5], q[6], q[7]));
-    }
-    static __device__ __forceinline__ void one(void* out, uint64_t e, float q) {
-        static_cast<float*>(out)[e] = q;
-    }
-};
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
-}
-
-template <>
-struct Store<uint16_t> {
-    static __device__ __forceinline__ void vec(void* out, uint64_t e, const float (&q)[8]) {
-        uint4 v = make_uint4(pack_bf16(q[0], q[1]), pack_bf16(q[2], q[3]),
-                             pack_bf16(q[4], q[5]), pack_bf16(q[6], q[7]));
-        st_v4u(static_cast<uint16_t*>(out) + e, v);
-    }
-    static __device__ __forceinline__ void one(void* out, uint64_t e, float q) {
-        static_cast<uint16_t*>(out)[e] = __bfloat16_as_ushort(__float2bfloat16_rn(q));
-    }
-};
-
-// Base values of delta rounds (dtype_out), 8 at a time or one.
+// ----------------------------------------------------------------- finalize
 template <typename Tout>
 struct LoadBase;
 
@@ -422,6 +508,19 @@ struct LoadBase<uint16_t> {
     }
 };
 
+template <typename Tout>
+__device__ __forceinline__ void global_store8(void* out, uint64_t e, const float (&q)[8]) {
+    if constexpr (sizeof(Tout) == 2) {
+        st_v4u(static_cast<uint16_t*>(out) + e,
+               make_uint4(pack_bf16(q[0], q[1]), pack_bf16(q[2], q[3]), pack_bf16(q[4], q[5]),
+                          pack_bf16(q[6], q[7])));
+    } else {
+        float* p = static_cast<float*>(out) + e;
+        st_v4f(p, make_float4(q[0], q[1], q[2], q[3]));
+        st_v4f(p + 4, make_float4(q[4], q[5], q[6], q[7]));
+    }
+}
+
 // q = sum / N (IEEE division); delta rounds then add server_lr * q to the base
 // with one rounding (fma).
 template <typename Tout, bool kApply>
@@ -436,7 +535,7 @@ __device__ __forceinline__ void fin_vec(const FinSeg& sg, uint64_t e, const floa
 #pragma unroll
         for (int i = 0; i < 8; ++i) q[i] = __fmaf_rn(lr, q[i], b[i]);
     }
-    Store<Tout>::vec(sg.out, e, q);
+    global_store8<Tout>(sg.out, e, q);
 }
 
 template <typename Tout, bool kApply>
@@ -444,7 +543,7 @@ __device__ __forceinline__ void fin_one(const FinSeg& sg, uint64_t e, const floa
                                         float lr) {
     float q = __fdiv_rn(*s, d);
     if constexpr (kApply) q = __fmaf_rn(lr, q, LoadBase<Tout>::one(sg.base, e));
-    Store<Tout>::one(sg.out, e, q);
+    store_one<Tout>(sg.out, e, q);
 }
 
 template <typename Tout, bool kApply>
@@ -494,62 +593,125 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
     }
 }
 
-template <typename Tin, int J>
-cudaError_t launch_acc_t(const AccArgs& a, int ctas_per_sm, int sms, cudaStream_t stream) {
-    if (a.ntiles == 0) return cudaSuccess;
-    uint32_t cap = static_cast<uint32_t>(sms > 0 ? sms : 1) *
-                   static_cast<uint32_t>(ctas_per_sm > 0 ? ctas_per_sm : 1);
-    uint32_t grid = a.ntiles < cap ? a.ntiles : cap;
-    accumulate_kernel<Tin, J><<<grid, kBlock, 0, stream>>>(a);
-    return cudaGetLastError();
-}
-
-template <typename Tin>
-constexpr size_t bulk_smem_bytes() {
-    return static_cast<size_t>(BulkStages<Tin>::kS) * kBulkTile * (sizeof(Tin) + sizeof(float)) +
-           static_cast<size_t>(BulkStages<Tin>::kS) * sizeof(uint64_t);
-}
-
-// Number the tiles of every segment for a kernel whose tile is `tile` elements.
-bool number_tiles(AccArgs* a, uint64_t tile) {
+// ----------------------------------------------------------------- host side
+template <typename Seg>
+bool number_tiles(Seg* segs, uint32_t nseg, uint64_t tile, uint32_t* ntiles) {
     uint64_t t = 0;
-    for (uint32_t i = 0; i < a->nseg; ++i) {
-        a->seg[i].tile0 = static_cast<uint32_t>(t);
-        t += (a->seg[i].len + tile - 1) / tile;
+    for (uint32_t i = 0; i < nseg; ++i) {
+        segs[i].tile0 = static_cast<uint32_t>(t);
+        t += (segs[i].len + tile - 1) / tile;
         if (t > 0xFFFFFFFFull) return false;
     }
-    a->ntiles = static_cast<uint32_t>(t);
+    *ntiles = static_cast<uint32_t>(t);
     return true;
 }
 
-template <typename Tin>
-cudaError_t launch_bulk(const AccArgs& a, int ctas_per_sm, int sms, cudaStream_t stream) {
-    if (a.ntiles == 0) return cudaSuccess;
+uint32_t grid_for(uint32_t ntiles, int sms, int per_sm) {
     uint32_t cap = static_cast<uint32_t>(sms > 0 ? sms : 1) *
-                   static_cast<uint32_t>(ctas_per_sm > 0 ? ctas_per_sm : 1);
-    uint32_t grid = a.ntiles < cap ? a.ntiles : cap;
-    accumulate_bulk_kernel<Tin><<<grid, kBlock, bulk_smem_bytes<Tin>(), stream>>>(a);
+                   static_cast<uint32_t>(per_sm > 0 ? per_sm : 1);
+    return ntiles < cap ? ntiles : cap;
+}
+
+// Elements per reduce tile: the largest multiple of 256 whose stage fits the budget.
+uint32_t reduce_tile(uint32_t elem_bytes) {
+    uint32_t t = kReduceStageBytes / elem_bytes / 256 * 256;
+    return t < 256 ? 256 : t;
+}
+
+template <typename Tin, typename Tout, bool kFinal>
+cudaError_t launch_reduce_t(RedArgs a, int per_sm, int sms, cudaStream_t stream) {
+    // note: occupancy (per_sm) is the same for every J specialisation
+    a.has_sum = kFinal ? 0u : 1u;
+    for (uint32_t i = 0; i < a.nseg; ++i) a.has_sum |= a.seg[i].read_sum;
+    const uint32_t eb = reduce_elem_bytes<kFinal, Tin, Tout>(a.J, a.has_sum != 0);
+    a.tile = reduce_tile(eb);
+    if (!number_tiles(a.seg, a.nseg, a.tile, &a.ntiles)) return cudaErrorInvalidValue;
+    if (a.ntiles == 0) return cudaSuccess;
+    const size_t smem = static_cast<size_t>(kStages) * a.tile * eb + kStages * sizeof(uint64_t);
+    const uint32_t grid = grid_for(a.ntiles, sms, per_sm);
+    if (a.J == 16)
+        reduce_bulk_kernel<Tin, Tout, kFinal, 16><<<grid, kBlock, smem, stream>>>(a);
+    else if (a.J == 8)
+        reduce_bulk_kernel<Tin, Tout, kFinal, 8><<<grid, kBlock, smem, stream>>>(a);
+    else
+        reduce_bulk_kernel<Tin, Tout, kFinal, 0><<<grid, kBlock, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 template <typename Tin>
-cudaError_t launch_acc_j(const AccArgs& a, const LaunchShape& s, int in, cudaStream_t stream) {
-    switch (a.J) {
-        case 1: return launch_bulk<Tin>(a, s.bulk_ctas_per_sm[in], s.sms, stream);
-        case 2: return launch_acc_t<Tin, 2>(a, s.acc_ctas_per_sm[in][1], s.sms, stream);
-        case 4: return launch_acc_t<Tin, 4>(a, s.acc_ctas_per_sm[in][2], s.sms, stream);
-        case 8: return launch_acc_t<Tin, 8>(a, s.acc_ctas_per_sm[in][3], s.sms, stream);
-        case 16: return launch_acc_t<Tin, 16>(a, s.acc_ctas_per_sm[in][4], s.sms, stream);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_stream_t(AccArgs a, int per_sm, int sms, cudaStream_t stream) {
+    if (!number_tiles(a.seg, a.nseg, kBulkTile, &a.ntiles)) return cudaErrorInvalidValue;
+    if (a.ntiles == 0) return cudaSuccess;
+    accumulate_bulk_kernel<Tin><<<grid_for(a.ntiles, sms, per_sm), kBlock, bulk_smem_bytes<Tin>(), stream>>>(a);
+    return cudaGetLastError();
 }
 
-template <typename Tin, int J>
-cudaError_t occ_acc(int* n) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, accumulate_kernel<Tin, J>, kBlock, 0);
+RedArgs to_reduce_args(const AccArgs& a) {
+    RedArgs r;
+    for (int j = 0; j < kMaxBatch; ++j) {
+        r.x[j] = a.x[j];
+        r.w[j] = a.w[j];
+    }
+    r.acc = a.acc;
+    r.J = a.J;
+    r.nseg = a.nseg;
+    r.ntiles = 0;
+    r.tile = 0;
+    r.has_sum = 1;
+    r.pad = 0;
+    r.vec_ok = a.vec_ok;
+    for (uint32_t i = 0; i < a.nseg; ++i) {
+        RedSeg& s = r.seg[i];
+        s.x_off = a.seg[i].x_off;
+        s.acc_idx = a.seg[i].acc_idx;
+        s.len = a.seg[i].len;
+        s.out = nullptr;
+        s.divisor = 1.0f;
+        s.read_sum = a.seg[i].first ? 0u : 1u;
+        s.tile0 = 0;
+        s.pad = 0;
+    }
+    return r;
+}
+
+template <typename Tin, typename Tout, bool kFinal, int kJ>
+cudaError_t prepare_reduce_j(int* occ) {
+    cudaError_t e = cudaFuncSetAttribute(reduce_bulk_kernel<Tin, Tout, kFinal, kJ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kReduceSmemBytes));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, reduce_bulk_kernel<Tin, Tout, kFinal, kJ>,
+                                                         kBlock, kReduceSmemBytes);
+}
+
+template <typename Tin, typename Tout, bool kFinal>
+cudaError_t prepare_reduce(int* occ) {
+    int o16 = 0, o8 = 0;
+    cudaError_t e = prepare_reduce_j<Tin, Tout, kFinal, 16>(&o16);
+    if (e == cudaSuccess) e = prepare_reduce_j<Tin, Tout, kFinal, 8>(&o8);
+    if (e == cudaSuccess) e = prepare_reduce_j<Tin, Tout, kFinal, 0>(occ);
+    if (e == cudaSuccess) *occ = std::min(*occ, std::min(o16, o8));
+    return e;
+}
+
+template <typename Tin>
+cudaError_t prepare_stream(int* occ) {
+    cudaError_t e = cudaFuncSetAttribute(accumulate_bulk_kernel<Tin>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bulk_smem_bytes<Tin>()));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, accumulate_bulk_kernel<Tin>, kBlock,
+                                                         bulk_smem_bytes<Tin>());
 }
 
 }  // namespace
+
+cudaError_t take_device_error(unsigned int* code) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned int));
+    if (e == cudaSuccess && *code != 0) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    return e;
+}
 
 cudaError_t query_launch_shape(LaunchShape* s) {
     int dev = 0;
@@ -559,26 +721,14 @@ cudaError_t query_launch_shape(LaunchShape* s) {
     if (e != cudaSuccess) return e;
     cudaError_t r = cudaSuccess;
     auto keep = [&r](cudaError_t x) { if (r == cudaSuccess) r = x; };
-    keep(occ_acc<float, 1>(&s->acc_ctas_per_sm[0][0]));
-    keep(occ_acc<float, 2>(&s->acc_ctas_per_sm[0][1]));
-    keep(occ_acc<float, 4>(&s->acc_ctas_per_sm[0][2]));
-    keep(occ_acc<float, 8>(&s->acc_ctas_per_sm[0][3]));
-    keep(occ_acc<float, 16>(&s->acc_ctas_per_sm[0][4]));
-    keep(occ_acc<uint16_t, 1>(&s->acc_ctas_per_sm[1][0]));
-    keep(occ_acc<uint16_t, 2>(&s->acc_ctas_per_sm[1][1]));
-    keep(occ_acc<uint16_t, 4>(&s->acc_ctas_per_sm[1][2]));
-    keep(occ_acc<uint16_t, 8>(&s->acc_ctas_per_sm[1][3]));
-    keep(occ_acc<uint16_t, 16>(&s->acc_ctas_per_sm[1][4]));
-    keep(cudaFuncSetAttribute(accumulate_bulk_kernel<float>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(bulk_smem_bytes<float>())));
-    keep(cudaFuncSetAttribute(accumulate_bulk_kernel<uint16_t>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(bulk_smem_bytes<uint16_t>())));
-    keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->bulk_ctas_per_sm[0], accumulate_bulk_kernel<float>,
-                                                       kBlock, bulk_smem_bytes<float>()));
-    keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->bulk_ctas_per_sm[1], accumulate_bulk_kernel<uint16_t>,
-                                                       kBlock, bulk_smem_bytes<uint16_t>()));
+    keep(prepare_stream<float>(&s->bulk_ctas_per_sm[0]));
+    keep(prepare_stream<uint16_t>(&s->bulk_ctas_per_sm[1]));
+    keep(prepare_reduce<float, float, false>(&s->reduce_ctas_per_sm[0][0]));
+    keep(prepare_reduce<float, float, true>(&s->reduce_ctas_per_sm[0][1]));
+    keep(prepare_reduce<float, uint16_t, true>(&s->reduce_ctas_per_sm[0][2]));
+    keep(prepare_reduce<uint16_t, float, false>(&s->reduce_ctas_per_sm[1][0]));
+    keep(prepare_reduce<uint16_t, float, true>(&s->reduce_ctas_per_sm[1][1]));
+    keep(prepare_reduce<uint16_t, uint16_t, true>(&s->reduce_ctas_per_sm[1][2]));
     keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->fin_ctas_per_sm[0][0],
                                                        finalize_kernel<float, false>, kBlock, 0));
     keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->fin_ctas_per_sm[0][1],
@@ -590,30 +740,41 @@ cudaError_t query_launch_shape(LaunchShape* s) {
     return r;
 }
 
-cudaError_t take_device_error(unsigned int* code) {
-    unsigned int zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned int));
-    if (e == cudaSuccess && *code != 0) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
-    return e;
+cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,
+                              cudaStream_t stream) {
+    if (a.nseg == 0 || a.nseg > static_cast<uint32_t>(kMaxSegs)) return cudaErrorInvalidValue;
+    if (a.J == 0 || a.J > static_cast<uint32_t>(kMaxBatch)) return cudaErrorInvalidValue;
+    const int in = dtype_in == 0 ? 0 : 1;
+    if (a.J == 1) {
+        return in == 0 ? launch_stream_t<float>(a, s.bulk_ctas_per_sm[0], s.sms, stream)
+                       : launch_stream_t<uint16_t>(a, s.bulk_ctas_per_sm[1], s.sms, stream);
+    }
+    const RedArgs r = to_reduce_args(a);
+    return in == 0 ? launch_reduce_t<float, float, false>(r, s.reduce_ctas_per_sm[0][0], s.sms, stream)
+                   : launch_reduce_t<uint16_t, float, false>(r, s.reduce_ctas_per_sm[1][0], s.sms, stream);
 }
 
-cudaError_t launch_accumulate(const AccArgs& args, int dtype_in, const LaunchShape& s,
-                              cudaStream_t stream) {
-    AccArgs a = args;
+cudaError_t launch_reduce_final(const RedArgs& a, int dtype_in, int dtype_out,
+                                const LaunchShape& s, cudaStream_t stream) {
     if (a.nseg == 0 || a.nseg > static_cast<uint32_t>(kMaxSegs)) return cudaErrorInvalidValue;
-    if (!number_tiles(&a, a.J == 1 ? kBulkTile : kTile)) return cudaErrorInvalidValue;
-    return dtype_in == 0 ? launch_acc_j<float>(a, s, 0, stream)
-                         : launch_acc_j<uint16_t>(a, s, 1, stream);
+    if (a.J == 0 || a.J > static_cast<uint32_t>(kMaxBatch)) return cudaErrorInvalidValue;
+    const int in = dtype_in == 0 ? 0 : 1;
+    const int oi = dtype_out == 0 ? 1 : 2;
+    if (in == 0) {
+        return dtype_out == 0
+                   ? launch_reduce_t<float, float, true>(a, s.reduce_ctas_per_sm[0][oi], s.sms, stream)
+                   : launch_reduce_t<float, uint16_t, true>(a, s.reduce_ctas_per_sm[0][oi], s.sms, stream);
+    }
+    return dtype_out == 0
+               ? launch_reduce_t<uint16_t, float, true>(a, s.reduce_ctas_per_sm[1][oi], s.sms, stream)
+               : launch_reduce_t<uint16_t, uint16_t, true>(a, s.reduce_ctas_per_sm[1][oi], s.sms, stream);
 }
 
 cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_out,
                             const float* acc, bool apply, float server_lr, const LaunchShape& s,
                             cudaStream_t stream) {
     if (ntiles == 0 || nseg == 0) return cudaSuccess;
-    int per = s.fin_ctas_per_sm[apply ? 1 : 0][dtype_out == 0 ? 0 : 1];
-    uint32_t cap = static_cast<uint32_t>(s.sms > 0 ? s.sms : 1) *
-                   static_cast<uint32_t>(per > 0 ? per : 1);
-    uint32_t grid = ntiles < cap ? ntiles : cap;
+    const uint32_t grid = grid_for(ntiles, s.sms, s.fin_ctas_per_sm[apply ? 1 : 0][dtype_out == 0 ? 0 : 1]);
     if (dtype_out == 0) {
         if (apply) finalize_kernel<float, true><<<grid, kBlock, 0, stream>>>(segs, nseg, ntiles, acc, server_lr);
         else finalize_kernel<float, false><<<grid, kBlock, 0, stream>>>(segs, nseg, ntiles, acc, server_lr);

@@ -2,15 +2,17 @@
 //
 //   accumulate  sum[i] = n_k * x[i]                (first contribution to element i)
 //               sum[i] = fma(n_k, x[i], sum[i])    (every later one)
-//               J >= 1 resident clients per launch: the same operation sequence,
-//               applied in client order with the partial sum kept in registers, so
-//               a batch is bit-identical to J single launches.
-//   finalize    out[i] = round_rne(sum[i] / N_p)   (IEEE division, then RNE to bf16
-//                                                   or a plain fp32 store)
+//   reduce      J resident clients in one pass, the same operation sequence in client
+//               order with the partial sum in registers; either writes the running sum
+//               (batched accumulate) or, in final mode, divides and rounds straight to
+//               the output (a whole round when every update is resident)
+//   finalize    out[i] = RNE(sum[i] / N_p)   (IEEE division, then RNE to bf16 or a
+//                                             plain fp32 store); delta rounds add
+//                                             server_lr * that quotient to a base
 //
-// All three are HBM-bandwidth bound streaming passes (about 0.1 flop per byte):
-// no tensor cores.  Layout: the fp32 running sum is padded per key to 32
-// elements, so each key starts 128-byte aligned.
+// All are HBM-bandwidth bound streaming passes (about 0.1 flop per byte): no tensor
+// cores.  Layout: the fp32 running sum is padded per key to 32 elements, so each key
+// starts 128-byte aligned.
 #pragma once
 
 #include <cstdint>
@@ -19,11 +21,12 @@
 namespace fa {
 
 constexpr int kBlock = 256;           // threads per CTA
-constexpr int kVec = 8;               // elements per vector (16 B of bf16, 2 x 16 B of fp32 sum)
-constexpr int kTile = 4096;           // elements per CTA work unit (direct-load kernels)
-constexpr int kBulkTile = 8192;       // elements per pipeline stage (bulk-copy kernel)
-constexpr int kMaxSegs = 48;          // segments per accumulate launch
-constexpr int kMaxBatch = 16;         // resident clients per accumulate launch
+constexpr int kVec = 8;               // elements per vector (16 B of bf16, 2 x 16 B of fp32)
+constexpr int kTile = 4096;           // elements per tile of the finalize kernel
+constexpr int kBulkTile = 8192;       // elements per pipeline stage of the streaming kernel
+constexpr int kMaxSegs = 48;          // segments per accumulate / reduce launch
+constexpr int kMaxBatch = 16;         // resident clients per launch
+constexpr int kReduceStageBytes = 73728;   // shared-memory budget per stage of the reduce kernel
 
 struct AccSeg {
     uint64_t x_off;     // element offset into every input chunk
@@ -37,11 +40,36 @@ struct AccArgs {
     const void* x[kMaxBatch];   // J input chunk bases (device), dtype_in
     float w[kMaxBatch];         // (float) n_k per input
     float* acc;
-    uint32_t J;
+    uint32_t J;                 // 1..16
     uint32_t nseg;
     uint32_t ntiles;            // set by launch_accumulate
     uint64_t vec_ok;            // bit s: segment s is 16-byte aligned for x and sum
     AccSeg seg[kMaxSegs];
+};
+
+struct RedSeg {
+    uint64_t x_off;     // element offset into every input
+    uint64_t acc_idx;   // element index into the running sum
+    uint64_t len;       // elements (>= 1)
+    void* out;          // final mode: destination of element 0 (dtype_out)
+    float divisor;      // final mode: (float) N_p
+    uint32_t read_sum;  // 1: earlier contributions are in the running sum
+    uint32_t tile0;     // first tile (set by the launcher)
+    uint32_t pad;
+};
+
+struct RedArgs {
+    const void* x[kMaxBatch];   // J input bases (device), dtype_in
+    float w[kMaxBatch];
+    float* acc;
+    uint32_t J;                 // 1..16
+    uint32_t nseg;
+    uint32_t ntiles;            // set by the launcher
+    uint32_t tile;              // elements per tile (set by the launcher)
+    uint32_t has_sum;           // set by the launcher: a stage holds a sum tile
+    uint32_t pad;
+    uint64_t vec_ok;            // bit s: segment s is 16-byte aligned for every pointer
+    RedSeg seg[kMaxSegs];
 };
 
 struct FinSeg {
@@ -55,9 +83,10 @@ struct FinSeg {
 
 struct LaunchShape {
     int sms = 0;
-    int bulk_ctas_per_sm[2] = {};     // [dtype_in], streaming (J = 1) bulk-copy kernel
-    int acc_ctas_per_sm[2][5] = {};   // [dtype_in][log2 J]
-    int fin_ctas_per_sm[2][2] = {};   // [apply][dtype_out]
+    int bulk_ctas_per_sm[2] = {};       // [dtype_in], streaming kernel
+    int reduce_ctas_per_sm[2][3] = {};  // [dtype_in][sum mode, final fp32 out, final bf16 out]
+                                        // (same for every specialisation of J)
+    int fin_ctas_per_sm[2][2] = {};     // [apply][dtype_out]
 };
 
 // Device-side error bits (file-scope word shared by every launch on a device).
@@ -70,12 +99,17 @@ cudaError_t take_device_error(unsigned int* code);
 // shared-memory limits).
 cudaError_t query_launch_shape(LaunchShape* s);
 
-// dtype codes: 0 = fp32, 1 = bf16.  J must be 1, 2, 4, 8 or 16.  The caller fills
-// x, w, acc, J, nseg, vec_ok and each segment's x_off / acc_idx / len / first; the
-// launcher numbers the tiles for the kernel it picks (J = 1: the bulk-copy kernel).
-// Returns cudaErrorInvalidValue if the tiles do not fit 32-bit numbering.
+// dtype codes: 0 = fp32, 1 = bf16.  The caller fills x, w, acc, J (1..16), nseg, vec_ok
+// and each segment's x_off / acc_idx / len / first; the launcher numbers the tiles for
+// the kernel it picks (J = 1: streaming kernel, else the reduce kernel in sum mode).
+// Returns cudaErrorInvalidValue if the arguments are out of range.
 cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,
                               cudaStream_t stream);
+
+// Final-mode reduce: out = RNE((sum so far +) J weighted inputs, / divisor) per segment.
+// The caller fills everything but tile / ntiles / tile0.
+cudaError_t launch_reduce_final(const RedArgs& a, int dtype_in, int dtype_out,
+                                const LaunchShape& s, cudaStream_t stream);
 
 // segs: device array of nseg FinSeg sorted by tile0.
 //   apply == false: out = RNE(sum / N)

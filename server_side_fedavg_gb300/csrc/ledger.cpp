@@ -60,6 +60,12 @@ int32_t Ledger::init(const uint64_t* numels, uint32_t n_keys, uint32_t max_clien
     return kOk;
 }
 
+bool Ledger::has_contributions() const {
+    for (uint64_t v : recv_)
+        if (v != 0) return true;
+    return false;
+}
+
 void Ledger::reset() {
     std::fill(weight_.begin(), weight_.end(), 0.0);
     std::fill(has_weight_.begin(), has_weight_.end(), 0);

@@ -87,6 +87,8 @@ public:
     uint64_t total_elems() const { return total_; }
     uint64_t padded_elems() const { return padded_; }
     bool closed() const { return closed_; }
+    // True once any client has sent any element this round.
+    bool has_contributions() const;
 
 private:
     // Split [a, b) of key p into runs that are fresh / already started, then

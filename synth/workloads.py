@@ -20,6 +20,7 @@ adaptive-partitioning summary's per-participant sample counts n_i):
             seeded client at 0.02*Student-t(3); n_k Zipf(1.2)-skewed;
             streamed in 256 MiB flat chunks
   decoder1l K=4, one layer of the 7B decoder (profiling size)
+  mlp16     K=16, gate and up projections of one 7B layer (profiling size)
 """
 from __future__ import annotations
 
@@ -241,10 +242,19 @@ def make(name: str) -> Workload:
         K = 4
         w = Workload(name, i, keys, K, BF16, BF16, 0.02, uniform_int_weights(seed, K),
                      [list(range(len(keys)))] * K, [DIST_NORMAL] * K, (256 << 20) // 2, seed)
+    elif name == "mlp16":
+        # the gate and up projections of one 7B decoder layer, K=16 clients all resident:
+        # the resident-reduce kernels of llama7b at about 3.4 GB of device memory
+        i = 6
+        seed = BASE_SEED + i
+        keys = llama7b_layout(layers=1)[5:7]
+        K = 16
+        w = Workload(name, i, keys, K, BF16, BF16, 0.02, uniform_int_weights(seed, K),
+                     [list(range(len(keys)))] * K, [DIST_NORMAL] * K, (256 << 20) // 2, seed)
     else:
         raise ValueError(f"unknown workload {name!r}")
     return _finish(w)
 
 
 NAMES = ("tiny", "unet3d", "lora", "vlm2b", "llama7b")
-EXTRA = ("decoder1l",)
+EXTRA = ("decoder1l", "mlp16")

@@ -125,7 +125,7 @@ def test_ring_geometry_bit_identical(small):
         assert np.array_equal(a[p], b[p]), f"key {p}"
 
 
-@pytest.mark.parametrize("J", [2, 3, 8, 11, 16])
+@pytest.mark.parametrize("J", [2, 3, 8, 11, 16, 19])
 def test_batch_bit_identical_to_sequential(J):
     """fa_accumulate_batch == the same clients through fa_accumulate, bit for bit."""
     rng = np.random.default_rng(J)
