@@ -98,6 +98,35 @@ def run_streamed_round(w, resident=False):
         fa.fa_close(ctx)
 
 
+def run_resident_round(w):
+    """Every client's full update generated into HBM, then one fa_reduce_resident round
+    exactly as the bench's `resident` measurement runs it; returns the flat output."""
+    import torch
+
+    import server_side_fedavg_gb300 as fa
+    import synth
+
+    tdt = torch.int16 if w.dtype_in == "bf16" else torch.float32
+    s = torch.cuda.current_stream()
+    bufs = [torch.empty(w.P, dtype=tdt, device="cuda") for _ in range(w.K)]
+    for k in range(w.K):
+        synth.client_fill_device(w, k, 0, w.P, bufs[k].data_ptr(), s.cuda_stream)
+    out = torch.empty(w.P, dtype=torch.int16 if w.dtype_out == "bf16" else torch.float32,
+                      device="cuda")
+    ctx = fa.fa_open([(n, m) for (n, _), m in zip(w.keys, w.numels)], w.dtype_in, w.dtype_out,
+                     w.K, flags=fa.FA_FLAT_OUT)
+    try:
+        fa.fa_reduce_resident(ctx, list(range(w.K)), w.weights, [b.data_ptr() for b in bufs],
+                              [out], s.cuda_stream)
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+    finally:
+        fa.fa_close(ctx)
+    del bufs
+    torch.cuda.empty_cache()
+    return out
+
+
 def algorithmic_bytes(w):
     """Per round, streaming path: first client s_in+4, later clients s_in+8,
     finalize 4+s_out bytes per element (all clients send every key here)."""
@@ -481,7 +510,8 @@ def run_e2e(args, w, layout, s, pg, world):
         t[:n].numpy().view(a.dtype)[:] = a
         pool.append(t)
     out = torch.empty(w.P, dtype=torch.int16 if so == 2 else torch.float32).pin_memory()
-    ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
+    ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT,
+                     ring_slots=args.ring_slots, slot_bytes=args.slot_mb << 20)
     sh = s.cuda_stream
 
     def step():
@@ -517,7 +547,8 @@ def run_e2e(args, w, layout, s, pg, world):
     return {"value": round(v, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
             "ms_per_step": round(dt / args.e2e_steps * 1e3, 2),
-            "host_pool": f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused"}
+            "host_pool": f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused",
+            "staging": f"{args.ring_slots or 4} device slots of {args.slot_mb or 64} MiB"}
 
 
 def main(argv=None):
@@ -532,6 +563,8 @@ def main(argv=None):
     ap.add_argument("--ref-elems", type=int, default=64 << 20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-resident", action="store_true")
+    ap.add_argument("--ring-slots", type=int, default=0, help="e2e staging slots (0 = library default)")
+    ap.add_argument("--slot-mb", type=int, default=0, help="e2e staging slot size in MiB (0 = default)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

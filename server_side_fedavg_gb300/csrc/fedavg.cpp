@@ -18,6 +18,7 @@
 #include <fedavg.h>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <chrono>
@@ -81,6 +82,13 @@ struct fa_ctx {
 };
 
 namespace {
+
+// An NVTX range over one library call (visible to Nsight tools, free otherwise).
+class Range {
+public:
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+};
 
 // Switches to the context's device for the duration of a call.
 class DeviceGuard {
@@ -456,6 +464,7 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
 fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64_t key,
                         uint64_t offset_elems, const void* chunk_ptr, uint64_t len_elems,
                         void* stream) {
+    Range range("fa_accumulate");
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
     DeviceGuard dg(ctx->device);
@@ -468,6 +477,7 @@ fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64
 fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
                               const double* weights, int64_t key, uint64_t offset_elems,
                               const void* const* chunk_ptrs, uint64_t len_elems, void* stream) {
+    Range range("fa_accumulate_batch");
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
     DeviceGuard dg(ctx->device);
@@ -595,6 +605,7 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
 extern "C" {
 
 fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
+    Range range("fa_finalize");
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
     DeviceGuard dg(ctx->device);
@@ -604,6 +615,7 @@ fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream) {
 
 fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* const* out_ptrs,
                             double server_lr, void* stream) {
+    Range range("fa_finalize_apply");
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
     DeviceGuard dg(ctx->device);
@@ -616,6 +628,7 @@ fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* con
 fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
                              const double* weights, const void* const* flat_ptrs,
                              void* const* out_ptrs, void* stream) {
+    Range range("fa_reduce_resident");
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
     DeviceGuard dg(ctx->device);
@@ -728,6 +741,7 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
 }
 
 fa_status fa_reset(fa_ctx* ctx) {
+    Range range("fa_reset");
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
     DeviceGuard dg(ctx->device);
@@ -762,6 +776,7 @@ fa_status fa_key_total(const fa_ctx* ctx, uint32_t key, double* sum_nk, uint32_t
 }
 
 fa_status fa_sync(fa_ctx* ctx) {
+    Range range("fa_sync");
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
     DeviceGuard dg(ctx->device);

@@ -238,6 +238,9 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
         blockIdx.x < a.ntiles ? (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     if (threadIdx.x == 0) mbar_init(bars, kStages);
     __syncthreads();
+    // launched as a programmatic dependent: set-up above overlaps the previous kernel's
+    // tail; nothing in global memory is touched before that kernel has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const Tin* x0 = static_cast<const Tin*>(a.x[0]);
     const float w = a.w[0];
     uint32_t pcur = 0, ccur = 0;      // segment cursors of the producer and the consumers
@@ -372,6 +375,7 @@ __global__ void __launch_bounds__(kBlock, 1) reduce_bulk_kernel(const __grid_con
         blockIdx.x < a.ntiles ? (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     if (threadIdx.x == 0) mbar_init(bars, kStages);
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // see accumulate_bulk_kernel
     uint32_t pcur = 0, ccur = 0, issued = 0;
 
     auto issue = [&](uint32_t i) {    // thread 0 only
@@ -594,6 +598,25 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
 }
 
 // ----------------------------------------------------------------- host side
+// Launch as a programmatic dependent of the previous kernel on the stream: its launch
+// and prologue overlap that kernel's tail (the kernel itself waits, with
+// griddepcontrol.wait, before reading or writing global memory).
+template <typename Arg>
+cudaError_t launch_dependent(void (*kern)(Arg), uint32_t grid, size_t smem, cudaStream_t stream,
+                             const Arg& arg) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kBlock);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, arg);
+}
+
 template <typename Seg>
 bool number_tiles(Seg* segs, uint32_t nseg, uint64_t tile, uint32_t* ntiles) {
     uint64_t t = 0;
@@ -629,21 +652,17 @@ cudaError_t launch_reduce_t(RedArgs a, int per_sm, int sms, cudaStream_t stream)
     if (a.ntiles == 0) return cudaSuccess;
     const size_t smem = static_cast<size_t>(kStages) * a.tile * eb + kStages * sizeof(uint64_t);
     const uint32_t grid = grid_for(a.ntiles, sms, per_sm);
-    if (a.J == 16)
-        reduce_bulk_kernel<Tin, Tout, kFinal, 16><<<grid, kBlock, smem, stream>>>(a);
-    else if (a.J == 8)
-        reduce_bulk_kernel<Tin, Tout, kFinal, 8><<<grid, kBlock, smem, stream>>>(a);
-    else
-        reduce_bulk_kernel<Tin, Tout, kFinal, 0><<<grid, kBlock, smem, stream>>>(a);
-    return cudaGetLastError();
+    if (a.J == 16) return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 16>, grid, smem, stream, a);
+    if (a.J == 8) return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 8>, grid, smem, stream, a);
+    return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 0>, grid, smem, stream, a);
 }
 
 template <typename Tin>
 cudaError_t launch_stream_t(AccArgs a, int per_sm, int sms, cudaStream_t stream) {
     if (!number_tiles(a.seg, a.nseg, kBulkTile, &a.ntiles)) return cudaErrorInvalidValue;
     if (a.ntiles == 0) return cudaSuccess;
-    accumulate_bulk_kernel<Tin><<<grid_for(a.ntiles, sms, per_sm), kBlock, bulk_smem_bytes<Tin>(), stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(accumulate_bulk_kernel<Tin>, grid_for(a.ntiles, sms, per_sm),
+                            bulk_smem_bytes<Tin>(), stream, a);
 }
 
 RedArgs to_reduce_args(const AccArgs& a) {

@@ -208,3 +208,26 @@ def test_full_size_streamed_sampled(name):
     want, N, cnt = oracle.fedavg_key(w.weights, [True] * w.K, xs, w.dtype_in, w.dtype_out)
     frac = check_bf16(got, want, name)
     print(f"{name}: {idx.size} sampled elements, {frac:.6%} bit-identical")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["vlm2b", "llama7b"])
+def test_full_size_resident_sampled(name):
+    """fa_reduce_resident over every client's full update resident in HBM (the bench's
+    `resident` configuration), sampled against the oracle."""
+    import bench
+    w = W.make(name)
+    free, _ = torch.cuda.mem_get_info()
+    need = w.K * w.P * 2 + w.P * 2 + w.P * 4 + (8 << 30)
+    if free < need:
+        pytest.fail(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
+    idx = _sample_indices(w, seed=2)
+    out = bench.run_resident_round(w)
+    got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+    assert bool(torch.isfinite(out.view(torch.bfloat16)).all())
+    del out
+    torch.cuda.empty_cache()
+    xs = [synth.client_gather(w, k, idx) for k in range(w.K)]
+    want, N, cnt = oracle.fedavg_key(w.weights, [True] * w.K, xs, w.dtype_in, w.dtype_out)
+    frac = check_bf16(got, want, name)
+    print(f"{name} resident: {idx.size} sampled elements, {frac:.6%} bit-identical")
