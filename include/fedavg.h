@@ -134,7 +134,10 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
  * Ownership: device and pinned-host chunks are read in order on `stream`: the caller
  * must not overwrite them until the work this call queued on `stream` has completed.
  * Pageable-host chunks have been copied into library staging when the call returns.
- * len_elems == 0 is a no-op.  Nothing is changed when an error is returned.
+ * len_elems == 0 is a no-op.  Argument, range, weight and state errors change nothing.
+ * A CUDA failure or timeout after the chunk was accepted (FA_ERR_CUDA, FA_ERR_TIMEOUT,
+ * FA_ERR_NOMEM) leaves the round inconsistent: every later call returns FA_ERR_CUDA
+ * until fa_reset.
  * Errors: FA_ERR_ARG, FA_ERR_RANGE, FA_ERR_WEIGHT, FA_ERR_STATE, FA_ERR_CUDA,
  * FA_ERR_TIMEOUT, FA_ERR_NOMEM. */
 fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64_t key,

@@ -362,49 +362,116 @@ __device__ __forceinline__ void red_one(const RedArgs& a, const RedSeg& sg, uint
         a.acc[sg.acc_idx + e] = r;
 }
 
+// Warp-specialised: warps 0-7 compute, warp 8 (one lane) moves data.  Per stage two
+// mbarriers: `full` (the producer arms it with the byte count of the stage's bulk loads)
+// and `done` (each compute warp arrives once it has finished the stage).  The producer
+// stores a stage's result tile when `done` completes and refills the stage once that
+// store has read it; the compute warps never wait for producer work except data.
+constexpr int kReduceWarps = kBlock / 32;               // compute warps
+constexpr int kReduceThreads = kBlock + 32;             // + one producer warp
+
 template <typename Tin, typename Tout, bool kFinal, int kJ>
-__global__ void __launch_bounds__(kBlock, 1) reduce_bulk_kernel(const __grid_constant__ RedArgs a) {
+__global__ void __launch_bounds__(kReduceThreads, 1) reduce_bulk_kernel(const __grid_constant__ RedArgs a) {
     const uint32_t T = a.tile;
     const uint32_t J = kJ > 0 ? static_cast<uint32_t>(kJ) : a.J;
     const uint32_t XB = T * sizeof(Tin);
     const uint32_t SB = a.has_sum ? T * static_cast<uint32_t>(sizeof(float)) : 0u;
     const uint32_t stage = T * reduce_elem_bytes<kFinal, Tin, Tout>(J, a.has_sum != 0);
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * stage);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage);
+    uint64_t* done = full + kStages;
     const uint32_t count =
         blockIdx.x < a.ntiles ? (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    if (threadIdx.x == 0) mbar_init(bars, kStages);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s])) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&done[s])),
+                         "r"(kReduceWarps) : "memory");
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");   // see accumulate_bulk_kernel
-    uint32_t pcur = 0, ccur = 0, issued = 0;
 
-    auto issue = [&](uint32_t i) {    // thread 0 only
-        const uint32_t s = i % kStages;
-        const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + i * gridDim.x, T, pcur);
-        const RedSeg& sg = a.seg[ta.si];
-        const uint32_t bar = smem_addr(&bars[s]);
-        const uint32_t n8 = ta.cnt / kVec;
-        if (((a.vec_ok >> ta.si) & 1ull) && n8 > 0) {
-            const uint32_t xb = n8 * kVec * sizeof(Tin);
-            const uint32_t sb = sg.read_sum ? n8 * kVec * 4u : 0u;
-            mbar_expect(bar, J * xb + sb);
+    if (threadIdx.x >= static_cast<unsigned>(kBlock)) {
+        // ------------------------------------------------------------ producer
+        if (threadIdx.x != static_cast<unsigned>(kBlock)) return;
+        uint32_t cur = 0, scur = 0;     // segment cursors for loads and for stores
+        bool ok = true;
+        auto store = [&](uint32_t i) {  // result tile of tile i, stage i % kStages
+            const uint32_t s = i % kStages;
+            const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + i * gridDim.x, T, scur);
+            const RedSeg& sg = a.seg[ta.si];
+            const uint32_t n8 = (((a.vec_ok >> ta.si) & 1ull) && ta.cnt >= static_cast<uint32_t>(kVec))
+                                    ? ta.cnt / kVec : 0u;
+            if (n8 == 0) return;
             uint8_t* st = smem + s * stage;
-            for (uint32_t j = 0; j < J; ++j)
-                bulk_load(st + j * XB, static_cast<const Tin*>(a.x[j]) + sg.x_off + ta.e0, xb, bar);
-            if (sb) bulk_load(st + J * XB, a.acc + sg.acc_idx + ta.e0, sb, bar);
-        } else {
-            mbar_arrive(bar);
+            if constexpr (kFinal)
+                bulk_store(static_cast<Tout*>(sg.out) + ta.e0, st + J * XB + SB, n8 * kVec * sizeof(Tout));
+            else
+                bulk_store(a.acc + sg.acc_idx + ta.e0, st + J * XB, n8 * kVec * 4u);
+        };
+        uint32_t stored = 0;
+        for (uint32_t j = 0; j < count && ok; ++j) {
+            const uint32_t s = j % kStages;
+            if (j >= static_cast<uint32_t>(kStages)) {
+                // stage s holds tile j - kStages: wait for the compute warps, store it,
+                // and wait until the store has read the stage before refilling it
+                ok = mbar_wait(smem_addr(&done[s]), ((j / kStages) - 1) & 1u);
+                if (!ok) break;
+                store(j - kStages);
+                bulk_commit();
+                stored = j - kStages + 1;
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            }
+            const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + j * gridDim.x, T, cur);
+            const RedSeg& sg = a.seg[ta.si];
+            const uint32_t bar = smem_addr(&full[s]);
+            const uint32_t n8 = ta.cnt / kVec;
+            if (((a.vec_ok >> ta.si) & 1ull) && n8 > 0) {
+                const uint32_t xb = n8 * kVec * sizeof(Tin);
+                const uint32_t sb = sg.read_sum ? n8 * kVec * 4u : 0u;
+                mbar_expect(bar, J * xb + sb);
+                uint8_t* st = smem + s * stage;
+#pragma unroll
+                for (uint32_t jj = 0; jj < (kJ > 0 ? static_cast<uint32_t>(kJ) : static_cast<uint32_t>(kMaxBatch)); ++jj) {
+                    if (kJ == 0 && jj >= J) break;
+                    bulk_load(st + jj * XB, static_cast<const Tin*>(a.x[jj]) + sg.x_off + ta.e0, xb, bar);
+                }
+                if (sb) bulk_load(st + J * XB, a.acc + sg.acc_idx + ta.e0, sb, bar);
+            } else {
+                mbar_arrive(bar);
+            }
         }
-    };
-
-    if (threadIdx.x == 0) {
-        for (uint32_t i = 0; i < count && i < static_cast<uint32_t>(kStages); ++i) issue(i);
-        issued = count < static_cast<uint32_t>(kStages) ? count : static_cast<uint32_t>(kStages);
+        // the last stages: wait for the compute warps and store
+        for (uint32_t i = stored; i < count && ok; ++i) {
+            ok = mbar_wait(smem_addr(&done[i % kStages]), (i / kStages) & 1u);
+            if (ok) {
+                store(i);
+                bulk_commit();
+            }
+        }
+        if (!ok) {
+            // a wait gave up: flag it, and let every load issued so far land before
+            // the CTA's shared memory can be released
+            atomicOr(&g_device_error, kErrWaitTimeout);
+            const uint32_t last = count < stored + kStages ? count : stored + kStages;
+            for (uint32_t i = stored; i < last; ++i)
+                mbar_wait(smem_addr(&full[i % kStages]), (i / kStages) & 1u);
+        }
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        return;
     }
-    uint32_t consumed = 0;
+
+    // ---------------------------------------------------------------- compute warps
+    uint32_t ccur = 0;
+    const uint32_t lane = threadIdx.x & 31u;
     for (uint32_t i = 0; i < count; ++i) {
         const uint32_t s = i % kStages;
-        const bool ok = mbar_wait(smem_addr(&bars[s]), (i / kStages) & 1u);
+        if (!mbar_wait(smem_addr(&full[s]), (i / kStages) & 1u)) {
+            atomicOr(&g_device_error, kErrWaitTimeout);
+            break;
+        }
         const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + i * gridDim.x, T, ccur);
         const RedSeg& sg = a.seg[ta.si];
         const bool bulk = ((a.vec_ok >> ta.si) & 1ull) && ta.cnt >= static_cast<uint32_t>(kVec);
@@ -412,7 +479,7 @@ __global__ void __launch_bounds__(kBlock, 1) reduce_bulk_kernel(const __grid_con
         uint8_t* st = smem + s * stage;
         float4* sum = reinterpret_cast<float4*>(st + J * XB);
         uint8_t* res = st + J * XB + SB;                      // final mode output tile
-        if (ok && bulk) {
+        if (bulk) {
             for (uint32_t v = threadIdx.x; v < n8; v += kBlock) {
                 float r[8];
                 {
@@ -450,34 +517,20 @@ __global__ void __launch_bounds__(kBlock, 1) reduce_bulk_kernel(const __grid_con
             }
             const uint32_t tail = ta.cnt - n8 * kVec;
             if (threadIdx.x < tail) red_one<Tin, Tout, kFinal>(a, sg, ta.e0 + n8 * kVec + threadIdx.x, J);
-        } else if (ok) {
+        } else {
             for (uint32_t e = threadIdx.x; e < ta.cnt; e += kBlock)
                 red_one<Tin, Tout, kFinal>(a, sg, ta.e0 + e, J);
         }
+        // shared-memory results become visible to the bulk store (async proxy); the
+        // warp's lane 0 then reports the stage done
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (!__syncthreads_and(ok)) break;
-        consumed = i + 1;
-        if (threadIdx.x == 0) {
-            if (n8 > 0) {
-                if constexpr (kFinal)
-                    bulk_store(static_cast<Tout*>(sg.out) + ta.e0, res, n8 * kVec * sizeof(Tout));
-                else
-                    bulk_store(a.acc + sg.acc_idx + ta.e0, sum, n8 * kVec * 4u);
-            }
-            bulk_commit();
-            if (i >= 1 && i - 1 + kStages < count) {
-                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                issue(i - 1 + kStages);
-                issued = i + kStages;
-            }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&done[s]));
     }
-    if (threadIdx.x == 0) pipeline_drain(bars, consumed, issued, count);
-    __syncthreads();
 }
 
 constexpr size_t kReduceSmemBytes =
-    static_cast<size_t>(kStages) * kReduceStageBytes + kStages * sizeof(uint64_t);
+    static_cast<size_t>(kStages) * kReduceStageBytes + 2 * kStages * sizeof(uint64_t);
 
 // ----------------------------------------------------------------- finalize
 template <typename Tout>
@@ -602,11 +655,11 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
 // and prologue overlap that kernel's tail (the kernel itself waits, with
 // griddepcontrol.wait, before reading or writing global memory).
 template <typename Arg>
-cudaError_t launch_dependent(void (*kern)(Arg), uint32_t grid, size_t smem, cudaStream_t stream,
-                             const Arg& arg) {
+cudaError_t launch_dependent(void (*kern)(Arg), uint32_t grid, uint32_t block, size_t smem,
+                             cudaStream_t stream, const Arg& arg) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kBlock);
+    cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
@@ -650,18 +703,20 @@ cudaError_t launch_reduce_t(RedArgs a, int per_sm, int sms, cudaStream_t stream)
     a.tile = reduce_tile(eb);
     if (!number_tiles(a.seg, a.nseg, a.tile, &a.ntiles)) return cudaErrorInvalidValue;
     if (a.ntiles == 0) return cudaSuccess;
-    const size_t smem = static_cast<size_t>(kStages) * a.tile * eb + kStages * sizeof(uint64_t);
+    const size_t smem = static_cast<size_t>(kStages) * a.tile * eb + 2 * kStages * sizeof(uint64_t);
     const uint32_t grid = grid_for(a.ntiles, sms, per_sm);
-    if (a.J == 16) return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 16>, grid, smem, stream, a);
-    if (a.J == 8) return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 8>, grid, smem, stream, a);
-    return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 0>, grid, smem, stream, a);
+    if (a.J == 16)
+        return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 16>, grid, kReduceThreads, smem, stream, a);
+    if (a.J == 8)
+        return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 8>, grid, kReduceThreads, smem, stream, a);
+    return launch_dependent(reduce_bulk_kernel<Tin, Tout, kFinal, 0>, grid, kReduceThreads, smem, stream, a);
 }
 
 template <typename Tin>
 cudaError_t launch_stream_t(AccArgs a, int per_sm, int sms, cudaStream_t stream) {
     if (!number_tiles(a.seg, a.nseg, kBulkTile, &a.ntiles)) return cudaErrorInvalidValue;
     if (a.ntiles == 0) return cudaSuccess;
-    return launch_dependent(accumulate_bulk_kernel<Tin>, grid_for(a.ntiles, sms, per_sm),
+    return launch_dependent(accumulate_bulk_kernel<Tin>, grid_for(a.ntiles, sms, per_sm), kBlock,
                             bulk_smem_bytes<Tin>(), stream, a);
 }
 
@@ -700,7 +755,7 @@ cudaError_t prepare_reduce_j(int* occ) {
                                          static_cast<int>(kReduceSmemBytes));
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, reduce_bulk_kernel<Tin, Tout, kFinal, kJ>,
-                                                         kBlock, kReduceSmemBytes);
+                                                         kReduceThreads, kReduceSmemBytes);
 }
 
 template <typename Tin, typename Tout, bool kFinal>
