@@ -73,6 +73,10 @@ struct fa_ctx {
     bool fin_pending = false;
     void* out_stage = nullptr;
 
+    cudaStream_t err_stream = nullptr;   // private non-blocking stream for the error word
+    cudaEvent_t err_ev = nullptr;
+    unsigned int* err_host = nullptr;    // pinned copy of the device error word
+
     bool broken = false;          // a CUDA call failed after the ledger was updated
     bool reduced = false;         // this round was written by fa_reduce_resident
     fa_stats stats{};
@@ -185,23 +189,50 @@ fa_status chain_out(fa_ctx* c, cudaStream_t s) {
     return FA_OK;
 }
 
+// Allocate the staging ring (device slots, events, copy stream) and, when a pageable
+// source needs them, the pinned host slots.  All or nothing: after a failure nothing is
+// kept, so a later call can try again.
 fa_status ensure_ring(fa_ctx* c, bool need_host) {
     if (c->dev_slot.empty()) {
-        FA_CUDA(c, cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking));
-        c->dev_slot.assign(c->slots, nullptr);
-        c->host_slot.assign(c->slots, nullptr);
-        c->ev_copied.assign(c->slots, nullptr);
-        c->ev_free.assign(c->slots, nullptr);
-        c->slot_used.assign(c->slots, 0);
-        for (uint32_t i = 0; i < c->slots; ++i) {
-            FA_CUDA(c, cudaMalloc(&c->dev_slot[i], c->slot_bytes));
-            FA_CUDA(c, cudaEventCreateWithFlags(&c->ev_copied[i], cudaEventDisableTiming));
-            FA_CUDA(c, cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming));
+        std::vector<void*> dev(c->slots, nullptr);
+        std::vector<cudaEvent_t> copied(c->slots, nullptr), freed(c->slots, nullptr);
+        cudaStream_t cs = nullptr;
+        cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+        for (uint32_t i = 0; e == cudaSuccess && i < c->slots; ++i) {
+            e = cudaMalloc(&dev[i], c->slot_bytes);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&copied[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&freed[i], cudaEventDisableTiming);
         }
+        if (e != cudaSuccess) {
+            for (void* p : dev)
+                if (p) cudaFree(p);
+            for (auto ev : copied)
+                if (ev) cudaEventDestroy(ev);
+            for (auto ev : freed)
+                if (ev) cudaEventDestroy(ev);
+            if (cs) cudaStreamDestroy(cs);
+            cudaGetLastError();
+            return cuda_fail(c, e, "staging ring");
+        }
+        c->copy_stream = cs;
+        c->dev_slot = dev;
+        c->ev_copied = copied;
+        c->ev_free = freed;
+        c->host_slot.assign(c->slots, nullptr);
+        c->slot_used.assign(c->slots, 0);
     }
     if (need_host && c->host_slot[0] == nullptr) {
-        for (uint32_t i = 0; i < c->slots; ++i)
-            FA_CUDA(c, cudaHostAlloc(&c->host_slot[i], c->slot_bytes, cudaHostAllocDefault));
+        std::vector<void*> host(c->slots, nullptr);
+        cudaError_t e = cudaSuccess;
+        for (uint32_t i = 0; e == cudaSuccess && i < c->slots; ++i)
+            e = cudaHostAlloc(&host[i], c->slot_bytes, cudaHostAllocDefault);
+        if (e != cudaSuccess) {
+            for (void* p : host)
+                if (p) cudaFreeHost(p);
+            cudaGetLastError();
+            return cuda_fail(c, e, "pinned staging");
+        }
+        c->host_slot = host;
     }
     return FA_OK;
 }
@@ -279,6 +310,11 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
             kind = m;
         }
     }
+    if (len > 0 && kind != Mem::kDevice) {
+        // staging first: a failed allocation must not leave the round half-recorded
+        fa_status rr = ensure_ring(c, kind == Mem::kPageable);
+        if (rr != FA_OK) return rr;
+    }
     std::string e;
     int32_t st = c->ledger.plan_accumulate(ids, weights, J, key, offset, len, &c->pieces, &e);
     if (st != fa::kOk) return fail(c, st, e);
@@ -295,7 +331,6 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
         if (r == FA_OK) r = chain_out(c, s);
     } else {
         // host memory: through the staging ring, slot-sized pieces
-        r = ensure_ring(c, kind == Mem::kPageable);
         const uint64_t per = c->slot_bytes / c->s_in;
         const char* src0 = static_cast<const char*>(ptrs[0]);
         if (r == FA_OK && kind == Mem::kPinned) {
@@ -366,6 +401,9 @@ void free_ctx(fa_ctx* c) {
     if (c->fin_dev) cudaFree(c->fin_dev);
     if (c->fin_host) cudaFreeHost(c->fin_host);
     if (c->out_stage) cudaFree(c->out_stage);
+    if (c->err_ev) cudaEventDestroy(c->err_ev);
+    if (c->err_stream) cudaStreamDestroy(c->err_stream);
+    if (c->err_host) cudaFreeHost(c->err_host);
     delete c;
 }
 
@@ -379,8 +417,13 @@ fa_status sync_impl(fa_ctx* c) {
         fa_status r = wait_event(c, c->ev_copied[k], "fa_sync (copy)");
         if (r != FA_OK) return r;
     }
-    unsigned int code = 0;
-    FA_CUDA(c, fa::take_device_error(&code));
+    // the device error word, read on a private stream and waited for with the same bound
+    *c->err_host = 0;
+    FA_CUDA(c, fa::take_device_error_async(c->err_host, c->err_stream));
+    FA_CUDA(c, cudaEventRecord(c->err_ev, c->err_stream));
+    fa_status rw = wait_event(c, c->err_ev, "fa_sync (error word)");
+    if (rw != FA_OK) return rw;
+    const unsigned int code = *c->err_host;
     if (code != 0) {
         c->broken = true;
         return fail(c, FA_ERR_INTERNAL, "a device-side wait gave up (bounded mbarrier wait): results of this round are invalid");
@@ -452,6 +495,10 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->fin_ev, cudaEventDisableTiming);
     if (ce == cudaSuccess) ce = cudaMalloc(&c->fin_dev, sizeof(fa::FinSeg) * n_keys);
     if (ce == cudaSuccess) ce = cudaHostAlloc(&c->fin_host, sizeof(fa::FinSeg) * n_keys, cudaHostAllocDefault);
+    if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&c->err_stream, cudaStreamNonBlocking);
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->err_ev, cudaEventDisableTiming);
+    if (ce == cudaSuccess)
+        ce = cudaHostAlloc(reinterpret_cast<void**>(&c->err_host), sizeof(unsigned int), cudaHostAllocDefault);
     if (ce != cudaSuccess) {
         cudaGetLastError();
         free_ctx(c);

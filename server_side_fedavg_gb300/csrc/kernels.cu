@@ -780,11 +780,14 @@ cudaError_t prepare_stream(int* occ) {
 
 }  // namespace
 
-cudaError_t take_device_error(unsigned int* code) {
-    unsigned int zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned int));
-    if (e == cudaSuccess && *code != 0) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
-    return e;
+cudaError_t take_device_error_async(unsigned int* host, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(host, g_device_error, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    void* word = nullptr;
+    e = cudaGetSymbolAddress(&word, g_device_error);
+    if (e != cudaSuccess) return e;
+    return cudaMemsetAsync(word, 0, sizeof(unsigned int), stream);
 }
 
 cudaError_t query_launch_shape(LaunchShape* s) {

@@ -92,8 +92,9 @@ struct LaunchShape {
 // Device-side error bits (file-scope word shared by every launch on a device).
 constexpr unsigned int kErrWaitTimeout = 1u;   // a bounded mbarrier wait gave up
 
-// Reads and clears the device error word of the current device.
-cudaError_t take_device_error(unsigned int* code);
+// Queue on `stream` a copy of the current device's error word into *host (pinned) followed
+// by clearing it; the caller waits for the stream before reading *host.
+cudaError_t take_device_error_async(unsigned int* host, cudaStream_t stream);
 
 // Fills the occupancy table for the current device (and sets the kernels'
 // shared-memory limits).

@@ -92,9 +92,13 @@ def np_dtype(dtype: str):
     return np.float32 if dtype == F32 else np.uint16
 
 
-def fill(seed, client, dist, sigma, dtype, first, n, threads=None) -> np.ndarray:
-    """Elements first..first+n-1 of client `client`'s stream (uint16 bits for bf16)."""
-    out = np.empty(n, dtype=np_dtype(dtype))
+def fill(seed, client, dist, sigma, dtype, first, n, threads=None, out=None) -> np.ndarray:
+    """Elements first..first+n-1 of client `client`'s stream (uint16 bits for bf16),
+    into `out` if given (a contiguous array of n elements of the stored dtype)."""
+    if out is None:
+        out = np.empty(n, dtype=np_dtype(dtype))
+    elif out.size != n or out.dtype != np.dtype(np_dtype(dtype)) or not out.flags.c_contiguous:
+        raise ValueError("out must be a contiguous array of n elements of the stored dtype")
     lib = host_lib()
     code = _dtype_code(dtype)
     threads = threads or min(32, os.cpu_count() or 1)
@@ -138,9 +142,9 @@ def to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
 
 
 # ------------------------------------------------------------ workload helpers
-def client_flat(w, k, first, n, threads=None) -> np.ndarray:
+def client_flat(w, k, first, n, threads=None, out=None) -> np.ndarray:
     """Client k's values for flat (unpadded, layout-order) elements first..first+n-1."""
-    return fill(w.seed, k, w.dists[k], w.sigma, w.dtype_in, first, n, threads)
+    return fill(w.seed, k, w.dists[k], w.sigma, w.dtype_in, first, n, threads, out)
 
 
 def client_key(w, k, p) -> np.ndarray:

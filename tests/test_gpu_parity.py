@@ -231,3 +231,35 @@ def test_full_size_resident_sampled(name):
     want, N, cnt = oracle.fedavg_key(w.weights, [True] * w.K, xs, w.dtype_in, w.dtype_out)
     frac = check_bf16(got, want, name)
     print(f"{name} resident: {idx.size} sampled elements, {frac:.6%} bit-identical")
+
+
+@pytest.mark.slow
+def test_full_size_host_fed_sampled():
+    """The 2.2B VLM streamed client by client from PINNED HOST memory in 64 MiB flat
+    chunks, through the library's staging ring (the bench's end-to-end path), sampled
+    against the oracle."""
+    w = W.make("vlm2b")
+    idx = _sample_indices(w, seed=3)
+    host = torch.empty(w.P, dtype=torch.int16).pin_memory()
+    hv = host.numpy().view(np.uint16)
+    ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
+    try:
+        s = torch.cuda.current_stream()
+        for k in range(w.K):
+            synth.client_flat(w, k, 0, w.P, out=hv)
+            for c0 in range(0, w.P, w.chunk_elems):
+                n = min(w.chunk_elems, w.P - c0)
+                fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, host.data_ptr() + 2 * c0, n, s)
+            s.synchronize()              # the DMA reads the pinned buffer: wait before refilling it
+        out = torch.empty(w.P, dtype=torch.int16, device="cuda")
+        fa.fa_finalize(ctx, [out], s)
+        fa.fa_sync(ctx)
+        st = fa.fa_get_stats(ctx)
+        assert st["h2d_bytes"] == w.K * w.P * 2
+    finally:
+        fa.fa_close(ctx)
+    got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+    xs = [synth.client_gather(w, k, idx) for k in range(w.K)]
+    want, N, cnt = oracle.fedavg_key(w.weights, [True] * w.K, xs, w.dtype_in, w.dtype_out)
+    frac = check_bf16(got, want, "vlm2b host-fed")
+    print(f"vlm2b host-fed: {idx.size} sampled elements, {frac:.6%} bit-identical")
