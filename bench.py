@@ -487,9 +487,23 @@ def run_ours(args, world, rank, local, pg):
     return 0
 
 
+def host_mem_available():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def run_e2e(args, w, layout, s, pg, world):
     """Client chunks from pinned host memory (a pool of distinct chunks, reused),
-    aggregate written to a pinned host buffer; copies inside the timed region."""
+    aggregate written to a pinned host buffer; copies inside the timed region.
+    Pinned memory is sized to this rank's share of the node's available memory
+    (ranks on one node share it); if it does not fit, the pool shrinks and the
+    output falls back to pageable memory."""
     import torch
 
     import server_side_fedavg_gb300 as fa
@@ -500,6 +514,16 @@ def run_e2e(args, w, layout, s, pg, world):
     ce = w.chunk_elems or w.P
     nchunk = -(-w.P // ce)
     pool_n = min(args.e2e_pool, w.K * nchunk)
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", str(world)))
+    avail = host_mem_available()
+    budget = None if avail is None else int(0.4 * avail / max(1, local_world))
+    out_pinned = True
+    if budget is not None:
+        out_bytes = w.P * so
+        while pool_n > 2 and pool_n * ce * si + out_bytes > budget:
+            pool_n //= 2
+        if pool_n * ce * si + out_bytes > budget:
+            out_pinned = False
     pool = []
     for i in range(pool_n):
         k, c = divmod(i, nchunk)
@@ -509,7 +533,9 @@ def run_e2e(args, w, layout, s, pg, world):
         a = synth.client_flat(w, k, c0, n)
         t[:n].numpy().view(a.dtype)[:] = a
         pool.append(t)
-    out = torch.empty(w.P, dtype=torch.int16 if so == 2 else torch.float32).pin_memory()
+    out = torch.empty(w.P, dtype=torch.int16 if so == 2 else torch.float32)
+    if out_pinned:
+        out = out.pin_memory()
     ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT,
                      ring_slots=args.ring_slots, slot_bytes=args.slot_mb << 20)
     sh = s.cuda_stream
@@ -548,6 +574,7 @@ def run_e2e(args, w, layout, s, pg, world):
             "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
             "ms_per_step": round(dt / args.e2e_steps * 1e3, 2),
             "host_pool": f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused",
+            "output": "pinned host buffer" if out_pinned else "pageable host buffer (pinned budget too small)",
             "staging": f"{args.ring_slots or 4} device slots of {args.slot_mb or 64} MiB"}
 
 
