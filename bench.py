@@ -248,9 +248,11 @@ def cpu_pass(w, xs, threads):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, elems, min_seconds=10.0, threads=None):
+def cpu_baseline(w, elems, min_seconds=10.0, threads=None, min_seconds_1t=3.0):
     """Oracle throughput on the host cores: passes over a bounded sample until
-    at least `min_seconds` of wall time; inputs are made before timing."""
+    at least `min_seconds` of wall time; inputs are made before timing.  The same
+    oracle on one thread (a quarter of the sample, at least `min_seconds_1t`) is
+    reported beside it."""
     threads = threads or (os.cpu_count() or 1)
     xs = cpu_sample(w, elems)
     si = 2 if w.dtype_in == "bf16" else 4
@@ -259,10 +261,19 @@ def cpu_baseline(w, elems, min_seconds=10.0, threads=None):
         dt += cpu_pass(w, xs, threads)
         passes += 1
     gbs = passes * w.K * elems * si / dt / 1e9
+    q = max(1, elems // 4)
+    xq = [x[:q] for x in xs]
+    p1, dt1 = 0, 0.0
+    while dt1 < min_seconds_1t:
+        dt1 += cpu_pass(w, xq, 1)
+        p1 += 1
+    gbs1 = p1 * w.K * q * si / dt1 / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "value_1thread": round(gbs1, 3),
             "sample": f"{w.name}: first {elems} flat elements x {w.K} clients "
                       f"({w.K * elems * si / 1e9:.2f} GB of client bytes), fp64 C oracle, "
-                      f"{passes} passes in {dt:.1f} s on {threads} threads"}
+                      f"{passes} passes in {dt:.1f} s on {threads} threads; 1 thread: first {q} "
+                      f"elements, {p1} passes in {dt1:.1f} s"}
 
 
 # --------------------------------------------------------------------------- distributed bits
@@ -445,7 +456,7 @@ def run_ours(args, world, rank, local, pg):
                          "hbm_frac": round(rbytes / (rms * 1e-3) / 1e9 / peak, 4),
                          "bytes_per_round": int(rbytes),
                          "launches_per_round": int((fa.fa_get_stats(ctx)["kernel_launches"] - l0) // args.steps),
-                         "kernel": "reduce_bulk_kernel<bf16,bf16,final>"}
+                         "kernel": f"reduce_bulk_kernel<{w.dtype_in},{w.dtype_out},final>"}
 
     fa.fa_close(ctx)
     del bufs, out
@@ -469,7 +480,7 @@ def run_ours(args, world, rank, local, pg):
                    "hbm_frac_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4),
                    "finalize_gbs": round(fin_gbs, 1),
                    "wall_s": round(wall, 3)},
-        "roofline": {"bound": "hbm", "kernel": "accumulate_kernel<bf16,1>",
+        "roofline": {"bound": "hbm", "kernel": f"accumulate_bulk_kernel<{w.dtype_in}>",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": int(acc_bytes_per_launch),
@@ -496,6 +507,23 @@ def host_mem_available():
     except OSError:
         pass
     return None
+
+
+def h2d_peak(src, s, reps=8):
+    """Plain pinned-host -> device copy rate of one buffer (GB/s, CUDA events on s):
+    the host link's ceiling for the end-to-end number."""
+    import torch
+    dst = torch.empty_like(src, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        dst.copy_(src, non_blocking=True)
+        e0.record(s)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record(s)
+    e1.synchronize()
+    nbytes = src.numel() * src.element_size()
+    return reps * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
 
 
 def run_e2e(args, w, layout, s, pg, world):
@@ -539,6 +567,7 @@ def run_e2e(args, w, layout, s, pg, world):
     ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT,
                      ring_slots=args.ring_slots, slot_bytes=args.slot_mb << 20)
     sh = s.cuda_stream
+    link = h2d_peak(pool[0], s)
 
     def step():
         fa.fa_reset(ctx)
@@ -573,6 +602,8 @@ def run_e2e(args, w, layout, s, pg, world):
     return {"value": round(v, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
             "ms_per_step": round(dt / args.e2e_steps * 1e3, 2),
+            "h2d_peak_gbs": round(link, 1),
+            "link_frac": round(h2d * args.e2e_steps / dt / 1e9 / link, 3),
             "host_pool": f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused",
             "output": "pinned host buffer" if out_pinned else "pageable host buffer (pinned budget too small)",
             "staging": f"{args.ring_slots or 4} device slots of {args.slot_mb or 64} MiB"}
