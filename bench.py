@@ -564,13 +564,17 @@ def run_e2e(args, w, layout, s, pg, world):
     out = torch.empty(w.P, dtype=torch.int16 if so == 2 else torch.float32)
     if out_pinned:
         out = out.pin_memory()
-    ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT,
+    flags = fa.FA_FLAT_OUT | (fa.FA_STAGE_HOST if args.stage_host else 0)
+    ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=flags,
                      ring_slots=args.ring_slots, slot_bytes=args.slot_mb << 20)
     sh = s.cuda_stream
     link = h2d_peak(pool[0], s)
 
-    def step():
+    def step(evs=None):
+        # evs: (start, after the accumulate calls, after finalize) on the stream
         fa.fa_reset(ctx)
+        if evs is not None:
+            evs[0].record(s)
         i = 0
         for k in range(w.K):
             for c0 in range(0, w.P, ce):
@@ -578,9 +582,14 @@ def run_e2e(args, w, layout, s, pg, world):
                 fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0,
                                  pool[i % pool_n].data_ptr(), n, sh)
                 i += 1
+        if evs is not None:
+            evs[1].record(s)
         fa.fa_finalize(ctx, [out], sh)
+        if evs is not None:
+            evs[2].record(s)
         fa.fa_sync(ctx)
 
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.e2e_steps)]
     try:
         for _ in range(max(1, args.warmup // 2)):
             step()
@@ -588,25 +597,32 @@ def run_e2e(args, w, layout, s, pg, world):
         barrier(pg)
         st0 = fa.fa_get_stats(ctx)
         t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            step()
+        for i in range(args.e2e_steps):
+            step(ev_sets[i])
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
         st1 = fa.fa_get_stats(ctx)
         dt = max_over_ranks(pg, dt)
     finally:
         fa.fa_close(ctx)
+    acc_ms = sum(e[0].elapsed_time(e[1]) for e in ev_sets) / args.e2e_steps
+    fin_ms = sum(e[1].elapsed_time(e[2]) for e in ev_sets) / args.e2e_steps
     h2d = (st1["h2d_bytes"] - st0["h2d_bytes"]) // args.e2e_steps
     d2h = (st1["d2h_bytes"] - st0["d2h_bytes"]) // args.e2e_steps
     v = world * w.K * w.P * si * args.e2e_steps / dt / 1e9
     return {"value": round(v, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
             "ms_per_step": round(dt / args.e2e_steps * 1e3, 2),
+            "accumulate_ms": round(acc_ms, 1), "finalize_ms": round(fin_ms, 1),
             "h2d_peak_gbs": round(link, 1),
             "link_frac": round(h2d * args.e2e_steps / dt / 1e9 / link, 3),
+            "accumulate_link_frac": round(h2d / (acc_ms * 1e-3) / 1e9 / link, 3),
             "host_pool": f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused",
-            "output": "pinned host buffer" if out_pinned else "pageable host buffer (pinned budget too small)",
-            "staging": f"{args.ring_slots or 4} device slots of {args.slot_mb or 64} MiB"}
+            "output": (("pinned host buffer, " + ("copied from a device buffer" if args.stage_host
+                                                  else "written in place by the finalize kernel"))
+                       if out_pinned else "pageable host buffer (pinned budget too small)"),
+            "ingest": (f"staging ring: {args.ring_slots or 4} device slots of {args.slot_mb or 64} MiB"
+                       if args.stage_host else "pinned chunks read in place by the accumulate kernel")}
 
 
 def main(argv=None):
@@ -623,6 +639,8 @@ def main(argv=None):
     ap.add_argument("--no-resident", action="store_true")
     ap.add_argument("--ring-slots", type=int, default=0, help="e2e staging slots (0 = library default)")
     ap.add_argument("--slot-mb", type=int, default=0, help="e2e staging slot size in MiB (0 = default)")
+    ap.add_argument("--stage-host", action="store_true",
+                    help="e2e: pinned chunks through the staging ring instead of read in place")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

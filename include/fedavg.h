@@ -86,7 +86,10 @@ typedef struct fa_ctx fa_ctx;   /* opaque; owned by the library */
 #define FA_KEY_FLAT (-1)
 
 /* fa_opts.flags */
-#define FA_FLAT_OUT 1u   /* fa_finalize takes ONE output pointer to the flat layout */
+#define FA_FLAT_OUT   1u   /* fa_finalize takes ONE output pointer to the flat layout */
+#define FA_STAGE_HOST 2u   /* pinned host chunks go through the staging ring, and pinned
+                              host outputs through a device buffer and a copy (copy
+                              engine), even where the device could address them in place */
 
 typedef struct {
     uint32_t size;        /* sizeof(fa_opts): lets the struct grow */
@@ -95,14 +98,16 @@ typedef struct {
                              the chunk-size knob of [FLARE]'s Tensor Downloader, here a
                              trade of pinned/device staging memory against per-copy overhead */
     uint32_t timeout_ms;  /* bound on every host-side wait (0 = default 60000) */
-    uint32_t flags;       /* FA_FLAT_OUT */
+    uint32_t flags;       /* FA_FLAT_OUT | FA_STAGE_HOST */
 } fa_opts;
 
 typedef struct {
     uint64_t kernel_launches;   /* kernels this context has launched since fa_open */
     uint64_t client_bytes;      /* bytes of client updates accumulated */
-    uint64_t h2d_bytes;         /* bytes copied host -> device by the staging ring */
-    uint64_t d2h_bytes;         /* bytes copied device -> host by fa_finalize */
+    uint64_t h2d_bytes;         /* bytes of client updates brought from host memory (staging
+                                   copies and in-place reads of pinned memory) */
+    uint64_t d2h_bytes;         /* bytes of aggregate fa_finalize sent to host memory (copies,
+                                   and in-place stores into pinned memory) */
     uint64_t chunks;            /* accepted fa_accumulate / fa_accumulate_batch calls */
 } fa_stats;
 
@@ -134,6 +139,10 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
  * Ownership: device and pinned-host chunks are read in order on `stream`: the caller
  * must not overwrite them until the work this call queued on `stream` has completed.
  * Pageable-host chunks have been copied into library staging when the call returns.
+ * Pinned chunks the device can address at the same pointer (unified addressing) are
+ * read in place by the accumulate kernel over the host link, with no staging copy --
+ * the server receives a client's update straight into its running sum; FA_STAGE_HOST
+ * sends them through the staging ring instead.  Both give the same bits.
  * len_elems == 0 is a no-op.  Argument, range, weight and state errors change nothing.
  * A CUDA failure or timeout after the chunk was accepted (FA_ERR_CUDA, FA_ERR_TIMEOUT,
  * FA_ERR_NOMEM) leaves the round inconsistent: every later call returns FA_ERR_CUDA
@@ -160,11 +169,14 @@ fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* c
  * Keys no client sent (or whose reporters all have weight 0) are NOT written, so the
  * caller's previous global values survive (the frozen-backbone / adapter case of [FLARE]).
  *   out_ptrs  n_keys pointers (one per key, numel elements of dtype_out each), or, with
- *             FA_FLAT_OUT, one pointer to the flat layout.  Device or host memory.
+ *             FA_FLAT_OUT, one pointer to the flat layout.  Device or host memory;
+ *             pinned host memory the device addresses at the same pointer is written
+ *             in place by the kernel (no device staging), other host memory through a
+ *             device buffer and a copy on `stream`.
  * Returns FA_ERR_INCOMPLETE, writing nothing, if a client sent part of a key.
  * Non-destructive: calling it again gives the same result.  After it, fa_accumulate
  * returns FA_ERR_STATE until fa_reset.  Output is complete once the work queued on
- * `stream` has completed (host outputs: once the call's copies on `stream` complete).
+ * `stream` has completed (host outputs included: their stores or copies are on `stream`).
  * Errors: FA_ERR_ARG, FA_ERR_INCOMPLETE, FA_ERR_CUDA, FA_ERR_NOMEM, FA_ERR_TIMEOUT. */
 fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream);
 

@@ -32,6 +32,7 @@ FA_F32 = 0
 FA_BF16 = 1
 FA_KEY_FLAT = -1
 FA_FLAT_OUT = 1
+FA_STAGE_HOST = 2
 FA_NOALLOC_MAX_ELEMS = 1 << 22
 
 DTYPES = {"f32": FA_F32, "bf16": FA_BF16, FA_F32: FA_F32, FA_BF16: FA_BF16}

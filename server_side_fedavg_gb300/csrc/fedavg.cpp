@@ -149,8 +149,9 @@ fa_status wait_event(fa_ctx* c, cudaEvent_t ev, const char* what) {
     }
 }
 
-Mem classify(const void* p, int device, bool* other_device) {
+Mem classify(const void* p, int device, bool* other_device, bool* in_place = nullptr) {
     *other_device = false;
+    if (in_place) *in_place = false;
     cudaPointerAttributes at;
     cudaError_t e = cudaPointerGetAttributes(&at, p);
     if (e != cudaSuccess) {
@@ -164,6 +165,9 @@ Mem classify(const void* p, int device, bool* other_device) {
         case cudaMemoryTypeManaged:
             return Mem::kDevice;
         case cudaMemoryTypeHost:
+            // pinned memory the current device reads at the same address (unified
+            // addressing): kernels may load it in place
+            if (in_place) *in_place = at.devicePointer == p;
             return Mem::kPinned;
         default:
             return Mem::kPageable;
@@ -241,7 +245,7 @@ fa_status ensure_ring(fa_ctx* c, bool need_host) {
 // [c0, c0 + n), reading inputs xs[0..J) whose element 0 is chunk element c0.
 fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_t c0,
                         uint64_t n, const void* const* xs, const float* ws, uint32_t J,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool direct = false) {
     // launches of up to 16 clients; after the first launch the sum is started everywhere
     uint32_t done = 0;
     while (done < J) {
@@ -257,7 +261,8 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
         a.J = jb;
         auto flush = [&]() -> fa_status {
             if (a.nseg == 0) return FA_OK;
-            FA_CUDA(c, fa::launch_accumulate(a, c->din, c->shape, s));
+            FA_CUDA(c, direct ? fa::launch_accumulate_direct(a, c->din, c->shape, s)
+                              : fa::launch_accumulate(a, c->din, c->shape, s));
             c->stats.kernel_launches++;
             a.nseg = 0;
             a.vec_ok = 0;
@@ -300,17 +305,20 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
             if (ptrs == nullptr || ptrs[j] == nullptr) return fail(c, FA_ERR_ARG, "chunk pointer is NULL");
     }
     Mem kind = Mem::kDevice;
+    bool in_place = false;
     if (len > 0) {
         for (uint32_t j = 0; j < J; ++j) {
             bool other = false;
-            Mem m = classify(ptrs[j], c->device, &other);
+            Mem m = classify(ptrs[j], c->device, &other, &in_place);
             if (other) return fail(c, FA_ERR_ARG, "chunk is in another GPU's memory");
             if (batch && m != Mem::kDevice)
                 return fail(c, FA_ERR_ARG, "fa_accumulate_batch takes device memory only");
             kind = m;
         }
     }
-    if (len > 0 && kind != Mem::kDevice) {
+    // pinned chunks the device can address are read in place unless staging is asked for
+    const bool direct = kind == Mem::kPinned && in_place && (c->flags & FA_STAGE_HOST) == 0;
+    if (len > 0 && kind != Mem::kDevice && !direct) {
         // staging first: a failed allocation must not leave the round half-recorded
         fa_status rr = ensure_ring(c, kind == Mem::kPageable);
         if (rr != FA_OK) return rr;
@@ -329,6 +337,12 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
         r = chain_in(c, s);
         if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, J, s);
         if (r == FA_OK) r = chain_out(c, s);
+    } else if (direct) {
+        // pinned host memory read by the kernel over the host link, ordered on `s`
+        r = chain_in(c, s);
+        if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, 1, s, true);
+        if (r == FA_OK) r = chain_out(c, s);
+        if (r == FA_OK) c->stats.h2d_bytes += len * c->s_in;
     } else {
         // host memory: through the staging ring, slot-sized pieces
         const uint64_t per = c->slot_bytes / c->s_in;
@@ -555,12 +569,13 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
     }
     std::vector<Mem> kind(c->items.size());
     bool any_host = false;
+    uint64_t written_in_place = 0;   // bytes the kernel stores straight into pinned host memory
     for (size_t i = 0; i < c->items.size(); ++i) {
         const auto& it = c->items[i];
         void* dst = flat ? out_ptrs[0] : out_ptrs[it.key];
         if (dst == nullptr) return fail(c, FA_ERR_ARG, "output pointer is NULL for a key to be written");
-        bool other = false;
-        kind[i] = classify(dst, c->device, &other);
+        bool other = false, in_place = false;
+        kind[i] = classify(dst, c->device, &other, &in_place);
         if (other) return fail(c, FA_ERR_ARG, "output is in another GPU's memory");
         if (apply) {
             const void* b = flat ? base_ptrs[0] : base_ptrs[it.key];
@@ -569,6 +584,12 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
                 return fail(c, FA_ERR_ARG, "fa_finalize_apply: base values must be in this GPU's memory");
             if (kind[i] != Mem::kDevice)
                 return fail(c, FA_ERR_ARG, "fa_finalize_apply: outputs must be in this GPU's memory");
+        }
+        // pinned outputs the device addresses at the same pointer are written by the
+        // finalize kernel itself, over the host link, unless staging is asked for
+        if (kind[i] == Mem::kPinned && in_place && (c->flags & FA_STAGE_HOST) == 0) {
+            kind[i] = Mem::kDevice;
+            written_in_place += it.numel * c->s_out;
         }
         any_host = any_host || kind[i] != Mem::kDevice;
     }
@@ -615,6 +636,7 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
         FA_CUDA(c, fa::launch_finalize(c->fin_dev, nseg, ntiles, c->dout, c->acc, apply,
                                        static_cast<float>(server_lr), c->shape, s));
         c->stats.kernel_launches++;
+        c->stats.d2h_bytes += written_in_place;
         // host outputs: copy the staged keys back, merging neighbours in the flat layout
         for (size_t i = 0; i < c->items.size();) {
             if (kind[i] == Mem::kDevice) {

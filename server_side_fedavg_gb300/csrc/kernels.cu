@@ -10,6 +10,8 @@
 //    that store has read it.  Persistent grids, one or two CTAs per SM, keep about
 //    150-200 KB of copies in flight per SM -- a timed sweep of tile sizes, stage
 //    counts and direct-load variants on GB300 chose these shapes;
+//  - accumulate_direct_kernel reads its input in place with plain loads: the form for
+//    pinned host memory read over the NVLink-C2C link, where the link sets the pace;
 //  - finalize_kernel reads the sum with 128-bit loads and writes 128-bit stores;
 //  - ragged tails (< 8 elements) and segments whose pointers are not 16-byte
 //    aligned use direct per-element loads and stores.
@@ -326,6 +328,99 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
     }
     if (threadIdx.x == 0) pipeline_drain(bars, consumed, issued, count);
     __syncthreads();
+}
+
+// ----------------------------------------------------------------- direct accumulate
+// Input read in place with plain coherent loads (no bulk copies, no read-only path),
+// the form for pinned host memory the device reads over the NVLink-C2C link: the
+// link moves about 0.2 TB/s against 6.7 TB/s of HBM, so the sum's read-modify-write
+// in HBM is not the limit and no shared-memory staging is needed.  Tiles of
+// kDirectTile elements, one 8-element vector per thread; many CTAs per SM keep enough
+// loads in flight to cover the link's latency.
+__device__ __forceinline__ uint4 ld_plain_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+template <typename Tin>
+__device__ __forceinline__ float load_plain(const Tin* p);
+
+template <>
+__device__ __forceinline__ float load_plain<uint16_t>(const uint16_t* p) {
+    uint16_t u;
+    asm volatile("ld.global.u16 %0, [%1];" : "=h"(u) : "l"(p));
+    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
+
+template <>
+__device__ __forceinline__ float load_plain<float>(const float* p) {
+    float f;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(f) : "l"(p));
+    return f;
+}
+
+// Eight elements of dtype Tin from a 16-byte aligned global address.
+template <typename Tin>
+__device__ __forceinline__ void plain_vec8(const Tin* p, float (&x)[8]) {
+    if constexpr (sizeof(Tin) == 2) {
+        const uint4 q = ld_plain_v4(p);
+        x[0] = bf16_lo(q.x); x[1] = bf16_hi(q.x);
+        x[2] = bf16_lo(q.y); x[3] = bf16_hi(q.y);
+        x[4] = bf16_lo(q.z); x[5] = bf16_hi(q.z);
+        x[6] = bf16_lo(q.w); x[7] = bf16_hi(q.w);
+    } else {
+        const uint4 a = ld_plain_v4(p);
+        const uint4 b = ld_plain_v4(p + 4);
+        x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+        x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+        x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+        x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+    }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kBlock) accumulate_direct_kernel(const __grid_constant__ AccArgs a) {
+    static_assert(kDirectTile == kBlock * kVec, "one vector per thread per tile");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const Tin* x0 = static_cast<const Tin*>(a.x[0]);
+    const float w = a.w[0];
+    uint32_t cur = 0;
+    for (uint32_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
+        const TileAt ta = tile_at(a.seg, a.nseg, t, kDirectTile, cur);
+        const AccSeg& sg = a.seg[ta.si];
+        const bool first = sg.first != 0;
+        const Tin* xt = x0 + sg.x_off + ta.e0;
+        float* g = a.acc + sg.acc_idx + ta.e0;
+        const uint32_t n8 = ((a.vec_ok >> ta.si) & 1ull) ? ta.cnt / kVec : 0u;
+        if (threadIdx.x < n8) {
+            float xv[8];
+            plain_vec8<Tin>(xt + threadIdx.x * kVec, xv);
+            float* gp = g + threadIdx.x * kVec;
+            float4 lo, hi;
+            if (first) {
+                lo = make_float4(__fmul_rn(w, xv[0]), __fmul_rn(w, xv[1]), __fmul_rn(w, xv[2]),
+                                 __fmul_rn(w, xv[3]));
+                hi = make_float4(__fmul_rn(w, xv[4]), __fmul_rn(w, xv[5]), __fmul_rn(w, xv[6]),
+                                 __fmul_rn(w, xv[7]));
+            } else {
+                lo = ld_v4f(gp);
+                hi = ld_v4f(gp + 4);
+                lo.x = __fmaf_rn(w, xv[0], lo.x); lo.y = __fmaf_rn(w, xv[1], lo.y);
+                lo.z = __fmaf_rn(w, xv[2], lo.z); lo.w = __fmaf_rn(w, xv[3], lo.w);
+                hi.x = __fmaf_rn(w, xv[4], hi.x); hi.y = __fmaf_rn(w, xv[5], hi.y);
+                hi.z = __fmaf_rn(w, xv[6], hi.z); hi.w = __fmaf_rn(w, xv[7], hi.w);
+            }
+            st_v4f(gp, lo);
+            st_v4f(gp + 4, hi);
+        }
+        for (uint32_t e = n8 * kVec + threadIdx.x; e < ta.cnt; e += kBlock) {
+            const float xv = load_plain<Tin>(xt + e);
+            g[e] = first ? __fmul_rn(w, xv) : __fmaf_rn(w, xv, g[e]);
+        }
+    }
 }
 
 // ----------------------------------------------------------------- J-client reduce
@@ -720,6 +815,14 @@ cudaError_t launch_stream_t(AccArgs a, int per_sm, int sms, cudaStream_t stream)
                             bulk_smem_bytes<Tin>(), stream, a);
 }
 
+template <typename Tin>
+cudaError_t launch_direct_t(AccArgs a, int per_sm, int sms, cudaStream_t stream) {
+    if (!number_tiles(a.seg, a.nseg, kDirectTile, &a.ntiles)) return cudaErrorInvalidValue;
+    if (a.ntiles == 0) return cudaSuccess;
+    return launch_dependent(accumulate_direct_kernel<Tin>, grid_for(a.ntiles, sms, per_sm), kBlock,
+                            0, stream, a);
+}
+
 RedArgs to_reduce_args(const AccArgs& a) {
     RedArgs r;
     for (int j = 0; j < kMaxBatch; ++j) {
@@ -800,6 +903,10 @@ cudaError_t query_launch_shape(LaunchShape* s) {
     auto keep = [&r](cudaError_t x) { if (r == cudaSuccess) r = x; };
     keep(prepare_stream<float>(&s->bulk_ctas_per_sm[0]));
     keep(prepare_stream<uint16_t>(&s->bulk_ctas_per_sm[1]));
+    keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->direct_ctas_per_sm[0],
+                                                       accumulate_direct_kernel<float>, kBlock, 0));
+    keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->direct_ctas_per_sm[1],
+                                                       accumulate_direct_kernel<uint16_t>, kBlock, 0));
     keep(prepare_reduce<float, float, false>(&s->reduce_ctas_per_sm[0][0]));
     keep(prepare_reduce<float, float, true>(&s->reduce_ctas_per_sm[0][1]));
     keep(prepare_reduce<float, uint16_t, true>(&s->reduce_ctas_per_sm[0][2]));
@@ -815,6 +922,13 @@ cudaError_t query_launch_shape(LaunchShape* s) {
     keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->fin_ctas_per_sm[1][1],
                                                        finalize_kernel<uint16_t, true>, kBlock, 0));
     return r;
+}
+
+cudaError_t launch_accumulate_direct(const AccArgs& a, int dtype_in, const LaunchShape& s,
+                                     cudaStream_t stream) {
+    if (a.nseg == 0 || a.nseg > static_cast<uint32_t>(kMaxSegs) || a.J != 1) return cudaErrorInvalidValue;
+    return dtype_in == 0 ? launch_direct_t<float>(a, s.direct_ctas_per_sm[0], s.sms, stream)
+                         : launch_direct_t<uint16_t>(a, s.direct_ctas_per_sm[1], s.sms, stream);
 }
 
 cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,

@@ -24,6 +24,7 @@ constexpr int kBlock = 256;           // threads per CTA
 constexpr int kVec = 8;               // elements per vector (16 B of bf16, 2 x 16 B of fp32)
 constexpr int kTile = 4096;           // elements per tile of the finalize kernel
 constexpr int kBulkTile = 8192;       // elements per pipeline stage of the streaming kernel
+constexpr int kDirectTile = kBlock * kVec;   // elements per tile of the direct-load accumulate
 constexpr int kMaxSegs = 48;          // segments per accumulate / reduce launch
 constexpr int kMaxBatch = 16;         // resident clients per launch
 constexpr int kReduceStageBytes = 73728;   // shared-memory budget per stage of the reduce kernel
@@ -84,6 +85,7 @@ struct FinSeg {
 struct LaunchShape {
     int sms = 0;
     int bulk_ctas_per_sm[2] = {};       // [dtype_in], streaming kernel
+    int direct_ctas_per_sm[2] = {};     // [dtype_in], direct-load accumulate
     int reduce_ctas_per_sm[2][3] = {};  // [dtype_in][sum mode, final fp32 out, final bf16 out]
                                         // (same for every specialisation of J)
     int fin_ctas_per_sm[2][2] = {};     // [apply][dtype_out]
@@ -106,6 +108,13 @@ cudaError_t query_launch_shape(LaunchShape* s);
 // Returns cudaErrorInvalidValue if the arguments are out of range.
 cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,
                               cudaStream_t stream);
+
+// One client (a.J == 1) with the input read in place by plain loads, no bulk copies:
+// for inputs in host memory the device can address (pinned memory read over the
+// NVLink-C2C link), where the link sets the pace.  Same arguments and the same
+// per-element arithmetic as launch_accumulate, so the sums are bit-identical.
+cudaError_t launch_accumulate_direct(const AccArgs& a, int dtype_in, const LaunchShape& s,
+                                     cudaStream_t stream);
 
 // Final-mode reduce: out = RNE((sum so far +) J weighted inputs, / divisor) per segment.
 // The caller fills everything but tile / ntiles / tile0.

@@ -49,7 +49,7 @@ def test_constants_match_binding():
     for k, v in d.items():
         if hasattr(fa, k):
             assert getattr(fa, k) == v, k
-    assert d["FA_KEY_FLAT"] == -1 and d["FA_FLAT_OUT"] == 1
+    assert d["FA_KEY_FLAT"] == -1 and d["FA_FLAT_OUT"] == 1 and d["FA_STAGE_HOST"] == 2
 
 
 def test_strerror_covers_all_codes(lib):

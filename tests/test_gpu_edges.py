@@ -151,14 +151,19 @@ def test_error_codes():
 
 
 def test_host_outputs_match_device_outputs():
+    """Pinned outputs written in place by the kernel or staged through a device buffer
+    (FA_STAGE_HOST), pageable outputs, per key or flat (flat keys start unaligned):
+    the same bits as device outputs, and the bytes sent to the host are counted."""
     rng = np.random.default_rng(4)
     numels = [4096 * 2 + 3, 9, 70000]
     K = 3
     xs = [[_bf16(rng, n) for n in numels] for _ in range(K)]
     w = [10.0, 20.0, 30.0]
     res = {}
-    for mode in ("device", "pinned", "pageable", "flat_pinned"):
-        flags = fa.FA_FLAT_OUT if mode.startswith("flat") else 0
+    modes = ("device", "pinned", "pinned_staged", "pageable", "flat_pinned", "flat_pinned_staged")
+    for mode in modes:
+        flags = (fa.FA_FLAT_OUT if mode.startswith("flat") else 0) | \
+                (fa.FA_STAGE_HOST if mode.endswith("staged") else 0)
         ctx = fa.fa_open([(f"k{i}", n) for i, n in enumerate(numels)], "bf16", "bf16", K, flags=flags)
         try:
             for k in range(K):
@@ -166,7 +171,7 @@ def test_host_outputs_match_device_outputs():
                     fa.fa_accumulate(ctx, k, w[k], p, 0, to_dev(xs[k][p]), numels[p])
             if mode == "device":
                 outs = [sentinel(n, "bf16") for n in numels]
-            elif mode == "pinned":
+            elif mode.startswith("pinned"):
                 outs = [sentinel(n, "bf16", "cpu").pin_memory() for n in numels]
             elif mode == "pageable":
                 outs = [sentinel_np(n, "bf16").copy() for n in numels]
@@ -175,6 +180,8 @@ def test_host_outputs_match_device_outputs():
             fa.fa_finalize(ctx, outs)
             fa.fa_sync(ctx)
             torch.cuda.synchronize()
+            sent = fa.fa_get_stats(ctx)["d2h_bytes"]
+            assert sent == (0 if mode == "device" else 2 * (numels[0] + numels[2])), (mode, sent)
             got = [to_np(o, "bf16") if isinstance(o, torch.Tensor) else o for o in outs]
             if mode.startswith("flat"):
                 offs = np.cumsum([0] + numels)

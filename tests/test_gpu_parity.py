@@ -31,6 +31,8 @@ def _host_inputs(w):
 def run_per_key(w, host, mode="device", pieces=1, seed=0, **opts):
     """Feed every (client, key) as `pieces` ragged chunks; returns outputs (numpy)."""
     rng = np.random.default_rng(seed)
+    if mode == "pinned-staged":
+        opts["flags"] = opts.get("flags", 0) | fa.FA_STAGE_HOST
     ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, **opts)
     keep = []
     try:
@@ -40,7 +42,7 @@ def run_per_key(w, host, mode="device", pieces=1, seed=0, **opts):
                 x = host[(k, p)]
                 if mode == "device":
                     t = to_dev(x)
-                elif mode == "pinned":
+                elif mode.startswith("pinned"):
                     t = to_pinned(x)
                 else:
                     t = x
@@ -106,10 +108,11 @@ def test_lora_has_unreported_modules(small):
     assert len(sent) <= w.n_keys
 
 
-@pytest.mark.parametrize("mode", ["device", "pinned", "pageable"])
+@pytest.mark.parametrize("mode", ["device", "pinned", "pinned-staged", "pageable"])
 @pytest.mark.parametrize("pieces", [1, 5])
 def test_ingest_modes_bit_identical(small, mode, pieces):
-    """Host (pinned / pageable) and device ingest, whole or ragged chunks: same bits."""
+    """Host (pinned read in place, pinned through the staging ring, pageable) and device
+    ingest, whole or ragged chunks (ragged offsets leave pointers unaligned): same bits."""
     w, host = small("lora")
     ref, _ = run_per_key(w, host, "device", 1)
     got, _ = run_per_key(w, host, mode, pieces, seed=3, ring_slots=2, slot_bytes=1 << 20)
@@ -120,7 +123,7 @@ def test_ingest_modes_bit_identical(small, mode, pieces):
 def test_ring_geometry_bit_identical(small):
     w, host = small("unet3d")
     a, _ = run_per_key(w, host, "pageable", 3, seed=5, ring_slots=2, slot_bytes=4096)
-    b, _ = run_per_key(w, host, "pinned", 1, ring_slots=6, slot_bytes=1 << 24)
+    b, _ = run_per_key(w, host, "pinned-staged", 1, ring_slots=6, slot_bytes=1 << 24)
     for p in range(w.n_keys):
         assert np.array_equal(a[p], b[p]), f"key {p}"
 
@@ -234,15 +237,17 @@ def test_full_size_resident_sampled(name):
 
 
 @pytest.mark.slow
-def test_full_size_host_fed_sampled():
+@pytest.mark.parametrize("staged", [False, True])
+def test_full_size_host_fed_sampled(staged):
     """The 2.2B VLM streamed client by client from PINNED HOST memory in 64 MiB flat
-    chunks, through the library's staging ring (the bench's end-to-end path), sampled
-    against the oracle."""
+    chunks -- read in place by the kernel over the host link, or through the library's
+    staging ring (FA_STAGE_HOST) -- sampled against the oracle."""
     w = W.make("vlm2b")
     idx = _sample_indices(w, seed=3)
     host = torch.empty(w.P, dtype=torch.int16).pin_memory()
     hv = host.numpy().view(np.uint16)
-    ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
+    flags = fa.FA_FLAT_OUT | (fa.FA_STAGE_HOST if staged else 0)
+    ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, flags=flags)
     try:
         s = torch.cuda.current_stream()
         for k in range(w.K):
@@ -250,7 +255,7 @@ def test_full_size_host_fed_sampled():
             for c0 in range(0, w.P, w.chunk_elems):
                 n = min(w.chunk_elems, w.P - c0)
                 fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, host.data_ptr() + 2 * c0, n, s)
-            s.synchronize()              # the DMA reads the pinned buffer: wait before refilling it
+            s.synchronize()              # the pinned buffer is read on `s`: wait before refilling it
         out = torch.empty(w.P, dtype=torch.int16, device="cuda")
         fa.fa_finalize(ctx, [out], s)
         fa.fa_sync(ctx)
@@ -261,5 +266,6 @@ def test_full_size_host_fed_sampled():
     got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
     xs = [synth.client_gather(w, k, idx) for k in range(w.K)]
     want, N, cnt = oracle.fedavg_key(w.weights, [True] * w.K, xs, w.dtype_in, w.dtype_out)
-    frac = check_bf16(got, want, "vlm2b host-fed")
-    print(f"vlm2b host-fed: {idx.size} sampled elements, {frac:.6%} bit-identical")
+    what = "vlm2b host-fed " + ("staged" if staged else "in place")
+    frac = check_bf16(got, want, what)
+    print(f"{what}: {idx.size} sampled elements, {frac:.6%} bit-identical")
