@@ -87,9 +87,9 @@ typedef struct fa_ctx fa_ctx;   /* opaque; owned by the library */
 
 /* fa_opts.flags */
 #define FA_FLAT_OUT   1u   /* fa_finalize takes ONE output pointer to the flat layout */
-#define FA_STAGE_HOST 2u   /* pinned host chunks go through the staging ring, and pinned
-                              host outputs through a device buffer and a copy (copy
-                              engine), even where the device could address them in place */
+#define FA_STAGE_HOST 2u   /* host chunks go through the staging ring, and pinned host
+                              outputs through a device buffer and a copy (copy engine),
+                              even where the device could address them in place */
 
 typedef struct {
     uint32_t size;        /* sizeof(fa_opts): lets the struct grow */
@@ -105,9 +105,9 @@ typedef struct {
     uint64_t kernel_launches;   /* kernels this context has launched since fa_open */
     uint64_t client_bytes;      /* bytes of client updates accumulated */
     uint64_t h2d_bytes;         /* bytes of client updates brought from host memory (staging
-                                   copies and in-place reads of pinned memory) */
-    uint64_t d2h_bytes;         /* bytes of aggregate fa_finalize sent to host memory (copies,
-                                   and in-place stores into pinned memory) */
+                                   copies and in-place reads) */
+    uint64_t d2h_bytes;         /* bytes of aggregate fa_finalize sent to host memory (copies
+                                   and in-place stores) */
     uint64_t chunks;            /* accepted fa_accumulate / fa_accumulate_batch calls */
 } fa_stats;
 
@@ -138,11 +138,17 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
  * client and key must not overlap; the library counts elements).
  * Ownership: device and pinned-host chunks are read in order on `stream`: the caller
  * must not overwrite them until the work this call queued on `stream` has completed.
- * Pageable-host chunks have been copied into library staging when the call returns.
- * Pinned chunks the device can address at the same pointer (unified addressing) are
- * read in place by the accumulate kernel over the host link, with no staging copy --
- * the server receives a client's update straight into its running sum; FA_STAGE_HOST
- * sends them through the staging ring instead.  Both give the same bits.
+ * Pageable-host chunks have been consumed when the call returns: the caller may reuse
+ * them at once.
+ * Host chunks the device can address are read in place by the accumulate kernel over
+ * the host link, with no staging copy -- the server receives a client's update straight
+ * into its running sum: pinned memory mapped at the same pointer (unified addressing),
+ * and pageable memory where the device reads through the host's page tables
+ * (cudaDevAttrPageableMemoryAccessUsesHostPageTables; the call then waits, bounded by
+ * timeout_ms, for the read to finish).  Other pageable chunks are copied into pinned
+ * staging; FA_STAGE_HOST sends every host chunk through the staging ring.  All paths
+ * give the same bits.  If a pageable in-place read times out (FA_ERR_TIMEOUT) it may
+ * still be in flight: keep the chunk until the work queued on `stream` has completed.
  * len_elems == 0 is a no-op.  Argument, range, weight and state errors change nothing.
  * A CUDA failure or timeout after the chunk was accepted (FA_ERR_CUDA, FA_ERR_TIMEOUT,
  * FA_ERR_NOMEM) leaves the round inconsistent: every later call returns FA_ERR_CUDA

@@ -60,6 +60,8 @@ struct fa_ctx {
     bool chain_valid = false;
     unsigned long long chain_stream_id = 0;   // stream the chain event was last recorded on
     cudaEvent_t user_ev = nullptr;
+    cudaEvent_t read_ev = nullptr;   // end of an in-place read of a pageable chunk
+    bool pageable_in_place = false;  // the device reads pageable memory through the host page tables
 
     cudaStream_t copy_stream = nullptr;
     std::vector<void*> dev_slot, host_slot;
@@ -316,8 +318,13 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
             kind = m;
         }
     }
-    // pinned chunks the device can address are read in place unless staging is asked for
-    const bool direct = kind == Mem::kPinned && in_place && (c->flags & FA_STAGE_HOST) == 0;
+    // host chunks the device can address are read in place unless staging is asked for:
+    // pinned memory mapped at the same pointer, and pageable memory where the device walks
+    // the host page tables (then the call waits for the read, so the caller may reuse the
+    // chunk on return as with staging)
+    const bool stage = (c->flags & FA_STAGE_HOST) != 0;
+    const bool direct = !stage && ((kind == Mem::kPinned && in_place) ||
+                                   (kind == Mem::kPageable && c->pageable_in_place));
     if (len > 0 && kind != Mem::kDevice && !direct) {
         // staging first: a failed allocation must not leave the round half-recorded
         fa_status rr = ensure_ring(c, kind == Mem::kPageable);
@@ -338,10 +345,15 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
         if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, J, s);
         if (r == FA_OK) r = chain_out(c, s);
     } else if (direct) {
-        // pinned host memory read by the kernel over the host link, ordered on `s`
+        // host memory read by the kernel over the host link, ordered on `s`
         r = chain_in(c, s);
         if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, 1, s, true);
+        if (r == FA_OK && kind == Mem::kPageable) {
+            cudaError_t ce = cudaEventRecord(c->read_ev, s);
+            if (ce != cudaSuccess) r = cuda_fail(c, ce, "pageable read");
+        }
         if (r == FA_OK) r = chain_out(c, s);
+        if (r == FA_OK && kind == Mem::kPageable) r = wait_event(c, c->read_ev, "pageable chunk read");
         if (r == FA_OK) c->stats.h2d_bytes += len * c->s_in;
     } else {
         // host memory: through the staging ring, slot-sized pieces
@@ -411,6 +423,7 @@ void free_ctx(fa_ctx* c) {
     if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
     if (c->chain) cudaEventDestroy(c->chain);
     if (c->user_ev) cudaEventDestroy(c->user_ev);
+    if (c->read_ev) cudaEventDestroy(c->read_ev);
     if (c->fin_ev) cudaEventDestroy(c->fin_ev);
     if (c->fin_dev) cudaFree(c->fin_dev);
     if (c->fin_host) cudaFreeHost(c->fin_host);
@@ -506,6 +519,16 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
     if (ce == cudaSuccess) ce = cudaMalloc(&c->acc, c->ledger.padded_elems() * sizeof(float));
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->chain, cudaEventDisableTiming);
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->user_ev, cudaEventDisableTiming);
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->read_ev, cudaEventDisableTiming);
+    if (ce == cudaSuccess) {
+        // pageable memory is read and written in place only where the device reaches it
+        // through the host's own page tables (no migration of the caller's pages)
+        int pma = 0, host_pt = 0;
+        ce = cudaDeviceGetAttribute(&pma, cudaDevAttrPageableMemoryAccess, c->device);
+        if (ce == cudaSuccess)
+            ce = cudaDeviceGetAttribute(&host_pt, cudaDevAttrPageableMemoryAccessUsesHostPageTables, c->device);
+        c->pageable_in_place = pma == 1 && host_pt == 1;
+    }
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->fin_ev, cudaEventDisableTiming);
     if (ce == cudaSuccess) ce = cudaMalloc(&c->fin_dev, sizeof(fa::FinSeg) * n_keys);
     if (ce == cudaSuccess) ce = cudaHostAlloc(&c->fin_host, sizeof(fa::FinSeg) * n_keys, cudaHostAllocDefault);
@@ -586,7 +609,10 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
                 return fail(c, FA_ERR_ARG, "fa_finalize_apply: outputs must be in this GPU's memory");
         }
         // pinned outputs the device addresses at the same pointer are written by the
-        // finalize kernel itself, over the host link, unless staging is asked for
+        // finalize kernel itself, over the host link, unless staging is asked for.
+        // Pageable outputs stay staged: an output buffer is often freshly allocated, and
+        // the device's first touch of each of its pages is a fault serviced by the host
+        // (a 7B aggregate took seconds in place against ~80 ms through the copy engine)
         if (kind[i] == Mem::kPinned && in_place && (c->flags & FA_STAGE_HOST) == 0) {
             kind[i] = Mem::kDevice;
             written_in_place += it.numel * c->s_out;

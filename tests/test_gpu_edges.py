@@ -152,15 +152,17 @@ def test_error_codes():
 
 def test_host_outputs_match_device_outputs():
     """Pinned outputs written in place by the kernel or staged through a device buffer
-    (FA_STAGE_HOST), pageable outputs, per key or flat (flat keys start unaligned):
-    the same bits as device outputs, and the bytes sent to the host are counted."""
+    (FA_STAGE_HOST), pageable outputs (always staged), per key or flat (flat keys start
+    unaligned): the same bits as device outputs, and the bytes sent to the host are
+    counted."""
     rng = np.random.default_rng(4)
     numels = [4096 * 2 + 3, 9, 70000]
     K = 3
     xs = [[_bf16(rng, n) for n in numels] for _ in range(K)]
     w = [10.0, 20.0, 30.0]
     res = {}
-    modes = ("device", "pinned", "pinned_staged", "pageable", "flat_pinned", "flat_pinned_staged")
+    modes = ("device", "pinned", "pinned_staged", "pageable", "pageable_staged", "flat_pinned",
+             "flat_pinned_staged", "flat_pageable")
     for mode in modes:
         flags = (fa.FA_FLAT_OUT if mode.startswith("flat") else 0) | \
                 (fa.FA_STAGE_HOST if mode.endswith("staged") else 0)
@@ -173,8 +175,10 @@ def test_host_outputs_match_device_outputs():
                 outs = [sentinel(n, "bf16") for n in numels]
             elif mode.startswith("pinned"):
                 outs = [sentinel(n, "bf16", "cpu").pin_memory() for n in numels]
-            elif mode == "pageable":
+            elif mode.startswith("pageable"):
                 outs = [sentinel_np(n, "bf16").copy() for n in numels]
+            elif mode == "flat_pageable":
+                outs = [sentinel_np(sum(numels), "bf16").copy()]
             else:
                 outs = [sentinel(sum(numels), "bf16", "cpu").pin_memory()]
             fa.fa_finalize(ctx, outs)
@@ -193,6 +197,33 @@ def test_host_outputs_match_device_outputs():
         for p in range(len(numels)):
             assert np.array_equal(res[mode][p], res["device"][p]), (mode, p)
     assert np.array_equal(res["device"][1], sentinel_np(numels[1], "bf16"))
+
+
+@pytest.mark.parametrize("staged", [False, True])
+def test_pageable_chunk_reusable_on_return(staged):
+    """A pageable chunk has been consumed when fa_accumulate returns (read in place and
+    waited for, or copied into staging): overwriting it at once changes nothing."""
+    rng = np.random.default_rng(12)
+    n = 3 * 4096 * 8 + 5
+    xs = [_bf16(rng, n) for _ in range(3)]
+    w = [3.0, 5.0, 7.0]
+    flags = fa.FA_STAGE_HOST if staged else 0
+    ctx = fa.fa_open([("k", n)], "bf16", "bf16", 3, flags=flags, ring_slots=2, slot_bytes=1 << 16)
+    try:
+        s = torch.cuda.Stream()
+        buf = np.empty(n, np.uint16)
+        for k in range(3):
+            buf[:] = xs[k]
+            fa.fa_accumulate(ctx, k, w[k], 0, 0, buf, n, s)
+            buf[:] = 0x7FC0                            # NaN bits: must not reach the sum
+        out = sentinel(n, "bf16")
+        fa.fa_finalize(ctx, [out], s)
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+        want, _, _ = oracle.fedavg_key(w, [True] * 3, xs, "bf16", "bf16")
+        check_bf16(to_np(out, "bf16"), want, "pageable reuse")
+    finally:
+        fa.fa_close(ctx)
 
 
 def test_bounded_wait_times_out_then_recovers():

@@ -3,9 +3,9 @@
 One context runs several rounds (fa_reset between them).  Each round mixes, in a
 shuffled call order: a random subset of keys per client (partial participation,
 including clients that send nothing), ragged chunks of each key, every ingest kind
-(device memory; pinned host memory read in place or staged; pageable host memory
-through a small staging ring), FLAT chunks that span key boundaries, and a
-fa_accumulate_batch group over part of one key.
+(device memory; pinned and pageable host memory, read in place or through a small
+staging ring), FLAT chunks that span key boundaries, and a fa_accumulate_batch group
+over part of one key.
 
 The GPU applies contributions in call order and the oracle sums in client-id order
 (the arrival-order reading of FedAvg's weighted mean), so outputs are compared with
@@ -102,7 +102,7 @@ def test_random_rounds(din, dout):
     rng = np.random.default_rng(seed)
     numels = [rng_py.choice(SIZES) for _ in range(9)]
     K = 7
-    # odd seeds send pinned chunks through the staging ring, even ones read them in place
+    # odd seeds send host chunks through the staging ring, even ones read them in place
     ctx = fa.fa_open([(f"k{i}", n) for i, n in enumerate(numels)], din, dout, K,
                      ring_slots=3, slot_bytes=64 << 10, flags=fa.FA_STAGE_HOST if seed % 2 else 0)
     s = torch.cuda.Stream()

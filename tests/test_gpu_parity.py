@@ -31,7 +31,7 @@ def _host_inputs(w):
 def run_per_key(w, host, mode="device", pieces=1, seed=0, **opts):
     """Feed every (client, key) as `pieces` ragged chunks; returns outputs (numpy)."""
     rng = np.random.default_rng(seed)
-    if mode == "pinned-staged":
+    if mode.endswith("-staged"):
         opts["flags"] = opts.get("flags", 0) | fa.FA_STAGE_HOST
     ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, **opts)
     keep = []
@@ -108,11 +108,12 @@ def test_lora_has_unreported_modules(small):
     assert len(sent) <= w.n_keys
 
 
-@pytest.mark.parametrize("mode", ["device", "pinned", "pinned-staged", "pageable"])
+@pytest.mark.parametrize("mode", ["device", "pinned", "pinned-staged", "pageable", "pageable-staged"])
 @pytest.mark.parametrize("pieces", [1, 5])
 def test_ingest_modes_bit_identical(small, mode, pieces):
-    """Host (pinned read in place, pinned through the staging ring, pageable) and device
-    ingest, whole or ragged chunks (ragged offsets leave pointers unaligned): same bits."""
+    """Host (pinned or pageable, read in place by the kernel where the device can address
+    it, or through the staging ring) and device ingest, whole or ragged chunks (ragged
+    offsets leave pointers unaligned): same bits."""
     w, host = small("lora")
     ref, _ = run_per_key(w, host, "device", 1)
     got, _ = run_per_key(w, host, mode, pieces, seed=3, ring_slots=2, slot_bytes=1 << 20)
@@ -122,7 +123,7 @@ def test_ingest_modes_bit_identical(small, mode, pieces):
 
 def test_ring_geometry_bit_identical(small):
     w, host = small("unet3d")
-    a, _ = run_per_key(w, host, "pageable", 3, seed=5, ring_slots=2, slot_bytes=4096)
+    a, _ = run_per_key(w, host, "pageable-staged", 3, seed=5, ring_slots=2, slot_bytes=4096)
     b, _ = run_per_key(w, host, "pinned-staged", 1, ring_slots=6, slot_bytes=1 << 24)
     for p in range(w.n_keys):
         assert np.array_equal(a[p], b[p]), f"key {p}"
