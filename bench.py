@@ -285,6 +285,8 @@ def dist_setup():
     if world > 1:
         import torch.distributed as dist
         import torch
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)          # one GPU per rank, bound before NCCL starts
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend)
         pg = dist
@@ -293,7 +295,11 @@ def dist_setup():
 
 def barrier(pg):
     if pg is not None:
-        pg.barrier()
+        import torch
+        if pg.get_backend() == "nccl":
+            pg.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            pg.barrier()
 
 
 def max_over_ranks(pg, v: float) -> float:
