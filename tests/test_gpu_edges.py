@@ -8,7 +8,7 @@ import torch
 import oracle
 import server_side_fedavg_gb300 as fa
 from tests.compare import Bf16Tally, check_bf16, check_f32, check_f32_to_bf16
-from tests.gpu_helpers import sentinel, sentinel_np, to_dev, to_np
+from tests.gpu_helpers import sentinel, sentinel_np, to_dev, to_np, to_pinned
 
 pytestmark = pytest.mark.gpu
 
@@ -148,6 +148,61 @@ def test_error_codes():
         assert fa.fa_get_stats(ctx)["chunks"] == 2
     finally:
         fa.fa_close(ctx)
+
+
+def _classes(v):
+    """0 finite, 1 NaN, 2 +inf, 3 -inf."""
+    return np.where(np.isnan(v), 1, np.where(v == np.inf, 2, np.where(v == -np.inf, 3, 0)))
+
+
+@pytest.mark.parametrize("din,dout", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16")])
+@pytest.mark.parametrize("mode", ["device", "pinned"])
+def test_non_finite_values_propagate_as_ieee(din, dout, mode):
+    """No special cases for non-finite inputs (IEEE propagation): +inf and -inf pass
+    through, inf + (-inf) and NaN give NaN, and a zero-weight client's inf gives NaN
+    (0 * inf) -- as the fp64 oracle computes; finite elements keep their bounds."""
+    rng = np.random.default_rng(21)
+    n = 3 * 4096 + 7
+    K = 3
+    w = [3.0, 5.0, 0.0]
+    xs = [(_f32(rng, n) if din == "f32" else _bf16(rng, n)) for _ in range(K)]
+    if din == "f32":
+        pinf, ninf, nan = np.float32(np.inf), np.float32(-np.inf), np.float32(np.nan)
+    else:
+        pinf, ninf, nan = np.uint16(0x7F80), np.uint16(0xFF80), np.uint16(0x7FC0)
+    plant = {(0, 10): pinf, (1, 20): nan, (0, 30): pinf, (1, 30): ninf, (2, 40): pinf,
+             (0, 50): ninf, (0, 4100): nan, (1, n - 1): pinf}
+    for (k, i), v in plant.items():
+        xs[k][i] = v
+    ctx = fa.fa_open([("k", n)], din, dout, K)
+    try:
+        keep = []
+        for k in range(K):
+            t = to_dev(xs[k]) if mode == "device" else to_pinned(xs[k])
+            keep.append(t)
+            fa.fa_accumulate(ctx, k, w[k], 0, 0, t, n)
+        out = sentinel(n, dout)
+        fa.fa_finalize(ctx, [out])
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+    finally:
+        fa.fa_close(ctx)
+    got = to_np(out, dout)
+    want, _, _ = oracle.fedavg_key(w, [True] * K, xs, din, dout)
+    as_f = (lambda b: (b.astype(np.uint32) << 16).view(np.float32)) if dout == "bf16" else (lambda a: a)
+    g, wv = as_f(got), as_f(want)
+    assert np.array_equal(_classes(g), _classes(wv))
+    expect_bad = {10: 2, 20: 1, 30: 1, 40: 1, 50: 3, 4100: 1, n - 1: 2}
+    for i, c in expect_bad.items():
+        assert _classes(wv[i:i + 1])[0] == c, i
+    fin = _classes(wv) == 0
+    mx = max(float(np.abs(np.nan_to_num((xs[k].astype(np.uint32) << 16).view(np.float32)
+                                         if din == "bf16" else xs[k], posinf=0, neginf=0)).max())
+             for k in range(K))
+    if dout == "f32":
+        check_f32(got[fin], want[fin], mx, K, "finite elements")
+    else:
+        check_f32_to_bf16(got[fin], want[fin], mx, K, "finite elements")
 
 
 def test_host_outputs_match_device_outputs():
