@@ -619,7 +619,7 @@ def run_e2e(args, w, layout, s, pg, world):
     return {"value": round(v, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
             "ms_per_step": round(dt / args.e2e_steps * 1e3, 2),
-            "accumulate_ms": round(acc_ms, 1), "finalize_ms": round(fin_ms, 1),
+            "accumulate_ms": round(acc_ms, 3), "finalize_ms": round(fin_ms, 3),
             "h2d_peak_gbs": round(link, 1),
             "link_frac": round(h2d * args.e2e_steps / dt / 1e9 / link, 3),
             "accumulate_link_frac": round(h2d / (acc_ms * 1e-3) / 1e9 / link, 3),

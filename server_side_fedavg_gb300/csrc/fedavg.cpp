@@ -129,8 +129,10 @@ fa_status cuda_fail(fa_ctx* c, cudaError_t e, const char* where) {
         if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
     } while (0)
 
-// Poll an event until it completes or the deadline passes.
-fa_status wait_event(fa_ctx* c, cudaEvent_t ev, const char* what) {
+// Poll an event until it completes or the deadline (timeout_ms) passes: yielding, then
+// in 50 us sleeps -- or, with `spin`, yielding only (for short waits on the critical
+// path, where a sleep's overshoot would leave the GPU idle).
+fa_status wait_event(fa_ctx* c, cudaEvent_t ev, const char* what, bool spin = false) {
     auto t0 = std::chrono::steady_clock::now();
     uint32_t spins = 0;
     for (;;) {
@@ -144,7 +146,7 @@ fa_status wait_event(fa_ctx* c, cudaEvent_t ev, const char* what) {
             c->err = std::string(what) + ": no completion within timeout_ms";
             return FA_ERR_TIMEOUT;
         }
-        if (++spins < 64)
+        if (spin || ++spins < 64)
             std::this_thread::yield();
         else
             std::this_thread::sleep_for(std::chrono::microseconds(50));
@@ -353,7 +355,7 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
             if (ce != cudaSuccess) r = cuda_fail(c, ce, "pageable read");
         }
         if (r == FA_OK) r = chain_out(c, s);
-        if (r == FA_OK && kind == Mem::kPageable) r = wait_event(c, c->read_ev, "pageable chunk read");
+        if (r == FA_OK && kind == Mem::kPageable) r = wait_event(c, c->read_ev, "pageable chunk read", true);
         if (r == FA_OK) c->stats.h2d_bytes += len * c->s_in;
     } else {
         // host memory: through the staging ring, slot-sized pieces

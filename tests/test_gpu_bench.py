@@ -1,0 +1,71 @@
+"""bench.py end to end on the GPU, on the small tiny-CNN workload: one JSON line with
+every key of the contract, byte counts that match the workload, and the reference
+arm's line.  Runs bench.py as its own process, as the benchmark driver does."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args):
+    r = subprocess.run([sys.executable, "bench.py", *args], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-3000:]
+    return json.loads(lines[0])
+
+
+def test_bench_line_has_the_contract():
+    w = W.make("tiny")
+    si = 2 if w.dtype_in == "bf16" else 4
+    so = 2 if w.dtype_out == "bf16" else 4
+    d = _run("--workload", "tiny", "--steps", "2", "--warmup", "3", "--e2e-steps", "2",
+             "--ref-elems", str(1 << 16))
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+        assert k in d, k
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert d["vs_baseline"] is None and d["data"] == "synthetic" and d["dtype"] == "f32"
+    assert d["config"]["workload"] == "tiny" and d["config"]["P"] == w.P and d["config"]["K"] == w.K
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    # value = client bytes per step / time per step
+    client = w.K * w.P * si
+    assert abs(d["value"] - client / (d["ms_per_step"] * 1e-3) / 1e9) <= 0.05 * d["value"]   # rounding of ms
+    r = d["roofline"]
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in r, k
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    c = d["cpu_baseline"]
+    assert c["kind"] == "oracle" and c["unit"] == "GB/s" and c["cores"] >= 1 and c["value"] > 0
+    assert c["value_1thread"] > 0 and c["sample"]
+    e = d["e2e"]
+    assert e["unit"] == "GB/s" and e["value"] > 0
+    assert e["h2d_bytes_per_step"] == client               # every client byte crosses the link
+    assert e["d2h_bytes_per_step"] == w.P * so             # the aggregate comes back
+    assert e["accumulate_ms"] > 0 and e["finalize_ms"] > 0 and e["h2d_peak_gbs"] > 0
+    assert d["gpu_launches"] >= 2 * (w.K + 1)              # >= one accumulate per client + finalize, per step
+    assert d["resident"]["value"] > 0 and d["resident"]["launches_per_round"] >= 1
+    clk = d["clocks"]
+    if clk is not None:
+        assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
+
+
+def test_reference_arm_line():
+    d = _run("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3",
+             "--ref-elems", str(1 << 16))
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["unit"] == "GB/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
