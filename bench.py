@@ -27,6 +27,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -176,14 +177,23 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, device: int):
+        # nvidia-smi addresses the GPU by UUID: its indexes need not match CUDA's when
+        # CUDA_VISIBLE_DEVICES remaps them
+        self.gpu = str(device)
+        try:
+            import torch
+            uuid = getattr(torch.cuda.get_device_properties(device), "uuid", None)
+            if uuid is not None:
+                self.gpu = f"GPU-{uuid}"
+        except Exception:  # pragma: no cover - property missing in this torch
+            pass
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="fedavg_clocks_", suffix=".csv")
+        os.close(fd)
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -211,6 +221,7 @@ class ClockSampler:
                     rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
                 except ValueError:
                     continue
+        os.unlink(self.path)
         if not rows:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
