@@ -55,3 +55,46 @@ def test_f32_to_bf16_bound():
     c[0] += 3                         # three ulps at 1.0 (0.023) > 2e-7 + 0.0078
     with pytest.raises(AssertionError):
         check_f32_to_bf16(c, a, 0.05, 4)
+
+
+def _bits(vals):
+    return (np.asarray(vals, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_fp32_sum_model_hand_case():
+    """3*1 + 5*2 = 13, / 8 = 1.625, exact in every format."""
+    from tests.compare import fp32_sum_model
+    xs = [_bits([1.0]), _bits([2.0])]
+    assert fp32_sum_model([3.0, 5.0], [True, True], xs, "f32")[0] == np.float32(1.625)
+    assert fp32_sum_model([3.0, 5.0], [True, True], xs, "bf16")[0] == _bits([1.625])[0]
+    # a client that did not report contributes nothing, and is not in N
+    xs3 = xs + [_bits([100.0])]
+    assert fp32_sum_model([3.0, 5.0, 7.0], [True, True, False], xs3, "f32")[0] == np.float32(1.625)
+
+
+def test_fp32_sum_model_keeps_sequential_rounding():
+    """2^24 + 1 rounds back to 2^24 in fp32 (ties to even), so 2^24 + 1 - 2^24 is 0 in
+    the fp32 sum while the exact mean is 1/3: the model must show the fp32 result."""
+    from tests.compare import fp32_sum_model
+    xs = [_bits([2.0 ** 24]), _bits([1.0]), _bits([-(2.0 ** 24)])]
+    assert fp32_sum_model([1.0, 1.0, 1.0], [True] * 3, xs, "f32")[0] == 0.0
+    import oracle
+    y, _, _ = oracle.fedavg_key([1.0, 1.0, 1.0], [True] * 3, xs, "bf16", "f32")
+    assert y[0] == np.float32(1.0 / 3.0)
+
+
+def test_tally_accepts_beyond_one_ulp_only_where_the_fp32_sum_explains_it():
+    from tests.compare import Bf16Tally
+    want = np.array([0x3F80, 0x3F80], np.uint16)
+    got = want.copy()
+    got[1] += 10                                  # 10 ulps at 1.0 (0.078)
+    model = got.copy()
+    t = Bf16Tally()
+    t.add(got, want, "explained", model=model, bound=0.1)
+    assert t.beyond == 1
+    with pytest.raises(AssertionError):           # no model: the plain rule
+        Bf16Tally().add(got, want, "plain")
+    with pytest.raises(AssertionError):           # the model disagrees with the device
+        Bf16Tally().add(got, want, "unexplained", model=want, bound=0.1)
+    with pytest.raises(AssertionError):           # beyond the fp32 bound
+        Bf16Tally().add(got, want, "too far", model=model, bound=1e-3)
