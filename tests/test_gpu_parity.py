@@ -306,12 +306,15 @@ def test_full_size_resident_sampled(name):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("staged", [False, True])
-def test_full_size_host_fed_sampled(staged):
-    """The 2.2B VLM streamed client by client from PINNED HOST memory in 64 MiB flat
+@pytest.mark.parametrize("name,staged,host_out", [("vlm2b", False, False), ("vlm2b", True, False),
+                                                  ("llama7b", False, True)])
+def test_full_size_host_fed_sampled(name, staged, host_out):
+    """A full-size workload streamed client by client from PINNED HOST memory in its flat
     chunks -- read in place by the kernel over the host link, or through the library's
-    staging ring (FA_STAGE_HOST) -- sampled against the oracle."""
-    w = W.make("vlm2b")
+    staging ring (FA_STAGE_HOST) -- and, for the 7B decoder as bench.py's end-to-end run
+    does it, the aggregate written in place into a pinned host buffer; sampled against
+    the oracle."""
+    w = W.make(name)
     idx = _sample_indices(w, seed=3)
     host = torch.empty(w.P, dtype=torch.int16).pin_memory()
     hv = host.numpy().view(np.uint16)
@@ -325,15 +328,27 @@ def test_full_size_host_fed_sampled(staged):
                 n = min(w.chunk_elems, w.P - c0)
                 fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, host.data_ptr() + 2 * c0, n, s)
             s.synchronize()              # the pinned buffer is read on `s`: wait before refilling it
-        out = torch.empty(w.P, dtype=torch.int16, device="cuda")
+        if host_out:
+            out = host                   # the input buffer is free now: reuse it as the output
+            out.fill_(0x7FBF)
+        else:
+            out = torch.empty(w.P, dtype=torch.int16, device="cuda")
         fa.fa_finalize(ctx, [out], s)
         fa.fa_sync(ctx)
+        s.synchronize()
         st = fa.fa_get_stats(ctx)
         assert st["h2d_bytes"] == w.K * w.P * 2
+        assert st["d2h_bytes"] == (w.P * 2 if host_out else 0)
     finally:
         fa.fa_close(ctx)
-    got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+    if host_out:
+        got = hv[idx.astype(np.int64)].copy()
+        # the sentinel is a NaN pattern and every aggregate is finite: all P elements written
+        assert not np.any((hv & 0x7F80) == 0x7F80), "an output element is not finite (or not written)"
+    else:
+        got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+    del host
     xs = [synth.client_gather(w, k, idx) for k in range(w.K)]
-    what = "vlm2b host-fed " + ("staged" if staged else "in place")
+    what = f"{name} host-fed " + ("staged" if staged else "in place") + (", host output" if host_out else "")
     frac = _check_sampled(got, xs, w, what)
     print(f"{what}: {idx.size} sampled elements, {frac:.6%} bit-identical")
