@@ -6,8 +6,9 @@ import pytest
 import torch
 
 import oracle
+import synth
 import server_side_fedavg_gb300 as fa
-from tests.compare import Bf16Tally, check_bf16, check_f32, check_f32_to_bf16
+from tests.compare import Bf16Tally, check_bf16, check_f32, check_f32_to_bf16, fp32_sum_model
 from tests.gpu_helpers import sentinel, sentinel_np, to_dev, to_np, to_pinned
 
 pytestmark = pytest.mark.gpu
@@ -345,3 +346,56 @@ def test_concurrent_client_threads():
             assert fa.fa_key_total(ctx, p) == (N, cnt)
     finally:
         fa.fa_close(ctx)
+
+
+@pytest.mark.slow
+def test_key_of_more_than_2_pow_32_elements():
+    """One key of 2^32 + 77 bf16 elements, so offsets inside a single segment pass 2^31 and
+    2^32: two clients streamed whole, then the same two reduced resident (fa_reduce_resident),
+    sampled against the oracle around 2^31, 2^32 and the ragged end."""
+    n = (1 << 32) + 77
+    need = 2 * n * 2 + n * 4 + n * 2 + (4 << 30)
+    free, _ = torch.cuda.mem_get_info()
+    if free < need:
+        pytest.fail(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
+    seed, sigma = 4242, 0.02
+    w = [700.0, 300.0]
+    s = torch.cuda.current_stream()
+    xd = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(2)]
+    for k in range(2):
+        synth.fill_device(seed, k, 0, sigma, "bf16", 0, n, xd[k].data_ptr(), s.cuda_stream)
+    rng = np.random.default_rng(5)
+    idx = np.unique(np.concatenate([
+        np.arange(0, 64), np.arange((1 << 31) - 64, (1 << 31) + 64),
+        np.arange((1 << 32) - 64, (1 << 32) + 64), np.arange(n - 200, n),
+        rng.integers(0, n, 20000)])).astype(np.int64)
+    tidx = torch.from_numpy(idx).cuda()
+    out = torch.empty(n, dtype=torch.int16, device="cuda")
+    got = {}
+    ctx = fa.fa_open([("big", n)], "bf16", "bf16", 2)
+    try:
+        for k in range(2):
+            fa.fa_accumulate(ctx, k, w[k], 0, 0, xd[k], n, s)
+        fa.fa_finalize(ctx, [out], s)
+        fa.fa_sync(ctx)
+        got["streamed"] = out[tidx].cpu().numpy().view(np.uint16)
+    finally:
+        fa.fa_close(ctx)
+    out.fill_(0x7FBF)
+    ctx = fa.fa_open([("big", n)], "bf16", "bf16", 2)
+    try:
+        fa.fa_reduce_resident(ctx, [0, 1], w, xd, [out], s)
+        fa.fa_sync(ctx)
+        got["resident"] = out[tidx].cpu().numpy().view(np.uint16)
+    finally:
+        fa.fa_close(ctx)
+    del xd, out
+    torch.cuda.empty_cache()
+    xs = [synth.gather(seed, k, 0, sigma, "bf16", idx.astype(np.uint64)) for k in range(2)]
+    want, N, cnt = oracle.fedavg_key(w, [True, True], xs, "bf16", "bf16")
+    assert (N, cnt) == (1000.0, 2)
+    model = fp32_sum_model(w, [True, True], xs, "bf16")
+    mx = max(float(np.abs(synth.to_f64(x, "bf16")).max()) for x in xs)
+    for how, g in got.items():
+        check_bf16(g, want, f"2^32 + 77 elements, {how}", model=model, bound=1e-6 * mx * 2)
+    assert np.array_equal(got["streamed"], got["resident"])
