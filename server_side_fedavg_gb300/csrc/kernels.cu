@@ -723,10 +723,28 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
         if constexpr (kApply) amask |= reinterpret_cast<uintptr_t>(sg.base) + e0 * sizeof(Tout);
         if ((amask & 15u) == 0) {
             if (cnt == kTile) {
+                // every load of the tile first: a store (asm volatile, memory clobber) would
+                // otherwise hold the next vector's loads back, leaving one in flight per thread
+                float4 lo[kUnroll], hi[kUnroll];
+                float b[kUnroll][8];
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
                     const uint32_t v = threadIdx.x + u * kBlock;
-                    fin_vec<Tout, kApply>(sg, e0 + v * kVec, s0 + v * kVec, d, lr);
+                    lo[u] = ld_v4f(s0 + v * kVec);
+                    hi[u] = ld_v4f(s0 + v * kVec + 4);
+                    if constexpr (kApply) LoadBase<Tout>::vec(sg.base, e0 + v * kVec, b[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const uint32_t v = threadIdx.x + u * kBlock;
+                    float q[8] = {__fdiv_rn(lo[u].x, d), __fdiv_rn(lo[u].y, d), __fdiv_rn(lo[u].z, d),
+                                  __fdiv_rn(lo[u].w, d), __fdiv_rn(hi[u].x, d), __fdiv_rn(hi[u].y, d),
+                                  __fdiv_rn(hi[u].z, d), __fdiv_rn(hi[u].w, d)};
+                    if constexpr (kApply) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) q[i] = __fmaf_rn(lr, q[i], b[u][i]);
+                    }
+                    global_store8<Tout>(sg.out, e0 + v * kVec, q);
                 }
             } else {
                 const uint32_t nv = cnt / kVec;
@@ -965,7 +983,8 @@ cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, 
                             const float* acc, bool apply, float server_lr, const LaunchShape& s,
                             cudaStream_t stream) {
     if (ntiles == 0 || nseg == 0) return cudaSuccess;
-    const uint32_t grid = grid_for(ntiles, s.sms, s.fin_ctas_per_sm[apply ? 1 : 0][dtype_out == 0 ? 0 : 1]);
+    const int occ = s.fin_ctas_per_sm[apply ? 1 : 0][dtype_out == 0 ? 0 : 1];
+    const uint32_t grid = grid_for(ntiles, s.sms, std::min(occ, kFinCtasPerSm));
     if (dtype_out == 0) {
         if (apply) finalize_kernel<float, true><<<grid, kBlock, 0, stream>>>(segs, nseg, ntiles, acc, server_lr);
         else finalize_kernel<float, false><<<grid, kBlock, 0, stream>>>(segs, nseg, ntiles, acc, server_lr);

@@ -25,6 +25,9 @@ constexpr int kVec = 8;               // elements per vector (16 B of bf16, 2 x 
 constexpr int kTile = 4096;           // elements per tile of the finalize kernel
 constexpr int kBulkTile = 8192;       // elements per pipeline stage of the streaming kernel
 constexpr int kDirectTile = kBlock * kVec;   // elements per tile of the direct-load accumulate
+// Finalize CTAs per SM: with a tile's loads issued together, 4 CTAs (about 64 KB of loads
+// in flight per SM) gave the best rate in a sweep of 2..8 on GB300; more in flight was slower.
+constexpr int kFinCtasPerSm = 4;
 constexpr int kMaxSegs = 48;          // segments per accumulate / reduce launch
 constexpr int kMaxBatch = 16;         // resident clients per launch
 constexpr int kReduceStageBytes = 73728;   // shared-memory budget per stage of the reduce kernel
