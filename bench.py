@@ -627,6 +627,15 @@ def run_e2e(args, w, layout, s, pg, world):
     h2d = (st1["h2d_bytes"] - st0["h2d_bytes"]) // args.e2e_steps
     d2h = (st1["d2h_bytes"] - st0["d2h_bytes"]) // args.e2e_steps
     v = world * w.K * w.P * si * args.e2e_steps / dt / 1e9
+    # HBM traffic of the host-fed round: the running sum (written by the first client, read
+    # and written by every later one, read by finalize); staging adds each chunk's write and
+    # read in HBM, and a staged output its device copy (written, then read by the copy)
+    hbm = w.P * (4 + 8 * (w.K - 1) + 4)
+    if args.stage_host:
+        hbm += w.K * w.P * 2 * si
+    if args.stage_host or not out_pinned:
+        hbm += 2 * w.P * so
+    peak, _ = _peaks()
     return {"value": round(v, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
             "ms_per_step": round(dt / args.e2e_steps * 1e3, 2),
@@ -634,6 +643,8 @@ def run_e2e(args, w, layout, s, pg, world):
             "h2d_peak_gbs": round(link, 1),
             "link_frac": round(h2d * args.e2e_steps / dt / 1e9 / link, 3),
             "accumulate_link_frac": round(h2d / (acc_ms * 1e-3) / 1e9 / link, 3),
+            "hbm_gbs": round(hbm * args.e2e_steps / dt / 1e9, 1),
+            "hbm_frac": round(hbm * args.e2e_steps / dt / 1e9 / peak, 4),
             "host_pool": f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused",
             "output": (("pinned host buffer, " + ("copied from a device buffer" if args.stage_host
                                                   else "written in place by the finalize kernel"))

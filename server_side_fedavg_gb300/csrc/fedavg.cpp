@@ -3,13 +3,16 @@
 // One context = one round's state on one GPU:
 //  - the fp32 running sum in device memory (padded layout, see ledger.hpp);
 //  - the host ledger (weights, reporter masks, element counts, per-key totals);
-//  - a staging ring for chunks that arrive in host memory: R device slots fed by
-//    cudaMemcpyAsync on a copy stream, overlapped with the kernels on the caller's
-//    stream, plus R pinned host slots used only for pageable sources.  This is the
-//    chunked, memory-bounded ingest that "Building Federated Multimodal AI Workflows
-//    with NVIDIA FLARE" motivates ("Moving and aggregating large model updates
-//    efficiently": the Tensor Downloader's chunk size trades per-request overhead
-//    against per-chunk memory);
+//  - host chunks the device can address (pinned memory mapped at the same pointer;
+//    pageable memory where the device walks the host page tables) are read in place
+//    by the direct-load accumulate kernel over the host link, straight into the sum;
+//  - a staging ring for the other host chunks (and all of them under FA_STAGE_HOST):
+//    R device slots fed by cudaMemcpyAsync on a copy stream, overlapped with the
+//    kernels on the caller's stream, plus R pinned host slots used only for pageable
+//    sources.  This is the chunked, memory-bounded ingest that "Building Federated
+//    Multimodal AI Workflows with NVIDIA FLARE" motivates ("Moving and aggregating
+//    large model updates efficiently": the Tensor Downloader's chunk size trades
+//    per-request overhead against per-chunk memory);
 //  - an event chain: after every launch an event is recorded on the stream used and
 //    the next launch (on any stream) waits for it, so contributions land in call
 //    order and streams never race on the running sum.

@@ -55,6 +55,7 @@ def test_bench_line_has_the_contract():
     assert e["h2d_bytes_per_step"] == client               # every client byte crosses the link
     assert e["d2h_bytes_per_step"] == w.P * so             # the aggregate comes back
     assert e["accumulate_ms"] > 0 and e["finalize_ms"] > 0 and e["h2d_peak_gbs"] > 0
+    assert 0 < e["hbm_frac"] < 1 and e["hbm_gbs"] > 0
     assert d["gpu_launches"] >= 2 * (w.K + 1)              # >= one accumulate per client + finalize, per step
     assert d["resident"]["value"] > 0 and d["resident"]["launches_per_round"] >= 1
     clk = d["clocks"]
