@@ -399,3 +399,48 @@ def test_key_of_more_than_2_pow_32_elements():
     for how, g in got.items():
         check_bf16(g, want, f"2^32 + 77 elements, {how}", model=model, bound=1e-6 * mx * 2)
     assert np.array_equal(got["streamed"], got["resident"])
+
+
+def test_caller_registered_host_memory():
+    """Host memory the caller page-locked with cudaHostRegister (a NumPy buffer, say) is
+    pinned memory to the library: read in place where the device maps it at the same
+    address, else staged.  Same bits as device ingest, ragged chunks included."""
+    rng = np.random.default_rng(33)
+    n = 5 * 4096 + 13
+    K = 3
+    xs = [_bf16(rng, n) for _ in range(K)]
+    w = [11.0, 13.0, 17.0]
+    cudart = torch.cuda.cudart()
+    bufs = [np.empty(n + 64, np.uint16) for _ in range(K)]     # registered as a whole
+    for b in bufs:
+        assert int(cudart.cudaHostRegister(b.ctypes.data, b.nbytes, 0)) == 0
+    outs = {}
+    try:
+        for how in ("registered", "device"):
+            ctx = fa.fa_open([("k", n)], "bf16", "bf16", K)
+            try:
+                keep = []
+                for k in range(K):
+                    if how == "registered":
+                        bufs[k][3:3 + n] = xs[k]                # an odd start inside the region
+                        base = bufs[k].ctypes.data + 6
+                    else:
+                        t = to_dev(xs[k])
+                        keep.append(t)
+                        base = t.data_ptr()
+                    for a, b in [(0, 4097), (4097, 4100), (4100, n)]:
+                        fa.fa_accumulate(ctx, k, w[k], 0, a, base + 2 * a, b - a)
+                out = sentinel(n, "bf16")
+                fa.fa_finalize(ctx, [out])
+                fa.fa_sync(ctx)
+                torch.cuda.synchronize()
+                outs[how] = to_np(out, "bf16")
+            finally:
+                fa.fa_close(ctx)
+    finally:
+        torch.cuda.synchronize()
+        for b in bufs:
+            cudart.cudaHostUnregister(b.ctypes.data)
+    assert np.array_equal(outs["registered"], outs["device"])
+    want, _, _ = oracle.fedavg_key(w, [True] * K, xs, "bf16", "bf16")
+    check_bf16(outs["device"], want, "registered host memory")
