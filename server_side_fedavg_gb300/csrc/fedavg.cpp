@@ -665,7 +665,8 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
         FA_CUDA(c, cudaEventRecord(c->fin_ev, s));
         c->fin_pending = true;
         FA_CUDA(c, fa::launch_finalize(c->fin_dev, nseg, ntiles, c->dout, c->acc, apply,
-                                       static_cast<float>(server_lr), c->shape, s));
+                                       static_cast<float>(server_lr), written_in_place > 0,
+                                       c->shape, s));
         c->stats.kernel_launches++;
         c->stats.d2h_bytes += written_in_place;
         // host outputs: copy the staged keys back, merging neighbours in the flat layout

@@ -980,11 +980,11 @@ cudaError_t launch_reduce_final(const RedArgs& a, int dtype_in, int dtype_out,
 }
 
 cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_out,
-                            const float* acc, bool apply, float server_lr, const LaunchShape& s,
-                            cudaStream_t stream) {
+                            const float* acc, bool apply, float server_lr, bool host_out,
+                            const LaunchShape& s, cudaStream_t stream) {
     if (ntiles == 0 || nseg == 0) return cudaSuccess;
     const int occ = s.fin_ctas_per_sm[apply ? 1 : 0][dtype_out == 0 ? 0 : 1];
-    const uint32_t grid = grid_for(ntiles, s.sms, std::min(occ, kFinCtasPerSm));
+    const uint32_t grid = grid_for(ntiles, s.sms, host_out ? occ : std::min(occ, kFinCtasPerSm));
     if (dtype_out == 0) {
         if (apply) finalize_kernel<float, true><<<grid, kBlock, 0, stream>>>(segs, nseg, ntiles, acc, server_lr);
         else finalize_kernel<float, false><<<grid, kBlock, 0, stream>>>(segs, nseg, ntiles, acc, server_lr);

@@ -127,8 +127,11 @@ cudaError_t launch_reduce_final(const RedArgs& a, int dtype_in, int dtype_out,
 // segs: device array of nseg FinSeg sorted by tile0.
 //   apply == false: out = RNE(sum / N)
 //   apply == true:  out = RNE(fma(server_lr, sum / N, base))   (delta rounds)
+// host_out: some outputs are host memory written in place over the host link; the grid
+// then runs at full occupancy (more stores in flight for the link) instead of
+// kFinCtasPerSm, the HBM-bound optimum.
 cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_out,
-                            const float* acc, bool apply, float server_lr, const LaunchShape& s,
-                            cudaStream_t stream);
+                            const float* acc, bool apply, float server_lr, bool host_out,
+                            const LaunchShape& s, cudaStream_t stream);
 
 }  // namespace fa
