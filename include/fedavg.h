@@ -108,7 +108,8 @@ typedef struct {
                                    copies and in-place reads) */
     uint64_t d2h_bytes;         /* bytes of aggregate fa_finalize sent to host memory (copies
                                    and in-place stores) */
-    uint64_t chunks;            /* accepted fa_accumulate / fa_accumulate_batch calls */
+    uint64_t chunks;            /* accepted chunks: one per fa_accumulate / fa_accumulate_batch
+                                   call, n_chunks per fa_accumulate_keys call */
 } fa_stats;
 
 /* Create an aggregation context on the current CUDA device.
@@ -169,6 +170,28 @@ fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64
 fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
                               const double* weights, int64_t key, uint64_t offset_elems,
                               const void* const* chunk_ptrs, uint64_t len_elems, void* stream);
+
+/* Several chunks of ONE client in one call: chunk i covers elements
+ * [offsets[i], offsets[i] + lens[i]) of key keys[i] (FA_KEY_FLAT: of the flat layout)
+ * and is read from chunk_ptrs[i].  Equivalent to n_chunks calls of fa_accumulate with
+ * the same client, weight and stream, in index order, and bit-identical to them; the
+ * library packs the chunks into launches of up to 48 key segments, so a client that
+ * sends many small tensors -- an adapter subset, [FLARE]'s FedUMM LoRA modules --
+ * costs a few launches instead of one per tensor.  Validated as a whole: on an
+ * argument, range, weight or state error nothing is recorded.
+ *   keys, offsets, lens, chunk_ptrs   n_chunks entries each (caller-owned, read during
+ *                  the call); chunks of one key must not overlap, as for fa_accumulate
+ * The chunks are read in place: all in this GPU's memory, or all in host memory the
+ * device addresses (as for fa_accumulate: pinned memory mapped at the same pointer, or
+ * pageable memory where the device walks the host page tables, in which case the call
+ * waits for the reads).  Other memory, a mix, or host chunks under FA_STAGE_HOST give
+ * FA_ERR_ARG: send those through fa_accumulate.  Ownership and stream ordering as for
+ * fa_accumulate; n_chunks == 0 or all lens zero is a no-op.
+ * Errors: FA_ERR_ARG, FA_ERR_RANGE, FA_ERR_WEIGHT, FA_ERR_STATE, FA_ERR_CUDA,
+ * FA_ERR_TIMEOUT. */
+fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, uint32_t n_chunks,
+                             const int64_t* keys, const uint64_t* offsets,
+                             const void* const* chunk_ptrs, const uint64_t* lens, void* stream);
 
 /* Write the aggregate: for every key with N_p > 0,
  *     out[p][i] = round_to_dtype_out( sum[p][i] / (float)N_p )      (IEEE division, RNE)

@@ -84,6 +84,8 @@ def lib():
         L.fa_accumulate.argtypes = [vp, u32, f64, i64, u64, vp, u64, vp]
         L.fa_accumulate_batch.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64), i64,
                                           u64, ctypes.POINTER(vp), u64, vp]
+        L.fa_accumulate_keys.argtypes = [vp, u32, f64, u32, ctypes.POINTER(i64), ctypes.POINTER(u64),
+                                         ctypes.POINTER(vp), ctypes.POINTER(u64), vp]
         L.fa_finalize.argtypes = [vp, ctypes.POINTER(vp), vp]
         L.fa_reduce_resident.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64),
                                          ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
@@ -102,7 +104,7 @@ def lib():
         L.fa_strerror.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = [vp]
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_finalize",
+        for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_accumulate_keys", "fa_finalize",
                      "fa_finalize_apply", "fa_reduce_resident", "fa_reset",
                      "fa_close", "fa_key_total", "fa_sync", "fa_get_stats"):
             getattr(L, name).restype = i32
@@ -176,6 +178,28 @@ def fa_accumulate_batch(ctx, client_ids, weights, key, offset_elems, chunks, len
     ps = (ctypes.c_void_p * J)(*[_ptr(c) for c in chunks])
     _check(lib().fa_accumulate_batch(ctx, J, ids, ws, key, offset_elems, ps, len_elems,
                                      _stream(stream)), ctx)
+
+
+def fa_accumulate_keys(ctx, client_id, weight_nk, keys, offsets, chunks, lens, stream=None):
+    """One client's chunks in one call: chunk i is `lens[i]` elements at `offsets[i]` of
+    key `keys[i]` (FA_KEY_FLAT: of the flat layout), read from `chunks[i]` (pointers as
+    ints or a uint64 array, or tensors / arrays).  Sequences or NumPy arrays."""
+    import numpy as np
+    ks = np.ascontiguousarray(keys, dtype=np.int64)
+    os_ = np.ascontiguousarray(offsets, dtype=np.uint64)
+    ls = np.ascontiguousarray(lens, dtype=np.uint64)
+    if isinstance(chunks, np.ndarray):
+        ps = np.ascontiguousarray(chunks, dtype=np.uint64)
+    else:
+        ps = np.fromiter((_ptr(c) for c in chunks), dtype=np.uint64, count=len(chunks))
+    n = ks.size
+    if not (os_.size == ps.size == ls.size == n):
+        raise ValueError("keys, offsets, chunks and lens must have the same length")
+    _check(lib().fa_accumulate_keys(
+        ctx, client_id, float(weight_nk), n, ks.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        os_.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+        ps.ctypes.data_as(ctypes.POINTER(ctypes.c_void_p)),
+        ls.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), _stream(stream)), ctx)
 
 
 def fa_finalize(ctx, outs, stream=None):

@@ -249,7 +249,9 @@ fa_status ensure_ring(fa_ctx* c, bool need_host) {
 }
 
 // Launch the accumulate kernel(s) for the pieces that fall in chunk elements
-// [c0, c0 + n), reading inputs xs[0..J) whose element 0 is chunk element c0.
+// [c0, c0 + n), reading inputs xs[0..J) whose element 0 is chunk element c0 -- or, for
+// one client's several chunks (J = 1, fa_accumulate_keys), xs[i] is chunk i and each
+// piece reads the chunk it was cut from.
 fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_t c0,
                         uint64_t n, const void* const* xs, const float* ws, uint32_t J,
                         cudaStream_t s, bool direct = false) {
@@ -284,13 +286,16 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
                 if (st != FA_OK) return st;
             }
             fa::AccSeg& g = a.seg[a.nseg];
+            // one client: each piece reads its own chunk (xs[p.chunk]); J > 1: xs[j]
+            g.x = jb == 1 ? xs[done + p.chunk] : a.x[0];
             g.x_off = b - c0;
             g.acc_idx = p.acc_idx + (b - p.chunk_off);
             g.len = e - b;
             g.first = (p.first && done == 0) ? 1u : 0u;
             bool ok = (reinterpret_cast<uintptr_t>(c->acc + g.acc_idx) & 15u) == 0;
             for (uint32_t j = 0; j < jb && ok; ++j) {
-                uintptr_t xa = reinterpret_cast<uintptr_t>(a.x[j]) + g.x_off * c->s_in;
+                const void* base = jb == 1 ? g.x : a.x[j];
+                uintptr_t xa = reinterpret_cast<uintptr_t>(base) + g.x_off * c->s_in;
                 ok = (xa & 15u) == 0;
             }
             if (ok) a.vec_ok |= 1ull << a.nseg;
@@ -577,6 +582,66 @@ fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* c
                            len_elems, static_cast<cudaStream_t>(stream), true);
 }
 
+fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, uint32_t n_chunks,
+                             const int64_t* keys, const uint64_t* offsets,
+                             const void* const* chunk_ptrs, const uint64_t* lens, void* stream) {
+    Range range("fa_accumulate_keys");
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    ctx->err.clear();
+    fa_ctx* c = ctx;
+    if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
+    if (n_chunks > 0 && (keys == nullptr || offsets == nullptr || lens == nullptr || chunk_ptrs == nullptr))
+        return fail(c, FA_ERR_ARG, "keys, offsets, chunk_ptrs or lens is NULL");
+    // every chunk is read in place: all device memory, or all host memory the device
+    // addresses
+    bool any = false, all_device = true, all_host = true, pageable = false;
+    uint64_t total = 0;
+    for (uint32_t i = 0; i < n_chunks; ++i) {
+        if (lens[i] == 0) continue;
+        if (chunk_ptrs[i] == nullptr) return fail(c, FA_ERR_ARG, "chunk pointer is NULL");
+        bool other = false, in_place = false;
+        const Mem m = classify(chunk_ptrs[i], c->device, &other, &in_place);
+        if (other) return fail(c, FA_ERR_ARG, "chunk is in another GPU's memory");
+        const bool host_ok = (c->flags & FA_STAGE_HOST) == 0 &&
+                             ((m == Mem::kPinned && in_place) ||
+                              (m == Mem::kPageable && c->pageable_in_place));
+        all_device = all_device && m == Mem::kDevice;
+        all_host = all_host && host_ok;
+        pageable = pageable || m == Mem::kPageable;
+        any = true;
+        total += lens[i];
+    }
+    if (any && !all_device && !all_host)
+        return fail(c, FA_ERR_ARG,
+                    "fa_accumulate_keys reads its chunks in place: all in this GPU's memory, or all "
+                    "in host memory the device addresses; send others through fa_accumulate");
+    std::string e;
+    int32_t st = c->ledger.plan_accumulate_keys(client_id, weight_nk, n_chunks, keys, offsets, lens,
+                                                &c->pieces, &e);
+    if (st != fa::kOk) return fail(c, st, e);
+    if (!any) return FA_OK;
+    const float w = static_cast<float>(weight_nk);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    fa_status r = chain_in(c, s);
+    if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, UINT64_MAX, chunk_ptrs, &w, 1, s, !all_device);
+    if (r == FA_OK && !all_device && pageable) {
+        cudaError_t ce = cudaEventRecord(c->read_ev, s);
+        if (ce != cudaSuccess) r = cuda_fail(c, ce, "pageable read");
+    }
+    if (r == FA_OK) r = chain_out(c, s);
+    if (r == FA_OK && !all_device && pageable) r = wait_event(c, c->read_ev, "pageable chunk read", true);
+    if (r != FA_OK) {
+        c->broken = true;
+        return r;
+    }
+    for (uint32_t i = 0; i < n_chunks; ++i) c->stats.chunks += lens[i] > 0 ? 1 : 0;
+    c->stats.client_bytes += total * c->s_in;
+    if (!all_device) c->stats.h2d_bytes += total * c->s_in;
+    return FA_OK;
+}
+
 }  // extern "C"
 
 namespace {
@@ -795,6 +860,7 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
             a.vec_ok = 0;
             for (; p < nk && a.nseg < static_cast<uint32_t>(fa::kMaxSegs); ++p) {
                 fa::AccSeg& sg = a.seg[a.nseg];
+                sg.x = a.x[0];
                 sg.x_off = c->ledger.flat_off(p);
                 sg.acc_idx = c->ledger.acc_off(p);
                 sg.len = c->ledger.numel(p);

@@ -243,7 +243,6 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
     // launched as a programmatic dependent: set-up above overlaps the previous kernel's
     // tail; nothing in global memory is touched before that kernel has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const Tin* x0 = static_cast<const Tin*>(a.x[0]);
     const float w = a.w[0];
     uint32_t pcur = 0, ccur = 0;      // segment cursors of the producer and the consumers
     uint32_t issued = 0;
@@ -258,7 +257,7 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
             const uint32_t xb = n8 * kVec * sizeof(Tin);
             const uint32_t sb = sg.first ? 0u : n8 * kVec * sizeof(float);
             mbar_expect(bar, xb + sb);
-            bulk_load(xs + s * XB, x0 + sg.x_off + ta.e0, xb, bar);
+            bulk_load(xs + s * XB, static_cast<const Tin*>(sg.x) + sg.x_off + ta.e0, xb, bar);
             if (sb) bulk_load(ss + s * SB, a.acc + sg.acc_idx + ta.e0, sb, bar);
         } else {
             mbar_arrive(bar);
@@ -276,7 +275,7 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
         const TileAt ta = tile_at(a.seg, a.nseg, blockIdx.x + i * gridDim.x, kBulkTile, ccur);
         const AccSeg& sg = a.seg[ta.si];
         const bool first = sg.first != 0;
-        const uint64_t xe0 = sg.x_off + ta.e0;
+        const Tin* xg = static_cast<const Tin*>(sg.x) + sg.x_off + ta.e0;   // tile in global memory
         float* g0 = a.acc + sg.acc_idx + ta.e0;
         const bool bulk = ((a.vec_ok >> ta.si) & 1ull) && ta.cnt >= static_cast<uint32_t>(kVec);
         const uint32_t n8 = bulk ? ta.cnt / kVec : 0;
@@ -306,11 +305,11 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
             const uint32_t tail = ta.cnt - n8 * kVec;
             if (threadIdx.x < tail) {
                 const uint32_t e = n8 * kVec + threadIdx.x;
-                acc_one<Tin>(x0 + xe0 + e, w, g0 + e, first);
+                acc_one<Tin>(xg + e, w, g0 + e, first);
             }
         } else if (ok) {
             for (uint32_t e = threadIdx.x; e < ta.cnt; e += kBlock)
-                acc_one<Tin>(x0 + xe0 + e, w, g0 + e, first);
+                acc_one<Tin>(xg + e, w, g0 + e, first);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (!__syncthreads_and(ok)) break;
@@ -385,14 +384,13 @@ template <typename Tin>
 __global__ void __launch_bounds__(kBlock) accumulate_direct_kernel(const __grid_constant__ AccArgs a) {
     static_assert(kDirectTile == kBlock * kVec, "one vector per thread per tile");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const Tin* x0 = static_cast<const Tin*>(a.x[0]);
     const float w = a.w[0];
     uint32_t cur = 0;
     for (uint32_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
         const TileAt ta = tile_at(a.seg, a.nseg, t, kDirectTile, cur);
         const AccSeg& sg = a.seg[ta.si];
         const bool first = sg.first != 0;
-        const Tin* xt = x0 + sg.x_off + ta.e0;
+        const Tin* xt = static_cast<const Tin*>(sg.x) + sg.x_off + ta.e0;
         float* g = a.acc + sg.acc_idx + ta.e0;
         const uint32_t n8 = ((a.vec_ok >> ta.si) & 1ull) ? ta.cnt / kVec : 0u;
         if (threadIdx.x < n8) {

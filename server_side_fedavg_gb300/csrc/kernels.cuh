@@ -33,7 +33,9 @@ constexpr int kMaxBatch = 16;         // resident clients per launch
 constexpr int kReduceStageBytes = 73728;   // shared-memory budget per stage of the reduce kernel
 
 struct AccSeg {
-    uint64_t x_off;     // element offset into every input chunk
+    const void* x;      // one-client launches: this segment's input chunk (segments of one
+                        // launch may come from different chunks); J > 1 uses AccArgs::x
+    uint64_t x_off;     // element offset into the input chunk(s)
     uint64_t acc_idx;   // element index into the running sum
     uint64_t len;       // elements (>= 1)
     uint32_t first;     // 1: the first client of the launch starts the sum here
@@ -106,8 +108,9 @@ cudaError_t take_device_error_async(unsigned int* host, cudaStream_t stream);
 cudaError_t query_launch_shape(LaunchShape* s);
 
 // dtype codes: 0 = fp32, 1 = bf16.  The caller fills x, w, acc, J (1..16), nseg, vec_ok
-// and each segment's x_off / acc_idx / len / first; the launcher numbers the tiles for
-// the kernel it picks (J = 1: streaming kernel, else the reduce kernel in sum mode).
+// and each segment's x (J = 1) / x_off / acc_idx / len / first; the launcher numbers the
+// tiles for the kernel it picks (J = 1: streaming kernel, else the reduce kernel in sum
+// mode).
 // Returns cudaErrorInvalidValue if the arguments are out of range.
 cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,
                               cudaStream_t stream);

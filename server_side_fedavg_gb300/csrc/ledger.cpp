@@ -115,6 +115,74 @@ void Ledger::split_and_mark(uint32_t p, uint64_t a, uint64_t b,
     iv.swap(merged);
 }
 
+int32_t Ledger::check_client(uint32_t c, double w, std::string* err) const {
+    if (c >= max_clients_) {
+        *err = fmt("client id %llu >= max_clients %llu", c, max_clients_);
+        return kErrArg;
+    }
+    if (!std::isfinite(w) || w < 0.0 || w > kMaxWeight) {
+        *err = fmt("client %llu: weight must be finite, >= 0 and <= 2^24", c);
+        return kErrWeight;
+    }
+    if (has_weight_[c] && weight_[c] != w) {
+        *err = fmt("client %llu: weight differs from its earlier chunks this round", c);
+        return kErrWeight;
+    }
+    return kOk;
+}
+
+int32_t Ledger::chunk_spans(int64_t key, uint64_t offset, uint64_t len, std::vector<Span>* spans,
+                            std::string* err) const {
+    const uint32_t nk = n_keys();
+    if (key != -1 && (key < 0 || key >= static_cast<int64_t>(nk))) {
+        *err = fmt("key %llu out of range (n_keys %llu)", static_cast<unsigned long long>(key), nk);
+        return kErrArg;
+    }
+    const uint64_t limit = key == -1 ? total_ : numel_[static_cast<uint32_t>(key)];
+    if (offset > limit || len > limit - offset) {
+        *err = fmt("chunk [%llu, +%llu) past the end (%llu elements)", offset, len, limit);
+        return kErrRange;
+    }
+    if (len == 0) return kOk;
+    if (key >= 0) {
+        spans->push_back({static_cast<uint32_t>(key), offset, len, 0});
+        return kOk;
+    }
+    auto it = std::upper_bound(flat_off_.begin(), flat_off_.end(), offset);
+    uint32_t p = static_cast<uint32_t>(it - flat_off_.begin()) - 1;
+    uint64_t pos = offset, end = offset + len;
+    while (pos < end) {
+        uint64_t kend = flat_off_[p] + numel_[p];
+        uint64_t e = std::min(end, kend);
+        spans->push_back({p, pos - flat_off_[p], e - pos, pos - offset});
+        pos = e;
+        ++p;
+    }
+    return kOk;
+}
+
+void Ledger::emit_pieces(const std::vector<Span>& spans, size_t from, size_t to, uint32_t chunk,
+                         std::vector<Piece>* out) {
+    std::vector<std::pair<uint64_t, bool>> runs;
+    for (size_t i = from; i < to; ++i) {
+        const Span& s = spans[i];
+        runs.clear();
+        split_and_mark(s.p, s.koff, s.koff + s.n, &runs);
+        uint64_t a = s.koff;
+        for (const auto& r : runs) {
+            Piece pc;
+            pc.key = s.p;
+            pc.chunk = chunk;
+            pc.chunk_off = s.coff + (a - s.koff);
+            pc.acc_idx = acc_off_[s.p] + a;
+            pc.len = r.first - a;
+            pc.first = r.second;
+            out->push_back(pc);
+            a = r.first;
+        }
+    }
+}
+
 int32_t Ledger::plan_accumulate(const uint32_t* clients, const double* weights, uint32_t J,
                                 int64_t key, uint64_t offset, uint64_t len,
                                 std::vector<Piece>* out, std::string* err) {
@@ -128,59 +196,20 @@ int32_t Ledger::plan_accumulate(const uint32_t* clients, const double* weights, 
         return kErrArg;
     }
     for (uint32_t j = 0; j < J; ++j) {
-        uint32_t c = clients[j];
-        if (c >= max_clients_) {
-            *err = fmt("client id %llu >= max_clients %llu", c, max_clients_);
-            return kErrArg;
-        }
+        const uint32_t c = clients[j];
         for (uint32_t i = 0; i < j; ++i) {
             if (clients[i] == c) {
                 *err = fmt("client id %llu appears twice in one batch", c);
                 return kErrArg;
             }
         }
-        double w = weights[j];
-        if (!std::isfinite(w) || w < 0.0 || w > kMaxWeight) {
-            *err = fmt("client %llu: weight must be finite, >= 0 and <= 2^24", c);
-            return kErrWeight;
-        }
-        if (has_weight_[c] && weight_[c] != w) {
-            *err = fmt("client %llu: weight differs from its earlier chunks this round", c);
-            return kErrWeight;
-        }
+        int32_t st = check_client(c, weights[j], err);
+        if (st != kOk) return st;
     }
-    const uint32_t nk = n_keys();
-    if (key != -1 && (key < 0 || key >= static_cast<int64_t>(nk))) {
-        *err = fmt("key %llu out of range (n_keys %llu)", static_cast<unsigned long long>(key), nk);
-        return kErrArg;
-    }
-    const uint64_t limit = key == -1 ? total_ : numel_[static_cast<uint32_t>(key)];
-    if (offset > limit || len > limit - offset) {
-        *err = fmt("chunk [%llu, +%llu) past the end (%llu elements)", offset, len, limit);
-        return kErrRange;
-    }
-    if (len == 0) return kOk;
-
-    // pieces per key: (key, offset within key, length, offset within chunk)
-    struct Span {
-        uint32_t p;
-        uint64_t koff, n, coff;
-    };
     std::vector<Span> spans;
-    if (key >= 0) {
-        spans.push_back({static_cast<uint32_t>(key), offset, len, 0});
-    } else {
-        auto it = std::upper_bound(flat_off_.begin(), flat_off_.end(), offset);
-        uint32_t p = static_cast<uint32_t>(it - flat_off_.begin()) - 1;
-        uint64_t pos = offset, end = offset + len;
-        while (pos < end) {
-            uint64_t kend = flat_off_[p] + numel_[p];
-            uint64_t e = std::min(end, kend);
-            spans.push_back({p, pos - flat_off_[p], e - pos, pos - offset});
-            pos = e;
-            ++p;
-        }
-    }
+    int32_t st = chunk_spans(key, offset, len, &spans, err);
+    if (st != kOk || len == 0) return st;
+    const uint32_t nk = n_keys();
     for (uint32_t j = 0; j < J; ++j) {
         uint32_t c = clients[j];
         for (const auto& s : spans) {
@@ -199,22 +228,63 @@ int32_t Ledger::plan_accumulate(const uint32_t* clients, const double* weights, 
         has_weight_[c] = 1;
         for (const auto& s : spans) recv_[static_cast<size_t>(c) * nk + s.p] += s.n;
     }
-    std::vector<std::pair<uint64_t, bool>> runs;
-    for (const auto& s : spans) {
-        runs.clear();
-        split_and_mark(s.p, s.koff, s.koff + s.n, &runs);
-        uint64_t a = s.koff;
-        for (const auto& r : runs) {
-            Piece pc;
-            pc.key = s.p;
-            pc.chunk_off = s.coff + (a - s.koff);
-            pc.acc_idx = acc_off_[s.p] + a;
-            pc.len = r.first - a;
-            pc.first = r.second;
-            out->push_back(pc);
-            a = r.first;
+    emit_pieces(spans, 0, spans.size(), 0, out);
+    return kOk;
+}
+
+int32_t Ledger::plan_accumulate_keys(uint32_t client, double weight, uint32_t n,
+                                     const int64_t* keys, const uint64_t* offsets,
+                                     const uint64_t* lens, std::vector<Piece>* out,
+                                     std::string* err) {
+    out->clear();
+    if (closed_) {
+        *err = "round already finalized: call fa_reset before accumulating again";
+        return kErrState;
+    }
+    if (n > 0 && (keys == nullptr || offsets == nullptr || lens == nullptr)) {
+        *err = "keys, offsets or lengths is NULL";
+        return kErrArg;
+    }
+    int32_t st = check_client(client, weight, err);
+    if (st != kOk) return st;
+    // every chunk's spans, and the counts this call adds per key, checked before anything
+    // is recorded
+    std::vector<Span> spans;
+    std::vector<size_t> first_span(n + 1, 0);
+    const uint32_t nk = n_keys();
+    for (uint32_t i = 0; i < n; ++i) {
+        first_span[i] = spans.size();
+        st = chunk_spans(keys[i], offsets[i], lens[i], &spans, err);
+        if (st != kOk) {
+            *err = fmt("chunk %llu: ", i) + *err;
+            return st;
         }
     }
+    first_span[n] = spans.size();
+    std::vector<uint64_t> pending;   // per key touched, sorted by key
+    std::vector<uint32_t> touched;
+    for (const auto& s : spans) touched.push_back(s.p);
+    std::sort(touched.begin(), touched.end());
+    touched.erase(std::unique(touched.begin(), touched.end()), touched.end());
+    pending.assign(touched.size(), 0);
+    for (const auto& s : spans) {
+        const size_t t = static_cast<size_t>(
+            std::lower_bound(touched.begin(), touched.end(), s.p) - touched.begin());
+        pending[t] += s.n;
+        const uint64_t have = recv_[static_cast<size_t>(client) * nk + s.p];
+        if (pending[t] > numel_[s.p] - have) {
+            *err = fmt("client %llu would send more than numel (%llu) elements of key %llu",
+                       client, numel_[s.p], s.p);
+            return kErrRange;
+        }
+    }
+    // commit
+    if (spans.empty()) return kOk;
+    weight_[client] = weight;
+    has_weight_[client] = 1;
+    for (size_t t = 0; t < touched.size(); ++t)
+        recv_[static_cast<size_t>(client) * nk + touched[t]] += pending[t];
+    for (uint32_t i = 0; i < n; ++i) emit_pieces(spans, first_span[i], first_span[i + 1], i, out);
     return kOk;
 }
 

@@ -40,6 +40,7 @@ enum Status : int32_t {
 // One contiguous run of a chunk that lands in one key.
 struct Piece {
     uint32_t key;
+    uint32_t chunk;       // which chunk of the call (0 for a single-chunk call)
     uint64_t chunk_off;   // element offset within the chunk
     uint64_t acc_idx;     // element index in the padded running sum
     uint64_t len;         // elements
@@ -69,6 +70,14 @@ public:
                             int64_t key, uint64_t offset, uint64_t len,
                             std::vector<Piece>* out, std::string* err);
 
+    // Validate and record n chunks of ONE client, chunk i covering [offsets[i], +lens[i])
+    // of key keys[i] (or of the flat layout for -1), as n plain accumulates in that order
+    // would -- counts sent earlier in the same call included.  All or nothing: on error
+    // nothing changes.  Pieces come in chunk order, each tagged with its chunk index.
+    int32_t plan_accumulate_keys(uint32_t client, double weight, uint32_t n, const int64_t* keys,
+                                 const uint64_t* offsets, const uint64_t* lens,
+                                 std::vector<Piece>* out, std::string* err);
+
     // Check completeness and list the keys to write (N_p > 0).  Changes nothing.
     int32_t plan_finalize(std::vector<FinItem>* out, std::string* err) const;
 
@@ -91,6 +100,19 @@ public:
     bool has_contributions() const;
 
 private:
+    // One run of a chunk inside one key.
+    struct Span {
+        uint32_t p;
+        uint64_t koff, n, coff;   // offset within the key, length, offset within the chunk
+    };
+    // Range-check a chunk and cut it at key boundaries (appends to *spans).
+    int32_t chunk_spans(int64_t key, uint64_t offset, uint64_t len, std::vector<Span>* spans,
+                        std::string* err) const;
+    int32_t check_client(uint32_t c, double w, std::string* err) const;
+    // Pieces of spans[from, to) in order (marks them started), tagged with chunk `chunk`.
+    void emit_pieces(const std::vector<Span>& spans, size_t from, size_t to, uint32_t chunk,
+                     std::vector<Piece>* out);
+
     // Split [a, b) of key p into runs that are fresh / already started, then
     // mark all of [a, b) started.
     void split_and_mark(uint32_t p, uint64_t a, uint64_t b,

@@ -127,6 +127,7 @@ extern "C" fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weig
         a.J = jb;
         a.nseg = 1;
         a.vec_ok = aligned ? 1ull : 0ull;
+        a.seg[0].x = a.x[0];
         a.seg[0].x_off = 0;
         a.seg[0].acc_idx = 0;
         a.seg[0].len = numel;

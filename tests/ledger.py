@@ -29,6 +29,8 @@ def lib():
         L.lg_error.restype = ctypes.c_char_p
         L.lg_accumulate.argtypes = [vp, vp, vp, u32, i64, u64, u64, vp, u32, ctypes.POINTER(u32)]
         L.lg_accumulate.restype = i32
+        L.lg_accumulate_keys.argtypes = [vp, u32, f64, u32, vp, vp, vp, vp, u32, ctypes.POINTER(u32)]
+        L.lg_accumulate_keys.restype = i32
         L.lg_finalize.argtypes = [vp, vp, vp, u32, ctypes.POINTER(u32)]
         L.lg_finalize.restype = i32
         L.lg_reset.argtypes = [vp]
@@ -66,6 +68,19 @@ class Ledger:
         st = lib().lg_accumulate(self.h, c, w, J, key, offset, length, rows, 4096, ctypes.byref(n))
         pieces = [tuple(rows[5 * i:5 * i + 5]) for i in range(min(n.value, 4096))]
         return st, pieces
+
+    def accumulate_keys(self, client, weight, chunks):
+        """chunks: [(key, offset, length)] of one client.  Returns (status, pieces) with
+        pieces as (chunk, key, chunk_off, acc_idx, len, first)."""
+        n = len(chunks)
+        keys = (ctypes.c_int64 * max(n, 1))(*[c[0] for c in chunks])
+        offs = (ctypes.c_uint64 * max(n, 1))(*[c[1] for c in chunks])
+        lens = (ctypes.c_uint64 * max(n, 1))(*[c[2] for c in chunks])
+        rows = (ctypes.c_uint64 * (6 * 4096))()
+        m = ctypes.c_uint32()
+        st = lib().lg_accumulate_keys(self.h, client, weight, n, keys, offs, lens, rows, 4096,
+                                      ctypes.byref(m))
+        return st, [tuple(rows[6 * i:6 * i + 6]) for i in range(min(m.value, 4096))]
 
     def finalize(self):
         rows = (ctypes.c_uint64 * (5 * 4096))()

@@ -52,6 +52,27 @@ int32_t lg_accumulate(void* p, const uint32_t* clients, const double* weights, u
     return st;
 }
 
+// one client, n chunks; pieces out: rows of (chunk, key, chunk_off, acc_idx, len, first)
+int32_t lg_accumulate_keys(void* p, uint32_t client, double weight, uint32_t n,
+                           const int64_t* keys, const uint64_t* offsets, const uint64_t* lens,
+                           uint64_t* rows, uint32_t max_rows, uint32_t* n_rows) {
+    auto* h = static_cast<Handle*>(p);
+    int32_t st = h->lg.plan_accumulate_keys(client, weight, n, keys, offsets, lens, &h->pieces,
+                                            &h->err);
+    *n_rows = static_cast<uint32_t>(h->pieces.size());
+    for (uint32_t i = 0; i < *n_rows && i < max_rows; ++i) {
+        const auto& q = h->pieces[i];
+        uint64_t* r = rows + 6 * i;
+        r[0] = q.chunk;
+        r[1] = q.key;
+        r[2] = q.chunk_off;
+        r[3] = q.acc_idx;
+        r[4] = q.len;
+        r[5] = q.first ? 1 : 0;
+    }
+    return st;
+}
+
 // items out: rows of (key, acc_idx, flat_off, numel, reporters) and totals
 int32_t lg_finalize(void* p, uint64_t* rows, double* totals, uint32_t max_rows, uint32_t* n_rows) {
     auto* h = static_cast<Handle*>(p);

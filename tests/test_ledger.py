@@ -198,3 +198,123 @@ def test_random_operations_against_model():
         st, items = lg.finalize()
         complete = all(recv[k, p] in (0, numels[p]) for k in range(K) for p in range(len(numels)))
         assert st == (OK if complete else INCOMPLETE)
+
+
+def _spans(numels, offs, key, off, ln):
+    spans = []
+    if key == -1:
+        pos = off
+        while pos < off + ln:
+            p = int(np.searchsorted(offs, pos, side="right") - 1)
+            e = min(off + ln, int(offs[p + 1]))
+            spans.append((p, pos - int(offs[p]), e - pos, pos - off))
+            pos = e
+    elif ln:
+        spans.append((key, off, ln, 0))
+    return spans
+
+
+def test_accumulate_keys_against_model():
+    """One client's several chunks per call: the same pieces, first-contribution flags and
+    counts as the chunks sent one by one would give; over-coverage is seen across chunks
+    of the call; on any error nothing is recorded."""
+    rng = random.Random(23)
+    for trial in range(40):
+        numels = [rng.randint(1, 30) for _ in range(rng.randint(1, 6))]
+        K = rng.randint(1, 4)
+        lg = Ledger(numels, K)
+        offs = np.cumsum([0] + numels)
+        started = [np.zeros(n, bool) for n in numels]
+        recv = np.zeros((K, len(numels)), np.int64)
+        weight = {}
+        for _ in range(40):
+            c = rng.randrange(K)
+            w = weight.get(c, float(rng.randint(0, 9)))
+            chunks = []
+            for _ in range(rng.randint(0, 5)):
+                if rng.random() < 0.3:
+                    off = rng.randint(0, int(offs[-1]))
+                    chunks.append((-1, off, rng.randint(0, int(offs[-1]) - off)))
+                else:
+                    key = rng.randrange(len(numels))
+                    off = rng.randint(0, numels[key])
+                    chunks.append((key, off, rng.randint(0, numels[key] - off)))
+            if rng.random() < 0.1 and chunks:                 # a chunk past the end
+                i = rng.randrange(len(chunks))
+                k, o, n = chunks[i]
+                chunks[i] = (k, o, (offs[-1] if k == -1 else numels[k]) - o + 1)
+                bad_range = True
+            else:
+                bad_range = False
+            before = [lg.key_total(p) for p in range(len(numels))]
+            st, pieces = lg.accumulate_keys(c, w, chunks)
+            pending = recv[c].copy()
+            over = False
+            for (k, o, n) in ([] if bad_range else chunks):
+                for (p, _, m, _) in _spans(numels, offs, k, o, n):
+                    pending[p] += m
+                    over = over or pending[p] > numels[p]
+            if bad_range or over:
+                assert st == RANGE, (st, lg.error())
+                assert pieces == []
+                assert [lg.key_total(p) for p in range(len(numels))] == before
+                continue
+            assert st == OK, lg.error()
+            if all(n == 0 for (_, _, n) in chunks):
+                assert pieces == []
+                continue
+            weight[c] = w
+            recv[c] = pending
+            got = {}
+            for (ch, p, coff, acc, n, first) in pieces:
+                for i in range(n):
+                    got[(ch, p, acc - lg.acc_off(p) + i)] = (first, coff + i)
+            for ch, (k, o, n) in enumerate(chunks):
+                for (p, koff, m, coff) in _spans(numels, offs, k, o, n):
+                    for i in range(m):
+                        f, ci = got.pop((ch, p, koff + i))
+                        assert ci == coff + i
+                        assert f == (0 if started[p][koff + i] else 1)
+                        started[p][koff + i] = True
+            assert not got
+        for p in range(len(numels)):
+            rep = [k for k in range(K) if recv[k, p] > 0]
+            assert lg.key_total(p) == (OK, sum(weight[k] for k in rep), len(rep))
+
+
+def test_accumulate_keys_errors_record_nothing():
+    lg = Ledger([10, 20], 2)
+    assert lg.accumulate_keys(0, 5.0, [(0, 0, 10), (1, 0, 20)])[0] == OK
+    # weight unlike the client's earlier chunks, bad key, bad client: nothing recorded
+    assert lg.accumulate_keys(0, 6.0, [(0, 0, 1)])[0] == WEIGHT
+    assert lg.accumulate_keys(1, 3.0, [(0, 0, 10), (7, 0, 1)])[0] == ARG
+    assert "chunk 1" in lg.error()
+    assert lg.accumulate_keys(2, 3.0, [(0, 0, 10)])[0] == ARG
+    # two chunks of one key in one call that together exceed it
+    assert lg.accumulate_keys(1, 3.0, [(1, 0, 15), (1, 0, 15)])[0] == RANGE
+    assert lg.key_total(0) == (OK, 5.0, 1) and lg.key_total(1) == (OK, 5.0, 1)
+    # client 1 can still send everything
+    st, pieces = lg.accumulate_keys(1, 3.0, [(-1, 0, 30)])
+    assert st == OK and [p[0] for p in pieces] == [0, 0]
+    assert lg.key_total(1) == (OK, 8.0, 2)
+    assert lg.finalize()[0] == OK
+    assert lg.accumulate_keys(1, 3.0, [(0, 0, 1)])[0] == STATE
+
+
+def test_accumulate_keys_matches_single_calls():
+    """The pieces of a multi-chunk call equal those of the same chunks sent one by one."""
+    numels = [7, 33, 1, 64, 5]
+    a, b = Ledger(numels, 3), Ledger(numels, 3)
+    calls = [(0, 2.0, [(1, 0, 10), (3, 5, 20), (-1, 0, 7)]),
+             (1, 4.0, [(-1, 3, 50), (4, 0, 5)]),
+             (0, 2.0, [(1, 10, 23), (3, 0, 5), (3, 25, 39), (2, 0, 1)])]
+    for c, w, chunks in calls:
+        st, multi = a.accumulate_keys(c, w, chunks)
+        assert st == OK, a.error()
+        single = []
+        for (k, o, n) in chunks:
+            st, ps = b.accumulate([c], [w], k, o, n)
+            assert st == OK, b.error()
+            single += [tuple(int(v) for v in q) for q in ps]
+        assert [tuple(int(v) for v in q[1:]) for q in multi] == single
+    assert [a.key_total(p) for p in range(5)] == [b.key_total(p) for p in range(5)]
