@@ -4,8 +4,9 @@ One context runs several rounds (fa_reset between them).  Each round mixes, in a
 shuffled call order: a random subset of keys per client (partial participation,
 including clients that send nothing), ragged chunks of each key, every ingest kind
 (device memory; pinned and pageable host memory, read in place or through a small
-staging ring), FLAT chunks that span key boundaries, and a fa_accumulate_batch group
-over part of one key.
+staging ring), FLAT chunks that span key boundaries, a fa_accumulate_batch group
+over part of one key, and clients that send all their chunks in one
+fa_accumulate_keys call.
 
 The GPU applies contributions in call order and the oracle sums in client-id order
 (the arrival-order reading of FedAvg's weighted mean), so outputs are compared with
@@ -82,17 +83,24 @@ def _plan(rng, numels, K):
     in_batch = set(batch[1]) if batch else set()
     flat = [k for k in full if k not in in_batch and rng.random() < 0.5]
     calls = []
+    grouped = []     # clients whose chunks go in one fa_accumulate_keys call
     for k in range(K):
         if k in flat:
             for a, b in _cuts(rng, offs[-1], 5):                 # spans keys
                 calls.append((k, fa.FA_KEY_FLAT, a, b, offs[0] + a))
             continue
+        mine = []
         for p in reports[k]:
             if batch and p == batch[0] and k in in_batch:
                 continue
             for a, b in _cuts(rng, numels[p], 3):
-                calls.append((k, p, a, b, offs[p] + a))
-    return offs, reports, batch, calls
+                mine.append((k, p, a, b, offs[p] + a))
+        if mine and rng.random() < 0.3:
+            rng.shuffle(mine)
+            grouped.append((k, mine))
+        else:
+            calls += mine
+    return offs, reports, batch, calls, grouped
 
 
 @pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32"), ("f32", "bf16")])
@@ -108,11 +116,11 @@ def test_random_rounds(din, dout):
     s = torch.cuda.Stream()
     try:
         for rnd in range(5):
-            offs, reports, batch, calls = _plan(rng_py, numels, K)
+            offs, reports, batch, calls, grouped = _plan(rng_py, numels, K)
             weights = [float(rng_py.choice([0, 1, 7, 250, 3000, rng_py.randint(1, 1 << 14)]))
                        for _ in range(K)]
             data = [_values(rng, offs[-1], din) for _ in range(K)]   # client k's flat update
-            ops = [("one",) + c for c in calls]
+            ops = [("one",) + c for c in calls] + [("keys", k, mine) for k, mine in grouped]
             if batch:
                 p, ks, ranges = batch
                 ops += [("batch", p, ks, a, b) for a, b in ranges]
@@ -123,6 +131,20 @@ def test_random_rounds(din, dout):
                     _, p, ks, a, b = op
                     ptrs = [_put(data[k][offs[p] + a:offs[p] + b], "device", keep) for k in ks]
                     fa.fa_accumulate_batch(ctx, ks, [weights[k] for k in ks], p, a, ptrs, b - a, s)
+                elif op[0] == "keys":
+                    _, k, mine = op
+                    # one memory kind per call; host chunks only where they are read in place
+                    kind = "device" if seed % 2 else rng_py.choice(KINDS)
+                    args = ([c[1] for c in mine], [c[2] for c in mine], None, [c[3] - c[2] for c in mine])
+                    ptrs = [_put(data[k][g:g + (b - a)], kind, keep) for (_, _, a, b, g) in mine]
+                    try:
+                        fa.fa_accumulate_keys(ctx, k, weights[k], args[0], args[1], ptrs, args[3], s)
+                    except fa.FedAvgError as e:
+                        # a host without in-place pageable reads refuses the list, recording
+                        # nothing: send it from device memory instead
+                        assert e.status == fa.FA_ERR_ARG and kind == "pageable", e
+                        ptrs = [_put(data[k][g:g + (b - a)], "device", keep) for (_, _, a, b, g) in mine]
+                        fa.fa_accumulate_keys(ctx, k, weights[k], args[0], args[1], ptrs, args[3], s)
                 else:
                     _, k, key, a, b, g = op
                     ptr = _put(data[k][g:g + (b - a)], rng_py.choice(KINDS), keep)

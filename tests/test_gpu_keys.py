@@ -53,7 +53,12 @@ def _round(w, host, mode, split=False, **opts):
                 for key, a, ptr, n in zip(keys, offs, ptrs, lens):
                     fa.fa_accumulate(ctx, k, w.weights[k], key, a, ptr, n, s)
             else:
-                fa.fa_accumulate_keys(ctx, k, w.weights[k], keys, offs, ptrs, lens, s)
+                try:
+                    fa.fa_accumulate_keys(ctx, k, w.weights[k], keys, offs, ptrs, lens, s)
+                except fa.FedAvgError as e:
+                    if mode == "pageable" and e.status == fa.FA_ERR_ARG:
+                        pytest.skip("this device does not read pageable host memory in place")
+                    raise
         launches = fa.fa_get_stats(ctx)["kernel_launches"] - launches0
         outs = [sentinel(n, w.dtype_out) for n in w.numels]
         fa.fa_finalize(ctx, outs, s)
