@@ -308,6 +308,23 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
     return FA_OK;
 }
 
+// One client's pieces read in place -- from device memory (bulk kernel) or from host
+// memory the device addresses (direct kernel, over the host link) -- ordered after the
+// context's earlier work.  A pageable source is waited for before returning, so the caller
+// may reuse it at once.
+fa_status launch_in_place(fa_ctx* c, const void* const* ptrs, float w, cudaStream_t s, bool host,
+                          bool pageable) {
+    fa_status r = chain_in(c, s);
+    if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, UINT64_MAX, ptrs, &w, 1, s, host);
+    if (r == FA_OK && pageable) {
+        cudaError_t ce = cudaEventRecord(c->read_ev, s);
+        if (ce != cudaSuccess) r = cuda_fail(c, ce, "pageable read");
+    }
+    if (r == FA_OK) r = chain_out(c, s);
+    if (r == FA_OK && pageable) r = wait_event(c, c->read_ev, "pageable chunk read", true);
+    return r;
+}
+
 fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const double* weights,
                           int64_t key, uint64_t offset, const void* const* ptrs, uint64_t len,
                           cudaStream_t s, bool batch) {
@@ -356,14 +373,7 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
         if (r == FA_OK) r = chain_out(c, s);
     } else if (direct) {
         // host memory read by the kernel over the host link, ordered on `s`
-        r = chain_in(c, s);
-        if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, 1, s, true);
-        if (r == FA_OK && kind == Mem::kPageable) {
-            cudaError_t ce = cudaEventRecord(c->read_ev, s);
-            if (ce != cudaSuccess) r = cuda_fail(c, ce, "pageable read");
-        }
-        if (r == FA_OK) r = chain_out(c, s);
-        if (r == FA_OK && kind == Mem::kPageable) r = wait_event(c, c->read_ev, "pageable chunk read", true);
+        r = launch_in_place(c, ptrs, wv[0], s, true, kind == Mem::kPageable);
         if (r == FA_OK) c->stats.h2d_bytes += len * c->s_in;
     } else {
         // host memory: through the staging ring, slot-sized pieces
@@ -622,16 +632,9 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
                                                 &c->pieces, &e);
     if (st != fa::kOk) return fail(c, st, e);
     if (!any) return FA_OK;
-    const float w = static_cast<float>(weight_nk);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    fa_status r = chain_in(c, s);
-    if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, UINT64_MAX, chunk_ptrs, &w, 1, s, !all_device);
-    if (r == FA_OK && !all_device && pageable) {
-        cudaError_t ce = cudaEventRecord(c->read_ev, s);
-        if (ce != cudaSuccess) r = cuda_fail(c, ce, "pageable read");
-    }
-    if (r == FA_OK) r = chain_out(c, s);
-    if (r == FA_OK && !all_device && pageable) r = wait_event(c, c->read_ev, "pageable chunk read", true);
+    fa_status r = launch_in_place(c, chunk_ptrs, static_cast<float>(weight_nk),
+                                  static_cast<cudaStream_t>(stream), !all_device,
+                                  !all_device && pageable);
     if (r != FA_OK) {
         c->broken = true;
         return r;
