@@ -323,7 +323,9 @@ fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weights,
 /* Static text for a status code. */
 const char* fa_strerror(fa_status status);
 
-/* Detail of the last error on this context ("" if none); valid until the next call. */
+/* Detail of the last error on this context ("" if none); valid until the next call.
+ * With FA_LOG set in the environment (any value but "0"), each failure a call reports is
+ * also written to stderr as "[fedavg] <status text>: <detail>". */
 const char* fa_last_error(const fa_ctx* ctx);
 
 #ifdef __cplusplus

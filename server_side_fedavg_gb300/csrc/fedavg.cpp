@@ -27,6 +27,7 @@
 #include <chrono>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -116,14 +117,27 @@ private:
     bool restore_ = false;
 };
 
+// With FA_LOG set in the environment (to anything but "0"), every failure a call reports is
+// also written to stderr.
+void log_failure(fa_status s, const std::string& what) {
+    static const bool on = [] {
+        const char* v = std::getenv("FA_LOG");
+        return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+    }();
+    if (on) std::fprintf(stderr, "[fedavg] %s: %s\n", fa_strerror(s), what.c_str());
+}
+
 fa_status fail(fa_ctx* c, fa_status s, const std::string& what) {
     c->err = what;
+    log_failure(s, what);
     return s;
 }
 
 fa_status cuda_fail(fa_ctx* c, cudaError_t e, const char* where) {
     c->err = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
-    return e == cudaErrorMemoryAllocation ? FA_ERR_NOMEM : FA_ERR_CUDA;
+    const fa_status s = e == cudaErrorMemoryAllocation ? FA_ERR_NOMEM : FA_ERR_CUDA;
+    log_failure(s, c->err);
+    return s;
 }
 
 #define FA_CUDA(ctx, call)                                   \
@@ -146,8 +160,7 @@ fa_status wait_event(fa_ctx* c, cudaEvent_t ev, const char* what, bool spin = fa
                       std::chrono::steady_clock::now() - t0)
                       .count();
         if (ms > static_cast<long long>(c->timeout_ms)) {
-            c->err = std::string(what) + ": no completion within timeout_ms";
-            return FA_ERR_TIMEOUT;
+            return fail(c, FA_ERR_TIMEOUT, std::string(what) + ": no completion within timeout_ms");
         }
         if (spin || ++spins < 64)
             std::this_thread::yield();

@@ -444,3 +444,32 @@ def test_caller_registered_host_memory():
     assert np.array_equal(outs["registered"], outs["device"])
     want, _, _ = oracle.fedavg_key(w, [True] * K, xs, "bf16", "bf16")
     check_bf16(outs["device"], want, "registered host memory")
+
+
+def test_fa_log_reports_failures_on_stderr():
+    """FA_LOG=1 writes each reported failure to stderr; unset, the library prints nothing."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import numpy as np, server_side_fedavg_gb300 as fa, torch\n"
+        "ctx = fa.fa_open([('k', 8)], 'f32', 'f32', 1)\n"
+        "x = torch.zeros(8, device='cuda')\n"
+        "fa.fa_accumulate(ctx, 0, 2.0, 0, 0, x, 4)\n"
+        "try:\n"
+        "    fa.fa_accumulate(ctx, 0, 3.0, 0, 4, x, 4)\n"
+        "except fa.FedAvgError:\n"
+        "    pass\n"
+        "fa.fa_close(ctx)\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root)
+    for value, expect in (("1", True), (None, False)):
+        e = dict(env)
+        e.pop("FA_LOG", None)
+        if value is not None:
+            e["FA_LOG"] = value
+        r = subprocess.run([sys.executable, "-c", code], cwd=root, env=e, capture_output=True,
+                           text=True, timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        logged = "[fedavg]" in r.stderr and "weight differs" in r.stderr
+        assert logged == expect, r.stderr[-2000:]
