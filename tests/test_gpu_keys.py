@@ -187,3 +187,58 @@ def _status(fn, *args):
         return fa.FA_OK
     except fa.FedAvgError as e:
         return e.status
+
+
+@pytest.mark.parametrize("kind", ["device", "pageable"])
+def test_keys_calls_from_concurrent_threads(lora, kind):
+    """Every client sends its list from its own host thread and stream at the same time;
+    calls on one context serialize, contributions land in some client order, and the
+    result stays within the order-free bound of the oracle with exact totals."""
+    import threading
+    w, host = lora
+    ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K)
+    errors = []
+    keep = {}
+    for k in range(w.K):
+        keep[k] = [to_dev(host[(k, p)]) if kind == "device" else host[(k, p)].copy()
+                   for p in w.reports[k]]
+    torch.cuda.synchronize()
+
+    def client(k):
+        try:
+            s = torch.cuda.Stream()
+            ps = w.reports[k]
+            fa.fa_accumulate_keys(ctx, k, w.weights[k], ps, [0] * len(ps), keep[k],
+                                  [w.numels[p] for p in ps], s)
+            s.synchronize()
+        except fa.FedAvgError as e:
+            errors.append(e)
+
+    try:
+        th = [threading.Thread(target=client, args=(k,)) for k in range(w.K)]
+        for t in th:
+            t.start()
+        for t in th:
+            t.join()
+        if errors and kind == "pageable" and all(e.status == fa.FA_ERR_ARG for e in errors):
+            pytest.skip("this device does not read pageable host memory in place")
+        assert not errors, errors
+        outs = [sentinel(n, w.dtype_out) for n in w.numels]
+        fa.fa_finalize(ctx, outs)
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+        for p in range(w.n_keys):
+            rep = [p in set(w.reports[k]) for k in range(w.K)]
+            xs = [host.get((k, p)) for k in range(w.K)]
+            want, N, cnt = oracle.fedavg_key(w.weights, rep, xs, w.dtype_in, w.dtype_out)
+            assert fa.fa_key_total(ctx, p) == (N, cnt)
+            got = to_np(outs[p], w.dtype_out)
+            if want is None:
+                assert np.array_equal(got, sentinel_np(w.numels[p], w.dtype_out))
+                continue
+            from tests.compare import check_f32_to_bf16
+            mx = max(float(np.abs(synth.to_f64(xs[k], w.dtype_in)).max()) for k in range(w.K) if rep[k])
+            check_f32_to_bf16(got, want, mx, cnt, f"key {p}")
+    finally:
+        torch.cuda.synchronize()
+        fa.fa_close(ctx)
