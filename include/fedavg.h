@@ -161,12 +161,16 @@ fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64
                         void* stream);
 
 /* K-resident form of fa_accumulate: n_clients updates of the SAME element range,
- * all in device memory, reduced in one pass over the running sum.  Equivalent
+ * reduced in one pass over the running sum when they are in device memory.  Equivalent
  * to calling fa_accumulate for client_ids[0], client_ids[1], ... in that order,
  * and bit-identical to it.  Client ids within one call must be distinct.
  * [FLARE]: the second memory pressure -- many client updates held at once --
  * turned into one read of each update and one write of the sum.
- * Errors: as fa_accumulate; FA_ERR_ARG if any chunk_ptrs[j] is not device memory. */
+ * The chunks are read in place: all in this GPU's memory, or all in host memory the
+ * device addresses (as for fa_accumulate; then one launch per client, in order, over the
+ * host link, which bounds that case anyway, and a pageable batch is waited for).
+ * Errors: as fa_accumulate; FA_ERR_ARG for other memory, a mix, or host chunks under
+ * FA_STAGE_HOST. */
 fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
                               const double* weights, int64_t key, uint64_t offset_elems,
                               const void* const* chunk_ptrs, uint64_t len_elems, void* stream);

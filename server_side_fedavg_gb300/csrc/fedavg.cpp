@@ -268,11 +268,12 @@ fa_status ensure_ring(fa_ctx* c, bool need_host) {
 fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_t c0,
                         uint64_t n, const void* const* xs, const float* ws, uint32_t J,
                         cudaStream_t s, bool direct = false) {
-    // launches of up to 16 clients; after the first launch the sum is started everywhere
+    // launches of up to 16 clients (one at a time for the direct kernel, which takes one);
+    // after the first launch the sum is started everywhere
     uint32_t done = 0;
     while (done < J) {
         const uint32_t left = J - done;
-        const uint32_t jb = left < static_cast<uint32_t>(fa::kMaxBatch) ? left : fa::kMaxBatch;
+        const uint32_t jb = direct ? 1u : (left < static_cast<uint32_t>(fa::kMaxBatch) ? left : fa::kMaxBatch);
         fa::AccArgs a;
         std::memset(&a, 0, sizeof a);
         for (uint32_t j = 0; j < jb; ++j) {
@@ -321,14 +322,15 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
     return FA_OK;
 }
 
-// One client's pieces read in place -- from device memory (bulk kernel) or from host
-// memory the device addresses (direct kernel, over the host link) -- ordered after the
-// context's earlier work.  A pageable source is waited for before returning, so the caller
-// may reuse it at once.
-fa_status launch_in_place(fa_ctx* c, const void* const* ptrs, float w, cudaStream_t s, bool host,
-                          bool pageable) {
+// Pieces read in place -- from device memory (bulk or reduce kernel) or from host memory
+// the device addresses (direct kernel, over the host link, one client per launch) --
+// ordered after the context's earlier work.  ptrs/ws: J clients' chunks and weights, or
+// for fa_accumulate_keys one client's several chunks (J = 1).  A pageable source is
+// waited for before returning, so the caller may reuse it at once.
+fa_status launch_in_place(fa_ctx* c, const void* const* ptrs, const float* ws, uint32_t J,
+                          cudaStream_t s, bool host, bool pageable) {
     fa_status r = chain_in(c, s);
-    if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, UINT64_MAX, ptrs, &w, 1, s, host);
+    if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, UINT64_MAX, ptrs, ws, J, s, host);
     if (r == FA_OK && pageable) {
         cudaError_t ce = cudaEventRecord(c->read_ev, s);
         if (ce != cudaSuccess) r = cuda_fail(c, ce, "pageable read");
@@ -346,25 +348,32 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
         for (uint32_t j = 0; j < J; ++j)
             if (ptrs == nullptr || ptrs[j] == nullptr) return fail(c, FA_ERR_ARG, "chunk pointer is NULL");
     }
-    Mem kind = Mem::kDevice;
-    bool in_place = false;
-    if (len > 0) {
-        for (uint32_t j = 0; j < J; ++j) {
-            bool other = false;
-            Mem m = classify(ptrs[j], c->device, &other, &in_place);
-            if (other) return fail(c, FA_ERR_ARG, "chunk is in another GPU's memory");
-            if (batch && m != Mem::kDevice)
-                return fail(c, FA_ERR_ARG, "fa_accumulate_batch takes device memory only");
-            kind = m;
-        }
-    }
     // host chunks the device can address are read in place unless staging is asked for:
     // pinned memory mapped at the same pointer, and pageable memory where the device walks
     // the host page tables (then the call waits for the read, so the caller may reuse the
     // chunk on return as with staging)
     const bool stage = (c->flags & FA_STAGE_HOST) != 0;
-    const bool direct = !stage && ((kind == Mem::kPinned && in_place) ||
-                                   (kind == Mem::kPageable && c->pageable_in_place));
+    Mem kind = Mem::kDevice;
+    bool all_device = true, all_in_place = true, any_pageable = false;
+    if (len > 0) {
+        for (uint32_t j = 0; j < J; ++j) {
+            bool other = false, in_place = false;
+            const Mem m = classify(ptrs[j], c->device, &other, &in_place);
+            if (other) return fail(c, FA_ERR_ARG, "chunk is in another GPU's memory");
+            all_device = all_device && m == Mem::kDevice;
+            all_in_place = all_in_place && !stage &&
+                           ((m == Mem::kPinned && in_place) ||
+                            (m == Mem::kPageable && c->pageable_in_place));
+            any_pageable = any_pageable || m == Mem::kPageable;
+            kind = m;
+        }
+    }
+    if (batch && len > 0 && !all_device && !all_in_place)
+        return fail(c, FA_ERR_ARG,
+                    "fa_accumulate_batch reads its chunks in place: all in this GPU's memory, or all "
+                    "in host memory the device addresses");
+    const bool direct = !all_device && all_in_place;
+    if (direct) kind = any_pageable ? Mem::kPageable : Mem::kPinned;
     if (len > 0 && kind != Mem::kDevice && !direct) {
         // staging first: a failed allocation must not leave the round half-recorded
         fa_status rr = ensure_ring(c, kind == Mem::kPageable);
@@ -385,9 +394,10 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
         if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, J, s);
         if (r == FA_OK) r = chain_out(c, s);
     } else if (direct) {
-        // host memory read by the kernel over the host link, ordered on `s`
-        r = launch_in_place(c, ptrs, wv[0], s, true, kind == Mem::kPageable);
-        if (r == FA_OK) c->stats.h2d_bytes += len * c->s_in;
+        // host memory read by the kernel over the host link, ordered on `s` (a batch: one
+        // direct launch per client, in batch order)
+        r = launch_in_place(c, ptrs, wp, J, s, true, kind == Mem::kPageable);
+        if (r == FA_OK) c->stats.h2d_bytes += static_cast<uint64_t>(J) * len * c->s_in;
     } else {
         // host memory: through the staging ring, slot-sized pieces
         const uint64_t per = c->slot_bytes / c->s_in;
@@ -645,9 +655,9 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
                                                 &c->pieces, &e);
     if (st != fa::kOk) return fail(c, st, e);
     if (!any) return FA_OK;
-    fa_status r = launch_in_place(c, chunk_ptrs, static_cast<float>(weight_nk),
-                                  static_cast<cudaStream_t>(stream), !all_device,
-                                  !all_device && pageable);
+    const float w = static_cast<float>(weight_nk);
+    fa_status r = launch_in_place(c, chunk_ptrs, &w, 1, static_cast<cudaStream_t>(stream),
+                                  !all_device, !all_device && pageable);
     if (r != FA_OK) {
         c->broken = true;
         return r;

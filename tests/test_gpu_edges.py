@@ -140,7 +140,7 @@ def test_error_codes():
         assert code(fa.fa_accumulate, ctx, 0, 6.0, 0, 50, x, 50) == fa.FA_ERR_WEIGHT      # weight changed
         assert code(fa.fa_accumulate, ctx, 0, 5.0, 0, 20, x, 51) == fa.FA_ERR_RANGE       # over-coverage
         host = np.zeros(n, np.float32)
-        assert code(fa.fa_accumulate_batch, ctx, [1], [1.0], 0, 0, [host], n) == fa.FA_ERR_ARG
+        assert code(fa.fa_accumulate_batch, ctx, [1, 0], [1.0, 5.0], 0, 0, [host, x], n) == fa.FA_ERR_ARG   # mix
         assert code(fa.fa_accumulate_batch, ctx, [1, 1], [1.0, 1.0], 0, 0, [x, x], n) == fa.FA_ERR_ARG
         out = [torch.empty(n, dtype=torch.int16, device="cuda"), torch.empty(10, dtype=torch.int16, device="cuda")]
         assert code(fa.fa_finalize, ctx, out) == fa.FA_ERR_INCOMPLETE                      # client 0 sent half
@@ -473,3 +473,60 @@ def test_fa_log_reports_failures_on_stderr():
         assert r.returncode == 0, r.stderr[-2000:]
         logged = "[fedavg]" in r.stderr and "weight differs" in r.stderr
         assert logged == expect, r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("kind", ["pinned", "pageable"])
+def test_batch_from_host_memory_in_place(kind):
+    """fa_accumulate_batch over host chunks the device addresses: one in-place launch per
+    client, bit-identical to the same batch from device memory; a device/host mix and host
+    chunks under FA_STAGE_HOST are refused with nothing recorded."""
+    rng = np.random.default_rng(41)
+    n = 3 * 4096 + 11
+    J = 5
+    xs = [_bf16(rng, n) for _ in range(J)]
+    w = [float(v) for v in rng.integers(100, 1001, J)]
+    res = {}
+    for how in ("device", kind):
+        ctx = fa.fa_open([("k", n)], "bf16", "bf16", J)
+        try:
+            if how == "device":
+                ptrs = [to_dev(x) for x in xs]
+            elif how == "pinned":
+                ptrs = [to_pinned(x) for x in xs]
+            else:
+                ptrs = [x.copy() for x in xs]
+            s = torch.cuda.Stream()
+            try:
+                fa.fa_accumulate_batch(ctx, list(range(J)), w, 0, 0, ptrs, n, s)
+            except fa.FedAvgError as e:
+                if how == "pageable" and e.status == fa.FA_ERR_ARG:
+                    pytest.skip("this device does not read pageable host memory in place")
+                raise
+            out = sentinel(n, "bf16")
+            fa.fa_finalize(ctx, [out], s)
+            fa.fa_sync(ctx)
+            torch.cuda.synchronize()
+            res[how] = to_np(out, "bf16")
+            st = fa.fa_get_stats(ctx)
+            assert st["h2d_bytes"] == (0 if how == "device" else J * n * 2)
+        finally:
+            fa.fa_close(ctx)
+    assert np.array_equal(res[kind], res["device"])
+    want, _, _ = oracle.fedavg_key(w, [True] * J, xs, "bf16", "bf16")
+    check_bf16(res["device"], want, "batch")
+    ctx = fa.fa_open([("k", n)], "bf16", "bf16", J)
+    try:
+        mixed = [to_dev(xs[0]), to_pinned(xs[1])]
+        with pytest.raises(fa.FedAvgError) as e:
+            fa.fa_accumulate_batch(ctx, [0, 1], w[:2], 0, 0, mixed, n)
+        assert e.value.status == fa.FA_ERR_ARG and fa.fa_key_total(ctx, 0) == (0.0, 0)
+    finally:
+        fa.fa_close(ctx)
+    ctx = fa.fa_open([("k", n)], "bf16", "bf16", J, flags=fa.FA_STAGE_HOST)
+    try:
+        with pytest.raises(fa.FedAvgError) as e:
+            fa.fa_accumulate_batch(ctx, [0, 1], w[:2], 0, 0, [to_pinned(xs[0]), to_pinned(xs[1])], n)
+        assert e.value.status == fa.FA_ERR_ARG
+    finally:
+        torch.cuda.synchronize()
+        fa.fa_close(ctx)
