@@ -530,3 +530,60 @@ def test_batch_from_host_memory_in_place(kind):
     finally:
         torch.cuda.synchronize()
         fa.fa_close(ctx)
+
+
+def test_two_contexts_from_two_threads():
+    """Two independent aggregations (different layouts and dtypes) driven at once from two
+    host threads on one GPU: each matches the oracle; neither sees the other's state."""
+    import threading
+    rng = np.random.default_rng(55)
+    jobs = {
+        "a": ([4096 * 7 + 3, 100, 9000], "bf16", "bf16", 4),
+        "b": ([70000, 1, 4100], "f32", "f32", 3),
+    }
+    data, results, errors = {}, {}, []
+    for name, (numels, din, dout, K) in jobs.items():
+        xs = [[(_bf16(rng, n) if din == "bf16" else _f32(rng, n)) for n in numels] for _ in range(K)]
+        w = [float(v) for v in rng.integers(100, 1001, K)]
+        data[name] = (xs, w)
+
+    def run(name):
+        try:
+            numels, din, dout, K = jobs[name]
+            xs, w = data[name]
+            ctx = fa.fa_open([(f"{name}{i}", n) for i, n in enumerate(numels)], din, dout, K)
+            try:
+                s = torch.cuda.Stream()
+                for rnd in range(3):
+                    fa.fa_reset(ctx)
+                    keep = []
+                    for k in range(K):
+                        for p, n in enumerate(numels):
+                            t = to_dev(xs[k][p])
+                            keep.append(t)
+                            fa.fa_accumulate(ctx, k, w[k], p, 0, t, n, s)
+                    outs = [sentinel(n, dout) for n in numels]
+                    fa.fa_finalize(ctx, outs, s)
+                    fa.fa_sync(ctx)
+                    s.synchronize()
+                results[name] = [to_np(o, dout) for o in outs]
+            finally:
+                fa.fa_close(ctx)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    th = [threading.Thread(target=run, args=(name,)) for name in jobs]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not errors, errors
+    for name, (numels, din, dout, K) in jobs.items():
+        xs, w = data[name]
+        for p in range(len(numels)):
+            col = [xs[k][p] for k in range(K)]
+            want, _, _ = oracle.fedavg_key(w, [True] * K, col, din, dout)
+            if dout == "f32":
+                check_f32(results[name][p], want, max(float(np.abs(x).max()) for x in col), K, f"{name} {p}")
+            else:
+                check_bf16(results[name][p], want, f"{name} {p}")
