@@ -105,7 +105,17 @@ def _plan(rng, numels, K):
 
 @pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32"), ("f32", "bf16")])
 def test_random_rounds(din, dout):
-    seed = {"bf16bf16": 11, "f32f32": 12, "bf16f32": 13, "f32bf16": 14}[din + dout]
+    _random_rounds(din, dout, {"bf16bf16": 11, "f32f32": 12, "bf16f32": 13, "f32bf16": 14}[din + dout])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("seed", range(101, 109))
+def test_random_rounds_more_seeds(seed):
+    pairs = [("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32"), ("f32", "bf16")]
+    _random_rounds(*pairs[seed % 4], seed)
+
+
+def _random_rounds(din, dout, seed):
     rng_py = random.Random(seed)
     rng = np.random.default_rng(seed)
     numels = [rng_py.choice(SIZES) for _ in range(9)]
