@@ -129,8 +129,10 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
  * ([Part]: the client's sample count; [Clara]: weighted aggregation).
  *   key            a key id, or FA_KEY_FLAT
  *   offset_elems   first element of the chunk within the key (or the flat layout)
- *   chunk_ptr      len_elems contiguous values of dtype_in, in device memory or host
- *                  memory (pinned or pageable; detected per call)
+ *   chunk_ptr      len_elems contiguous values of dtype_in, in device memory, managed
+ *                  memory, or host memory (pinned or pageable; detected per call).
+ *                  Managed memory (cudaMallocManaged) is read in place with plain loads,
+ *                  since its pages may be on the host; stream-ordered like device memory.
  *   stream         cudaStream_t (as void*) ordering the read of chunk_ptr
  * The first chunk of a client in a round fixes its weight: later chunks must pass the
  * same value (else FA_ERR_WEIGHT).  weight_nk must be finite, >= 0 and <= 2^24 (the
@@ -166,9 +168,10 @@ fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64
  * and bit-identical to it.  Client ids within one call must be distinct.
  * [FLARE]: the second memory pressure -- many client updates held at once --
  * turned into one read of each update and one write of the sum.
- * The chunks are read in place: all in this GPU's memory, or all in host memory the
- * device addresses (as for fa_accumulate; then one launch per client, in order, over the
- * host link, which bounds that case anyway, and a pageable batch is waited for).
+ * The chunks are read in place: all in this GPU's memory, or all in managed memory or
+ * host memory the device addresses (as for fa_accumulate; then one plain-load launch per
+ * client, in order -- the host link bounds that case anyway -- and a pageable batch is
+ * waited for).
  * Errors: as fa_accumulate; FA_ERR_ARG for other memory, a mix, or host chunks under
  * FA_STAGE_HOST. */
 fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
@@ -185,10 +188,10 @@ fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* c
  * argument, range, weight or state error nothing is recorded.
  *   keys, offsets, lens, chunk_ptrs   n_chunks entries each (caller-owned, read during
  *                  the call); chunks of one key must not overlap, as for fa_accumulate
- * The chunks are read in place: all in this GPU's memory, or all in host memory the
- * device addresses (as for fa_accumulate: pinned memory mapped at the same pointer, or
- * pageable memory where the device walks the host page tables, in which case the call
- * waits for the reads).  Other memory, a mix, or host chunks under FA_STAGE_HOST give
+ * The chunks are read in place: all in this GPU's memory, or all in managed memory or
+ * host memory the device addresses (as for fa_accumulate: pinned memory mapped at the same
+ * pointer, or pageable memory where the device walks the host page tables, in which case
+ * the call waits for the reads).  Other memory, a mix, or host chunks under FA_STAGE_HOST give
  * FA_ERR_ARG: send those through fa_accumulate.  Ownership and stream ordering as for
  * fa_accumulate; n_chunks == 0 or all lens zero is a no-op.
  * Errors: FA_ERR_ARG, FA_ERR_RANGE, FA_ERR_WEIGHT, FA_ERR_STATE, FA_ERR_CUDA,
@@ -219,7 +222,8 @@ fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream);
  * computed as q = sum / (float)N_p (IEEE division), fma((float)server_lr, q, base) (one
  * rounding), then the RNE cast.  server_lr = 1 is plain FedAvg on deltas; the pages fix no
  * other value.  base_ptrs / out_ptrs: n_keys pointers each (or one flat pointer with
- * FA_FLAT_OUT), dtype_out values in this GPU's memory; out may equal base (in place).
+ * FA_FLAT_OUT), dtype_out values in this GPU's memory (cudaMalloc'd: managed memory is
+ * refused); out may equal base (in place).
  * Keys with N_p == 0 are not written (out keeps its contents; in place, the model is
  * unchanged).  Otherwise as fa_finalize (closes the round, non-destructive, may repeat).
  * Errors: as fa_finalize; FA_ERR_ARG for host memory or a non-finite server_lr. */
@@ -233,7 +237,7 @@ fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* con
  * K*s_in + s_out bytes per element instead of streaming's ~10 per client-element).
  *   client_ids[j], weights[j]  as fa_accumulate; contributions apply in this order
  *   flat_ptrs[j]  client j's update over the whole flat layout (total numel values of
- *                 dtype_in, in this GPU's memory)
+ *                 dtype_in, in this GPU's memory, cudaMalloc'd: managed memory is refused)
  *   out_ptrs      as fa_finalize (n_keys pointers, or one with FA_FLAT_OUT), in this
  *                 GPU's memory
  * Every client counts as having sent every key.  The result is bit-identical to

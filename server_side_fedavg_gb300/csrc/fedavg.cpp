@@ -43,7 +43,9 @@ constexpr uint64_t kDefaultSlotBytes = 64ull << 20;
 constexpr uint32_t kDefaultSlots = 4;
 constexpr uint32_t kDefaultTimeoutMs = 60000;
 
-enum class Mem { kDevice, kPinned, kPageable };
+// kManaged: cudaMallocManaged memory, read in place with plain loads only (its pages may be
+// on the host: plain loads take the migration faults; bulk copies are kept off it)
+enum class Mem { kDevice, kManaged, kPinned, kPageable };
 
 }  // namespace
 
@@ -183,7 +185,7 @@ Mem classify(const void* p, int device, bool* other_device, bool* in_place = nul
             *other_device = at.device != device;
             return Mem::kDevice;
         case cudaMemoryTypeManaged:
-            return Mem::kDevice;
+            return Mem::kManaged;
         case cudaMemoryTypeHost:
             // pinned memory the current device reads at the same address (unified
             // addressing): kernels may load it in place
@@ -355,25 +357,27 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
     const bool stage = (c->flags & FA_STAGE_HOST) != 0;
     Mem kind = Mem::kDevice;
     bool all_device = true, all_in_place = true, any_pageable = false;
+    uint32_t host_chunks = 0;
     if (len > 0) {
         for (uint32_t j = 0; j < J; ++j) {
             bool other = false, in_place = false;
             const Mem m = classify(ptrs[j], c->device, &other, &in_place);
             if (other) return fail(c, FA_ERR_ARG, "chunk is in another GPU's memory");
             all_device = all_device && m == Mem::kDevice;
-            all_in_place = all_in_place && !stage &&
-                           ((m == Mem::kPinned && in_place) ||
-                            (m == Mem::kPageable && c->pageable_in_place));
+            all_in_place = all_in_place &&
+                           (m == Mem::kManaged ||
+                            (!stage && ((m == Mem::kPinned && in_place) ||
+                                        (m == Mem::kPageable && c->pageable_in_place))));
             any_pageable = any_pageable || m == Mem::kPageable;
+            host_chunks += (m == Mem::kPinned || m == Mem::kPageable) ? 1u : 0u;
             kind = m;
         }
     }
     if (batch && len > 0 && !all_device && !all_in_place)
         return fail(c, FA_ERR_ARG,
                     "fa_accumulate_batch reads its chunks in place: all in this GPU's memory, or all "
-                    "in host memory the device addresses");
+                    "in managed memory or host memory the device addresses");
     const bool direct = !all_device && all_in_place;
-    if (direct) kind = any_pageable ? Mem::kPageable : Mem::kPinned;
     if (len > 0 && kind != Mem::kDevice && !direct) {
         // staging first: a failed allocation must not leave the round half-recorded
         fa_status rr = ensure_ring(c, kind == Mem::kPageable);
@@ -396,8 +400,8 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
     } else if (direct) {
         // host memory read by the kernel over the host link, ordered on `s` (a batch: one
         // direct launch per client, in batch order)
-        r = launch_in_place(c, ptrs, wp, J, s, true, kind == Mem::kPageable);
-        if (r == FA_OK) c->stats.h2d_bytes += static_cast<uint64_t>(J) * len * c->s_in;
+        r = launch_in_place(c, ptrs, wp, J, s, true, any_pageable);
+        if (r == FA_OK) c->stats.h2d_bytes += static_cast<uint64_t>(host_chunks) * len * c->s_in;
     } else {
         // host memory: through the staging ring, slot-sized pieces
         const uint64_t per = c->slot_bytes / c->s_in;
@@ -630,26 +634,29 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
     // every chunk is read in place: all device memory, or all host memory the device
     // addresses
     bool any = false, all_device = true, all_host = true, pageable = false;
-    uint64_t total = 0;
+    uint64_t total = 0, host_total = 0;
     for (uint32_t i = 0; i < n_chunks; ++i) {
         if (lens[i] == 0) continue;
         if (chunk_ptrs[i] == nullptr) return fail(c, FA_ERR_ARG, "chunk pointer is NULL");
         bool other = false, in_place = false;
         const Mem m = classify(chunk_ptrs[i], c->device, &other, &in_place);
         if (other) return fail(c, FA_ERR_ARG, "chunk is in another GPU's memory");
-        const bool host_ok = (c->flags & FA_STAGE_HOST) == 0 &&
-                             ((m == Mem::kPinned && in_place) ||
-                              (m == Mem::kPageable && c->pageable_in_place));
+        const bool host_ok = m == Mem::kManaged ||
+                             ((c->flags & FA_STAGE_HOST) == 0 &&
+                              ((m == Mem::kPinned && in_place) ||
+                               (m == Mem::kPageable && c->pageable_in_place)));
         all_device = all_device && m == Mem::kDevice;
         all_host = all_host && host_ok;
         pageable = pageable || m == Mem::kPageable;
         any = true;
         total += lens[i];
+        if (m == Mem::kPinned || m == Mem::kPageable) host_total += lens[i];
     }
     if (any && !all_device && !all_host)
         return fail(c, FA_ERR_ARG,
                     "fa_accumulate_keys reads its chunks in place: all in this GPU's memory, or all "
-                    "in host memory the device addresses; send others through fa_accumulate");
+                    "in managed memory or host memory the device addresses; send others through "
+                    "fa_accumulate");
     std::string e;
     int32_t st = c->ledger.plan_accumulate_keys(client_id, weight_nk, n_chunks, keys, offsets, lens,
                                                 &c->pieces, &e);
@@ -664,7 +671,7 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
     }
     for (uint32_t i = 0; i < n_chunks; ++i) c->stats.chunks += lens[i] > 0 ? 1 : 0;
     c->stats.client_bytes += total * c->s_in;
-    if (!all_device) c->stats.h2d_bytes += total * c->s_in;
+    c->stats.h2d_bytes += host_total * c->s_in;
     return FA_OK;
 }
 
@@ -713,6 +720,7 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
             kind[i] = Mem::kDevice;
             written_in_place += it.numel * c->s_out;
         }
+        if (kind[i] == Mem::kManaged) kind[i] = Mem::kDevice;   // plain stores, no staging
         any_host = any_host || kind[i] != Mem::kDevice;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);

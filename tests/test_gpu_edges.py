@@ -587,3 +587,86 @@ def test_two_contexts_from_two_threads():
                 check_f32(results[name][p], want, max(float(np.abs(x).max()) for x in col), K, f"{name} {p}")
             else:
                 check_bf16(results[name][p], want, f"{name} {p}")
+
+
+def _managed(n, dtype):
+    """n elements of cudaMallocManaged memory (as a NumPy view for the host) and a freer."""
+    import ctypes
+    fa.lib()                                          # loads the runtime the library links
+    rt = ctypes.CDLL("libcudart.so.13")
+    rt.cudaMallocManaged.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
+    rt.cudaFree.argtypes = [ctypes.c_void_p]
+    p = ctypes.c_void_p()
+    itemsize = np.dtype(dtype).itemsize
+    assert rt.cudaMallocManaged(ctypes.byref(p), n * itemsize, 1) == 0   # cudaMemAttachGlobal
+    view = np.ctypeslib.as_array((ctypes.c_uint8 * (n * itemsize)).from_address(p.value)).view(dtype)
+    return p.value, view, lambda: rt.cudaFree(p.value)
+
+
+def test_managed_memory_inputs_and_outputs():
+    """cudaMallocManaged chunks are read in place with plain loads (single calls, a batch,
+    a multi-chunk call) and a managed output is written by the finalize kernel: the same
+    bits as device memory.  The resident round and delta-apply bases refuse managed memory."""
+    rng = np.random.default_rng(61)
+    n = 2 * 4096 + 9
+    K = 4
+    xs = [_bf16(rng, n) for _ in range(K)]
+    w = [float(v) for v in rng.integers(100, 1001, K)]
+    frees = []
+    try:
+        mptr = []
+        for x in xs:
+            p, view, free = _managed(n, np.uint16)
+            view[:] = x
+            mptr.append(p)
+            frees.append(free)
+        out_p, out_view, free = _managed(n, np.uint16)
+        frees.append(free)
+        res = {}
+        for how in ("device", "managed"):
+            ctx = fa.fa_open([("k", n)], "bf16", "bf16", K)
+            try:
+                ptrs = [to_dev(x) for x in xs] if how == "device" else mptr
+                fa.fa_accumulate(ctx, 0, w[0], 0, 0, ptrs[0], n)                      # single
+                fa.fa_accumulate_batch(ctx, [1, 2], w[1:3], 0, 0, ptrs[1:3], n)        # batch
+                p3 = ptrs[3] if isinstance(ptrs[3], int) else ptrs[3].data_ptr()
+                fa.fa_accumulate_keys(ctx, 3, w[3], [0, 0], [0, 5000], [p3, p3 + 2 * 5000],
+                                      [5000, n - 5000])                               # keys
+                if how == "device":
+                    out = sentinel(n, "bf16")
+                    fa.fa_finalize(ctx, [out])
+                    fa.fa_sync(ctx)
+                    torch.cuda.synchronize()
+                    res[how] = to_np(out, "bf16")
+                else:
+                    out_view[:] = 0x7FBF
+                    fa.fa_finalize(ctx, [out_p])
+                    fa.fa_sync(ctx)
+                    torch.cuda.synchronize()
+                    res[how] = out_view.copy()
+                    assert fa.fa_get_stats(ctx)["h2d_bytes"] == 0 and fa.fa_get_stats(ctx)["d2h_bytes"] == 0
+            finally:
+                fa.fa_close(ctx)
+        assert np.array_equal(res["managed"], res["device"])
+        want, _, _ = oracle.fedavg_key(w, [True] * K, xs, "bf16", "bf16")
+        check_bf16(res["device"], want, "managed")
+        ctx = fa.fa_open([("k", n)], "bf16", "bf16", K)
+        try:
+            with pytest.raises(fa.FedAvgError) as e:
+                fa.fa_reduce_resident(ctx, list(range(K)), w, mptr, [to_dev(xs[0])])
+            assert e.value.status == fa.FA_ERR_ARG
+        finally:
+            fa.fa_close(ctx)
+        ctx = fa.fa_open([("k", n)], "bf16", "bf16", K)
+        try:
+            fa.fa_accumulate(ctx, 0, w[0], 0, 0, to_dev(xs[0]), n)
+            with pytest.raises(fa.FedAvgError) as e:
+                fa.fa_finalize_apply(ctx, [mptr[0]], [sentinel(n, "bf16")], 1.0)
+            assert e.value.status == fa.FA_ERR_ARG
+        finally:
+            torch.cuda.synchronize()
+            fa.fa_close(ctx)
+    finally:
+        torch.cuda.synchronize()
+        for f in frees:
+            f()
