@@ -312,8 +312,10 @@ fa_status fa_partition_plan(uint32_t m, const double* time_s, const double* ener
  * library's device image instead of allocated memory: FA_NOALLOC_MAX_ELEMS floats
  * (16 MiB), held on every GPU that loads the library until the process exits.
  *   weights[j]       n_j: finite, >= 0, <= 2^24
- *   client_ptrs[j]   numel values of dtype_in in this device's memory
- *   out              numel values of dtype_out in this device's memory; left untouched
+ *   client_ptrs[j]   numel values of dtype_in in this device's memory (cudaMalloc'd;
+ *                    managed memory is refused)
+ *   out              numel values of dtype_out in this device's memory (or managed memory,
+ *                    written with plain stores); left untouched
  *                    if sum(weights) == 0
  *   stream           cudaStream_t (as void*) the work is queued on; the call does not wait
  * The first call on each device looks up the array's device address (set-up); make that

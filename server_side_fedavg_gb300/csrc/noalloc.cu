@@ -71,13 +71,16 @@ __global__ void finalize_noalloc_kernel(uint64_t n, float divisor, Tout* __restr
     }
 }
 
-bool is_device_memory(const void* p, int dev) {
+// Memory of device `dev`; managed memory only where plain stores touch it (the output):
+// inputs are read with bulk copies, which are kept off pages that may sit on the host.
+bool is_device_memory(const void* p, int dev, bool allow_managed) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    return (at.type == cudaMemoryTypeDevice && at.device == dev) || at.type == cudaMemoryTypeManaged;
+    return (at.type == cudaMemoryTypeDevice && at.device == dev) ||
+           (allow_managed && at.type == cudaMemoryTypeManaged);
 }
 
 }  // namespace
@@ -102,8 +105,8 @@ extern "C" fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weig
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
     for (uint32_t j = 0; j < n_clients; ++j)
-        if (client_ptrs[j] == nullptr || !is_device_memory(client_ptrs[j], dev)) return FA_ERR_ARG;
-    if (!is_device_memory(out, dev)) return FA_ERR_ARG;
+        if (client_ptrs[j] == nullptr || !is_device_memory(client_ptrs[j], dev, false)) return FA_ERR_ARG;
+    if (!is_device_memory(out, dev, true)) return FA_ERR_ARG;
     DeviceSetup* d = nullptr;
     if (setup_for(dev, &d) != cudaSuccess) return FA_ERR_CUDA;
 

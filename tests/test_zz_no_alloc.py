@@ -76,3 +76,25 @@ def test_rejects_sizes_beyond_the_array():
     with pytest.raises(fa.FedAvgError) as e:
         fa.fa_aggregate_noalloc([1.0], [x], fa.FA_NOALLOC_MAX_ELEMS + 1, "f32", "f32", x)
     assert e.value.status == fa.FA_ERR_RANGE
+
+
+def test_rejects_inputs_outside_cudamalloc_memory():
+    """Inputs are read with bulk copies, so managed and host memory are refused (nothing is
+    launched); a managed output, written with plain stores, is accepted."""
+    from tests.test_gpu_edges import _managed
+    n = 4096
+    x = torch.ones(n, dtype=torch.float32, device="cuda")
+    mp, mview, free = _managed(n, np.float32)
+    try:
+        mview[:] = 1.0
+        for bad in (mp, np.ones(n, np.float32)):
+            with pytest.raises(fa.FedAvgError) as e:
+                fa.fa_aggregate_noalloc([1.0], [bad], n, "f32", "f32", x)
+            assert e.value.status == fa.FA_ERR_ARG
+        mview[:] = -7.0
+        fa.fa_aggregate_noalloc([2.0, 6.0], [x, x], n, "f32", "f32", mp)
+        torch.cuda.synchronize()
+        assert np.all(mview == 1.0)
+    finally:
+        torch.cuda.synchronize()
+        free()
