@@ -94,3 +94,29 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         fa.lib()
+
+
+def build_c_example():
+    """Compile tests/native/abi_example.c -- plain C11 against include/fedavg.h, linked to
+    the library and the CUDA runtime -- and return the executable's path."""
+    import subprocess
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    out_dir = os.path.join(here, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "abi_example")
+    libdir = os.path.dirname(fa.LIB_PATH)
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    cmd = ["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-O1",
+           "-I", os.path.join(root, "include"), "-I", os.path.join(cuda, "include"),
+           os.path.join(here, "native", "abi_example.c"), "-L", libdir, "-lfedavg",
+           "-L", os.path.join(cuda, "lib64"), "-lcudart",
+           f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}", "-o", exe]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return exe
+
+
+def test_header_is_c_and_links(lib):
+    """The header compiles as plain C11 (warnings as errors) and a C program links against
+    the library: the ABI needs neither Python nor C++."""
+    assert os.path.exists(build_c_example())
