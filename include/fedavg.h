@@ -257,19 +257,25 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
  * (bounded) for the context's queued work first.  Errors: FA_ERR_TIMEOUT, FA_ERR_CUDA. */
 fa_status fa_reset(fa_ctx* ctx);
 
-/* Wait (bounded by opts.timeout_ms) for the context's queued work, then free it.
- * NULL is accepted.  Errors: FA_ERR_TIMEOUT (the context is then still freed). */
+/* Wait (bounded by opts.timeout_ms) for the context's queued work, then free it (context
+ * lifetime; no counterpart in the pages).  NULL is accepted.
+ * Errors: FA_ERR_TIMEOUT (the context is then still freed). */
 fa_status fa_close(fa_ctx* ctx);
 
 /* Per-key weight total N_p (fp64, summed in ascending client id) and the number of
- * clients that sent key p, from the host bookkeeping -- exact, no device access. */
+ * clients that sent key p, from the host bookkeeping -- exact, no device access.  The
+ * per-component totals of [FLARE]'s client update contract ("Coordinating training across
+ * clients"), over the sample counts of [Part] section 2. */
 fa_status fa_key_total(const fa_ctx* ctx, uint32_t key, double* sum_nk, uint32_t* n_clients);
 
-/* Wait, bounded by opts.timeout_ms, until all work the context queued has completed.
- * Returns FA_ERR_TIMEOUT (never hangs) or FA_ERR_CUDA if that work failed. */
+/* Wait, bounded by opts.timeout_ms, until all work the context queued has completed
+ * (no counterpart in the pages).  Returns FA_ERR_TIMEOUT (never hangs) or FA_ERR_CUDA if
+ * that work failed. */
 fa_status fa_sync(fa_ctx* ctx);
 
-/* Counters since fa_open (host-side, exact). */
+/* Counters since fa_open (host-side, exact): among them the client bytes received per
+ * round, the quantity [FLARE]'s "Federating small adapters on a frozen VLM with FedUMM"
+ * compares between full-model and adapter-only updates. */
 fa_status fa_get_stats(const fa_ctx* ctx, fa_stats* out);
 
 /* Options of fa_partition_plan (NULL = {1, 0, 0.5, 0.05}: the "time only" policy). */
@@ -330,10 +336,11 @@ fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weights,
                                const void* const* client_ptrs, uint64_t numel, fa_dtype dtype_in,
                                fa_dtype dtype_out, void* out, void* stream);
 
-/* Static text for a status code. */
+/* Static text for a status code (no counterpart in the pages). */
 const char* fa_strerror(fa_status status);
 
-/* Detail of the last error on this context ("" if none); valid until the next call.
+/* Detail of the last error on this context ("" if none; no counterpart in the pages);
+ * valid until the next call.
  * With FA_LOG set in the environment (any value but "0"), each failure a call reports is
  * also written to stderr as "[fedavg] <status text>: <detail>". */
 const char* fa_last_error(const fa_ctx* ctx);
