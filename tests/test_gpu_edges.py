@@ -349,12 +349,14 @@ def test_concurrent_client_threads():
 
 
 @pytest.mark.slow
-def test_key_of_more_than_2_pow_32_elements():
+@pytest.mark.parametrize("dout", ["bf16", "f32"])
+def test_key_of_more_than_2_pow_32_elements(dout):
     """One key of 2^32 + 77 bf16 elements, so offsets inside a single segment pass 2^31 and
     2^32: two clients streamed whole, then the same two reduced resident (fa_reduce_resident),
-    sampled against the oracle around 2^31, 2^32 and the ragged end."""
+    sampled against the oracle around 2^31, 2^32 and the ragged end; bf16 and fp32 output."""
     n = (1 << 32) + 77
-    need = 2 * n * 2 + n * 4 + n * 2 + (4 << 30)
+    so = 2 if dout == "bf16" else 4
+    need = 2 * n * 2 + n * 4 + n * so + (4 << 30)
     free, _ = torch.cuda.mem_get_info()
     if free < need:
         pytest.fail(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
@@ -370,34 +372,38 @@ def test_key_of_more_than_2_pow_32_elements():
         np.arange((1 << 32) - 64, (1 << 32) + 64), np.arange(n - 200, n),
         rng.integers(0, n, 20000)])).astype(np.int64)
     tidx = torch.from_numpy(idx).cuda()
-    out = torch.empty(n, dtype=torch.int16, device="cuda")
+    odt = torch.int16 if dout == "bf16" else torch.float32
+    out = torch.empty(n, dtype=odt, device="cuda")
     got = {}
-    ctx = fa.fa_open([("big", n)], "bf16", "bf16", 2)
+    ctx = fa.fa_open([("big", n)], "bf16", dout, 2)
     try:
         for k in range(2):
             fa.fa_accumulate(ctx, k, w[k], 0, 0, xd[k], n, s)
         fa.fa_finalize(ctx, [out], s)
         fa.fa_sync(ctx)
-        got["streamed"] = out[tidx].cpu().numpy().view(np.uint16)
+        got["streamed"] = to_np(out[tidx], dout)
     finally:
         fa.fa_close(ctx)
-    out.fill_(0x7FBF)
-    ctx = fa.fa_open([("big", n)], "bf16", "bf16", 2)
+    out.fill_(0x7FBF if dout == "bf16" else -7.0)
+    ctx = fa.fa_open([("big", n)], "bf16", dout, 2)
     try:
         fa.fa_reduce_resident(ctx, [0, 1], w, xd, [out], s)
         fa.fa_sync(ctx)
-        got["resident"] = out[tidx].cpu().numpy().view(np.uint16)
+        got["resident"] = to_np(out[tidx], dout)
     finally:
         fa.fa_close(ctx)
     del xd, out
     torch.cuda.empty_cache()
     xs = [synth.gather(seed, k, 0, sigma, "bf16", idx.astype(np.uint64)) for k in range(2)]
-    want, N, cnt = oracle.fedavg_key(w, [True, True], xs, "bf16", "bf16")
+    want, N, cnt = oracle.fedavg_key(w, [True, True], xs, "bf16", dout)
     assert (N, cnt) == (1000.0, 2)
-    model = fp32_sum_model(w, [True, True], xs, "bf16")
     mx = max(float(np.abs(synth.to_f64(x, "bf16")).max()) for x in xs)
     for how, g in got.items():
-        check_bf16(g, want, f"2^32 + 77 elements, {how}", model=model, bound=1e-6 * mx * 2)
+        if dout == "f32":
+            check_f32(g, want, mx, 2, f"2^32 + 77 elements, {how}")
+        else:
+            check_bf16(g, want, f"2^32 + 77 elements, {how}",
+                       model=fp32_sum_model(w, [True, True], xs, "bf16"), bound=1e-6 * mx * 2)
     assert np.array_equal(got["streamed"], got["resident"])
 
 
