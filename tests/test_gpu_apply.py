@@ -91,3 +91,52 @@ def test_apply_rejects_host_base():
         assert e.value.status == fa.FA_ERR_ARG
     finally:
         fa.fa_close(ctx)
+
+
+@pytest.mark.slow
+def test_full_size_delta_round_sampled():
+    """The 2.2B VLM as a delta round: 8 clients streamed in its 64 MiB flat chunks, then
+    fa_finalize_apply(server_lr = 0.5) onto a base model, sampled against the oracle.  The
+    bound is the fp32 running-sum bound scaled by server_lr plus one bf16 ulp, and at least
+    99.99 % of the sampled elements must be bit-identical."""
+    import synth
+    from synth import workloads as W
+    from tests.compare import check_f32_to_bf16
+    w = W.make("vlm2b")
+    free, _ = torch.cuda.mem_get_info()
+    need = w.K * w.P * 2 + 2 * w.P * 2 + w.P * 4 + (8 << 30)
+    if free < need:
+        pytest.fail(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
+    lr = 0.5
+    s = torch.cuda.current_stream()
+    bufs = [torch.empty(w.P, dtype=torch.int16, device="cuda") for _ in range(w.K)]
+    for k in range(w.K):
+        synth.client_fill_device(w, k, 0, w.P, bufs[k].data_ptr(), s.cuda_stream)
+    base = torch.empty(w.P, dtype=torch.int16, device="cuda")
+    synth.fill_device(w.seed, w.K, 0, w.sigma, "bf16", 0, w.P, base.data_ptr(), s.cuda_stream)
+    out = torch.empty(w.P, dtype=torch.int16, device="cuda")
+    ctx = fa.fa_open([(n, k) for (n, _), k in zip(w.keys, w.numels)], "bf16", "bf16", w.K,
+                     flags=fa.FA_FLAT_OUT)
+    try:
+        for k in range(w.K):
+            for c0 in range(0, w.P, w.chunk_elems):
+                n = min(w.chunk_elems, w.P - c0)
+                fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0,
+                                 bufs[k].data_ptr() + 2 * c0, n, s)
+        fa.fa_finalize_apply(ctx, [base], [out], lr, s)
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+    finally:
+        fa.fa_close(ctx)
+    rng = np.random.default_rng(4)
+    idx = np.unique(np.concatenate([rng.integers(0, w.P, 300_000), np.arange(w.P - 300, w.P)]))
+    got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+    del bufs, base, out
+    torch.cuda.empty_cache()
+    xs = [synth.client_gather(w, k, idx.astype(np.uint64)) for k in range(w.K)]
+    b = synth.gather(w.seed, w.K, 0, w.sigma, "bf16", idx.astype(np.uint64))
+    want, _, _ = oracle.fedavg_apply_key(w.weights, [True] * w.K, xs, "bf16", b, lr, "bf16")
+    mx = max(float(np.abs(synth.to_f64(x, "bf16")).max()) for x in xs)
+    differ = check_f32_to_bf16(got, want, lr * mx, w.K, "vlm2b delta round")
+    assert differ <= 1e-4 * idx.size, f"{differ} of {idx.size} sampled elements not bit-identical"
+    print(f"vlm2b delta round: {idx.size} sampled, {1 - differ / idx.size:.6%} bit-identical")
