@@ -7,8 +7,9 @@ sum in HBM), fa_finalize (divide by the per-key weight total, RNE to bf16).
   value  client-update GB/s with every client's update already resident in HBM
          (the chunks a NIC or copy engine would have landed there)
   e2e    the same metric through the same C ABI calls with pinned HOST buffers:
-         every step copies the client updates host->device through the library's
-         staging ring and the aggregate back device->host
+         every step the kernels read the client updates from host memory in place
+         over NVLink-C2C (--stage-host: through the library's staging ring instead)
+         and write the aggregate into a pinned host buffer
   roofline  the accumulate kernel (the dominant one): algorithmic bytes per launch
          (bf16 input read + fp32 sum read + fp32 sum write; the first client's
          launches skip the sum read) over its CUDA-event-timed duration
