@@ -93,7 +93,8 @@ typedef struct fa_ctx fa_ctx;   /* opaque; owned by the library */
 
 typedef struct {
     uint32_t size;        /* sizeof(fa_opts): lets the struct grow */
-    uint32_t ring_slots;  /* device staging slots for host-memory chunks (0 = default 4) */
+    uint32_t ring_slots;  /* device staging slots for host chunks that are staged, not read
+                             in place (0 = default 4) */
     uint64_t slot_bytes;  /* bytes per staging slot (0 = default 64 MiB; rounded up to 256 B) --
                              the chunk-size knob of [FLARE]'s Tensor Downloader, here a
                              trade of pinned/device staging memory against per-copy overhead */
@@ -120,7 +121,7 @@ typedef struct {
  *   max_clients        client ids are 0..max_clients-1 (>= 1)
  *   opts               NULL for defaults
  * Allocates the fp32 running sum (sum of numel rounded up to 32 per key, x 4 bytes)
- * in device memory, the staging ring lazily on first host-memory chunk.
+ * in device memory, the staging ring lazily on the first host chunk that is staged.
  * Errors: FA_ERR_ARG, FA_ERR_DTYPE, FA_ERR_NOMEM, FA_ERR_CUDA.  *out is NULL on error. */
 fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_dtype dtype_out,
                   uint32_t max_clients, const fa_opts* opts, fa_ctx** out);
