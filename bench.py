@@ -288,6 +288,30 @@ def cpu_baseline(w, elems, min_seconds=10.0, threads=None, min_seconds_1t=3.0):
                       f"elements, {p1} passes in {dt1:.1f} s"}
 
 
+def partition_plan_us(m, reps=20000):
+    """Host time of one fa_partition_plan call for m participants (the library call itself:
+    arrays are built once), in microseconds."""
+    import ctypes
+
+    import server_side_fedavg_gb300 as fa
+    rng = np.random.default_rng(0)
+    t = rng.uniform(1.0, 2.0, m)
+    e = rng.uniform(1.0, 2.0, m)
+    n = rng.integers(100, 1000, m).astype(np.uint64)
+    tau = np.full(m, np.nan)
+    eps = np.full(m, np.nan)
+    out = np.zeros(m, np.uint64)
+    opts = fa.fa_partition_opts(1.0, 0.0, 0.5, 0.05)
+    lib = fa.lib()
+    args = (m, t.ctypes.data, e.ctypes.data, n.ctypes.data, tau.ctypes.data, eps.ctypes.data,
+            ctypes.byref(opts), out.ctypes.data)
+    assert lib.fa_partition_plan(*args) == 0
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        lib.fa_partition_plan(*args)
+    return round((time.perf_counter() - t0) / reps * 1e6, 3)
+
+
 # --------------------------------------------------------------------------- distributed bits
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -446,6 +470,22 @@ def run_ours(args, world, rank, local, pg):
     ms_per_step = ms_total / args.steps
     value = world * client_bytes / (ms_per_step * 1e-3) / 1e9
 
+    # ---- a delta round's finalize: the same aggregate applied in place to a base model
+    # (fa_finalize_apply, server_lr 0.5): reads the sum and the base, writes the output
+    for _ in range(2):
+        fa.fa_finalize_apply(ctx, [out], [out], 0.5, sh)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(s)
+    for _ in range(args.steps):
+        fa.fa_finalize_apply(ctx, [out], [out], 0.5, sh)
+    a1.record(s)
+    torch.cuda.synchronize()
+    ams = a0.elapsed_time(a1) / args.steps
+    abytes = w.P * (4 + 2 * so)
+    apply_line = {"gbs": round(abytes / (ams * 1e-3) / 1e9, 1),
+                  "frac": round(abytes / (ams * 1e-3) / 1e9 / peak, 4), "ms": round(ams, 3),
+                  "bytes": int(abytes), "kernel": f"finalize_kernel<{w.dtype_out},apply>"}
+
     # ---- the same round with every update resident, reduced in one pass (fa_reduce_resident)
     resident_line = None
     if resident == w.K and not args.no_resident:
@@ -506,6 +546,8 @@ def run_ours(args, world, rank, local, pg):
                      "traffic": profiled_traffic(acc_bytes_per_launch)},
         "gpu_launches": int(launches),
         "resident": resident_line,
+        "delta_apply": apply_line,
+        "partition_plan_us": partition_plan_us(w.K),
         "clocks": clk,
         "e2e": e2e,
     }
@@ -654,6 +696,92 @@ def run_e2e(args, w, layout, s, pg, world):
                        if args.stage_host else "pinned chunks read in place by the accumulate kernel")}
 
 
+def run_hierarchical(args, world, rank, local, pg):
+    """Two-level FedAvg (silos, then a FedAvg over the silos' fp32 means weighted by each
+    silo's total): S silos of K/S clients each.  One step = one two-level round; value =
+    client-update GB/s.  Prints its own JSON line ("mode": "hierarchical")."""
+    import torch
+
+    import server_side_fedavg_gb300 as fa
+    import synth
+    from synth import workloads as W
+
+    torch.cuda.set_device(local)
+    w = W.make(args.workload)
+    S = args.hierarchical
+    if w.K % S:
+        raise SystemExit(f"{w.K} clients do not split into {S} silos")
+    if w.dtype_in != "bf16":
+        raise SystemExit("the hierarchical mode streams bf16 client updates")
+    per = w.K // S
+    layout = [(name, n) for (name, _), n in zip(w.keys, w.numels)]
+    s = torch.cuda.Stream()
+    sh = s.cuda_stream
+    peak, peak_kind = _peaks()
+    need = w.K * w.P * 2 + S * w.P * 4 + 2 * w.P * 4 + w.P * 2 + (6 << 30)
+    free, _ = torch.cuda.mem_get_info()
+    if free < need:
+        raise SystemExit(f"{w.name} with {S} silos needs {need / 1e9:.0f} GB of HBM, {free / 1e9:.0f} free")
+    bufs = [torch.empty(w.P, dtype=torch.int16, device="cuda") for _ in range(w.K)]
+    for k in range(w.K):
+        synth.client_fill_device(w, k, 0, w.P, bufs[k].data_ptr(), sh)
+    means = [torch.empty(w.P, dtype=torch.float32, device="cuda") for _ in range(S)]
+    out = torch.empty(w.P, dtype=torch.int16, device="cuda")
+    silo = fa.fa_open(layout, "bf16", "f32", per, flags=fa.FA_FLAT_OUT)
+    top = fa.fa_open(layout, "f32", "bf16", S, flags=fa.FA_FLAT_OUT)
+    ce = w.chunk_elems or w.P
+    totals = [sum(w.weights[g * per:(g + 1) * per]) for g in range(S)]
+
+    def step():
+        for g in range(S):
+            fa.fa_reset(silo)
+            for j in range(per):
+                k = g * per + j
+                for c0 in range(0, w.P, ce):
+                    fa.fa_accumulate(silo, j, w.weights[k], fa.FA_KEY_FLAT, c0,
+                                     bufs[k].data_ptr() + 2 * c0, min(ce, w.P - c0), sh)
+            fa.fa_finalize(silo, [means[g]], sh)
+        fa.fa_reset(top)
+        ce32 = ce // 2                       # the same chunk bytes in fp32
+        for g in range(S):
+            for c0 in range(0, w.P, ce32):
+                fa.fa_accumulate(top, g, totals[g], fa.FA_KEY_FLAT, c0,
+                                 means[g].data_ptr() + 4 * c0, min(ce32, w.P - c0), sh)
+        fa.fa_finalize(top, [out], sh)
+
+    try:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        barrier(pg)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(args.steps):
+            step()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(pg, e0.elapsed_time(e1) / args.steps)
+    finally:
+        fa.fa_close(silo)
+        fa.fa_close(top)
+    client_bytes = w.K * w.P * 2
+    # silo streaming (first client 2 + 4, later 2 + 8 per element), silo finalize (4 + 4),
+    # top level over fp32 means (first 4 + 4, later 4 + 8), top finalize (4 + 2)
+    hbm = w.P * (S * (6 + 10 * (per - 1) + 8) + 8 + 12 * (S - 1) + 6)
+    line = {"metric": METRIC, "mode": "hierarchical", "value": round(world * client_bytes / (ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "P": w.P, "K": w.K, "silos": S, "clients_per_silo": per,
+                       "silo_means": "fp32", "chunk_bytes": ce * 2},
+            "hbm": {"bytes_per_round": int(hbm), "gbs": round(hbm / (ms * 1e-3) / 1e9, 1),
+                    "frac": round(hbm / (ms * 1e-3) / 1e9 / peak, 4), "peak": peak,
+                    "peak_kind": peak_kind}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -668,6 +796,8 @@ def main(argv=None):
     ap.add_argument("--no-resident", action="store_true")
     ap.add_argument("--ring-slots", type=int, default=0, help="e2e staging slots (0 = library default)")
     ap.add_argument("--slot-mb", type=int, default=0, help="e2e staging slot size in MiB (0 = default)")
+    ap.add_argument("--hierarchical", type=int, default=0, metavar="S",
+                    help="time a two-level round instead: S silos, then FedAvg over the silo means")
     ap.add_argument("--stage-host", action="store_true",
                     help="e2e: pinned chunks through the staging ring instead of read in place")
     args = ap.parse_args(argv)
@@ -677,6 +807,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank, pg)
+        if args.hierarchical > 0:
+            return run_hierarchical(args, world, rank, local, pg)
         return run_ours(args, world, rank, local, pg)
     finally:
         if pg is not None:

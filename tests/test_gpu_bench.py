@@ -58,6 +58,8 @@ def test_bench_line_has_the_contract():
     assert 0 < e["hbm_frac"] < 1 and e["hbm_gbs"] > 0
     assert d["gpu_launches"] >= 2 * (w.K + 1)              # >= one accumulate per client + finalize, per step
     assert d["resident"]["value"] > 0 and d["resident"]["launches_per_round"] >= 1
+    assert d["delta_apply"]["gbs"] > 0 and d["delta_apply"]["bytes"] == w.P * (4 + 2 * so)
+    assert 0 < d["partition_plan_us"] < 1000
     clk = d["clocks"]
     if clk is not None:
         assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
@@ -70,3 +72,13 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_hierarchical_mode_line():
+    from synth import workloads as W
+    w = W.make("lora")
+    d = _run("--workload", "lora", "--hierarchical", "2", "--steps", "2", "--warmup", "3")
+    assert d["mode"] == "hierarchical" and d["config"]["silos"] == 2
+    assert d["config"]["clients_per_silo"] == w.K // 2 and d["value"] > 0
+    per = w.K // 2
+    assert d["hbm"]["bytes_per_round"] == w.P * (2 * (6 + 10 * (per - 1) + 8) + 8 + 12 + 6)
