@@ -696,20 +696,39 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
     std::vector<Mem> kind(c->items.size());
     bool any_host = false;
     uint64_t written_in_place = 0;   // bytes the kernel stores straight into pinned host memory
+    // a flat output (and base) is one buffer: classify it once, not once per key
+    bool flat_done = false, flat_other = false, flat_in_place = false, flat_base_ok = false;
+    Mem flat_kind = Mem::kDevice;
     for (size_t i = 0; i < c->items.size(); ++i) {
         const auto& it = c->items[i];
         void* dst = flat ? out_ptrs[0] : out_ptrs[it.key];
         if (dst == nullptr) return fail(c, FA_ERR_ARG, "output pointer is NULL for a key to be written");
         bool other = false, in_place = false;
-        kind[i] = classify(dst, c->device, &other, &in_place);
+        if (flat && flat_done) {
+            kind[i] = flat_kind;
+            other = flat_other;
+            in_place = flat_in_place;
+        } else {
+            kind[i] = classify(dst, c->device, &other, &in_place);
+        }
         if (other) return fail(c, FA_ERR_ARG, "output is in another GPU's memory");
         if (apply) {
             const void* b = flat ? base_ptrs[0] : base_ptrs[it.key];
             bool bo = false;
-            if (b == nullptr || classify(b, c->device, &bo) != Mem::kDevice || bo)
+            const bool base_ok = flat && flat_done
+                                     ? flat_base_ok
+                                     : b != nullptr && classify(b, c->device, &bo) == Mem::kDevice && !bo;
+            if (flat && !flat_done) flat_base_ok = base_ok;
+            if (!base_ok)
                 return fail(c, FA_ERR_ARG, "fa_finalize_apply: base values must be in this GPU's memory");
             if (kind[i] != Mem::kDevice)
                 return fail(c, FA_ERR_ARG, "fa_finalize_apply: outputs must be in this GPU's memory");
+        }
+        if (flat && !flat_done) {
+            flat_kind = kind[i];
+            flat_other = other;
+            flat_in_place = in_place;
+            flat_done = true;
         }
         // pinned outputs the device addresses at the same pointer are written by the
         // finalize kernel itself, over the host link, unless staging is asked for.
