@@ -284,6 +284,39 @@ def test_full_size_streamed_sampled(name):
 
 
 @pytest.mark.slow
+def test_full_size_per_key_streamed_sampled():
+    """The 7B decoder streamed key by key (one fa_accumulate per client and key: 291 launches
+    per client, the 131M-element embedding and head in one launch each) instead of in flat
+    chunks, sampled against the oracle."""
+    w = W.make("llama7b")
+    free, _ = torch.cuda.mem_get_info()
+    need = w.P * 2 + w.P * 4 + w.P * 2 + (8 << 30)
+    assert free > need, f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}"
+    idx = _sample_indices(w, seed=7)
+    s = torch.cuda.current_stream()
+    x = torch.empty(w.P, dtype=torch.int16, device="cuda")      # one client's update at a time
+    out = torch.empty(w.P, dtype=torch.int16, device="cuda")
+    ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
+    try:
+        offs = w.flat_offsets()
+        for k in range(w.K):
+            synth.client_fill_device(w, k, 0, w.P, x.data_ptr(), s.cuda_stream)
+            for p, n in enumerate(w.numels):
+                fa.fa_accumulate(ctx, k, w.weights[k], p, 0, x.data_ptr() + 2 * offs[p], n, s)
+        fa.fa_finalize(ctx, [out], s)
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+    finally:
+        fa.fa_close(ctx)
+    got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
+    del x, out
+    torch.cuda.empty_cache()
+    xs = [synth.client_gather(w, k, idx) for k in range(w.K)]
+    frac = _check_sampled(got, xs, w, "llama7b per key")
+    print(f"llama7b per key: {idx.size} sampled elements, {frac:.6%} bit-identical")
+
+
+@pytest.mark.slow
 @pytest.mark.parametrize("name", ["vlm2b", "llama7b"])
 def test_full_size_resident_sampled(name):
     """fa_reduce_resident over every client's full update resident in HBM (the bench's
