@@ -317,6 +317,60 @@ def test_full_size_per_key_streamed_sampled():
 
 
 @pytest.mark.slow
+def test_full_size_partial_participation_sampled():
+    """The 7B decoder where each client sends a seeded subset of the keys (about 70 %, the
+    embedding and head among those skipped by some) and a few keys are sent by nobody: every
+    key is divided by its own reporters' total, unsent keys keep the caller's values."""
+    w = W.make("llama7b")
+    free, _ = torch.cuda.mem_get_info()
+    need = w.P * 2 + w.P * 4 + w.P * 2 + (8 << 30)
+    assert free > need, f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}"
+    rng = np.random.default_rng(17)
+    nobody = {5, 100, 200}
+    reports = [[p for p in range(w.n_keys) if p not in nobody and rng.random() < 0.7]
+               for _ in range(w.K)]
+    s = torch.cuda.current_stream()
+    x = torch.empty(w.P, dtype=torch.int16, device="cuda")
+    out = torch.full((w.P,), 0x7FBF, dtype=torch.int16, device="cuda")
+    offs = w.flat_offsets()
+    ctx = fa.fa_open(_layout(w), w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
+    try:
+        for k in range(w.K):
+            synth.client_fill_device(w, k, 0, w.P, x.data_ptr(), s.cuda_stream)
+            ps = reports[k]
+            fa.fa_accumulate_keys(ctx, k, w.weights[k], ps, [0] * len(ps),
+                                  [x.data_ptr() + 2 * offs[p] for p in ps], [w.numels[p] for p in ps], s)
+            s.synchronize()          # x is refilled for the next client
+        fa.fa_finalize(ctx, [out], s)
+        fa.fa_sync(ctx)
+        torch.cuda.synchronize()
+        totals = [fa.fa_key_total(ctx, p) for p in range(w.n_keys)]
+    finally:
+        fa.fa_close(ctx)
+    idx = _sample_indices(w, seed=9).astype(np.int64)
+    got = out[torch.from_numpy(idx).cuda()].cpu().numpy().view(np.uint16)
+    del x, out
+    torch.cuda.empty_cache()
+    key_of = np.searchsorted(np.asarray(offs, np.int64), idx, side="right") - 1
+    tally = Bf16Tally()
+    for p in np.unique(key_of):
+        sel = key_of == p
+        ii = idx[sel].astype(np.uint64)
+        rep = [p in set(reports[k]) for k in range(w.K)]
+        xs = [synth.client_gather(w, k, ii) if rep[k] else None for k in range(w.K)]
+        want, N, cnt = oracle.fedavg_key(w.weights, rep, xs, w.dtype_in, w.dtype_out)
+        assert totals[p] == (N, cnt), p
+        if want is None:
+            assert p in nobody and np.all(got[sel] == 0x7FBF), p
+            continue
+        mx = max(float(np.abs(synth.to_f64(xs[k], w.dtype_in)).max()) for k in range(w.K) if rep[k])
+        tally.add(got[sel], want, f"key {p}", model=fp32_sum_model(w.weights, rep, xs, "bf16"),
+                  bound=1e-6 * mx * cnt)
+    frac = tally.check("llama7b partial")
+    print(f"llama7b partial participation: {idx.size} sampled elements, {frac:.6%} bit-identical")
+
+
+@pytest.mark.slow
 @pytest.mark.parametrize("name", ["vlm2b", "llama7b"])
 def test_full_size_resident_sampled(name):
     """fa_reduce_resident over every client's full update resident in HBM (the bench's
