@@ -676,3 +676,83 @@ def test_managed_memory_inputs_and_outputs():
         torch.cuda.synchronize()
         for f in frees:
             f()
+
+
+def _free_mib():
+    torch.cuda.synchronize()
+    free, _ = torch.cuda.mem_get_info()
+    return free / 2 ** 20
+
+
+def test_many_rounds_do_not_grow_memory():
+    """200 rounds through one context, mixing device, pinned, pageable and staged-pinned chunks,
+    batches and multi-chunk calls, with device and host outputs: device memory does not grow
+    after the first rounds (staging is allocated once), and every round is right."""
+    rng = np.random.default_rng(71)
+    numels = [4096 + 5, 300, 70000]
+    K = 3
+    xs = [[_f32(rng, n) for n in numels] for _ in range(K)]
+    w = [2.0, 3.0, 5.0]
+    want = [oracle.fedavg_key(w, [True] * K, [xs[k][p] for k in range(K)], "f32", "f32")[0]
+            for p in range(len(numels))]
+    dev = [[to_dev(x) for x in row] for row in xs]
+    pin = [[to_pinned(x) for x in row] for row in xs]
+    ctx = fa.fa_open([(f"k{i}", n) for i, n in enumerate(numels)], "f32", "f32", K,
+                     ring_slots=2, slot_bytes=1 << 16)
+    outs_dev = [torch.empty(n, dtype=torch.float32, device="cuda") for n in numels]
+    outs_host = [np.empty(n, np.float32) for n in numels]
+    try:
+        def one_round(r):
+            fa.fa_reset(ctx)
+            mode = r % 4
+            for p, n in enumerate(numels):
+                if mode == 0:
+                    fa.fa_accumulate_batch(ctx, list(range(K)), w, p, 0, [dev[k][p] for k in range(K)], n)
+                else:
+                    for k in range(K):
+                        src = (dev, pin, None)[mode - 1] if mode < 3 else None
+                        x = src[k][p] if src is not None else xs[k][p]
+                        fa.fa_accumulate(ctx, k, w[k], p, 0, x, n)
+            outs = outs_host if r % 2 else outs_dev
+            fa.fa_finalize(ctx, outs)
+            fa.fa_sync(ctx)
+            for p in range(len(numels)):
+                got = outs[p] if r % 2 else outs[p].cpu().numpy()
+                check_f32(got, want[p], 0.3, K, f"round {r} key {p}")
+        for r in range(8):
+            one_round(r)
+        before = _free_mib()
+        for r in range(8, 200):
+            one_round(r)
+        after = _free_mib()
+        assert abs(before - after) < 4, (before, after)
+    finally:
+        fa.fa_close(ctx)
+
+
+def test_open_close_cycles_release_everything():
+    """Contexts that allocated their sum, staging ring, pinned slots and output staging are
+    freed completely by fa_close: 40 open/use/close cycles leave device memory as it was."""
+    n = 1 << 20
+    x = np.ones(n, np.float32)
+    out_host = np.empty(n, np.float32)
+    torch.cuda.synchronize()
+
+    def cycle():
+        ctx = fa.fa_open([("k", n)], "f32", "f32", 2, ring_slots=2, slot_bytes=1 << 20,
+                         flags=fa.FA_STAGE_HOST)
+        try:
+            fa.fa_accumulate(ctx, 0, 1.0, 0, 0, x, n)                 # pageable: ring + pinned slots
+            fa.fa_accumulate(ctx, 1, 1.0, 0, 0, to_pinned(x), n)      # staged pinned
+            fa.fa_finalize(ctx, [out_host])                           # host output: output staging
+            fa.fa_sync(ctx)
+        finally:
+            fa.fa_close(ctx)
+        assert np.all(out_host == 1.0)
+
+    cycle()
+    before = _free_mib()
+    for _ in range(40):
+        cycle()
+    after = _free_mib()
+    assert abs(before - after) < 4, (before, after)
