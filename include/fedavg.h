@@ -90,6 +90,29 @@ typedef struct fa_ctx fa_ctx;   /* opaque; owned by the library */
 #define FA_STAGE_HOST 2u   /* host chunks go through the staging ring, and pinned host
                               outputs through a device buffer and a copy (copy engine),
                               even where the device could address them in place */
+#define FA_COMPENSATED 4u  /* compensated running sum: a pair (hi, lo) of fp32 arrays updated
+                              by the Dot2 scheme (Ogita, Rump & Oishi, "Accurate sum and dot
+                              product", SIAM J. Sci. Comput. 26(6), 2005: an error-free
+                              product by fma, Knuth's error-free TwoSum, errors summed into
+                              lo), as accurate as a sum held in about twice fp32's precision,
+                              so that the aggregate stays within one output ulp of the exact
+                              weighted mean even where the sum nearly cancels.  [NVFP4]:
+                              low-precision updates fold into fp32 master values; this keeps
+                              that fold exact to the output's rounding.  Costs twice the sum's
+                              device memory and 8 more bytes of HBM traffic per later
+                              client-element when streaming (18 instead of 10 for bf16);
+                              resident and batched reduces keep the pair in registers.  Every
+                              path (streamed, batched, resident, in place from host memory)
+                              gives the same bits in this mode, as in the default one. */
+#define FA_TEST_WAIT_EXPIRES 0x80000000u
+                           /* test aid, never for production: in the streaming accumulate
+                              kernel each CTA's first data wait gives up at once, as if its
+                              bound ran out, so that a test can check how a device-side
+                              timeout is reported (fa_sync returns FA_ERR_INTERNAL and the
+                              round's results are invalid) without hanging or faulting the
+                              GPU.  The CTA still waits (bounded) for its loads in flight.
+                              Applies until the context's first fa_reset, so the round after
+                              it runs normally. */
 
 typedef struct {
     uint32_t size;        /* sizeof(fa_opts): lets the struct grow */
@@ -99,7 +122,7 @@ typedef struct {
                              the chunk-size knob of [FLARE]'s Tensor Downloader, here a
                              trade of pinned/device staging memory against per-copy overhead */
     uint32_t timeout_ms;  /* bound on every host-side wait (0 = default 60000) */
-    uint32_t flags;       /* FA_FLAT_OUT | FA_STAGE_HOST */
+    uint32_t flags;       /* FA_FLAT_OUT | FA_STAGE_HOST | FA_COMPENSATED */
 } fa_opts;
 
 typedef struct {
@@ -136,8 +159,11 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
  *                  since its pages may be on the host; stream-ordered like device memory.
  *   stream         cudaStream_t (as void*) ordering the read of chunk_ptr
  * The first chunk of a client in a round fixes its weight: later chunks must pass the
- * same value (else FA_ERR_WEIGHT).  weight_nk must be finite, >= 0 and <= 2^24 (the
- * device multiplies by (float)weight_nk, exact for integers in that range).
+ * same value (else FA_ERR_WEIGHT).  weight_nk must be finite, >= 0 and <= 2^24.  The
+ * device multiplies by (float)weight_nk: exact for integers in that range (sample counts,
+ * the intended use); another value is rounded to fp32 first (a relative change of at
+ * most 2^-24).  The per-key total N_p is summed in fp64 from the weights as given and
+ * divided as a pair of floats, so totals above 2^24 keep their precision.
  * A client that sends a key must send all of it before fa_finalize (chunks of one
  * client and key must not overlap; the library counts elements).
  * Ownership: device and pinned-host chunks are read in order on `stream`: the caller
@@ -202,7 +228,11 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
                              const void* const* chunk_ptrs, const uint64_t* lens, void* stream);
 
 /* Write the aggregate: for every key with N_p > 0,
- *     out[p][i] = round_to_dtype_out( sum[p][i] / (float)N_p )      (IEEE division, RNE)
+ *     out[p][i] = round_to_dtype_out( sum[p][i] / N_p )      (RNE)
+ * where the quotient is one IEEE fp32 division when N_p is exact in fp32 (every integer
+ * total up to 2^24); otherwise N_p = hi + lo as two floats and the quotient sum / hi is
+ * corrected by its exact remainder (fma) less the lo part.  With FA_COMPENSATED, sum is
+ * the pair hi + lo and the quotient is corrected the same way.
  * Keys no client sent (or whose reporters all have weight 0) are NOT written, so the
  * caller's previous global values survive (the frozen-backbone / adapter case of [FLARE]).
  *   out_ptrs  n_keys pointers (one per key, numel elements of dtype_out each), or, with
@@ -252,10 +282,40 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
                              const double* weights, const void* const* flat_ptrs,
                              void* const* out_ptrs, void* stream);
 
+/* A whole round of key subsets resident in device memory, reduced in one pass: the
+ * adapter round of [FLARE] "Federating small adapters on a frozen VLM with FedUMM" (each
+ * client sends only its adapter modules, a subset of the keys) combined per component as
+ * "Coordinating training across clients" has it.  Client j sends the n_keys[j] whole keys
+ * keys[o_j .. o_j + n_keys[j]) (o_j = n_keys[0] + ... + n_keys[j-1]), packed back to back
+ * in that order in one buffer client_ptrs[j] (dtype_in values, this GPU's memory,
+ * cudaMalloc'd).  For every key p with N_p > 0
+ *     out[p][i] = round_to_dtype_out( sum over the clients that sent p, in call order, of
+ *                                     n_k * x_k[p][i], / N_p )
+ * straight from the client buffers: (J_p * s_in + s_out) bytes per element of key p, J_p
+ * its reporters, where streaming moves s_in + 8 per client-element plus the finalize.
+ * Bit-identical to fa_accumulate_keys for each client in call order followed by
+ * fa_finalize.  Up to 16 reporters per key take one pass; if some key has more, the call
+ * runs that sequence itself (the same bits).  Keys nobody sent, or whose reporters all
+ * have weight 0, are not written.  A client id may appear once; weights as fa_accumulate.
+ * Needs a round with no contributions yet (fa_reset); closes it (fa_key_total works,
+ * fa_finalize then returns FA_ERR_STATE).  All or nothing: after an argument, range,
+ * weight or state error the round is left empty.
+ *   out_ptrs  as fa_finalize (n_keys pointers, or one with FA_FLAT_OUT), this GPU's memory
+ * Ownership: the client buffers are read in order on `stream`; keep them until the work
+ * queued there has completed.
+ * Errors: FA_ERR_ARG, FA_ERR_RANGE, FA_ERR_WEIGHT, FA_ERR_STATE, FA_ERR_CUDA, FA_ERR_NOMEM,
+ * FA_ERR_TIMEOUT. */
+fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
+                            const double* weights, const void* const* client_ptrs,
+                            const uint32_t* n_keys, const int64_t* keys, void* const* out_ptrs,
+                            void* stream);
+
 /* Start a new round ([Clara] "Server-side workflow": the loop repeats per round):
  * forget weights, per-key totals, reporter masks and element counts.  The running sum
  * is not cleared (the first contribution of the next round overwrites it).  Waits
- * (bounded) for the context's queued work first.  Errors: FA_ERR_TIMEOUT, FA_ERR_CUDA. */
+ * (bounded) for the context's queued work first.  If a device-side wait of the round
+ * being discarded gave up (see fa_sync), the reset still happens and FA_ERR_INTERNAL is
+ * returned.  Errors: FA_ERR_TIMEOUT, FA_ERR_CUDA (nothing reset), FA_ERR_INTERNAL. */
 fa_status fa_reset(fa_ctx* ctx);
 
 /* Wait (bounded by opts.timeout_ms) for the context's queued work, then free it (context
@@ -271,7 +331,11 @@ fa_status fa_key_total(const fa_ctx* ctx, uint32_t key, double* sum_nk, uint32_t
 
 /* Wait, bounded by opts.timeout_ms, until all work the context queued has completed
  * (no counterpart in the pages).  Returns FA_ERR_TIMEOUT (never hangs) or FA_ERR_CUDA if
- * that work failed. */
+ * that work failed.  Every mbarrier wait inside the kernels is bounded too; one that gave
+ * up sets a bit in this context's own device error word (never another context's), and
+ * fa_sync (also fa_reset and fa_close, which call it) then returns FA_ERR_INTERNAL: that
+ * round's results are invalid, and later calls return FA_ERR_CUDA until fa_reset, which
+ * clears the word. */
 fa_status fa_sync(fa_ctx* ctx);
 
 /* Counters since fa_open (host-side, exact): among them the client bytes received per
@@ -315,9 +379,11 @@ fa_status fa_partition_plan(uint32_t m, const double* time_s, const double* ener
  * framework's caching pool, a server that reserves its memory at start-up) or that
  * forbids allocation on its request path.  It computes what fa_open + fa_accumulate
  * (client 0, 1, ... in order) + fa_finalize + fa_close compute for a one-key layout,
- * with the same kernels, but keeps the fp32 running sum in a fixed array inside the
- * library's device image instead of allocated memory: FA_NOALLOC_MAX_ELEMS floats
- * (16 MiB), held on every GPU that loads the library until the process exits.
+ * with the same accumulate and finalize kernels and the same bits, but keeps its device
+ * state in fixed arrays inside the library's device image instead of allocated memory:
+ * the fp32 running sum (FA_NOALLOC_MAX_ELEMS floats, 16 MiB), a one-entry finalize
+ * table (written by a one-thread kernel on `stream`) and an error word of its own --
+ * held on every GPU that loads the library until the process exits.
  *   weights[j]       n_j: finite, >= 0, <= 2^24
  *   client_ptrs[j]   numel values of dtype_in in this device's memory (cudaMalloc'd;
  *                    managed memory is refused)
@@ -330,12 +396,26 @@ fa_status fa_partition_plan(uint32_t m, const double* time_s, const double* ener
  * previous call's contents: each call overwrites what it uses before reading it, and
  * calls that overlap on the GPU (different streams, or different host threads without
  * ordering) race on it.  Calls no cudaMalloc, cudaFree or other allocating routine.
+ * The call does not wait, so a device-side wait that gave up (see fa_sync) cannot be
+ * reported by it: fa_aggregate_noalloc_status reports it.  The status returned is that of
+ * this call's own launches.
  * Errors: FA_ERR_RANGE if numel > FA_NOALLOC_MAX_ELEMS (nothing is launched),
  * FA_ERR_ARG, FA_ERR_WEIGHT, FA_ERR_DTYPE, FA_ERR_CUDA.  numel == 0 or n_clients == 0
  * is a no-op. */
 fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weights,
                                const void* const* client_ptrs, uint64_t numel, fa_dtype dtype_in,
                                fa_dtype dtype_out, void* out, void* stream);
+
+/* Whether the fa_aggregate_noalloc calls on the current device since the last check ran
+ * clean (no counterpart in the pages).  Waits, bounded by timeout_ms (0 = 60000), for the
+ * work queued on `stream` (the stream the calls used), then reads the no-allocation error
+ * word of the current device and clears it.  Allocates nothing.  The word is shared by
+ * every fa_aggregate_noalloc call on the device (never by contexts, which have their own),
+ * so check after the calls whose results are to be trusted.
+ * Returns FA_OK, FA_ERR_INTERNAL (a bounded device-side wait gave up in one of those
+ * calls: their outputs are invalid), FA_ERR_TIMEOUT (the stream's work did not finish in
+ * time; nothing was read) or FA_ERR_CUDA. */
+fa_status fa_aggregate_noalloc_status(void* stream, uint32_t timeout_ms);
 
 /* Static text for a status code (no counterpart in the pages). */
 const char* fa_strerror(fa_status status);

@@ -33,6 +33,8 @@ FA_BF16 = 1
 FA_KEY_FLAT = -1
 FA_FLAT_OUT = 1
 FA_STAGE_HOST = 2
+FA_COMPENSATED = 4
+FA_TEST_WAIT_EXPIRES = 0x80000000
 FA_NOALLOC_MAX_ELEMS = 1 << 22
 
 DTYPES = {"f32": FA_F32, "bf16": FA_BF16, FA_F32: FA_F32, FA_BF16: FA_BF16}
@@ -90,6 +92,9 @@ def lib():
         L.fa_reduce_resident.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64),
                                          ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
         L.fa_finalize_apply.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), f64, vp]
+        L.fa_reduce_subsets.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64),
+                                        ctypes.POINTER(vp), ctypes.POINTER(u32), ctypes.POINTER(i64),
+                                        ctypes.POINTER(vp), vp]
         L.fa_reset.argtypes = [vp]
         L.fa_close.argtypes = [vp]
         L.fa_key_total.argtypes = [vp, u32, ctypes.POINTER(f64), ctypes.POINTER(u32)]
@@ -98,6 +103,8 @@ def lib():
         L.fa_aggregate_noalloc.argtypes = [u32, ctypes.POINTER(f64), ctypes.POINTER(vp), u64, i32, i32,
                                            vp, vp]
         L.fa_aggregate_noalloc.restype = i32
+        L.fa_aggregate_noalloc_status.argtypes = [vp, u32]
+        L.fa_aggregate_noalloc_status.restype = i32
         L.fa_partition_plan.argtypes = [u32, vp, vp, vp, vp, vp, ctypes.POINTER(fa_partition_opts), vp]
         L.fa_partition_plan.restype = i32
         L.fa_strerror.argtypes = [i32]
@@ -105,7 +112,7 @@ def lib():
         L.fa_last_error.argtypes = [vp]
         L.fa_last_error.restype = ctypes.c_char_p
         for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_accumulate_keys", "fa_finalize",
-                     "fa_finalize_apply", "fa_reduce_resident", "fa_reset",
+                     "fa_finalize_apply", "fa_reduce_resident", "fa_reduce_subsets", "fa_reset",
                      "fa_close", "fa_key_total", "fa_sync", "fa_get_stats"):
             getattr(L, name).restype = i32
         _lib = L
@@ -170,8 +177,15 @@ def fa_accumulate(ctx, client_id, weight_nk, key, offset_elems, chunk, len_elems
                                len_elems, _stream(stream)), ctx)
 
 
+def _same_length(**seqs):
+    n = {k: len(v) for k, v in seqs.items()}
+    if len(set(n.values())) > 1:
+        raise ValueError("lengths differ: " + ", ".join(f"{k}={v}" for k, v in n.items()))
+
+
 def fa_accumulate_batch(ctx, client_ids, weights, key, offset_elems, chunks, len_elems,
                         stream=None):
+    _same_length(client_ids=client_ids, weights=weights, chunks=chunks)
     J = len(client_ids)
     ids = (ctypes.c_uint32 * J)(*client_ids)
     ws = (ctypes.c_double * J)(*[float(w) for w in weights])
@@ -218,12 +232,44 @@ def fa_finalize_apply(ctx, bases, outs, server_lr=1.0, stream=None):
 
 def fa_reduce_resident(ctx, client_ids, weights, flat_updates, outs, stream=None):
     """Whole round from resident full updates (one flat buffer per client) straight to outs."""
+    _same_length(client_ids=client_ids, weights=weights, flat_updates=flat_updates)
     J = len(client_ids)
     ids = (ctypes.c_uint32 * J)(*client_ids)
     ws = (ctypes.c_double * J)(*[float(w) for w in weights])
     ps = (ctypes.c_void_p * J)(*[_ptr(x) for x in flat_updates])
     os_ = (ctypes.c_void_p * max(len(outs), 1))(*[_ptr(o) for o in outs])
     _check(lib().fa_reduce_resident(ctx, J, ids, ws, ps, os_, _stream(stream)), ctx)
+
+
+def subset_table(client_keys):
+    """Marshal per-client key lists once: (n_keys uint32 array, concatenated int64 keys)."""
+    import numpy as np
+    nk = np.ascontiguousarray([len(k) for k in client_keys], dtype=np.uint32)
+    ks = np.ascontiguousarray(np.concatenate([np.asarray(k, np.int64) for k in client_keys])
+                              if len(client_keys) else np.zeros(0, np.int64), dtype=np.int64)
+    return nk, ks
+
+
+def fa_reduce_subsets(ctx, client_ids, weights, client_bufs, client_keys, outs, stream=None):
+    """A round of key subsets resident in device memory, straight to outs: client j's
+    buffer client_bufs[j] holds its keys client_keys[j] (a list of key ids) packed back to
+    back in that order.  client_keys may also be a subset_table(...) result."""
+    import numpy as np
+    if isinstance(client_keys, tuple) and len(client_keys) == 2 and isinstance(client_keys[0], np.ndarray):
+        nk, ks = client_keys
+        _same_length(client_ids=client_ids, weights=weights, client_bufs=client_bufs, n_keys=nk)
+    else:
+        _same_length(client_ids=client_ids, weights=weights, client_bufs=client_bufs,
+                     client_keys=client_keys)
+        nk, ks = subset_table(client_keys)
+    J = len(client_ids)
+    ids = (ctypes.c_uint32 * J)(*client_ids)
+    ws = (ctypes.c_double * J)(*[float(w) for w in weights])
+    ps = (ctypes.c_void_p * J)(*[_ptr(b) for b in client_bufs])
+    os_ = (ctypes.c_void_p * max(len(outs), 1))(*[_ptr(o) for o in outs])
+    _check(lib().fa_reduce_subsets(ctx, J, ids, ws, ps, nk.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)),
+                                   ks.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), os_,
+                                   _stream(stream)), ctx)
 
 
 def fa_reset(ctx):
@@ -255,11 +301,18 @@ def fa_aggregate_noalloc(weights, chunks, numel, dtype_in, dtype_out, out, strea
     """One tensor, all clients resident, no allocation: the running sum lives in a
     fixed 16 MiB array of the library (see include/fedavg.h).  For callers that must
     not have a library allocate device memory."""
+    _same_length(weights=weights, chunks=chunks)
     J = len(chunks)
     ws = (ctypes.c_double * max(J, 1))(*[float(w) for w in weights])
     ps = (ctypes.c_void_p * max(J, 1))(*[_ptr(c) for c in chunks])
     _check(lib().fa_aggregate_noalloc(J, ws, ps, numel, DTYPES[dtype_in], DTYPES[dtype_out],
                                       _ptr(out), _stream(stream)))
+
+
+def fa_aggregate_noalloc_status(stream=None, timeout_ms=0):
+    """Raises FedAvgError (FA_ERR_INTERNAL) if a device-side wait gave up in an
+    fa_aggregate_noalloc call on the current device since the last check."""
+    _check(lib().fa_aggregate_noalloc_status(_stream(stream), timeout_ms))
 
 
 def fa_partition_plan(time_s, energy_j, samples, ema_tau=None, ema_eps=None, w_time=1.0,

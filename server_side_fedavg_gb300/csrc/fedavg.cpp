@@ -59,7 +59,8 @@ struct fa_ctx {
     uint32_t timeout_ms = kDefaultTimeoutMs;
     uint32_t slots = kDefaultSlots;
     uint64_t slot_bytes = kDefaultSlotBytes;
-    float* acc = nullptr;
+    float* acc = nullptr;         // fp32 running sum (compensated mode: its hi part)
+    float* acc_lo = nullptr;      // compensated mode (FA_COMPENSATED): the error part
     fa::LaunchShape shape;
 
     cudaEvent_t chain = nullptr;  // recorded after the last queued operation
@@ -79,9 +80,17 @@ struct fa_ctx {
     fa::FinSeg* fin_host = nullptr;
     cudaEvent_t fin_ev = nullptr;
     bool fin_pending = false;
+
+    // fa_reduce_subsets: segment and source tables, pinned host copy and device copy
+    uint8_t* gath_host = nullptr;
+    uint8_t* gath_dev = nullptr;
+    size_t gath_cap = 0;
+    cudaEvent_t gath_ev = nullptr;
+    bool gath_pending = false;
     void* out_stage = nullptr;
 
-    cudaStream_t err_stream = nullptr;   // private non-blocking stream for the error word
+    unsigned int* err_dev = nullptr;     // this context's device error word (kernels OR bits in)
+    cudaStream_t err_stream = nullptr;   // private non-blocking stream for reading it
     cudaEvent_t err_ev = nullptr;
     unsigned int* err_host = nullptr;    // pinned copy of the device error word
 
@@ -283,6 +292,9 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
             a.w[j] = ws[done + j];
         }
         a.acc = c->acc;
+        a.acc_lo = c->acc_lo;
+        a.err = c->err_dev;
+        a.debug = (c->flags & FA_TEST_WAIT_EXPIRES) ? fa::kDebugFirstWaitExpires : 0u;
         a.J = jb;
         auto flush = [&]() -> fa_status {
             if (a.nseg == 0) return FA_OK;
@@ -474,10 +486,14 @@ void free_ctx(fa_ctx* c) {
     if (c->fin_ev) cudaEventDestroy(c->fin_ev);
     if (c->fin_dev) cudaFree(c->fin_dev);
     if (c->fin_host) cudaFreeHost(c->fin_host);
+    if (c->gath_host) cudaFreeHost(c->gath_host);
+    if (c->gath_dev) cudaFree(c->gath_dev);
+    if (c->gath_ev) cudaEventDestroy(c->gath_ev);
     if (c->out_stage) cudaFree(c->out_stage);
     if (c->err_ev) cudaEventDestroy(c->err_ev);
     if (c->err_stream) cudaStreamDestroy(c->err_stream);
     if (c->err_host) cudaFreeHost(c->err_host);
+    if (c->err_dev) cudaFree(c->err_dev);
     delete c;
 }
 
@@ -491,9 +507,12 @@ fa_status sync_impl(fa_ctx* c) {
         fa_status r = wait_event(c, c->ev_copied[k], "fa_sync (copy)");
         if (r != FA_OK) return r;
     }
-    // the device error word, read on a private stream and waited for with the same bound
+    // this context's device error word, read and cleared on a private stream and waited
+    // for with the same bound (every kernel that could set it has completed by now)
     *c->err_host = 0;
-    FA_CUDA(c, fa::take_device_error_async(c->err_host, c->err_stream));
+    FA_CUDA(c, cudaMemcpyAsync(c->err_host, c->err_dev, sizeof(unsigned int), cudaMemcpyDeviceToHost,
+                               c->err_stream));
+    FA_CUDA(c, cudaMemsetAsync(c->err_dev, 0, sizeof(unsigned int), c->err_stream));
     FA_CUDA(c, cudaEventRecord(c->err_ev, c->err_stream));
     fa_status rw = wait_event(c, c->err_ev, "fa_sync (error word)");
     if (rw != FA_OK) return rw;
@@ -563,7 +582,12 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
     }
     cudaError_t ce = cudaGetDevice(&c->device);
     if (ce == cudaSuccess) ce = fa::query_launch_shape(&c->shape);
-    if (ce == cudaSuccess) ce = cudaMalloc(&c->acc, c->ledger.padded_elems() * sizeof(float));
+    const bool comp = (c->flags & FA_COMPENSATED) != 0;
+    if (ce == cudaSuccess)
+        ce = cudaMalloc(&c->acc, c->ledger.padded_elems() * sizeof(float) * (comp ? 2 : 1));
+    if (ce == cudaSuccess && comp) c->acc_lo = c->acc + c->ledger.padded_elems();
+    if (ce == cudaSuccess) ce = cudaMalloc(&c->err_dev, 256);
+    if (ce == cudaSuccess) ce = cudaMemset(c->err_dev, 0, 256);
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->chain, cudaEventDisableTiming);
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->user_ev, cudaEventDisableTiming);
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->read_ev, cudaEventDisableTiming);
@@ -577,6 +601,7 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
         c->pageable_in_place = pma == 1 && host_pt == 1;
     }
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->fin_ev, cudaEventDisableTiming);
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->gath_ev, cudaEventDisableTiming);
     if (ce == cudaSuccess) ce = cudaMalloc(&c->fin_dev, sizeof(fa::FinSeg) * n_keys);
     if (ce == cudaSuccess) ce = cudaHostAlloc(&c->fin_host, sizeof(fa::FinSeg) * n_keys, cudaHostAllocDefault);
     if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&c->err_stream, cudaStreamNonBlocking);
@@ -766,7 +791,7 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
             const char* b = static_cast<const char*>(flat ? base_ptrs[0] : base_ptrs[it.key]);
             g.base = flat ? b + it.flat_off * c->s_out : b;
         }
-        g.divisor = static_cast<float>(it.total);
+        g.div = fa::make_divisor(it.total);
         g.tile0 = ntiles;
         uint64_t t = (it.numel + fa::kTile - 1) / fa::kTile;
         if (t > 0xFFFFFFFFull - ntiles) return fail(c, FA_ERR_RANGE, "layout too large for one finalize");
@@ -782,7 +807,7 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
                                    cudaMemcpyHostToDevice, s));
         FA_CUDA(c, cudaEventRecord(c->fin_ev, s));
         c->fin_pending = true;
-        FA_CUDA(c, fa::launch_finalize(c->fin_dev, nseg, ntiles, c->dout, c->acc, apply,
+        FA_CUDA(c, fa::launch_finalize(c->fin_dev, nseg, ntiles, c->dout, c->acc, c->acc_lo, apply,
                                        static_cast<float>(server_lr), written_in_place > 0,
                                        c->shape, s));
         c->stats.kernel_launches++;
@@ -908,6 +933,8 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
             a.w[j] = w[g + j];
         }
         a.acc = c->acc;
+        a.acc_lo = c->acc_lo;
+        a.err = c->err_dev;
         for (uint32_t p = 0; p < nk;) {
             a.nseg = 0;
             a.vec_ok = 0;
@@ -935,6 +962,8 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
         ra.w[j] = w[head + j];
     }
     ra.acc = c->acc;
+    ra.acc_lo = c->acc_lo;
+    ra.err = c->err_dev;
     for (size_t i = 0; i < c->items.size();) {
         ra.nseg = 0;
         ra.vec_ok = 0;
@@ -947,7 +976,7 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
             char* dst = static_cast<char*>(flat ? out_ptrs[0] : out_ptrs[it.key]);
             if (flat) dst += it.flat_off * c->s_out;
             sg.out = dst;
-            sg.divisor = static_cast<float>(it.total);
+            sg.div = fa::make_divisor(it.total);
             sg.read_sum = head > 0 ? 1u : 0u;
             bool ok = aligned(dst, 0);
             for (uint32_t j = 0; j < last; ++j) ok = ok && aligned(ra.x[j], sg.x_off * c->s_in);
@@ -960,18 +989,218 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
     return chain_out(c, s);
 }
 
+fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
+                            const double* weights, const void* const* client_ptrs,
+                            const uint32_t* n_keys, const int64_t* keys, void* const* out_ptrs,
+                            void* stream) {
+    Range range("fa_reduce_subsets");
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    fa_ctx* c = ctx;
+    c->err.clear();
+    if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
+    if (n_clients == 0 || client_ids == nullptr || weights == nullptr || client_ptrs == nullptr ||
+        n_keys == nullptr || out_ptrs == nullptr)
+        return fail(c, FA_ERR_ARG, "empty client list or NULL argument");
+    if (c->ledger.closed() || c->ledger.has_contributions())
+        return fail(c, FA_ERR_STATE, "fa_reduce_subsets needs a round with no contributions yet (fa_reset)");
+    const uint32_t nk = c->ledger.n_keys();
+    {
+        std::vector<uint8_t> seen(c->ledger.max_clients(), 0);
+        for (uint32_t j = 0; j < n_clients; ++j) {
+            if (client_ids[j] >= c->ledger.max_clients())
+                return fail(c, FA_ERR_ARG, "client id >= max_clients");
+            if (seen[client_ids[j]]++) return fail(c, FA_ERR_ARG, "a client id appears twice");
+        }
+    }
+    uint64_t n_entries = 0;
+    for (uint32_t j = 0; j < n_clients; ++j) n_entries += n_keys[j];
+    if (n_entries > 0 && keys == nullptr) return fail(c, FA_ERR_ARG, "keys is NULL");
+    for (uint64_t e = 0; e < n_entries; ++e)
+        if (keys[e] < 0 || keys[e] >= static_cast<int64_t>(nk))
+            return fail(c, FA_ERR_ARG, "fa_reduce_subsets takes whole keys: every entry names a key id");
+    // every client buffer is read with bulk copies: this GPU's memory (cudaMalloc'd)
+    for (uint32_t j = 0; j < n_clients; ++j) {
+        if (n_keys[j] == 0) continue;
+        bool other = false;
+        if (client_ptrs[j] == nullptr || classify(client_ptrs[j], c->device, &other) != Mem::kDevice || other)
+            return fail(c, FA_ERR_ARG, "every client buffer must be in this GPU's memory (cudaMalloc'd)");
+    }
+    // bookkeeping, client by client in call order; the round was empty, so a failure is
+    // undone by resetting it (all or nothing)
+    std::string e;
+    uint64_t o = 0;
+    for (uint32_t j = 0; j < n_clients; ++j) {
+        const uint32_t n = n_keys[j];
+        int32_t st = c->ledger.record_whole_keys(client_ids[j], weights[j], n, keys + o, &e);
+        if (st != fa::kOk) {
+            c->ledger.reset();
+            return fail(c, st, "client index " + std::to_string(j) + ": " + e);
+        }
+        o += n;
+    }
+    int32_t st = c->ledger.plan_finalize(&c->items, &e);
+    if (st != fa::kOk) {
+        c->ledger.reset();
+        return fail(c, FA_ERR_INTERNAL, e);
+    }
+    // outputs: this GPU's memory
+    const bool flat = (c->flags & FA_FLAT_OUT) != 0;
+    if (!c->items.empty()) {
+        for (size_t i = 0; i < (flat ? 1 : c->items.size()); ++i) {
+            void* dst = flat ? out_ptrs[0] : out_ptrs[c->items[i].key];
+            bool other = false;
+            if (dst == nullptr || classify(dst, c->device, &other) != Mem::kDevice || other) {
+                c->ledger.reset();
+                return fail(c, FA_ERR_ARG, "fa_reduce_subsets: outputs must be in this GPU's memory");
+            }
+        }
+    }
+    // reporters per key in call order (compressed rows), and each entry's element offset
+    // within its client's packed buffer
+    std::vector<uint32_t> cnt(nk + 1, 0);
+    for (uint64_t i = 0; i < n_entries; ++i) cnt[static_cast<uint32_t>(keys[i]) + 1]++;
+    uint32_t jmax = 0;
+    for (uint32_t p = 0; p < nk; ++p) {
+        jmax = std::max(jmax, cnt[p + 1]);
+        cnt[p + 1] += cnt[p];
+    }
+    std::vector<uint32_t> fill(cnt.begin(), cnt.end() - 1);
+    std::vector<const void*> src_x(n_entries);
+    std::vector<float> src_w(n_entries);
+    std::vector<uint8_t> src_first(n_entries, 0);
+    o = 0;
+    for (uint32_t j = 0; j < n_clients; ++j) {
+        uint64_t off = 0;
+        for (uint32_t i = 0; i < n_keys[j]; ++i, ++o) {
+            const uint32_t p = static_cast<uint32_t>(keys[o]);
+            const uint32_t slot = fill[p]++;
+            src_x[slot] = static_cast<const char*>(client_ptrs[j]) + off * c->s_in;
+            src_w[slot] = static_cast<float>(weights[j]);
+            off += c->ledger.numel(p);
+        }
+    }
+    c->ledger.close();
+    c->reduced = true;
+    c->stats.chunks += n_entries;
+    for (uint64_t i = 0; i < n_entries; ++i)
+        c->stats.client_bytes += c->ledger.numel(static_cast<uint32_t>(keys[i])) * c->s_in;
+    if (c->items.empty()) return FA_OK;   // nothing sent with weight: nothing is written
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    fa_status r = chain_in(c, s);
+    if (r != FA_OK) return r;
+    if (jmax > static_cast<uint32_t>(fa::kMaxBatch)) {
+        // more reporters on a key than one pass takes: each client's keys through the
+        // streaming kernel (in call order), then the finalize kernel -- the same bits
+        c->reduced = false;
+        o = 0;
+        std::vector<fa::Piece> pieces;
+        std::vector<const void*> ptrs;
+        std::vector<uint8_t> started(nk, 0);
+        for (uint32_t j = 0; j < n_clients; ++j) {
+            pieces.clear();
+            ptrs.clear();
+            uint64_t off = 0;
+            for (uint32_t i = 0; i < n_keys[j]; ++i, ++o) {
+                const uint32_t p = static_cast<uint32_t>(keys[o]);
+                ptrs.push_back(static_cast<const char*>(client_ptrs[j]) + off * c->s_in);
+                pieces.push_back({p, i, 0, c->ledger.acc_off(p), c->ledger.numel(p), started[p] == 0});
+                started[p] = 1;
+                off += c->ledger.numel(p);
+            }
+            if (pieces.empty()) continue;
+            const float w = static_cast<float>(weights[j]);
+            r = launch_pieces(c, pieces, 0, UINT64_MAX, ptrs.data(), &w, 1, s);
+            if (r != FA_OK) {
+                c->broken = true;
+                return r;
+            }
+        }
+        r = chain_out(c, s);
+        if (r == FA_OK) r = finalize_impl(c, nullptr, out_ptrs, 1.0, stream);
+        c->reduced = true;
+        if (r != FA_OK) c->broken = true;
+        return r;
+    }
+    // segment table (one entry per key to write) and source table
+    const uint32_t nseg = static_cast<uint32_t>(c->items.size());
+    const size_t seg_bytes = (sizeof(fa::GathSeg) * nseg + 15) / 16 * 16;
+    const size_t need = seg_bytes + sizeof(fa::GathSrc) * n_entries;
+    if (c->gath_pending) {
+        r = wait_event(c, c->gath_ev, "subset table reuse");
+        if (r != FA_OK) return r;
+        c->gath_pending = false;
+    }
+    if (need > c->gath_cap) {
+        if (c->gath_host) cudaFreeHost(c->gath_host);
+        if (c->gath_dev) cudaFree(c->gath_dev);
+        c->gath_host = nullptr;
+        c->gath_dev = nullptr;
+        c->gath_cap = 0;
+        const size_t cap = std::max<size_t>(need, 64 << 10);
+        FA_CUDA(c, cudaHostAlloc(reinterpret_cast<void**>(&c->gath_host), cap, cudaHostAllocDefault));
+        FA_CUDA(c, cudaMalloc(reinterpret_cast<void**>(&c->gath_dev), cap));
+        c->gath_cap = cap;
+    }
+    auto* segs = reinterpret_cast<fa::GathSeg*>(c->gath_host);
+    auto* srcs = reinterpret_cast<fa::GathSrc*>(c->gath_host + seg_bytes);
+    for (uint64_t i = 0; i < n_entries; ++i) srcs[i] = fa::GathSrc{src_x[i], src_w[i], 0u};
+    for (uint32_t i = 0; i < nseg; ++i) {
+        const fa::FinItem& it = c->items[i];
+        char* dst = static_cast<char*>(flat ? out_ptrs[0] : out_ptrs[it.key]);
+        if (flat) dst += it.flat_off * c->s_out;
+        fa::GathSeg& g = segs[i];
+        g.len = it.numel;
+        g.out = dst;
+        g.div = fa::make_divisor(it.total);
+        g.src0 = cnt[it.key];
+        g.J = cnt[it.key + 1] - cnt[it.key];
+        g.tile0 = 0;
+        bool ok = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+        for (uint32_t q = 0; q < g.J && ok; ++q) ok = (reinterpret_cast<uintptr_t>(srcs[g.src0 + q].x) & 15u) == 0;
+        g.vec_ok = ok ? 1u : 0u;
+    }
+    fa::GathArgs ga;
+    ga.segs = reinterpret_cast<const fa::GathSeg*>(c->gath_dev);
+    ga.src = reinterpret_cast<const fa::GathSrc*>(c->gath_dev + seg_bytes);
+    ga.err = c->err_dev;
+    ga.nseg = nseg;
+    ga.jmax = jmax;
+    ga.tile = fa::gather_tile(jmax, c->din, c->dout);
+    if (!fa::plan_gather_tiles(segs, nseg, ga.tile, &ga.ntiles)) {
+        c->broken = true;
+        return fail(c, FA_ERR_RANGE, "layout too large for one subset reduce");
+    }
+    FA_CUDA(c, cudaMemcpyAsync(c->gath_dev, c->gath_host, need, cudaMemcpyHostToDevice, s));
+    FA_CUDA(c, cudaEventRecord(c->gath_ev, s));
+    c->gath_pending = true;
+    cudaError_t ce = fa::launch_gather_final(ga, c->din, c->dout, c->acc_lo != nullptr, c->shape, s);
+    if (ce != cudaSuccess) {
+        c->broken = true;
+        return cuda_fail(c, ce, "subset reduce launch");
+    }
+    c->stats.kernel_launches++;
+    return chain_out(c, s);
+}
+
 fa_status fa_reset(fa_ctx* ctx) {
     Range range("fa_reset");
     if (!ctx) return FA_ERR_ARG;
     std::lock_guard<std::mutex> lk(ctx->mu);
     DeviceGuard dg(ctx->device);
     ctx->err.clear();
+    // a device-side wait that gave up (FA_ERR_INTERNAL) invalidates the round being
+    // discarded, not the context: the word is cleared, the reset goes ahead and the
+    // status is still returned
     fa_status r = sync_impl(ctx);
-    if (r != FA_OK) return r;
+    if (r != FA_OK && r != FA_ERR_INTERNAL) return r;
     ctx->ledger.reset();
     ctx->broken = false;
     ctx->reduced = false;
-    return FA_OK;
+    ctx->flags &= ~FA_TEST_WAIT_EXPIRES;   // the test aid covers the first round only
+    return r;
 }
 
 fa_status fa_close(fa_ctx* ctx) {

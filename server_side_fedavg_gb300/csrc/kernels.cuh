@@ -10,9 +10,16 @@
 //                                             plain fp32 store); delta rounds add
 //                                             server_lr * that quotient to a base
 //
+// Compensated mode (acc_lo != nullptr): the running sum is a pair (hi, lo) of fp32
+// arrays updated by the Dot2 scheme of Ogita, Rump and Oishi ("Accurate sum and dot
+// product", SIAM J. Sci. Comput. 26(6), 2005): each product n_k * x is split exactly
+// into a rounded part and its error (fma), the rounded part is added to hi with an
+// error-free TwoSum (Knuth), and both error terms are summed into lo.  The result is
+// as accurate as a sum kept in about twice fp32's precision; finalize divides hi + lo.
+//
 // All are HBM-bandwidth bound streaming passes (about 0.1 flop per byte): no tensor
 // cores.  Layout: the fp32 running sum is padded per key to 32 elements, so each key
-// starts 128-byte aligned.
+// starts 128-byte aligned; in compensated mode lo has the same layout.
 #pragma once
 
 #include <cstdint>
@@ -24,6 +31,7 @@ constexpr int kBlock = 256;           // threads per CTA
 constexpr int kVec = 8;               // elements per vector (16 B of bf16, 2 x 16 B of fp32)
 constexpr int kTile = 4096;           // elements per tile of the finalize kernel
 constexpr int kBulkTile = 8192;       // elements per pipeline stage of the streaming kernel
+constexpr int kBulkTileComp = 6144;   // the same in compensated mode (a stage also holds lo)
 constexpr int kDirectTile = kBlock * kVec;   // elements per tile of the direct-load accumulate
 // Finalize CTAs per SM: with a tile's loads issued together, 4 CTAs (about 64 KB of loads
 // in flight per SM) gave the best rate in a sweep of 2..8 on GB300; more in flight was slower.
@@ -31,6 +39,22 @@ constexpr int kFinCtasPerSm = 4;
 constexpr int kMaxSegs = 48;          // segments per accumulate / reduce launch
 constexpr int kMaxBatch = 16;         // resident clients per launch
 constexpr int kReduceStageBytes = 73728;   // shared-memory budget per stage of the reduce kernel
+
+// Device-side error bits, OR-ed into the caller's error word (AccArgs::err, RedArgs::err).
+constexpr unsigned int kErrWaitTimeout = 1u;   // a bounded mbarrier wait gave up
+
+// AccArgs::debug bits (test aids; 0 in normal use).
+constexpr uint32_t kDebugFirstWaitExpires = 1u;   // streaming kernel: each CTA's first data
+                                                  // wait gives up as if its bound ran out
+
+// A divisor N (fp64 on the host) as an unevaluated pair of floats, hi = (float)N and
+// lo = (float)(N - hi), with rcp = (float)(1 / hi).  lo is 0 whenever N is exact in fp32
+// (every integer up to 2^24); the division then is one IEEE division.
+struct Divisor {
+    float hi;
+    float lo;
+    float rcp;
+};
 
 struct AccSeg {
     const void* x;      // one-client launches: this segment's input chunk (segments of one
@@ -45,10 +69,13 @@ struct AccSeg {
 struct AccArgs {
     const void* x[kMaxBatch];   // J input chunk bases (device), dtype_in
     float w[kMaxBatch];         // (float) n_k per input
-    float* acc;
+    float* acc;                 // running sum (compensated mode: its hi part)
+    float* acc_lo;              // compensated mode: the error part, same layout; else nullptr
+    unsigned int* err;          // the caller's device error word (never nullptr)
     uint32_t J;                 // 1..16
     uint32_t nseg;
     uint32_t ntiles;            // set by launch_accumulate
+    uint32_t debug;             // kDebug* bits
     uint64_t vec_ok;            // bit s: segment s is 16-byte aligned for x and sum
     AccSeg seg[kMaxSegs];
 };
@@ -58,16 +85,17 @@ struct RedSeg {
     uint64_t acc_idx;   // element index into the running sum
     uint64_t len;       // elements (>= 1)
     void* out;          // final mode: destination of element 0 (dtype_out)
-    float divisor;      // final mode: (float) N_p
+    Divisor div;        // final mode: N_p
     uint32_t read_sum;  // 1: earlier contributions are in the running sum
     uint32_t tile0;     // first tile (set by the launcher)
-    uint32_t pad;
 };
 
 struct RedArgs {
     const void* x[kMaxBatch];   // J input bases (device), dtype_in
     float w[kMaxBatch];
     float* acc;
+    float* acc_lo;              // compensated mode, else nullptr
+    unsigned int* err;          // the caller's device error word
     uint32_t J;                 // 1..16
     uint32_t nseg;
     uint32_t ntiles;            // set by the launcher
@@ -83,34 +111,60 @@ struct FinSeg {
     uint64_t len;       // elements
     void* out;          // destination of element 0 (device), dtype_out
     const void* base;   // delta rounds: current global model (dtype_out), else unused
-    float divisor;      // (float) N_p
+    Divisor div;        // N_p
     uint32_t tile0;     // first tile of this segment
+};
+
+// Round-level reduce of client key subsets (fa_reduce_subsets): one segment per key to
+// write, each with its own reporters.  Reporter j of segment s is src[s.src0 + j], in the
+// order the contributions apply.
+struct GathSeg {
+    uint64_t len;       // elements of the key
+    void* out;          // destination of element 0 (dtype_out)
+    Divisor div;        // N_p
+    uint32_t J;         // reporters (1..16)
+    uint32_t src0;      // first reporter in the source table
+    uint32_t tile0;     // first tile (set by launch_gather_final)
+    uint32_t vec_ok;    // 1: the output and every reporter's input are 16-byte aligned
+};
+
+struct GathSrc {
+    const void* x;      // the reporter's values of this key (dtype_in, device memory)
+    float w;            // (float) n_k
+    uint32_t pad;
+};
+
+struct GathArgs {
+    const GathSeg* segs;   // device table, nseg entries sorted by tile0
+    const GathSrc* src;    // device table
+    unsigned int* err;     // the caller's device error word
+    uint32_t nseg;
+    uint32_t ntiles;       // set by the launcher
+    uint32_t tile;         // elements per tile (set by the launcher)
+    uint32_t jmax;         // largest J over the segments (1..16)
 };
 
 struct LaunchShape {
     int sms = 0;
-    int bulk_ctas_per_sm[2] = {};       // [dtype_in], streaming kernel
-    int direct_ctas_per_sm[2] = {};     // [dtype_in], direct-load accumulate
-    int reduce_ctas_per_sm[2][3] = {};  // [dtype_in][sum mode, final fp32 out, final bf16 out]
-                                        // (same for every specialisation of J)
-    int fin_ctas_per_sm[2][2] = {};     // [apply][dtype_out]
+    int bulk_ctas_per_sm[2][2] = {};       // [compensated][dtype_in], streaming kernel
+    int direct_ctas_per_sm[2][2] = {};     // [compensated][dtype_in], direct-load accumulate
+    int reduce_ctas_per_sm[2][2][3] = {};  // [compensated][dtype_in][sum mode, final fp32 out,
+                                           // final bf16 out] (same for every J)
+    int fin_ctas_per_sm[2][2][2] = {};     // [compensated][apply][dtype_out]
+    int gather_ctas_per_sm[2][2][2] = {};  // [compensated][dtype_in][dtype_out]
 };
 
-// Device-side error bits (file-scope word shared by every launch on a device).
-constexpr unsigned int kErrWaitTimeout = 1u;   // a bounded mbarrier wait gave up
-
-// Queue on `stream` a copy of the current device's error word into *host (pinned) followed
-// by clearing it; the caller waits for the stream before reading *host.
-cudaError_t take_device_error_async(unsigned int* host, cudaStream_t stream);
+// The pair form of a divisor given in fp64.
+Divisor make_divisor(double n);
 
 // Fills the occupancy table for the current device (and sets the kernels'
 // shared-memory limits).
 cudaError_t query_launch_shape(LaunchShape* s);
 
-// dtype codes: 0 = fp32, 1 = bf16.  The caller fills x, w, acc, J (1..16), nseg, vec_ok
-// and each segment's x (J = 1) / x_off / acc_idx / len / first; the launcher numbers the
-// tiles for the kernel it picks (J = 1: streaming kernel, else the reduce kernel in sum
-// mode).
+// dtype codes: 0 = fp32, 1 = bf16.  The caller fills x, w, acc, acc_lo, err, J (1..16),
+// nseg, vec_ok, debug and each segment's x (J = 1) / x_off / acc_idx / len / first; the
+// launcher numbers the tiles for the kernel it picks (J = 1: streaming kernel, else the
+// reduce kernel in sum mode).
 // Returns cudaErrorInvalidValue if the arguments are out of range.
 cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,
                               cudaStream_t stream);
@@ -127,14 +181,27 @@ cudaError_t launch_accumulate_direct(const AccArgs& a, int dtype_in, const Launc
 cudaError_t launch_reduce_final(const RedArgs& a, int dtype_in, int dtype_out,
                                 const LaunchShape& s, cudaStream_t stream);
 
+// Round-level subset reduce: out = RNE(sum over the segment's reporters, in order, / N_p)
+// per segment, straight from the reporters' inputs (no running sum); comp: compensated
+// arithmetic (Dot2), the same operation sequence as every other path.  The caller picks
+// tile = gather_tile(jmax, ...), numbers the tiles of its host copy of the segment table
+// with plan_gather_tiles, uploads the tables, and launches with a.tile and a.ntiles set.
+uint32_t gather_tile(uint32_t jmax, int dtype_in, int dtype_out);
+// Sets tile0 of every segment for `tile` elements per tile; false if there would be more
+// than 2^32 - 1 tiles.
+bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t* ntiles);
+cudaError_t launch_gather_final(const GathArgs& a, int dtype_in, int dtype_out, bool comp,
+                                const LaunchShape& s, cudaStream_t stream);
+
 // segs: device array of nseg FinSeg sorted by tile0.
 //   apply == false: out = RNE(sum / N)
 //   apply == true:  out = RNE(fma(server_lr, sum / N, base))   (delta rounds)
+// acc_lo: compensated mode (sum = acc + acc_lo), else nullptr.
 // host_out: some outputs are host memory written in place over the host link; the grid
 // then runs at full occupancy (more stores in flight for the link) instead of
 // kFinCtasPerSm, the HBM-bound optimum.
 cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_out,
-                            const float* acc, bool apply, float server_lr, bool host_out,
-                            const LaunchShape& s, cudaStream_t stream);
+                            const float* acc, const float* acc_lo, bool apply, float server_lr,
+                            bool host_out, const LaunchShape& s, cudaStream_t stream);
 
 }  // namespace fa

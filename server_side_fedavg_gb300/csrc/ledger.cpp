@@ -288,6 +288,48 @@ int32_t Ledger::plan_accumulate_keys(uint32_t client, double weight, uint32_t n,
     return kOk;
 }
 
+int32_t Ledger::record_whole_keys(uint32_t client, double weight, uint32_t n, const int64_t* keys,
+                                  std::string* err) {
+    if (closed_) {
+        *err = "round already finalized: call fa_reset before accumulating again";
+        return kErrState;
+    }
+    if (n > 0 && keys == nullptr) {
+        *err = "keys is NULL";
+        return kErrArg;
+    }
+    int32_t st = check_client(client, weight, err);
+    if (st != kOk) return st;
+    const uint32_t nk = n_keys();
+    uint64_t* row = recv_.data() + static_cast<size_t>(client) * nk;
+    uint32_t i = 0;
+    for (; i < n; ++i) {
+        const int64_t k = keys[i];
+        if (k < 0 || k >= static_cast<int64_t>(nk)) {
+            *err = fmt("entry %llu: key %llu out of range (n_keys %llu)", i,
+                       static_cast<unsigned long long>(k), nk);
+            st = kErrArg;
+            break;
+        }
+        if (row[k] != 0) {
+            *err = fmt("client %llu would send more than numel (%llu) elements of key %llu",
+                       client, numel_[static_cast<size_t>(k)], static_cast<unsigned long long>(k));
+            st = kErrRange;
+            break;
+        }
+        row[k] = numel_[static_cast<size_t>(k)];
+    }
+    if (st != kOk) {
+        for (uint32_t j = 0; j < i; ++j) row[keys[j]] = 0;   // undo this call's marks
+        return st;
+    }
+    if (n > 0) {
+        weight_[client] = weight;
+        has_weight_[client] = 1;
+    }
+    return kOk;
+}
+
 int32_t Ledger::plan_finalize(std::vector<FinItem>* out, std::string* err) const {
     out->clear();
     const uint32_t nk = n_keys();

@@ -78,6 +78,14 @@ public:
                                  const uint64_t* offsets, const uint64_t* lens,
                                  std::vector<Piece>* out, std::string* err);
 
+    // Record n WHOLE keys sent by one client (a round-level subset reduce): every key id
+    // in range, none sent by this client before (in this call or earlier), the weight
+    // valid and consistent.  O(n); no pieces (the caller reduces the round in one pass,
+    // so the first-contribution tracking is not needed; the round is closed right after).
+    // All or nothing: on error nothing changes.
+    int32_t record_whole_keys(uint32_t client, double weight, uint32_t n, const int64_t* keys,
+                              std::string* err);
+
     // Check completeness and list the keys to write (N_p > 0).  Changes nothing.
     int32_t plan_finalize(std::vector<FinItem>* out, std::string* err) const;
 

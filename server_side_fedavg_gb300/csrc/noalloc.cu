@@ -4,35 +4,43 @@
 // framework's caching pool, a server that reserves its memory at start-up)
 // or that forbids allocation on its request path.
 //
-// The fp32 running sum lives in a fixed array in this library's device image
-// (FA_NOALLOC_MAX_ELEMS floats, 16 MiB), which every GPU that loads the
-// library keeps until the process exits.  Host code cannot use the array's
-// name as a device address: on the first call on each device the entry point
-// looks the address up with cudaGetSymbolAddress (with that device current)
-// and caches it; that first call should therefore come before any stream
-// capture.  All calls share the array and it keeps the last call's contents:
-// the first client's launch overwrites every element it uses (no clearing is
-// needed), and calls that overlap on the GPU race on it.
+// Its device state lives in fixed arrays of this library's device image, which
+// every GPU that loads the library keeps until the process exits: the fp32
+// running sum (FA_NOALLOC_MAX_ELEMS floats, 16 MiB), the finalize kernel's
+// one-entry segment table, and an error word of its own (read and cleared by
+// fa_aggregate_noalloc_status).  Host code cannot use
+// these names as device addresses: on the first call on each device the entry
+// point looks the addresses up with cudaGetSymbolAddress (with that device
+// current) and caches them; that first call should therefore come before any
+// stream capture.  All calls share the arrays and they keep the last call's
+// contents: the first client's launch overwrites every element of the sum it
+// uses and each call writes its segment entry before the finalize reads it (no
+// clearing is needed), and calls that overlap on the GPU race on them.
 #include <fedavg.h>
 
-#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <thread>
 
 #include "kernels.cuh"
 
 namespace {
 
 __device__ __align__(256) float g_noalloc_sum[FA_NOALLOC_MAX_ELEMS];
+__device__ __align__(16) fa::FinSeg g_noalloc_fin;
+__device__ unsigned int g_noalloc_error;
 
 constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
     bool ready = false;
-    float* sum = nullptr;       // device address of g_noalloc_sum on this device
+    float* sum = nullptr;            // device address of g_noalloc_sum on this device
+    fa::FinSeg* fin = nullptr;       // ... of g_noalloc_fin
+    unsigned int* err = nullptr;     // ... of g_noalloc_error
     fa::LaunchShape shape;
 };
 
@@ -44,32 +52,26 @@ cudaError_t setup_for(int dev, DeviceSetup** out) {
     std::lock_guard<std::mutex> lk(g_setup_mu);
     DeviceSetup& d = g_setup[dev];
     if (!d.ready) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_sum);
+        void* sum = nullptr;
+        void* fin = nullptr;
+        void* err = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&sum, g_noalloc_sum);
+        if (e == cudaSuccess) e = cudaGetSymbolAddress(&fin, g_noalloc_fin);
+        if (e == cudaSuccess) e = cudaGetSymbolAddress(&err, g_noalloc_error);
+        if (e == cudaSuccess) e = fa::query_launch_shape(&d.shape);
         if (e != cudaSuccess) return e;
-        e = fa::query_launch_shape(&d.shape);
-        if (e != cudaSuccess) return e;
-        d.sum = static_cast<float*>(p);
+        d.sum = static_cast<float*>(sum);
+        d.fin = static_cast<fa::FinSeg*>(fin);
+        d.err = static_cast<unsigned int*>(err);
         d.ready = true;
     }
     *out = &d;
     return cudaSuccess;
 }
 
-// The finalize step over the fixed array: out[i] = RNE(sum[i] / N), the same
-// IEEE division and cast as the regular finalize kernel.
-template <typename Tout>
-__global__ void finalize_noalloc_kernel(uint64_t n, float divisor, Tout* __restrict__ out) {
-    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-    for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const float q = __fdiv_rn(g_noalloc_sum[i], divisor);
-        if constexpr (sizeof(Tout) == 4) {
-            out[i] = q;
-        } else {
-            out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(q));
-        }
-    }
-}
+// Writes the finalize kernel's one-entry segment table, on the stream, from the kernel's
+// own parameters (no host buffer and no copy).
+__global__ void set_noalloc_segment(const __grid_constant__ fa::FinSeg seg) { g_noalloc_fin = seg; }
 
 // Memory of device `dev`; managed memory only where plain stores touch it (the output):
 // inputs are read with bulk copies, which are kept off pages that may sit on the host.
@@ -127,6 +129,8 @@ extern "C" fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weig
             aligned = aligned && (reinterpret_cast<uintptr_t>(a.x[j]) & 15u) == 0;
         }
         a.acc = d->sum;
+        a.acc_lo = nullptr;
+        a.err = d->err;
         a.J = jb;
         a.nseg = 1;
         a.vec_ok = aligned ? 1ull : 0ull;
@@ -138,14 +142,55 @@ extern "C" fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weig
         if (fa::launch_accumulate(a, din, d->shape, s) != cudaSuccess) return FA_ERR_CUDA;
         done += jb;
     }
-    const float divisor = static_cast<float>(total);
-    const int per = d->shape.fin_ctas_per_sm[0][dtype_out == FA_F32 ? 0 : 1];
-    uint64_t want = (numel + fa::kBlock - 1) / fa::kBlock;
-    uint64_t cap = static_cast<uint64_t>(d->shape.sms > 0 ? d->shape.sms : 1) * (per > 0 ? per : 1);
-    const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-    if (dtype_out == FA_F32)
-        finalize_noalloc_kernel<float><<<grid, fa::kBlock, 0, s>>>(numel, divisor, static_cast<float*>(out));
-    else
-        finalize_noalloc_kernel<uint16_t><<<grid, fa::kBlock, 0, s>>>(numel, divisor, static_cast<uint16_t*>(out));
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    // the finalize step: the library's tiled finalize kernel over a one-entry segment
+    // table in the fixed array, written on `s` just before it
+    fa::FinSeg seg;
+    std::memset(&seg, 0, sizeof seg);
+    seg.acc_idx = 0;
+    seg.len = numel;
+    seg.out = out;
+    seg.base = nullptr;
+    seg.div = fa::make_divisor(total);
+    seg.tile0 = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1);
+    cfg.stream = s;
+    if (cudaLaunchKernelEx(&cfg, set_noalloc_segment, seg) != cudaSuccess) return FA_ERR_CUDA;
+    const uint64_t ntiles = (numel + fa::kTile - 1) / fa::kTile;
+    const cudaError_t fe = fa::launch_finalize(d->fin, 1, static_cast<uint32_t>(ntiles),
+                                               dtype_out == FA_F32 ? 0 : 1, d->sum, nullptr, false,
+                                               1.0f, false, d->shape, s);
+    return fe == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" fa_status fa_aggregate_noalloc_status(void* stream, uint32_t timeout_ms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    DeviceSetup* d = nullptr;
+    if (setup_for(dev, &d) != cudaSuccess) return FA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // wait, bounded, for the work queued on `stream` (polling: never blocks without bound)
+    const auto t0 = std::chrono::steady_clock::now();
+    const uint32_t limit = timeout_ms ? timeout_ms : 60000u;
+    for (uint32_t spins = 0;; ++spins) {
+        const cudaError_t q = cudaStreamQuery(s);
+        if (q == cudaSuccess) break;
+        if (q != cudaErrorNotReady) return FA_ERR_CUDA;
+        const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                            std::chrono::steady_clock::now() - t0).count();
+        if (ms > static_cast<long long>(limit)) return FA_ERR_TIMEOUT;
+        if (spins < 64)
+            std::this_thread::yield();
+        else
+            std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+    // the stream is idle: read the word (a 4-byte copy into this stack variable) and clear it
+    unsigned int word = 0;
+    // (a copy into pageable memory returns once it has completed)
+    if (cudaMemcpyAsync(&word, d->err, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (word == 0) return FA_OK;
+    if (cudaMemsetAsync(d->err, 0, sizeof word, s) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_INTERNAL;
 }
