@@ -103,11 +103,12 @@ def bf16_values(bits: np.ndarray) -> np.ndarray:
 
 
 def check_f32_to_bf16(got_bits, want_bits, max_abs_in: float, K: int, what: str = "") -> int:
-    """fp32 inputs, bf16 output: the fp32 running-sum bound plus one bf16 ulp of the
-    result.  (With fp32 inputs the products n_k*x round inside the sum, so near-total
-    cancellation can move a small result by several bf16 ulps; the bf16 rule above
-    is for bf16 inputs, whose products are exact.)  Returns the number of elements
-    that are not bit-identical."""
+    """bf16 output where the products n_k*x are not exact in fp32 -- fp32 inputs, or
+    weights with more than 16 significant bits (totals above 2^24) or not integers: the
+    fp32 running-sum bound plus one bf16 ulp of the result.  (Those products round inside
+    the sum, so near-total cancellation can move a small result by several bf16 ulps; the
+    bf16 rule above is for bf16 inputs and integer weights up to 2^16, whose products are
+    exact.)  Returns the number of elements that are not bit-identical."""
     g = bf16_values(got_bits.view(np.uint16))
     w = bf16_values(want_bits)
     mag = np.maximum(np.abs(w), 2.0 ** -126)
@@ -125,3 +126,22 @@ def check_f32(got: np.ndarray, want: np.ndarray, max_abs_in: float, K: int, what
     worst = float(d.max()) if d.size else 0.0
     assert worst <= tol, f"{what}: fp32 error {worst:.3e} > tol {tol:.3e}"
     return worst
+
+
+def check_f32_compensated(got: np.ndarray, want: np.ndarray, max_abs_in: float, what: str = "") -> float:
+    """fp32 output of the compensated mode (FA_COMPENSATED): its Dot2 sum is as accurate as
+    one held in about twice fp32's precision (error at most ~K^2 * 2^-48 of the sum of
+    |terms|, itself at most max|x| times the divisor), and the corrected division adds
+    under one ulp of the quotient.  So every element is within two fp32 ulps of the
+    oracle's correctly rounded value, plus 2^-38 * max|x| where the weighted sum nearly
+    cancels.  Returns the largest error in ulps of the oracle value."""
+    g = got.astype(np.float64)
+    w = want.astype(np.float64)
+    mag = np.maximum(np.abs(w), np.float64(np.finfo(np.float32).tiny))
+    ulp = np.exp2(np.floor(np.log2(mag)) - 23)
+    d = np.abs(g - w)
+    tol = 2.0 * ulp + 2.0 ** -38 * max_abs_in
+    bad = d > tol
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond the compensated bound " \
+                          f"(worst {float((d / ulp).max()):.1f} ulp)"
+    return float((d / ulp).max()) if d.size else 0.0

@@ -31,6 +31,8 @@ def lib():
         L.lg_accumulate.restype = i32
         L.lg_accumulate_keys.argtypes = [vp, u32, f64, u32, vp, vp, vp, vp, u32, ctypes.POINTER(u32)]
         L.lg_accumulate_keys.restype = i32
+        L.lg_whole_keys.argtypes = [vp, u32, f64, u32, vp]
+        L.lg_whole_keys.restype = i32
         L.lg_finalize.argtypes = [vp, vp, vp, u32, ctypes.POINTER(u32)]
         L.lg_finalize.restype = i32
         L.lg_reset.argtypes = [vp]
@@ -81,6 +83,11 @@ class Ledger:
         st = lib().lg_accumulate_keys(self.h, client, weight, n, keys, offs, lens, rows, 4096,
                                       ctypes.byref(m))
         return st, [tuple(rows[6 * i:6 * i + 6]) for i in range(min(m.value, 4096))]
+
+    def whole_keys(self, client, weight, keys):
+        n = len(keys)
+        ks = (ctypes.c_int64 * max(n, 1))(*keys)
+        return lib().lg_whole_keys(self.h, client, weight, n, ks)
 
     def finalize(self):
         rows = (ctypes.c_uint64 * (5 * 4096))()

@@ -73,6 +73,11 @@ int32_t lg_accumulate_keys(void* p, uint32_t client, double weight, uint32_t n,
     return st;
 }
 
+int32_t lg_whole_keys(void* p, uint32_t client, double weight, uint32_t n, const int64_t* keys) {
+    auto* h = static_cast<Handle*>(p);
+    return h->lg.record_whole_keys(client, weight, n, keys, &h->err);
+}
+
 // items out: rows of (key, acc_idx, flat_off, numel, reporters) and totals
 int32_t lg_finalize(void* p, uint64_t* rows, double* totals, uint32_t max_rows, uint32_t* n_rows) {
     auto* h = static_cast<Handle*>(p);

@@ -79,6 +79,28 @@ def test_argument_errors_need_no_device(lib):
     assert fa.fa_last_error(None) == ""
 
 
+def test_binding_checks_batch_lengths(lib):
+    """Lists of clients, weights and chunks of different lengths are refused before the
+    library is called (ctypes would otherwise pad missing weights with zeros)."""
+    with pytest.raises(ValueError, match="lengths differ"):
+        fa.fa_accumulate_batch(None, [0, 1], [1.0], 0, 0, [0, 0], 4)
+    with pytest.raises(ValueError, match="lengths differ"):
+        fa.fa_reduce_resident(None, [0, 1], [1.0, 2.0], [0], [0])
+    with pytest.raises(ValueError, match="lengths differ"):
+        fa.fa_aggregate_noalloc([1.0, 2.0, 3.0], [0, 0], 4, "f32", "f32", 0)
+
+
+def test_noalloc_argument_errors_need_no_device(lib):
+    w = (ctypes.c_double * 1)(1.0)
+    p = (ctypes.c_void_p * 1)(None)
+    assert lib.fa_aggregate_noalloc(1, w, p, fa.FA_NOALLOC_MAX_ELEMS + 1, 0, 0, None, None) == fa.FA_ERR_RANGE
+    assert lib.fa_aggregate_noalloc(1, w, p, 8, 5, 0, None, None) == fa.FA_ERR_DTYPE
+    assert lib.fa_aggregate_noalloc(1, w, p, 8, 0, 0, None, None) == fa.FA_ERR_ARG
+    bad = (ctypes.c_double * 1)(float("nan"))
+    assert lib.fa_aggregate_noalloc(1, bad, p, 8, 0, 0, 1, None) == fa.FA_ERR_WEIGHT
+    assert lib.fa_aggregate_noalloc(0, w, p, 8, 0, 0, None, None) == fa.FA_OK
+
+
 def test_open_without_a_device_fails_cleanly(lib):
     import torch
     if torch.cuda.is_available():

@@ -59,6 +59,9 @@ def test_bench_line_has_the_contract():
     assert d["gpu_launches"] >= 2 * (w.K + 1)              # >= one accumulate per client + finalize, per step
     assert d["resident"]["value"] > 0 and d["resident"]["launches_per_round"] >= 1
     assert d["delta_apply"]["gbs"] > 0 and d["delta_apply"]["bytes"] == w.P * (4 + 2 * so)
+    cp = d["compensated"]
+    assert cp["value"] > 0 and cp["bytes_per_round"] == w.P * (si + 8 + (w.K - 1) * (si + 16) + 8 + so)
+    assert 0 < cp["accumulate"]["frac"] and cp["distinct_client_buffers"] >= 1
     assert 0 < d["partition_plan_us"] < 1000
     clk = d["clocks"]
     if clk is not None:
@@ -82,3 +85,21 @@ def test_hierarchical_mode_line():
     assert d["config"]["clients_per_silo"] == w.K // 2 and d["value"] > 0
     per = w.K // 2
     assert d["hbm"]["bytes_per_round"] == w.P * (2 * (6 + 10 * (per - 1) + 8) + 8 + 12 + 6)
+
+
+def test_adapter_round_line():
+    """The LoRA workload (clients send seeded subsets of the modules): the streamed round
+    sends each client's reported keys only, and the `subsets` field times the one-pass
+    round-level reduce over the same packed buffers."""
+    import bench
+    w = W.make("lora")
+    d = _run("--workload", "lora", "--steps", "3", "--warmup", "3", "--e2e-steps", "2",
+             "--no-cpu-baseline")
+    cb = w.client_bytes()
+    assert cb < w.K * w.P * 2                                # partial participation
+    assert abs(d["value"] - cb / (d["ms_per_step"] * 1e-3) / 1e9) <= 0.05 * d["value"]
+    sub = d["subsets"]
+    assert sub["bytes_per_round"] == bench.subset_bytes(w) and sub["launches_per_round"] == 1
+    assert sub["value"] > 0 and sub["hbm_frac"] > 0 and sub["wall_ms_per_round"] > 0
+    assert d["resident"] is None and d["compensated"] is None
+    assert d["e2e"]["h2d_bytes_per_step"] == cb

@@ -3,7 +3,9 @@
 Small workloads (tiny CNN, 3-D U-Net, LoRA adapters with partial participation)
 are compared element by element on every key; the two full-size streamed
 workloads (2.2B VLM, 7B decoder) run exactly as bench.py streams them and are
-compared on sampled elements the oracle recomputes one by one.
+compared on every element (tests/full_compare.py); their other ingest forms
+(per key, partial participation, resident, host-fed) on sampled elements the
+oracle recomputes one by one.
 Tolerances: tests/compare.py."""
 import numpy as np
 import pytest
@@ -200,87 +202,37 @@ def _sample_indices(w, n_random=200_000, seed=1):
     return np.unique(np.concatenate(idx)).astype(np.uint64)
 
 
-def _check_sampled(got, xs, w, what):
+def _check_sampled(got, xs, w, what, strict=False):
     """bf16 output of a full-size workload against the oracle on sampled elements (clients
     applied in id order, as bench.py streams them), with the fp32 sum model for the rare
-    elements where the weighted sum nearly cancels."""
+    elements where the weighted sum nearly cancels -- or, `strict` (the compensated mode),
+    with no such escape."""
     want, N, cnt = oracle.fedavg_key(w.weights, [True] * w.K, xs, w.dtype_in, w.dtype_out)
+    if strict:
+        return check_bf16(got, want, what)
     maxw = max(float(np.abs(synth.to_f64(x, w.dtype_in)).max()) for x in xs)
     return check_bf16(got, want, what, model=fp32_sum_model(w.weights, [True] * w.K, xs, "bf16"),
                       bound=1e-6 * maxw * w.K)
 
 
-def _heavy_layer(w):
-    """Flat range of the decoder layer holding the heavy-tailed (Student-t) client's largest
-    |value| -- the layer where the fp32 sum's rounding is most exposed.  The device
-    generator only picks the layer; the values checked come from the host generator."""
-    k = w.dists.index(W.DIST_STUDENT3)
-    x = torch.empty(w.P, dtype=torch.int16, device="cuda")
-    synth.client_fill_device(w, k, 0, w.P, x.data_ptr(), torch.cuda.current_stream().cuda_stream)
-    xb = x.view(torch.bfloat16)
-    best, layer = -1.0, None
-    for (name, _), off, n in zip(w.keys, w.flat_offsets(), w.numels):
-        if not name.startswith("layers."):
-            continue
-        m = float(xb[off:off + n].abs().max())
-        if m > best:
-            best, layer = m, name.split(".")[1]
-    del x, xb
-    torch.cuda.empty_cache()
-    rng = [(off, off + n) for (name, _), off, n in zip(w.keys, w.flat_offsets(), w.numels)
-           if name.startswith(f"layers.{layer}.")]
-    return int(layer), rng[0][0], rng[-1][1], best
-
-
-def _oracle_range(w, lo, hi, threads=16):
-    """The oracle over the contiguous flat range [lo, hi), split over host threads."""
-    from concurrent.futures import ThreadPoolExecutor
-    xs = [synth.client_flat(w, k, lo, hi - lo) for k in range(w.K)]
-    out = np.empty(hi - lo, np.uint16 if w.dtype_out == "bf16" else np.float32)
-    per = -(-(hi - lo) // threads)
-
-    def part(t):
-        a, b = t * per, min(hi - lo, (t + 1) * per)
-        if b > a:
-            oracle.fedavg_key(w.weights, [True] * w.K, [x[a:b] for x in xs], w.dtype_in,
-                              w.dtype_out, out=out[a:b])
-    with ThreadPoolExecutor(threads) as ex:
-        list(ex.map(part, range(threads)))
-    return out
-
-
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["vlm2b", "llama7b"])
-def test_full_size_streamed_sampled(name):
-    """The full-size round streamed as bench.py streams it, compared with the oracle on
-    sampled elements (every norm key in full); for the 7B decoder also on the whole
-    layer that holds the heavy-tailed client's largest value."""
+@pytest.mark.parametrize("name,flags", [("vlm2b", 0), ("llama7b", 0), ("llama7b", fa.FA_COMPENSATED)])
+def test_full_size_streamed_every_element(name, flags):
+    """The full-size round streamed exactly as bench.py streams it (flat chunks of 64 / 256
+    MiB, clients in id order), compared with the oracle on EVERY element, key by key.
+    Default mode: the bf16 rule with the fp32-sum escape; compensated mode
+    (FA_COMPENSATED): the plain rule, no escape."""
     import bench
+    from tests.full_compare import compare_every_element
     w = W.make(name)
     free, _ = torch.cuda.mem_get_info()
-    need = w.P * 2 * 2 + w.P * 4 + (8 << 30)
+    need = w.P * 2 * 2 + w.P * 4 * (2 if flags else 1) + (8 << 30)
     assert free > need, f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}"
-    idx = _sample_indices(w)
-    heavy = _heavy_layer(w) if W.DIST_STUDENT3 in w.dists else None
-    out = bench.run_streamed_round(w, resident=False)
-    got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
-    got_layer = out[heavy[1]:heavy[2]].cpu().numpy().view(np.uint16) if heavy else None
-    assert bool(torch.isfinite(out.view(torch.bfloat16)).all())
+    out = bench.run_streamed_round(w, flags=flags)
+    got = out.cpu().numpy().view(np.uint16)
     del out
     torch.cuda.empty_cache()
-    xs = [synth.client_gather(w, k, idx) for k in range(w.K)]
-    frac = _check_sampled(got, xs, w, name)
-    print(f"{name}: {idx.size} sampled elements, {frac:.6%} bit-identical")
-    if heavy:
-        layer, lo, hi, peak = heavy
-        want_layer = _oracle_range(w, lo, hi)
-        xl = [synth.client_flat(w, k, lo, hi - lo) for k in range(w.K)]
-        maxw = max(float(np.abs(synth.to_f64(x, w.dtype_in)).max()) for x in xl)
-        frac = check_bf16(got_layer, want_layer, f"{name} layer {layer}",
-                          model=fp32_sum_model(w.weights, [True] * w.K, xl, "bf16"),
-                          bound=1e-6 * maxw * w.K)
-        print(f"{name}: layer {layer} in full ({hi - lo} elements, heavy-tailed client's "
-              f"max |x| = {peak:.3g}), {frac:.6%} bit-identical")
+    compare_every_element(w, got, escape=not flags)
 
 
 @pytest.mark.slow
@@ -371,25 +323,27 @@ def test_full_size_partial_participation_sampled():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["vlm2b", "llama7b"])
-def test_full_size_resident_sampled(name):
+@pytest.mark.parametrize("name,flags", [("vlm2b", 0), ("llama7b", 0), ("llama7b", fa.FA_COMPENSATED)])
+def test_full_size_resident_sampled(name, flags):
     """fa_reduce_resident over every client's full update resident in HBM (the bench's
-    `resident` configuration), sampled against the oracle."""
+    `resident` configuration), sampled against the oracle (compensated mode: the plain
+    bf16 rule, no escape)."""
     import bench
     w = W.make(name)
     free, _ = torch.cuda.mem_get_info()
-    need = w.K * w.P * 2 + w.P * 2 + w.P * 4 + (8 << 30)
+    need = w.K * w.P * 2 + w.P * 2 + w.P * 4 * (2 if flags else 1) + (8 << 30)
     if free < need:
         pytest.fail(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
     idx = _sample_indices(w, seed=2)
-    out = bench.run_resident_round(w)
+    out = bench.run_resident_round(w, flags=flags)
     got = out[torch.from_numpy(idx.astype(np.int64)).cuda()].cpu().numpy().view(np.uint16)
     assert bool(torch.isfinite(out.view(torch.bfloat16)).all())
     del out
     torch.cuda.empty_cache()
     xs = [synth.client_gather(w, k, idx) for k in range(w.K)]
-    frac = _check_sampled(got, xs, w, name + " resident")
-    print(f"{name} resident: {idx.size} sampled elements, {frac:.6%} bit-identical")
+    what = name + " resident" + (" compensated" if flags else "")
+    frac = _check_sampled(got, xs, w, what, strict=bool(flags))
+    print(f"{what}: {idx.size} sampled elements, {frac:.6%} bit-identical")
 
 
 @pytest.mark.slow

@@ -318,3 +318,42 @@ def test_accumulate_keys_matches_single_calls():
             single += [tuple(int(v) for v in q) for q in ps]
         assert [tuple(int(v) for v in q[1:]) for q in multi] == single
     assert [a.key_total(p) for p in range(5)] == [b.key_total(p) for p in range(5)]
+
+
+def test_whole_keys_records_like_accumulate_keys():
+    """record_whole_keys (the round-level subset reduce's bookkeeping) leaves the same totals,
+    reporter counts and finalize list as accumulate_keys with whole keys."""
+    numels = [5, 100, 7, 64, 1]
+    rng = random.Random(11)
+    for trial in range(20):
+        K = rng.randint(1, 6)
+        a, b = Ledger(numels, K + 2), Ledger(numels, K + 2)
+        for c in rng.sample(range(K + 2), K):
+            keys = rng.sample(range(len(numels)), rng.randint(0, len(numels)))
+            w = float(rng.choice([0, 1, 3, 1000, 2 ** 24]))
+            assert a.whole_keys(c, w, keys) == 0
+            st, _ = b.accumulate_keys(c, w, [(p, 0, numels[p]) for p in keys])
+            assert st == 0
+        for p in range(len(numels)):
+            assert a.key_total(p) == b.key_total(p)
+        assert a.finalize() == b.finalize()
+
+
+def test_whole_keys_errors_record_nothing():
+    numels = [5, 100, 7]
+    lg = Ledger(numels, 3)
+    assert lg.whole_keys(0, 2.0, [0, 2]) == 0
+    before = [lg.key_total(p) for p in range(3)]
+    assert lg.whole_keys(1, 1.0, [1, 3]) == -1          # key out of range
+    assert lg.whole_keys(1, 1.0, [1, -1]) == -1         # flat is not a whole key
+    assert lg.whole_keys(1, 1.0, [1, 2, 1]) == -2       # the same key twice
+    assert lg.whole_keys(0, 2.0, [1, 0]) == -2          # key 0 already sent by client 0
+    assert lg.whole_keys(0, 3.0, [1]) == -4             # weight differs from earlier
+    assert lg.whole_keys(2, -1.0, [1]) == -4            # invalid weight
+    assert lg.whole_keys(5, 1.0, [1]) == -1             # client id out of range
+    assert [lg.key_total(p) for p in range(3)] == before
+    assert lg.whole_keys(1, 1.0, [1, 2]) == 0           # still accepted afterwards
+    assert lg.key_total(2) == (0, 3.0, 2)
+    st, _ = lg.finalize()
+    assert st == 0
+    assert lg.whole_keys(2, 1.0, [0]) == -6             # closed

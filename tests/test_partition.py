@@ -41,6 +41,33 @@ def test_hand_worked_energy_and_ema():
     assert n2 == [15, 5] and eps2 == [1.0, 3.0]
 
 
+def test_hand_worked_zero_median_falls_back_to_the_mean():
+    # time and energy weighted equally (w_t = w_e = 1), 10 samples each.
+    # tau = t / n = (0, 0, 6): median 0 -> mean 2 -> normalised (0, 0, 3)
+    # eps = e / n = (1, 2, 4): median 2 -> normalised (0.5, 1, 2)
+    # c = (0.5, 1, 5) -> 1/c = (2, 1, 0.2), sum 3.2 -> shares (0.625, 0.3125, 0.0625)
+    # 27 left after one each: (16.875, 8.4375, 1.6875) -> floors (16, 8, 1), two left by
+    # largest fraction (0.875, 0.6875) -> (17, 8, 2) -> +1 each -> (18, 9, 3)
+    args = ([0.0, 0.0, 60.0], [10.0, 20.0, 40.0], [10, 10, 10])
+    kw = dict(w_time=1.0, w_energy=1.0)
+    want = [18, 9, 3]
+    assert partition_plan(*args, **kw)[0] == want
+    assert fa.fa_partition_plan(*args, **kw)[0] == want
+
+
+def test_hand_worked_all_zero_column_counts_as_ones():
+    # no energy reported (all zero, median and mean 0): that column normalises to
+    # (1, 1, 1) and no longer discriminates.  tau = (0, 2, 2): median 2 -> (0, 1, 1).
+    # w_t = w_e = 0.5: c = (0.5, 1, 1) -> 1/c = (2, 1, 1), shares (0.5, 0.25, 0.25)
+    # 27 left: (13.5, 6.75, 6.75) -> floors (13, 6, 6), two left by largest fraction
+    # (0.75, 0.75 at the lower indices 1, 2) -> (13, 7, 7) -> +1 each -> (14, 8, 8)
+    args = ([0.0, 20.0, 20.0], [0.0, 0.0, 0.0], [10, 10, 10])
+    kw = dict(w_time=0.5, w_energy=0.5)
+    want = [14, 8, 8]
+    assert partition_plan(*args, **kw)[0] == want
+    assert fa.fa_partition_plan(*args, **kw)[0] == want
+
+
 def test_deadband_keeps_allocation():
     n, _, _ = partition_plan([10.0, 10.5, 9.8], [0.0] * 3, [100, 100, 100])
     assert n == [100, 100, 100]

@@ -1,24 +1,29 @@
-"""The committed ncu summaries describe the kernels as they are: every summary that
-records a kernel source digest records the current one, so bench.py's roofline.traffic
-(read from them) is never taken from an older kernel."""
+"""The committed ncu figures describe the kernels as they are: every machine-readable
+profile summary (profiles/*.json) records the current kernel source digest, so
+bench.py's roofline.traffic (read from one of them) is never taken from an older
+kernel."""
+import json
 import os
-import re
 
 import bench
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+def _summaries():
+    pdir = os.path.join(ROOT, "profiles")
+    return {n: json.load(open(os.path.join(pdir, n))) for n in sorted(os.listdir(pdir))
+            if n.endswith(".json")}
+
+
 def test_profile_digests_match_the_kernel_source():
     now = bench.kernel_source_digest()
-    seen = 0
-    pdir = os.path.join(ROOT, "profiles")
-    for name in sorted(os.listdir(pdir)):
-        text = open(os.path.join(pdir, name)).read()
-        for d in re.findall(r"[Dd]igest[^`]*`([0-9a-f]{16})`", text):
-            assert d == now, f"{name} records kernel source {d}, the source is now {now}: retake it"
-            seen += 1
-    assert seen >= 3
+    sums = _summaries()
+    assert len(sums) >= 5, sorted(sums)
+    for name, d in sums.items():
+        assert d["kernel_source_digest"] == now, \
+            f"{name} records kernel source {d['kernel_source_digest']}, the source is now {now}: retake it"
+        assert d["command"].startswith("ncu ") and "--clock-control none" in d["command"], name
 
 
 def test_traffic_is_read_for_the_current_source():

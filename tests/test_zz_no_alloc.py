@@ -4,25 +4,39 @@ It serves callers that cannot let a library call cudaMalloc -- a process whose
 device memory belongs to another allocator or that forbids allocation on its
 request path -- by keeping the fp32 running sum in a fixed 16 MiB array of the
 library.  These tests call it through the C ABI and compare it with the regular
-fa_open / fa_accumulate / fa_finalize path on the same inputs, within the
-tolerances the other parity tests use, on two calls in a row (the second call
-runs over the first call's leftovers in the shared array).  This file is named
-to be collected last."""
+fa_open / fa_accumulate / fa_finalize path on the same inputs: the same kernels in
+the same client order, so the same bits, on two calls in a row (the second call runs
+over the first call's leftovers in the shared array), with aligned and unaligned
+client pointers; and with the fp64 oracle directly.  Its own error word is checked
+after the calls.  This file is named to be collected last."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import server_side_fedavg_gb300 as fa
 from tests.compare import check_bf16, check_f32
 
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(rng, K, n, dtype):
+def _host_inputs(rng, K, n, dtype):
     v = [(rng.standard_normal(n) * 0.02).astype(np.float32) for _ in range(K)]
     if dtype == "bf16":
-        v = [(a.view(np.uint32) >> 16).astype(np.uint16).view(np.int16) for a in v]
-    return [torch.from_numpy(a).cuda() for a in v]
+        v = [(a.view(np.uint32) >> 16).astype(np.uint16) for a in v]
+    return v
+
+
+def _inputs(rng, K, n, dtype, offset=0):
+    """Device copies; with `offset`, every tensor starts `offset` elements into its
+    allocation (an unaligned pointer for offset 1)."""
+    host = _host_inputs(rng, K, n, dtype)
+    dev = []
+    for a in host:
+        t = torch.from_numpy(np.concatenate([np.zeros(offset, a.dtype), a]).view(
+            np.int16 if dtype == "bf16" else np.float32)).cuda()
+        dev.append(t[offset:])
+    return host, dev
 
 
 def _regular(weights, xs, n, din, dout):
@@ -38,28 +52,45 @@ def _regular(weights, xs, n, din, dout):
         fa.fa_close(ctx)
 
 
-def test_matches_regular_path_two_calls_in_a_row():
-    rng = np.random.default_rng(42)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_same_bits_as_regular_path_two_calls_in_a_row(offset):
+    rng = np.random.default_rng(42 + offset)
     cases = [(5, 3_000_017, "bf16", "bf16"), (19, 1_234_567, "f32", "f32")]
     for call, (K, n, din, dout) in enumerate(cases):
         weights = [float(v) for v in rng.integers(100, 5000, K)]
-        xs = _inputs(rng, K, n, din)
+        _, xs = _inputs(rng, K, n, din, offset)
         out = torch.full((n,), 3, dtype=torch.float32 if dout == "f32" else torch.int16, device="cuda")
         fa.fa_aggregate_noalloc(weights, xs, n, din, dout, out)
         torch.cuda.synchronize()
         got = out.cpu().numpy()
         want = _regular(weights, xs, n, din, dout)
-        if dout == "bf16":
-            check_bf16(got.view(np.uint16), want.view(np.uint16), f"call {call}")
-        else:
-            mx = max(float(x.abs().max()) for x in xs)
-            check_f32(got, want, mx, K, f"call {call}")
+        assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), f"call {call}, offset {offset}"
+    fa.fa_aggregate_noalloc_status()
+
+
+@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f32", "f32")])
+def test_matches_the_oracle_at_the_largest_size(din, dout):
+    rng = np.random.default_rng(7 if din == "bf16" else 8)
+    n = fa.FA_NOALLOC_MAX_ELEMS
+    K = 6
+    weights = [float(v) for v in rng.integers(100, 1001, K)]
+    host, xs = _inputs(rng, K, n, din)
+    out = torch.empty(n, dtype=torch.float32 if dout == "f32" else torch.int16, device="cuda")
+    fa.fa_aggregate_noalloc(weights, xs, n, din, dout, out)
+    torch.cuda.synchronize()
+    fa.fa_aggregate_noalloc_status()
+    got = out.cpu().numpy()
+    want, _, _ = oracle.fedavg_key(weights, [True] * K, host, din, dout)
+    if dout == "bf16":
+        check_bf16(got.view(np.uint16), want, "noalloc vs oracle")
+    else:
+        check_f32(got, want, max(float(np.abs(h).max()) for h in host), K, "noalloc vs oracle")
 
 
 def test_no_device_memory_is_taken():
     rng = np.random.default_rng(7)
     n = 100_000
-    xs = _inputs(rng, 3, n, "bf16")
+    _, xs = _inputs(rng, 3, n, "bf16")
     out = torch.empty(n, dtype=torch.int16, device="cuda")
     fa.fa_aggregate_noalloc([1.0, 2.0, 3.0], xs, n, "bf16", "bf16", out)   # set-up on this device
     torch.cuda.synchronize()
