@@ -16,6 +16,9 @@ sum in HBM), fa_finalize (divide by the per-key weight total, RNE to bf16).
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
   resident  the same round when every update is resident, reduced in one pass by
          fa_reduce_resident (K*s_in + s_out bytes per element), for comparison
+  compensated  the streamed round in the compensated mode (FA_COMPENSATED: a (hi, lo)
+         pair sum, within one bf16 ulp of the exact mean everywhere), its HBM fraction
+         on that mode's bytes (s_in + 16 per later client-element)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs an independent replica (the path has no exchange
@@ -64,9 +67,10 @@ def stream_client(fa, ctx, w, k, base_ptr, stream):
     return calls
 
 
-def run_streamed_round(w, resident=False):
+def run_streamed_round(w, resident=False, flags=0):
     """One full round on the device, inputs from the device generator, streamed
-    client by client exactly as the bench does; returns the flat bf16 output."""
+    client by client exactly as the bench does; returns the flat bf16 output.
+    `flags` adds fa_opts flags (FA_COMPENSATED for the compensated mode)."""
     import torch
 
     import server_side_fedavg_gb300 as fa
@@ -75,7 +79,7 @@ def run_streamed_round(w, resident=False):
     tdt = torch.int16 if w.dtype_in == "bf16" else torch.float32
     s = torch.cuda.current_stream()
     ctx = fa.fa_open([(n, m) for (n, _), m in zip(w.keys, w.numels)], w.dtype_in, w.dtype_out,
-                     w.K, flags=fa.FA_FLAT_OUT)
+                     w.K, flags=fa.FA_FLAT_OUT | flags)
     try:
         if resident:
             bufs = [torch.empty(w.P, dtype=tdt, device="cuda") for _ in range(w.K)]
@@ -100,7 +104,7 @@ def run_streamed_round(w, resident=False):
         fa.fa_close(ctx)
 
 
-def run_resident_round(w):
+def run_resident_round(w, flags=0):
     """Every client's full update generated into HBM, then one fa_reduce_resident round
     exactly as the bench's `resident` measurement runs it; returns the flat output."""
     import torch
@@ -116,7 +120,7 @@ def run_resident_round(w):
     out = torch.empty(w.P, dtype=torch.int16 if w.dtype_out == "bf16" else torch.float32,
                       device="cuda")
     ctx = fa.fa_open([(n, m) for (n, _), m in zip(w.keys, w.numels)], w.dtype_in, w.dtype_out,
-                     w.K, flags=fa.FA_FLAT_OUT)
+                     w.K, flags=fa.FA_FLAT_OUT | flags)
     try:
         fa.fa_reduce_resident(ctx, list(range(w.K)), w.weights, [b.data_ptr() for b in bufs],
                               [out], s.cuda_stream)
@@ -129,15 +133,60 @@ def run_resident_round(w):
     return out
 
 
+def partial(w):
+    """True when some client sends only part of the keys (an adapter round)."""
+    return any(len(r) < w.n_keys for r in w.reports)
+
+
+def reporters(w):
+    """Per key, the number of clients that send it (and its total weight)."""
+    cnt = [0] * w.n_keys
+    tot = [0.0] * w.n_keys
+    for k in range(w.K):
+        for p in w.reports[k]:
+            cnt[p] += 1
+            tot[p] += w.weights[k]
+    return cnt, tot
+
+
 def algorithmic_bytes(w):
-    """Per round, streaming path: first client s_in+4, later clients s_in+8,
-    finalize 4+s_out bytes per element (all clients send every key here)."""
+    """Per round, streaming path: a key's first reporter s_in+4, later reporters s_in+8,
+    finalize 4+s_out bytes per element of every key written (N_p > 0)."""
     si = 2 if w.dtype_in == "bf16" else 4
     so = 2 if w.dtype_out == "bf16" else 4
-    acc_first = w.P * (si + 4)
-    acc_later = (w.K - 1) * w.P * (si + 8)
-    fin = w.P * (4 + so)
+    cnt, tot = reporters(w)
+    acc_first = sum(n * (si + 4) for n, c in zip(w.numels, cnt) if c > 0)
+    acc_later = sum(n * (c - 1) * (si + 8) for n, c in zip(w.numels, cnt) if c > 1)
+    fin = sum(n * (4 + so) for n, t in zip(w.numels, tot) if t > 0)
     return acc_first, acc_later, fin
+
+
+def subset_bytes(w):
+    """Per round, the one-pass subset reduce: J_p * s_in + s_out per element of every key
+    written."""
+    si = 2 if w.dtype_in == "bf16" else 4
+    so = 2 if w.dtype_out == "bf16" else 4
+    cnt, tot = reporters(w)
+    return sum(n * (c * si + so) for n, c, t in zip(w.numels, cnt, tot) if t > 0)
+
+
+def packed_offsets(w, k):
+    """Element offset of each of client k's keys in its packed buffer (keys back to back
+    in report order)."""
+    out, o = [], 0
+    for p in w.reports[k]:
+        out.append(o)
+        o += w.numels[p]
+    return out, o
+
+
+def fill_packed(w, k, ptr, stream, es):
+    """Client k's reported keys, back to back, generated on the device at ptr."""
+    import synth
+    offs, _ = packed_offsets(w, k)
+    flat = w.flat_offsets()
+    for p, o in zip(w.reports[k], offs):
+        synth.client_fill_device(w, k, flat[p], w.numels[p], ptr + o * es, stream)
 
 
 def kernel_source_digest():
@@ -150,24 +199,19 @@ def kernel_source_digest():
 
 
 def profiled_traffic(bytes_per_launch):
-    """DRAM bytes per accumulate launch from the committed ncu summary, scaled from the
-    captured launch to the average launch by algorithmic bytes; None once the kernel
-    source differs from the one the counters were taken on."""
-    path = os.path.join(ROOT, "profiles", "accumulate_decoder1l.md")
-    if not os.path.exists(path):
-        return None
-    fields = {}
-    with open(path) as f:
-        for line in f:
-            if line.startswith("- ") and ": " in line:
-                k, v = line[2:].split(": ", 1)
-                fields[k.strip()] = v.strip().strip("`")
+    """DRAM bytes per accumulate launch from the committed ncu figures
+    (profiles/accumulate_decoder1l.json), scaled from the captured launch to the average
+    launch by algorithmic bytes; None once the kernel source differs from the one the
+    counters were taken on."""
+    path = os.path.join(ROOT, "profiles", "accumulate_decoder1l.json")
     try:
-        if fields.get("kernel source digest") != kernel_source_digest():
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_digest") != kernel_source_digest():
             return None
-        dram = float(fields["dram bytes per launch"])
-        algo = float(fields["algorithmic bytes of the captured launch"])
-    except (KeyError, ValueError):
+        dram = float(d["dram_bytes_per_launch"])
+        algo = float(d["algorithmic_bytes_of_captured_launch"])
+    except (OSError, KeyError, ValueError):
         return None
     return int(dram / algo * bytes_per_launch)
 
@@ -395,17 +439,31 @@ def run_ours(args, world, rank, local, pg):
     layout = [(n, m) for (n, _), m in zip(w.keys, w.numels)]
     s = torch.cuda.Stream()
     sh = s.cuda_stream
-    client_bytes = w.K * w.P * si
+    client_bytes = w.client_bytes()
     peak, peak_kind = _peaks()
+    part = partial(w)
 
-    # ---- regime A: every client's update resident in HBM
+    # ---- regime A: every client's update resident in HBM (for an adapter round, each
+    # client's reported keys packed back to back)
     free, _ = torch.cuda.mem_get_info()
     per_client = w.P * si
     fixed = w.P * 4 + w.P * so + (6 << 30)
-    resident = max(1, min(w.K, int((free - fixed) // per_client)))
-    bufs = [torch.empty(w.P, dtype=tin, device="cuda") for _ in range(resident)]
-    for k in range(resident):
-        synth.client_fill_device(w, k, 0, w.P, bufs[k].data_ptr(), sh)
+    resident = w.K if part else max(1, min(w.K, int((free - fixed) // per_client)))
+    if part:
+        bufs = [torch.empty(max(1, packed_offsets(w, k)[1]), dtype=tin, device="cuda") for k in range(w.K)]
+        for k in range(w.K):
+            fill_packed(w, k, bufs[k].data_ptr(), sh, si)
+        import numpy as _np
+        key_args = []
+        for k in range(w.K):
+            offs, _ = packed_offsets(w, k)
+            key_args.append((_np.asarray(w.reports[k], _np.int64), _np.zeros(len(offs), _np.uint64),
+                             _np.asarray([bufs[k].data_ptr() + o * si for o in offs], _np.uint64),
+                             _np.asarray([w.numels[p] for p in w.reports[k]], _np.uint64)))
+    else:
+        bufs = [torch.empty(w.P, dtype=tin, device="cuda") for _ in range(resident)]
+        for k in range(resident):
+            synth.client_fill_device(w, k, 0, w.P, bufs[k].data_ptr(), sh)
     out = torch.empty(w.P, dtype=tout, device="cuda")
     ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT)
     torch.cuda.synchronize()
@@ -418,6 +476,10 @@ def run_ours(args, world, rank, local, pg):
         if evs is not None:
             evs[0].record(s)
         for k in range(w.K):
+            if part:
+                ks, os_, ps, ls = key_args[k]
+                fa.fa_accumulate_keys(ctx, k, w.weights[k], ks, os_, ps, ls, sh)
+                continue
             base = bufs[k % resident].data_ptr()
             P, ce = w.P, w.chunk_elems or w.P
             for c0 in range(0, P, ce):
@@ -435,7 +497,7 @@ def run_ours(args, world, rank, local, pg):
     barrier(pg)
     torch.cuda.synchronize()
 
-    n_calls = w.K * nchunk
+    n_calls = w.K * nchunk          # accumulate launches per round (flat chunks)
     ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = fa.fa_get_stats(ctx)["kernel_launches"]
@@ -450,6 +512,8 @@ def run_ours(args, world, rank, local, pg):
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     launches = fa.fa_get_stats(ctx)["kernel_launches"] - launches0
+    if part:
+        n_calls = max(1, launches // args.steps - 1)   # accumulate launches (all but finalize)
     barrier(pg)
     ms_total = t0e.elapsed_time(t1e)
     ms_total = max_over_ranks(pg, ms_total)
@@ -488,7 +552,10 @@ def run_ours(args, world, rank, local, pg):
 
     # ---- the same round with every update resident, reduced in one pass (fa_reduce_resident)
     resident_line = None
-    if resident == w.K and not args.no_resident:
+    subsets_line = None
+    if part and not args.no_resident:
+        subsets_line = run_subsets(args, w, ctx, bufs, out, s, peak)
+    if resident == w.K and not part and not args.no_resident:
         ids = list(range(w.K))
         ptrs = [b.data_ptr() for b in bufs]
 
@@ -517,6 +584,14 @@ def run_ours(args, world, rank, local, pg):
                          "kernel": f"reduce_bulk_kernel<{w.dtype_in},{w.dtype_out},final>"}
 
     fa.fa_close(ctx)
+    torch.cuda.synchronize()
+
+    # ---- the same streamed round in the compensated mode (FA_COMPENSATED): the running sum
+    # is a (hi, lo) pair, so each later client-element moves 8 more bytes
+    comp_line = None
+    if not args.no_compensated and not part:
+        comp_line = run_compensated(args, w, layout, bufs, out, s, peak)
+
     del bufs, out
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -525,6 +600,16 @@ def run_ours(args, world, rank, local, pg):
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(args, w, layout, s, pg, world)
+        if args.e2e_staged_steps > 0 and not args.stage_host:
+            # the same end-to-end round through the library's staging ring (FA_STAGE_HOST:
+            # copies on a copy stream into device slots, then the accumulate kernel)
+            import argparse
+            a2 = argparse.Namespace(**vars(args))
+            a2.stage_host = True
+            a2.e2e_steps = args.e2e_staged_steps
+            st = run_e2e(a2, w, layout, s, pg, world)
+            e2e["staged"] = {k: st[k] for k in ("value", "ms_per_step", "accumulate_ms", "finalize_ms",
+                                                 "link_frac", "accumulate_link_frac", "ingest", "output")}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -546,6 +631,8 @@ def run_ours(args, world, rank, local, pg):
                      "traffic": profiled_traffic(acc_bytes_per_launch)},
         "gpu_launches": int(launches),
         "resident": resident_line,
+        "subsets": subsets_line,
+        "compensated": comp_line,
         "delta_apply": apply_line,
         "partition_plan_us": partition_plan_us(w.K),
         "clocks": clk,
@@ -556,6 +643,134 @@ def run_ours(args, world, rank, local, pg):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_subsets(args, w, ctx, bufs, out, s, peak):
+    """An adapter round through fa_reduce_subsets (each client's reported keys, packed in
+    its resident buffer, reduced straight to the output): device time on the stream (CUDA
+    events around the call's table upload and kernel, with the host's work hidden behind
+    a device-side wait queued first) and wall time per round, back to back (the host
+    bookkeeping of every (client, key) entry and fa_reset's wait included)."""
+    import torch
+
+    import server_side_fedavg_gb300 as fa
+
+    ids = list(range(w.K))
+    ptrs = [b.data_ptr() for b in bufs]
+    table = fa.subset_table(w.reports)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(max(1, args.steps))]
+
+    def round_(e=None):
+        fa.fa_reset(ctx)
+        if e is not None:
+            # a short device-side wait ahead of the call, so that the call's host work is done
+            # before the GPU reaches the start event: the events then bracket device work only
+            with torch.cuda.stream(s):
+                torch.cuda._sleep(4_000_000)
+            e[0].record(s)
+        fa.fa_reduce_subsets(ctx, ids, w.weights, ptrs, table, [out], s.cuda_stream)
+        if e is not None:
+            e[1].record(s)
+
+    for _ in range(max(3, args.warmup)):
+        round_()
+    torch.cuda.synchronize()
+    l0 = fa.fa_get_stats(ctx)["kernel_launches"]
+    t0 = time.perf_counter()
+    for _ in range(len(ev)):
+        round_()
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) / len(ev)
+    launches = (fa.fa_get_stats(ctx)["kernel_launches"] - l0) // len(ev)
+    for e in ev:
+        round_(e)
+    torch.cuda.synchronize()
+    dev_ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    b = subset_bytes(w)
+    cb = w.client_bytes()
+    return {"value": round(cb / (dev_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "device_ms_per_round": round(dev_ms, 4), "wall_ms_per_round": round(wall * 1e3, 4),
+            "value_wall": round(cb / wall / 1e9, 2),
+            "hbm_gbs": round(b / (dev_ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(b / (dev_ms * 1e-3) / 1e9 / peak, 4),
+            "bytes_per_round": int(b), "launches_per_round": int(launches),
+            "kernel": f"reduce_gather_kernel<{w.dtype_in},{w.dtype_out}>"}
+
+
+def run_compensated(args, w, layout, bufs, out, s, peak):
+    """The bench's streamed round with FA_COMPENSATED: client-update GB/s, the round's
+    algorithmic HBM bytes (first client s_in + 8, later ones s_in + 16, finalize 8 + s_out
+    per element) over its time, and the accumulate launches' own fraction.  The pair sum
+    takes twice the default sum's memory: if the resident client buffers leave no room for
+    it, the last ones are dropped and clients reuse the remaining buffers (each read is
+    still a fresh pass over a buffer far larger than L2)."""
+    import torch
+
+    import server_side_fedavg_gb300 as fa
+
+    si = 2 if w.dtype_in == "bf16" else 4
+    so = 2 if w.dtype_out == "bf16" else 4
+    sh = s.cuda_stream
+    pad = sum(-(-n // 32) * 32 for n in w.numels)
+    need = 2 * pad * 4 + (4 << 30)
+    torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info()
+    bufs = list(bufs)
+    while free < need and len(bufs) > 1:
+        bufs.pop()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        free, _ = torch.cuda.mem_get_info()
+    if free < need:
+        return {"skipped": "no device memory for the pair sum"}
+    ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=fa.FA_FLAT_OUT | fa.FA_COMPENSATED)
+    try:
+        ce = w.chunk_elems or w.P
+        nchunk = -(-w.P // ce)
+
+        def step(evs=None):
+            fa.fa_reset(ctx)
+            if evs is not None:
+                evs[0].record(s)
+            for k in range(w.K):
+                base = bufs[k % len(bufs)].data_ptr()
+                for c0 in range(0, w.P, ce):
+                    fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base + c0 * si,
+                                     min(ce, w.P - c0), sh)
+            if evs is not None:
+                evs[1].record(s)
+            fa.fa_finalize(ctx, [out], sh)
+            if evs is not None:
+                evs[2].record(s)
+
+        for _ in range(max(1, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        steps = max(1, args.steps)
+        ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            step(ev_sets[i])
+        torch.cuda.synchronize()
+        acc_ms = sum(e[0].elapsed_time(e[1]) for e in ev_sets) / steps
+        fin_ms = sum(e[1].elapsed_time(e[2]) for e in ev_sets) / steps
+        round_ms = sum(e[0].elapsed_time(e[2]) for e in ev_sets) / steps
+    finally:
+        fa.fa_close(ctx)
+    acc_b = w.P * (si + 8) + (w.K - 1) * w.P * (si + 16)
+    fin_b = w.P * (8 + so)
+    acc_gbs = acc_b / (acc_ms * 1e-3) / 1e9
+    return {"value": round(w.K * w.P * si / (round_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_round": round(round_ms, 3),
+            "hbm_gbs": round((acc_b + fin_b) / (round_ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round((acc_b + fin_b) / (round_ms * 1e-3) / 1e9 / peak, 4),
+            "bytes_per_round": int(acc_b + fin_b),
+            "accumulate": {"kernel": f"accumulate_bulk_kernel<{w.dtype_in},compensated>",
+                           "achieved": round(acc_gbs, 1), "frac": round(acc_gbs / peak, 4),
+                           "bytes_per_launch": int(acc_b / (w.K * nchunk)),
+                           "launch_ms": round(acc_ms / (w.K * nchunk), 4)},
+            "finalize_gbs": round(fin_b / (fin_ms * 1e-3) / 1e9, 1),
+            "distinct_client_buffers": len(bufs)}
 
 
 def host_mem_available():
@@ -612,8 +827,26 @@ def run_e2e(args, w, layout, s, pg, world):
             pool_n //= 2
         if pool_n * ce * si + out_bytes > budget:
             out_pinned = False
+    part = partial(w)
     pool = []
-    for i in range(pool_n):
+    if part:
+        # an adapter round: each client's reported keys packed in one pinned buffer, sent
+        # with one fa_accumulate_keys call (read in place over the link)
+        import numpy as _np
+        pool_n = w.K
+        flat = w.flat_offsets()
+        key_args = []
+        for k in range(w.K):
+            offs, tot = packed_offsets(w, k)
+            t = torch.empty(max(1, tot), dtype=torch.int16 if si == 2 else torch.float32).pin_memory()
+            tv = t.numpy().view(_np.uint16 if si == 2 else _np.float32)
+            for p_, o in zip(w.reports[k], offs):
+                synth.client_flat(w, k, flat[p_], w.numels[p_], out=tv[o:o + w.numels[p_]])
+            pool.append(t)
+            key_args.append((_np.asarray(w.reports[k], _np.int64), _np.zeros(len(offs), _np.uint64),
+                             _np.asarray([t.data_ptr() + o * si for o in offs], _np.uint64),
+                             _np.asarray([w.numels[p_] for p_ in w.reports[k]], _np.uint64)))
+    for i in range(0 if part else pool_n):
         k, c = divmod(i, nchunk)
         c0 = c * ce
         n = min(ce, w.P - c0)
@@ -637,6 +870,14 @@ def run_e2e(args, w, layout, s, pg, world):
             evs[0].record(s)
         i = 0
         for k in range(w.K):
+            if part:
+                ks, os_, ps, ls = key_args[k]
+                if args.stage_host:     # staged host chunks go through fa_accumulate
+                    for p_, ptr, n in zip(ks, ps, ls):
+                        fa.fa_accumulate(ctx, k, w.weights[k], int(p_), 0, int(ptr), int(n), sh)
+                else:
+                    fa.fa_accumulate_keys(ctx, k, w.weights[k], ks, os_, ps, ls, sh)
+                continue
             for c0 in range(0, w.P, ce):
                 n = min(ce, w.P - c0)
                 fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0,
@@ -669,13 +910,15 @@ def run_e2e(args, w, layout, s, pg, world):
     fin_ms = sum(e[1].elapsed_time(e[2]) for e in ev_sets) / args.e2e_steps
     h2d = (st1["h2d_bytes"] - st0["h2d_bytes"]) // args.e2e_steps
     d2h = (st1["d2h_bytes"] - st0["d2h_bytes"]) // args.e2e_steps
-    v = world * w.K * w.P * si * args.e2e_steps / dt / 1e9
-    # HBM traffic of the host-fed round: the running sum (written by the first client, read
-    # and written by every later one, read by finalize); staging adds each chunk's write and
-    # read in HBM, and a staged output its device copy (written, then read by the copy)
-    hbm = w.P * (4 + 8 * (w.K - 1) + 4)
+    v = world * w.client_bytes() * args.e2e_steps / dt / 1e9
+    # HBM traffic of the host-fed round: the running sum (written by a key's first reporter,
+    # read and written by every later one, read by finalize); staging adds each chunk's
+    # write and read in HBM, and a staged output its device copy (written, then read by the
+    # copy)
+    a_first, a_later, a_fin = algorithmic_bytes(w)
+    hbm = a_first // (si + 4) * 4 + a_later // (si + 8) * 8 + a_fin // (4 + so) * 4
     if args.stage_host:
-        hbm += w.K * w.P * 2 * si
+        hbm += w.client_bytes() * 2
     if args.stage_host or not out_pinned:
         hbm += 2 * w.P * so
     peak, _ = _peaks()
@@ -688,7 +931,8 @@ def run_e2e(args, w, layout, s, pg, world):
             "accumulate_link_frac": round(h2d / (acc_ms * 1e-3) / 1e9 / link, 3),
             "hbm_gbs": round(hbm * args.e2e_steps / dt / 1e9, 1),
             "hbm_frac": round(hbm * args.e2e_steps / dt / 1e9 / peak, 4),
-            "host_pool": f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused",
+            "host_pool": (f"{w.K} pinned buffers, one per client, its reported keys packed" if part
+                          else f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused"),
             "output": (("pinned host buffer, " + ("copied from a device buffer" if args.stage_host
                                                   else "written in place by the finalize kernel"))
                        if out_pinned else "pageable host buffer (pinned budget too small)"),
@@ -791,9 +1035,13 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-pool", type=int, default=24)
+    ap.add_argument("--e2e-staged-steps", type=int, default=2,
+                    help="also time the e2e round through the staging ring (0 = skip)")
     ap.add_argument("--ref-elems", type=int, default=64 << 20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-resident", action="store_true")
+    ap.add_argument("--no-compensated", action="store_true",
+                    help="skip the round in the compensated mode (FA_COMPENSATED)")
     ap.add_argument("--ring-slots", type=int, default=0, help="e2e staging slots (0 = library default)")
     ap.add_argument("--slot-mb", type=int, default=0, help="e2e staging slot size in MiB (0 = default)")
     ap.add_argument("--hierarchical", type=int, default=0, metavar="S",
