@@ -189,10 +189,23 @@ def fill_packed(w, k, ptr, stream, es):
         synth.client_fill_device(w, k, flat[p], w.numels[p], ptr + o * es, stream)
 
 
-def kernel_source_digest():
+# The source files each kernel family is compiled from: an ncu summary records the digest
+# of its kernel's files, so a figure taken on an older kernel is never reported as current.
+KERNEL_SOURCES = {
+    "accumulate": ("kernels.cuh", "device.cuh", "tiles.hpp", "accumulate.cu"),
+    "reduce": ("kernels.cuh", "device.cuh", "tiles.hpp", "reduce.cu"),
+    "gather": ("kernels.cuh", "device.cuh", "tiles.hpp", "gather.cu", "gather_plan.cpp"),
+    "finalize": ("kernels.cuh", "device.cuh", "tiles.hpp", "finalize.cu"),
+}
+
+
+def kernel_source_digest(sources=None):
+    """sha256 (first 16 hex digits) of the named kernel sources (default: every family's)."""
     import hashlib
+    if sources is None:
+        sources = sorted({f for fs in KERNEL_SOURCES.values() for f in fs})
     h = hashlib.sha256()
-    for f in ("kernels.cu", "kernels.cuh"):
+    for f in sources:
         with open(os.path.join(ROOT, "server_side_fedavg_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -201,17 +214,17 @@ def kernel_source_digest():
 def profiled_traffic(bytes_per_launch):
     """DRAM bytes per accumulate launch from the committed ncu figures
     (profiles/accumulate_decoder1l.json), scaled from the captured launch to the average
-    launch by algorithmic bytes; None once the kernel source differs from the one the
+    launch by algorithmic bytes; None once the kernel's sources differ from the ones the
     counters were taken on."""
     path = os.path.join(ROOT, "profiles", "accumulate_decoder1l.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        if d.get("kernel_source_digest") != kernel_source_digest():
+        if d.get("kernel_source_digest") != kernel_source_digest(d["sources"]):
             return None
         dram = float(d["dram_bytes_per_launch"])
         algo = float(d["algorithmic_bytes_of_captured_launch"])
-    except (OSError, KeyError, ValueError):
+    except (OSError, KeyError, ValueError, TypeError):
         return None
     return int(dram / algo * bytes_per_launch)
 

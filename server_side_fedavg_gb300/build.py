@@ -16,7 +16,8 @@ BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(BUILD, "libfedavg.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["kernels.cu", "noalloc.cu", "fedavg.cpp", "ledger.cpp", "partition.cpp"]
+SOURCES = ["accumulate.cu", "reduce.cu", "gather.cu", "finalize.cu", "noalloc.cu", "fedavg.cpp",
+           "ledger.cpp", "partition.cpp", "gather_plan.cpp"]
 
 
 def _common():
@@ -39,6 +40,11 @@ def compile_commands(extra=None):
     return cmds
 
 
+def cmd_is_cuda(cmd):
+    """True for the compile command of a CUDA source (its ptxas -v report is kept)."""
+    return any(str(a).endswith(".cu") for a in cmd)
+
+
 def link_command(objs):
     return [NVCC, "-shared"] + ARCH + objs + ["-cudart", "shared",
                                               "-Xlinker", "-rpath,/usr/local/cuda/lib64",
@@ -49,17 +55,18 @@ def build(verbose: bool = False) -> str:
     procs = []
     for obj, cmd in compile_commands():
         procs.append((obj, cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
-    objs = []
+    objs, ptxas = [], []
     for obj, cmd, p in procs:
         log = p.communicate()[0].decode(errors="replace")
         if p.returncode != 0:
             raise RuntimeError(f"build failed: {' '.join(cmd)}\n{log}")
         if verbose and log.strip():
             print(log)
-        if obj.endswith("kernels.o"):
-            with open(os.path.join(BUILD, "ptxas.txt"), "w") as f:
-                f.write(log)
+        if cmd_is_cuda(cmd):
+            ptxas.append(log)
         objs.append(obj)
+    with open(os.path.join(BUILD, "ptxas.txt"), "w") as f:
+        f.write("".join(ptxas))
     r = subprocess.run(link_command(objs), stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))

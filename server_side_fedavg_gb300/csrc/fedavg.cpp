@@ -1126,8 +1126,11 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
     }
     // segment table (one entry per key to write) and source table
     const uint32_t nseg = static_cast<uint32_t>(c->items.size());
+    const bool comp = c->acc_lo != nullptr;
     const size_t seg_bytes = (sizeof(fa::GathSeg) * nseg + 15) / 16 * 16;
-    const size_t need = seg_bytes + sizeof(fa::GathSrc) * n_entries;
+    const size_t src_bytes = (sizeof(fa::GathSrc) * n_entries + 15) / 16 * 16;
+    const uint32_t grid_cap = fa::gather_grid(0xFFFFFFFFu, c->din, c->dout, comp, c->shape);
+    const size_t need = seg_bytes + src_bytes + 2 * sizeof(uint32_t) * (grid_cap + 1);
     if (c->gath_pending) {
         r = wait_event(c, c->gath_ev, "subset table reuse");
         if (r != FA_OK) return r;
@@ -1165,6 +1168,7 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
     fa::GathArgs ga;
     ga.segs = reinterpret_cast<const fa::GathSeg*>(c->gath_dev);
     ga.src = reinterpret_cast<const fa::GathSrc*>(c->gath_dev + seg_bytes);
+    ga.cta = reinterpret_cast<const uint32_t*>(c->gath_dev + seg_bytes + src_bytes);
     ga.err = c->err_dev;
     ga.nseg = nseg;
     ga.jmax = jmax;
@@ -1173,10 +1177,14 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
         c->broken = true;
         return fail(c, FA_ERR_RANGE, "layout too large for one subset reduce");
     }
-    FA_CUDA(c, cudaMemcpyAsync(c->gath_dev, c->gath_host, need, cudaMemcpyHostToDevice, s));
+    ga.grid = fa::gather_grid(ga.ntiles, c->din, c->dout, comp, c->shape);
+    auto* cta = reinterpret_cast<uint32_t*>(c->gath_host + seg_bytes + src_bytes);
+    fa::plan_gather_ctas(segs, nseg, ga.tile, ga.ntiles, c->din, c->dout, ga.grid, cta);
+    const size_t used = seg_bytes + src_bytes + 2 * sizeof(uint32_t) * (ga.grid + 1);
+    FA_CUDA(c, cudaMemcpyAsync(c->gath_dev, c->gath_host, used, cudaMemcpyHostToDevice, s));
     FA_CUDA(c, cudaEventRecord(c->gath_ev, s));
     c->gath_pending = true;
-    cudaError_t ce = fa::launch_gather_final(ga, c->din, c->dout, c->acc_lo != nullptr, c->shape, s);
+    cudaError_t ce = fa::launch_gather_final(ga, c->din, c->dout, comp, c->shape, s);
     if (ce != cudaSuccess) {
         c->broken = true;
         return cuda_fail(c, ce, "subset reduce launch");

@@ -1,0 +1,33 @@
+// Test-only C entry point over the host planning of a subset-reduce launch (compiled
+// with g++ on the CPU, no CUDA device code): lets the CPU suite check how the tiles of
+// a round are numbered and split among the CTAs.
+#include <cstdint>
+#include <vector>
+
+#include "kernels.cuh"
+
+extern "C" {
+
+// Segments of lens[i] elements with J[i] reporters each; tiles of gather_tile(jmax, din,
+// dout) elements.  Writes the tile size, the tile count, each segment's first tile and
+// the grid + 1 (first tile, segment) pairs of the CTA split.  Returns 0, or -1 if the
+// tiles do not fit 32 bits.
+int32_t gp_plan(const uint64_t* lens, const uint32_t* J, uint32_t nseg, int din, int dout,
+                uint32_t grid, uint32_t* tile, uint32_t* ntiles, uint32_t* tile0,
+                uint32_t* cta) {
+    std::vector<fa::GathSeg> segs(nseg);
+    uint32_t jmax = 1;
+    for (uint32_t i = 0; i < nseg; ++i) {
+        segs[i] = fa::GathSeg{};
+        segs[i].len = lens[i];
+        segs[i].J = J[i];
+        if (J[i] > jmax) jmax = J[i];
+    }
+    *tile = fa::gather_tile(jmax, din, dout);
+    if (!fa::plan_gather_tiles(segs.data(), nseg, *tile, ntiles)) return -1;
+    for (uint32_t i = 0; i < nseg; ++i) tile0[i] = segs[i].tile0;
+    fa::plan_gather_ctas(segs.data(), nseg, *tile, *ntiles, din, dout, grid, cta);
+    return 0;
+}
+
+}  // extern "C"

@@ -1,7 +1,7 @@
 """The committed ncu figures describe the kernels as they are: every machine-readable
-profile summary (profiles/*.json) records the current kernel source digest, so
-bench.py's roofline.traffic (read from one of them) is never taken from an older
-kernel."""
+profile summary (profiles/*.json) records the digest of the sources its kernel is built
+from, and that digest matches those files now, so bench.py's roofline.traffic (read from
+one of them) is never taken from an older kernel."""
 import json
 import os
 
@@ -17,10 +17,12 @@ def _summaries():
 
 
 def test_profile_digests_match_the_kernel_source():
-    now = bench.kernel_source_digest()
     sums = _summaries()
     assert len(sums) >= 5, sorted(sums)
     for name, d in sums.items():
+        srcs = d["sources"]
+        assert srcs and all(any(s in fs for fs in bench.KERNEL_SOURCES.values()) for s in srcs), name
+        now = bench.kernel_source_digest(srcs)
         assert d["kernel_source_digest"] == now, \
             f"{name} records kernel source {d['kernel_source_digest']}, the source is now {now}: retake it"
         assert d["command"].startswith("ncu ") and "--clock-control none" in d["command"], name
