@@ -194,7 +194,7 @@ def fill_packed(w, k, ptr, stream, es):
 KERNEL_SOURCES = {
     "accumulate": ("kernels.cuh", "device.cuh", "tiles.hpp", "accumulate.cu"),
     "reduce": ("kernels.cuh", "device.cuh", "tiles.hpp", "reduce.cu"),
-    "gather": ("kernels.cuh", "device.cuh", "tiles.hpp", "gather.cu", "gather_plan.cpp"),
+    "gather": ("kernels.cuh", "gather.cuh", "device.cuh", "tiles.hpp", "gather.cu", "gather_plan.cpp"),
     "finalize": ("kernels.cuh", "device.cuh", "tiles.hpp", "finalize.cu"),
 }
 
@@ -612,7 +612,8 @@ def run_ours(args, world, rank, local, pg):
     # ---- e2e: pinned host buffers through the same calls
     e2e = None
     if args.e2e_steps > 0:
-        e2e = run_e2e(args, w, layout, s, pg, world)
+        hb = e2e_buffers(args, w, world)
+        e2e = run_e2e(args, w, layout, s, pg, world, hb)
         if args.e2e_staged_steps > 0 and not args.stage_host:
             # the same end-to-end round through the library's staging ring (FA_STAGE_HOST:
             # copies on a copy stream into device slots, then the accumulate kernel)
@@ -620,7 +621,7 @@ def run_ours(args, world, rank, local, pg):
             a2 = argparse.Namespace(**vars(args))
             a2.stage_host = True
             a2.e2e_steps = args.e2e_staged_steps
-            st = run_e2e(a2, w, layout, s, pg, world)
+            st = run_e2e(a2, w, layout, s, pg, world, hb)
             e2e["staged"] = {k: st[k] for k in ("value", "ms_per_step", "accumulate_ms", "finalize_ms",
                                                  "link_frac", "accumulate_link_frac", "ingest", "output")}
 
@@ -814,15 +815,14 @@ def h2d_peak(src, s, reps=8):
     return reps * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
 
 
-def run_e2e(args, w, layout, s, pg, world):
-    """Client chunks from pinned host memory (a pool of distinct chunks, reused),
-    aggregate written to a pinned host buffer; copies inside the timed region.
-    Pinned memory is sized to this rank's share of the node's available memory
-    (ranks on one node share it); if it does not fit, the pool shrinks and the
-    output falls back to pageable memory."""
+def e2e_buffers(args, w, world):
+    """The host side of the end-to-end rounds: client chunks in pinned host memory (a
+    pool of distinct chunks, reused) and the output buffer, allocated once and shared by
+    the in-place and the staged variants.  Pinned memory is sized to this rank's share
+    of the node's available memory (ranks on one node share it); if it does not fit,
+    the pool shrinks and the output falls back to pageable memory."""
     import torch
 
-    import server_side_fedavg_gb300 as fa
     import synth
 
     si = 2 if w.dtype_in == "bf16" else 4
@@ -842,6 +842,7 @@ def run_e2e(args, w, layout, s, pg, world):
             out_pinned = False
     part = partial(w)
     pool = []
+    key_args = None
     if part:
         # an adapter round: each client's reported keys packed in one pinned buffer, sent
         # with one fa_accumulate_keys call (read in place over the link)
@@ -870,6 +871,23 @@ def run_e2e(args, w, layout, s, pg, world):
     out = torch.empty(w.P, dtype=torch.int16 if so == 2 else torch.float32)
     if out_pinned:
         out = out.pin_memory()
+    return {"pool": pool, "pool_n": pool_n, "out": out, "out_pinned": out_pinned, "part": part,
+            "key_args": key_args if part else None}
+
+
+def run_e2e(args, w, layout, s, pg, world, hb):
+    """One end-to-end variant over the buffers of e2e_buffers: every step reads the
+    client chunks from host memory and writes the aggregate to the host buffer, copies
+    inside the timed region."""
+    import torch
+
+    import server_side_fedavg_gb300 as fa
+
+    si = 2 if w.dtype_in == "bf16" else 4
+    so = 2 if w.dtype_out == "bf16" else 4
+    ce = w.chunk_elems or w.P
+    pool, pool_n, out, out_pinned, part = hb["pool"], hb["pool_n"], hb["out"], hb["out_pinned"], hb["part"]
+    key_args = hb["key_args"]
     flags = fa.FA_FLAT_OUT | (fa.FA_STAGE_HOST if args.stage_host else 0)
     ctx = fa.fa_open(layout, w.dtype_in, w.dtype_out, w.K, flags=flags,
                      ring_slots=args.ring_slots, slot_bytes=args.slot_mb << 20)

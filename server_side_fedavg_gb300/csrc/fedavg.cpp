@@ -34,6 +34,7 @@
 #include <thread>
 #include <vector>
 
+#include "gather.cuh"
 #include "kernels.cuh"
 #include "ledger.hpp"
 
@@ -1129,8 +1130,9 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
     const bool comp = c->acc_lo != nullptr;
     const size_t seg_bytes = (sizeof(fa::GathSeg) * nseg + 15) / 16 * 16;
     const size_t src_bytes = (sizeof(fa::GathSrc) * n_entries + 15) / 16 * 16;
-    const uint32_t grid_cap = fa::gather_grid(0xFFFFFFFFu, c->din, c->dout, comp, c->shape);
-    const size_t need = seg_bytes + src_bytes + 2 * sizeof(uint32_t) * (grid_cap + 1);
+    // + the largest chunk table and the counter word
+    const size_t need = seg_bytes + src_bytes +
+                        2 * sizeof(uint32_t) * (static_cast<size_t>(fa::kMaxGatherChunks) + 1) + 16;
     if (c->gath_pending) {
         r = wait_event(c, c->gath_ev, "subset table reuse");
         if (r != FA_OK) return r;
@@ -1178,9 +1180,15 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
         return fail(c, FA_ERR_RANGE, "layout too large for one subset reduce");
     }
     ga.grid = fa::gather_grid(ga.ntiles, c->din, c->dout, comp, c->shape);
+    ga.nchunk = fa::gather_chunks(ga.ntiles, ga.grid);
     auto* cta = reinterpret_cast<uint32_t*>(c->gath_host + seg_bytes + src_bytes);
-    fa::plan_gather_ctas(segs, nseg, ga.tile, ga.ntiles, c->din, c->dout, ga.grid, cta);
-    const size_t used = seg_bytes + src_bytes + 2 * sizeof(uint32_t) * (ga.grid + 1);
+    fa::plan_gather_ctas(segs, nseg, ga.tile, ga.ntiles, c->din, c->dout, ga.nchunk, cta);
+    // the chunk counter starts at 0: the word right after the chunk table, uploaded with
+    // the tables in one copy
+    const size_t counter_off = seg_bytes + src_bytes + 2 * sizeof(uint32_t) * (ga.nchunk + 1);
+    std::memset(c->gath_host + counter_off, 0, sizeof(uint32_t));
+    ga.counter = reinterpret_cast<uint32_t*>(c->gath_dev + counter_off);
+    const size_t used = counter_off + sizeof(uint32_t);
     FA_CUDA(c, cudaMemcpyAsync(c->gath_dev, c->gath_host, used, cudaMemcpyHostToDevice, s));
     FA_CUDA(c, cudaEventRecord(c->gath_ev, s));
     c->gath_pending = true;

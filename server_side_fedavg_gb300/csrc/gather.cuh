@@ -1,0 +1,83 @@
+// Subset reduce (fa_reduce_subsets): its launch interface and host planning.  Kept apart
+// from kernels.cuh so that the other kernels' sources do not depend on it.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kernels.cuh"
+
+namespace fa {
+
+// kGatherStages input stages (jmax reporter tiles each) and kGatherOutBufs output tiles,
+// kGatherSmemBudget bytes in all (the tile size is chosen to fit; see gather_tile).
+constexpr int kGatherStages = 3;
+constexpr int kGatherOutBufs = 2;
+constexpr int kGatherSmemBudget = 221184;
+
+// Round-level reduce of client key subsets (fa_reduce_subsets): one segment per key to
+// write, each with its own reporters.  Reporter j of segment s is src[s.src0 + j], in the
+// order the contributions apply.
+struct GathSeg {
+    uint64_t len;       // elements of the key
+    void* out;          // destination of element 0 (dtype_out)
+    Divisor div;        // N_p
+    uint32_t J;         // reporters (1..16)
+    uint32_t src0;      // first reporter in the source table
+    uint32_t tile0;     // first tile (set by launch_gather_final)
+    uint32_t vec_ok;    // 1: the output and every reporter's input are 16-byte aligned
+};
+
+struct GathSrc {
+    const void* x;      // the reporter's values of this key (dtype_in, device memory)
+    float w;            // (float) n_k
+    uint32_t pad;
+};
+
+struct GathArgs {
+    const GathSeg* segs;         // device table, nseg entries sorted by tile0
+    const GathSrc* src;          // device table
+    const uint32_t* cta;         // device table, nchunk + 1 pairs (plan_gather_ctas): chunk c
+                                 // is tiles [cta[2c], cta[2c + 2]), its first tile in
+                                 // segment cta[2c + 1]
+    uint32_t* counter;           // device word, 0 at launch: chunks taken after the first
+    unsigned int* err;           // the caller's device error word
+    uint32_t nseg;
+    uint32_t ntiles;             // tiles over all segments (plan_gather_tiles)
+    uint32_t tile;               // elements per tile (gather_tile)
+    uint32_t jmax;               // largest J over the segments (1..16)
+    uint32_t grid;               // CTAs (gather_grid)
+    uint32_t nchunk;             // chunks of work (gather_chunks, >= grid)
+};
+
+// Round-level subset reduce: out = RNE(sum over the segment's reporters, in order, / N_p)
+// per segment, straight from the reporters' inputs (no running sum); comp: compensated
+// arithmetic (Dot2), the same operation sequence as every other path.  The caller picks
+// tile = gather_tile(jmax, ...), numbers the tiles of its host copy of the segment table
+// with plan_gather_tiles, takes grid = gather_grid(...) and nchunk = gather_chunks(...),
+// splits the tiles into chunks with plan_gather_ctas, uploads the three tables and a
+// zero counter word, and launches with a.tile, a.ntiles, a.grid and a.nchunk set.  Each
+// CTA starts with chunk blockIdx.x and takes further chunks from the counter.
+uint32_t gather_tile(uint32_t jmax, int dtype_in, int dtype_out);
+// Sets tile0 of every segment for `tile` elements per tile; false if there would be more
+// than 2^32 - 1 tiles.
+bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t* ntiles);
+// CTAs of a subset-reduce launch over ntiles tiles (a persistent grid, at most one
+// resident wave).
+uint32_t gather_grid(uint32_t ntiles, int dtype_in, int dtype_out, bool comp, const LaunchShape& s);
+// Chunks of work of a subset-reduce launch: about four tiles each, at least one per CTA,
+// at most kMaxGatherChunks.
+constexpr uint32_t kMaxGatherChunks = 65536;
+uint32_t gather_chunks(uint32_t ntiles, uint32_t grid);
+// Splits tiles [0, ntiles) into `grid` contiguous runs (chunks) of about equal HBM bytes
+// (a tile of segment s moves cnt * (J_s * s_in + s_out) bytes), so that keys with more
+// reporters do not weigh more per chunk.  Writes grid + 1 pairs to cta: cta[2b] is chunk
+// b's first tile (0 for b = 0, ntiles for b = grid, and in between the first tile whose
+// preceding bytes reach b / grid of the total), cta[2b + 1] the last segment whose first
+// tile is at or before it.  Segments numbered by plan_gather_tiles.
+void plan_gather_ctas(const GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t ntiles,
+                      int dtype_in, int dtype_out, uint32_t grid, uint32_t* cta);
+cudaError_t launch_gather_final(const GathArgs& a, int dtype_in, int dtype_out, bool comp,
+                                const LaunchShape& s, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,14 +1,18 @@
 // Host planning of a subset-reduce launch (fa_reduce_subsets): tile size, tile numbering,
 // grid size and the split of the tiles among the CTAs.  Plain C++: the CPU tests compile
 // it without CUDA device code.
-#include "kernels.cuh"
+#include "gather.cuh"
 #include "tiles.hpp"
 
 namespace fa {
 
 uint32_t gather_tile(uint32_t jmax, int dtype_in, int dtype_out) {
-    const uint32_t eb = jmax * (dtype_in == 0 ? 4u : 2u) + (dtype_out == 0 ? 4u : 2u);
-    return reduce_tile(eb);
+    // the largest multiple of 256 elements whose input stages (jmax reporter tiles each)
+    // and output buffers fit kGatherSmemBudget
+    const uint32_t eb = kGatherStages * jmax * (dtype_in == 0 ? 4u : 2u) +
+                        kGatherOutBufs * (dtype_out == 0 ? 4u : 2u);
+    const uint32_t t = kGatherSmemBudget / eb / 256 * 256;
+    return t < 256 ? 256 : t;
 }
 
 bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t* ntiles) {
@@ -18,6 +22,13 @@ bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t* nt
 uint32_t gather_grid(uint32_t ntiles, int dtype_in, int dtype_out, bool comp, const LaunchShape& s) {
     const int per = s.gather_ctas_per_sm[comp ? 1 : 0][dtype_in == 0 ? 0 : 1][dtype_out == 0 ? 0 : 1];
     return grid_for(ntiles, s.sms, per);
+}
+
+uint32_t gather_chunks(uint32_t ntiles, uint32_t grid) {
+    uint32_t n = ntiles / 4;
+    if (n > kMaxGatherChunks) n = kMaxGatherChunks;
+    if (n < grid) n = grid;
+    return n < ntiles ? n : ntiles;
 }
 
 void plan_gather_ctas(const GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t ntiles,

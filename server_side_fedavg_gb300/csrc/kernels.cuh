@@ -115,39 +115,6 @@ struct FinSeg {
     uint32_t tile0;     // first tile of this segment
 };
 
-// Round-level reduce of client key subsets (fa_reduce_subsets): one segment per key to
-// write, each with its own reporters.  Reporter j of segment s is src[s.src0 + j], in the
-// order the contributions apply.
-struct GathSeg {
-    uint64_t len;       // elements of the key
-    void* out;          // destination of element 0 (dtype_out)
-    Divisor div;        // N_p
-    uint32_t J;         // reporters (1..16)
-    uint32_t src0;      // first reporter in the source table
-    uint32_t tile0;     // first tile (set by launch_gather_final)
-    uint32_t vec_ok;    // 1: the output and every reporter's input are 16-byte aligned
-};
-
-struct GathSrc {
-    const void* x;      // the reporter's values of this key (dtype_in, device memory)
-    float w;            // (float) n_k
-    uint32_t pad;
-};
-
-struct GathArgs {
-    const GathSeg* segs;         // device table, nseg entries sorted by tile0
-    const GathSrc* src;          // device table
-    const uint32_t* cta;         // device table, grid + 1 pairs (plan_gather_ctas): CTA b
-                                 // takes tiles [cta[2b], cta[2b + 2]); its first tile
-                                 // lies in segment cta[2b + 1]
-    unsigned int* err;           // the caller's device error word
-    uint32_t nseg;
-    uint32_t ntiles;             // tiles over all segments (plan_gather_tiles)
-    uint32_t tile;               // elements per tile (gather_tile)
-    uint32_t jmax;               // largest J over the segments (1..16)
-    uint32_t grid;               // CTAs (gather_grid)
-};
-
 struct LaunchShape {
     int sms = 0;
     int bulk_ctas_per_sm[2][2] = {};       // [compensated][dtype_in], streaming kernel
@@ -168,7 +135,7 @@ cudaError_t query_launch_shape(LaunchShape* s);
 // The parts of query_launch_shape that live with their kernels (reduce kernel, subset
 // reduce kernel, finalize kernel).
 cudaError_t prepare_reduce_shapes(LaunchShape* s);
-cudaError_t prepare_gather_shapes(LaunchShape* s);
+cudaError_t prepare_gather_shapes(LaunchShape* s);   // gather.cuh has the rest of its interface
 cudaError_t prepare_finalize_shapes(LaunchShape* s);
 
 // launch_accumulate with J = 2..16 resident clients: the reduce kernel in sum mode.
@@ -193,31 +160,6 @@ cudaError_t launch_accumulate_direct(const AccArgs& a, int dtype_in, const Launc
 // Final-mode reduce: out = RNE((sum so far +) J weighted inputs, / divisor) per segment.
 // The caller fills everything but tile / ntiles / tile0.
 cudaError_t launch_reduce_final(const RedArgs& a, int dtype_in, int dtype_out,
-                                const LaunchShape& s, cudaStream_t stream);
-
-// Round-level subset reduce: out = RNE(sum over the segment's reporters, in order, / N_p)
-// per segment, straight from the reporters' inputs (no running sum); comp: compensated
-// arithmetic (Dot2), the same operation sequence as every other path.  The caller picks
-// tile = gather_tile(jmax, ...), numbers the tiles of its host copy of the segment table
-// with plan_gather_tiles, takes grid = gather_grid(...) and splits the tiles among the
-// CTAs with plan_gather_ctas, uploads the three tables, and launches with a.tile,
-// a.ntiles and a.grid set.
-uint32_t gather_tile(uint32_t jmax, int dtype_in, int dtype_out);
-// Sets tile0 of every segment for `tile` elements per tile; false if there would be more
-// than 2^32 - 1 tiles.
-bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t* ntiles);
-// CTAs of a subset-reduce launch over ntiles tiles (a persistent grid, at most one
-// resident wave).
-uint32_t gather_grid(uint32_t ntiles, int dtype_in, int dtype_out, bool comp, const LaunchShape& s);
-// Splits tiles [0, ntiles) into `grid` contiguous runs of about equal HBM bytes (a tile
-// of segment s moves cnt * (J_s * s_in + s_out) bytes), so that keys with more reporters
-// do not leave one CTA with more data than the others.  Writes grid + 1 pairs to cta:
-// cta[2b] is CTA b's first tile (0 for b = 0, ntiles for b = grid, and in between the
-// first tile whose preceding bytes reach b / grid of the total), cta[2b + 1] the last
-// segment whose first tile is at or before it.  Segments numbered by plan_gather_tiles.
-void plan_gather_ctas(const GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t ntiles,
-                      int dtype_in, int dtype_out, uint32_t grid, uint32_t* cta);
-cudaError_t launch_gather_final(const GathArgs& a, int dtype_in, int dtype_out, bool comp,
                                 const LaunchShape& s, cudaStream_t stream);
 
 // segs: device array of nseg FinSeg sorted by tile0.

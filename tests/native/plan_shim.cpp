@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <vector>
 
-#include "kernels.cuh"
+#include "gather.cuh"
 
 extern "C" {
 
@@ -29,5 +29,7 @@ int32_t gp_plan(const uint64_t* lens, const uint32_t* J, uint32_t nseg, int din,
     fa::plan_gather_ctas(segs.data(), nseg, *tile, *ntiles, din, dout, grid, cta);
     return 0;
 }
+
+uint32_t gp_chunks(uint32_t ntiles, uint32_t grid) { return fa::gather_chunks(ntiles, grid); }
 
 }  // extern "C"

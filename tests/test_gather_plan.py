@@ -1,7 +1,7 @@
 """Host planning of a subset-reduce launch (the round-level adapter reduce): the tiles
-of every key written are numbered in order and split among the persistent CTAs in
-contiguous runs of about equal HBM bytes, each tile of key p moving
-cnt * (J_p * s_in + s_out) bytes, and each CTA is told the key its first tile is in.  Checked against a brute-force walk over every tile
+of every key written are numbered in order and split into chunks -- contiguous runs of
+about equal HBM bytes, each tile of key p moving cnt * (J_p * s_in + s_out) bytes, each
+chunk told the key its first tile is in -- which the persistent CTAs take one by one.  Checked against a brute-force walk over every tile
 in exact integers, and for the properties the kernel relies on (a monotone split that
 starts at tile 0 and ends at the last tile)."""
 import ctypes
@@ -27,7 +27,7 @@ def lib():
             pytest.skip("CUDA headers are not installed")
         os.makedirs(os.path.dirname(SO), exist_ok=True)
         srcs = [os.path.join(HERE, "native", "plan_shim.cpp"), os.path.join(CSRC, "gather_plan.cpp")]
-        deps = srcs + [os.path.join(CSRC, f) for f in ("kernels.cuh", "tiles.hpp")]
+        deps = srcs + [os.path.join(CSRC, f) for f in ("kernels.cuh", "gather.cuh", "tiles.hpp")]
         if not os.path.exists(SO) or any(os.path.getmtime(s) > os.path.getmtime(SO) for s in deps):
             subprocess.run(["g++", "-O1", "-g", "-std=c++17", "-fPIC", "-shared", "-I", CSRC,
                             "-I", CUDA_INC] + srcs + ["-o", SO], check=True)
@@ -35,6 +35,8 @@ def lib():
         vp, u32, i32 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32
         L.gp_plan.argtypes = [vp, vp, u32, ctypes.c_int, ctypes.c_int, u32, vp, vp, vp, vp]
         L.gp_plan.restype = i32
+        L.gp_chunks.argtypes = [u32, u32]
+        L.gp_chunks.restype = u32
         _lib = L
     return _lib
 
@@ -132,3 +134,14 @@ def test_more_ctas_than_bytes_need():
     assert ntiles == 1 and list(cta) == [0, 1]
     _, _, _, cta = plan([5, 7], [2, 3], 1, 1, 2)
     assert list(cta) == brute_split(tile_bytes([5, 7], [2, 3], tile, 1, 1), 2)
+
+
+def test_chunk_count():
+    f = lib().gp_chunks
+    assert f(4096, 152) == 1024          # about four tiles per chunk
+    assert f(100, 152) == 100            # never more chunks than tiles
+    assert f(300, 152) == 152            # at least one chunk per CTA
+    assert f(1 << 30, 152) == 65536      # a bounded table
+    for ntiles, grid in ((1, 1), (5, 5), (7, 3), (10 ** 6, 1216)):
+        n = f(ntiles, grid)
+        assert grid <= n <= ntiles and n <= max(grid, 65536)
