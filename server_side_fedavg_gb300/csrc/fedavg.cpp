@@ -29,6 +29,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <thread>
@@ -88,6 +89,10 @@ struct fa_ctx {
     size_t gath_cap = 0;
     cudaEvent_t gath_ev = nullptr;
     bool gath_pending = false;
+    // ... or, for a small round, its tables in the launch's parameters
+    std::unique_ptr<fa::GathInline> gath_inline;
+    uint32_t* gath_slots = nullptr;   // two tile counters; the kernel zeroes the unused one
+    uint32_t gath_slot = 0;           // the counter the next inline launch uses
     void* out_stage = nullptr;
 
     unsigned int* err_dev = nullptr;     // this context's device error word (kernels OR bits in)
@@ -490,6 +495,7 @@ void free_ctx(fa_ctx* c) {
     if (c->gath_host) cudaFreeHost(c->gath_host);
     if (c->gath_dev) cudaFree(c->gath_dev);
     if (c->gath_ev) cudaEventDestroy(c->gath_ev);
+    if (c->gath_slots) cudaFree(c->gath_slots);
     if (c->out_stage) cudaFree(c->out_stage);
     if (c->err_ev) cudaEventDestroy(c->err_ev);
     if (c->err_stream) cudaStreamDestroy(c->err_stream);
@@ -603,6 +609,8 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
     }
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->fin_ev, cudaEventDisableTiming);
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->gath_ev, cudaEventDisableTiming);
+    if (ce == cudaSuccess) ce = cudaMalloc(reinterpret_cast<void**>(&c->gath_slots), 2 * sizeof(uint32_t));
+    if (ce == cudaSuccess) ce = cudaMemset(c->gath_slots, 0, 2 * sizeof(uint32_t));
     if (ce == cudaSuccess) ce = cudaMalloc(&c->fin_dev, sizeof(fa::FinSeg) * n_keys);
     if (ce == cudaSuccess) ce = cudaHostAlloc(&c->fin_host, sizeof(fa::FinSeg) * n_keys, cudaHostAllocDefault);
     if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&c->err_stream, cudaStreamNonBlocking);
@@ -1070,7 +1078,8 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
     std::vector<uint32_t> fill(cnt.begin(), cnt.end() - 1);
     std::vector<const void*> src_x(n_entries);
     std::vector<float> src_w(n_entries);
-    std::vector<uint8_t> src_first(n_entries, 0);
+    std::vector<uint32_t> src_client(n_entries);
+    std::vector<uint64_t> src_off(n_entries);
     o = 0;
     for (uint32_t j = 0; j < n_clients; ++j) {
         uint64_t off = 0;
@@ -1079,6 +1088,8 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
             const uint32_t slot = fill[p]++;
             src_x[slot] = static_cast<const char*>(client_ptrs[j]) + off * c->s_in;
             src_w[slot] = static_cast<float>(weights[j]);
+            src_client[slot] = j;
+            src_off[slot] = off;
             off += c->ledger.numel(p);
         }
     }
@@ -1125,9 +1136,78 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
         if (r != FA_OK) c->broken = true;
         return r;
     }
-    // segment table (one entry per key to write) and source table
     const uint32_t nseg = static_cast<uint32_t>(c->items.size());
     const bool comp = c->acc_lo != nullptr;
+    auto out_of = [&](const fa::FinItem& it) {
+        char* dst = static_cast<char*>(flat ? out_ptrs[0] : out_ptrs[it.key]);
+        return flat ? dst + it.flat_off * c->s_out : dst;
+    };
+    auto aligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    {
+        // a small round: the tables travel in the launch's parameters (no upload, no table
+        // reads from global memory), when every key and client offset fits 32 bits
+        uint32_t so = 0, bo = 0, wo = 0;
+        bool small = fa::gather_inline_layout(nseg, static_cast<uint32_t>(std::min<uint64_t>(n_entries, 0xFFFFFFFFu)),
+                                              n_clients, &so, &bo, &wo);
+        for (uint32_t i = 0; small && i < nseg; ++i) small = c->items[i].numel <= 0xFFFFFFFFull;
+        for (uint64_t e2 = 0; small && e2 < n_entries; ++e2) small = src_off[e2] <= 0xFFFFFFFFull;
+        if (small) {
+            if (!c->gath_inline) c->gath_inline.reset(new fa::GathInline);
+            fa::GathInline& gp = *c->gath_inline;
+            gp.err = c->err_dev;
+            gp.slots = c->gath_slots;
+            gp.slot = c->gath_slot;
+            gp.nseg = nseg;
+            gp.nsrc = static_cast<uint32_t>(n_entries);
+            gp.nclient = n_clients;
+            gp.jmax = jmax;
+            gp.tile = fa::gather_tile(jmax, c->din, c->dout);
+            gp.src_off = so;
+            gp.base_off = bo;
+            gp.w_off = wo;
+            gp.pad = 0;
+            auto* gs = reinterpret_cast<fa::GathSegP*>(gp.blob);
+            auto* gr = reinterpret_cast<fa::GathSrcP*>(gp.blob + so);
+            auto* gb = reinterpret_cast<const void**>(gp.blob + bo);
+            auto* gw = reinterpret_cast<float*>(gp.blob + wo);
+            uint64_t tiles = 0;
+            for (uint32_t i = 0; i < nseg; ++i) {
+                const fa::FinItem& it = c->items[i];
+                fa::GathSegP& g = gs[i];
+                g.out = out_of(it);
+                g.div = fa::make_divisor(it.total);
+                g.len = static_cast<uint32_t>(it.numel);
+                g.tile0 = static_cast<uint32_t>(tiles);
+                g.src0 = static_cast<uint16_t>(cnt[it.key]);
+                g.J = static_cast<uint8_t>(cnt[it.key + 1] - cnt[it.key]);
+                bool ok = aligned(g.out);
+                for (uint32_t q = 0; q < g.J && ok; ++q) ok = aligned(src_x[g.src0 + q]);
+                g.vec_ok = ok ? 1u : 0u;
+                tiles += (it.numel + gp.tile - 1) / gp.tile;
+            }
+            if (tiles > 0xFFFFFFFFull) {
+                c->broken = true;
+                return fail(c, FA_ERR_RANGE, "layout too large for one subset reduce");
+            }
+            gp.ntiles = static_cast<uint32_t>(tiles);
+            for (uint64_t e2 = 0; e2 < n_entries; ++e2)
+                gr[e2] = fa::GathSrcP{static_cast<uint32_t>(src_off[e2]), src_client[e2]};
+            for (uint32_t j = 0; j < n_clients; ++j) {
+                gb[j] = client_ptrs[j];
+                gw[j] = static_cast<float>(weights[j]);
+            }
+            gp.grid = fa::gather_grid(gp.ntiles, c->din, c->dout, comp, c->shape);
+            cudaError_t ce = fa::launch_gather_inline(gp, c->din, c->dout, comp, c->shape, s);
+            if (ce != cudaSuccess) {
+                c->broken = true;
+                return cuda_fail(c, ce, "subset reduce launch");
+            }
+            if (gp.ntiles > 0) c->gath_slot ^= 1u;   // the kernel zeroed the other counter
+            c->stats.kernel_launches++;
+            return chain_out(c, s);
+        }
+    }
+    // segment table (one entry per key to write) and source table in device memory
     const size_t seg_bytes = (sizeof(fa::GathSeg) * nseg + 15) / 16 * 16;
     const size_t src_bytes = (sizeof(fa::GathSrc) * n_entries + 15) / 16 * 16;
     // + the largest chunk table and the counter word

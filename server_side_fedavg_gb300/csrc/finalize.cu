@@ -53,6 +53,9 @@ __device__ __forceinline__ void global_store8(void* out, uint64_t e, const float
     }
 }
 
+// Segments whose first tiles a finalize CTA keeps in shared memory (16 KB).
+constexpr uint32_t kFinSegCache = 4096;
+
 // q = sum / N; delta rounds then add server_lr * q to the base with one rounding (fma).
 template <typename Tout, bool kApply, bool kComp>
 __device__ __forceinline__ void fin_vec(const FinSeg& sg, uint64_t e, const float* s,
@@ -89,12 +92,27 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
                                                           float lr) {
     constexpr int kVecPerTile = kTile / kVec;
     constexpr int kUnroll = kVecPerTile / kBlock;
+    // each segment's first tile, in shared memory when the table is small enough: a CTA
+    // strides gridDim.x tiles at a time, which can skip many small keys at once, and the
+    // search for the next tile's segment then costs shared-memory reads, not a chain of
+    // dependent global loads
+    __shared__ uint32_t t0s[kFinSegCache];
+    const bool cached = nseg <= kFinSegCache;
+    if (cached) {
+        for (uint32_t i = threadIdx.x; i < nseg; i += kBlock) t0s[i] = segs[i].tile0;
+        __syncthreads();
+    }
+    auto tile0_of = [&](uint32_t i) { return cached ? t0s[i] : segs[i].tile0; };
     uint32_t si = 0;
-    uint32_t next0 = nseg > 1 ? segs[1].tile0 : 0xFFFFFFFFu;
     for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        while (t >= next0) {
-            ++si;
-            next0 = si + 1 < nseg ? segs[si + 1].tile0 : 0xFFFFFFFFu;
+        if (si + 1 < nseg && t >= tile0_of(si + 1)) {
+            // the last segment whose first tile is at or before t, in (si, nseg)
+            uint32_t lo = si + 1, hi = nseg;
+            while (hi - lo > 1) {
+                const uint32_t mid = (lo + hi) / 2;
+                if (tile0_of(mid) <= t) lo = mid; else hi = mid;
+            }
+            si = lo;
         }
         const FinSeg sg = segs[si];
         const uint64_t e0 = static_cast<uint64_t>(t - sg.tile0) * kTile;

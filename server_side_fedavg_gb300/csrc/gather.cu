@@ -12,19 +12,72 @@ namespace {
 
 // ----------------------------------------------------------------- subset reduce
 // A round of client key subsets straight to the output: one segment per key, each with
-// its own reporters (GathSeg / GathSrc tables in device memory) applied in table order --
-// the final mode of reduce_bulk_kernel with per-segment inputs and weights, warp-
-// specialised the same way (warps 0-7 compute, one producer lane issues a stage's bulk
-// loads and stores its output tile).  Stage = jmax input tiles + one output tile; a
-// segment with fewer reporters leaves part of the stage unused.  A plain launch: its
-// tables are uploaded on the stream just before it.
-template <typename Tin, typename Tout, bool kComp>
-__device__ __forceinline__ void gath_one(const GathArgs& a, const GathSeg& sg, uint64_t e) {
-    const GathSrc* src = a.src + sg.src0;
+// its own reporters applied in table order -- the final mode of reduce_bulk_kernel with
+// per-segment inputs and weights.  The tables are either in device memory (GathArgs,
+// uploaded on the stream just before a plain launch) or, for a small round, in the
+// launch's own parameters (GathInline, a programmatic dependent launch with no upload).
+
+// A segment as the kernel uses it, from either form of the tables.
+struct SegV {
+    uint64_t len;
+    void* out;
+    Divisor div;
+    uint32_t J;
+    uint32_t src0;
+    uint32_t tile0;
+    uint32_t vec_ok;
+};
+
+// Tables in device memory.
+struct DevTables {
+    const GathArgs* a;
+    __device__ __forceinline__ uint32_t nseg() const { return a->nseg; }
+    __device__ __forceinline__ uint32_t tile0(uint32_t i) const { return a->segs[i].tile0; }
+    __device__ __forceinline__ SegV seg(uint32_t i) const {
+        const GathSeg& g = a->segs[i];
+        return SegV{g.len, g.out, g.div, g.J, g.src0, g.tile0, g.vec_ok};
+    }
+    __device__ __forceinline__ const void* x(const SegV& s, uint32_t j, uint32_t) const {
+        return a->src[s.src0 + j].x;
+    }
+    __device__ __forceinline__ float w(const SegV& s, uint32_t j) const { return a->src[s.src0 + j].w; }
+};
+
+// Tables in the launch's parameters (read through the constant cache; every access is
+// uniform across a warp).
+struct ParTables {
+    const GathInline* p;
+    __device__ __forceinline__ const GathSegP& g(uint32_t i) const {
+        return reinterpret_cast<const GathSegP*>(p->blob)[i];
+    }
+    __device__ __forceinline__ const GathSrcP& r(uint32_t k) const {
+        return reinterpret_cast<const GathSrcP*>(p->blob + p->src_off)[k];
+    }
+    __device__ __forceinline__ uint32_t nseg() const { return p->nseg; }
+    __device__ __forceinline__ uint32_t tile0(uint32_t i) const { return g(i).tile0; }
+    __device__ __forceinline__ SegV seg(uint32_t i) const {
+        const GathSegP& s = g(i);
+        return SegV{s.len, s.out, s.div, s.J, s.src0, s.tile0, s.vec_ok};
+    }
+    __device__ __forceinline__ const void* x(const SegV& s, uint32_t j, uint32_t s_in) const {
+        const GathSrcP& q = r(s.src0 + j);
+        const char* base = reinterpret_cast<const char* const*>(p->blob + p->base_off)[q.client];
+        return base + static_cast<uint64_t>(q.off) * s_in;
+    }
+    __device__ __forceinline__ float w(const SegV& s, uint32_t j) const {
+        return reinterpret_cast<const float*>(p->blob + p->w_off)[r(s.src0 + j).client];
+    }
+};
+
+// One element through global memory (ragged tails, unaligned segments).
+template <typename Tin, typename Tout, bool kComp, typename Tab>
+__device__ __forceinline__ void gath_one(const Tab& tb, const SegV& sg, uint64_t e) {
     float r, rl = 0.0f;
-    contrib_first<kComp>(src[0].w, load_one<Tin>(static_cast<const Tin*>(src[0].x) + e), r, rl);
+    contrib_first<kComp>(tb.w(sg, 0), load_one<Tin>(static_cast<const Tin*>(tb.x(sg, 0, sizeof(Tin))) + e),
+                         r, rl);
     for (uint32_t j = 1; j < sg.J; ++j)
-        contrib_add<kComp>(src[j].w, load_one<Tin>(static_cast<const Tin*>(src[j].x) + e), r, rl);
+        contrib_add<kComp>(tb.w(sg, j), load_one<Tin>(static_cast<const Tin*>(tb.x(sg, j, sizeof(Tin))) + e),
+                           r, rl);
     store_one<Tout>(sg.out, e, quotient_out<kComp, Tout>(r, rl, sg.div));
 }
 
@@ -41,9 +94,7 @@ __host__ __device__ constexpr size_t gather_smem_bytes(uint32_t tile, uint32_t j
            (kGatherStages + kGatherOutBufs) * sizeof(uint2);
 }
 
-// Tile t of segment si (t lies in that segment).
-__device__ __forceinline__ TileAt gath_tile(const GathSeg* segs, uint32_t si, uint32_t t, uint32_t T) {
-    const GathSeg& sg = segs[si];
+__device__ __forceinline__ TileAt tile_in(const SegV& sg, uint32_t si, uint32_t t, uint32_t T) {
     TileAt r;
     r.si = si;
     r.e0 = static_cast<uint64_t>(t - sg.tile0) * T;
@@ -61,17 +112,19 @@ __device__ __forceinline__ TileAt gath_tile(const GathSeg* segs, uint32_t si, ui
 //    buffer o, release the stage (empty[s]) and hand the buffer on (ofull[o]);
 //  - the storer (one lane of warp 9) writes buffer o to the output with one bulk store
 //    and frees it once the store has read it.
-// Stores therefore never delay the next loads.  Work is handed out in chunks: contiguous
-// runs of tiles of about equal bytes planned on the host (cta: nchunk + 1 (first tile,
-// segment) pairs).  CTA b starts with chunk b and then takes chunk
-// grid + atomicAdd(counter, 1) until none is left, so CTAs that run faster (or start
-// earlier) take more of the round and all finish together; the loader asks for the next
-// chunk as soon as it starts one, so the atomic's latency is hidden behind that chunk.
-template <typename Tin, typename Tout, bool kComp>
-__global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const __grid_constant__ GathArgs a) {
-    const uint32_t T = a.tile;
+// Stores therefore never delay the next loads.  Work is handed out dynamically, so that
+// CTAs that run faster (or start earlier) take more of the round and all finish
+// together: CTA b starts with unit b and then takes unit grid + atomicAdd(counter, 1)
+// until none is left, the loader asking for the next unit as soon as it starts one, so
+// the atomic's latency is hidden.  A unit is a chunk of about equal bytes planned on the
+// host (device tables: nchunk + 1 (first tile, segment) pairs) or a single tile, whose
+// segment the loader finds by a binary search over the parameter tables (inline tables).
+template <typename Tin, typename Tout, bool kComp, bool kInline, typename Tab>
+__device__ __forceinline__ void gather_body(const Tab& tb, uint32_t ntiles, uint32_t T, uint32_t jmax,
+                                            uint32_t grid, uint32_t nunit, const uint32_t* cta,
+                                            uint32_t* counter, unsigned int* err) {
     const uint32_t XB = T * sizeof(Tin);          // one reporter's input tile
-    const uint32_t IB = a.jmax * XB;              // one input stage
+    const uint32_t IB = jmax * XB;                // one input stage
     const uint32_t OB = T * sizeof(Tout);         // one output buffer
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* ins = smem;
@@ -82,42 +135,42 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
     uint64_t* ofree = ofull + kGatherOutBufs;
     uint2* meta = reinterpret_cast<uint2*>(ofree + kGatherOutBufs);
     uint2* ometa = meta + kGatherStages;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kGatherStages; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s])) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[s])),
-                         "r"(kReduceWarps) : "memory");
-        }
-        for (int o = 0; o < kGatherOutBufs; ++o) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&ofull[o])),
-                         "r"(kReduceWarps) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&ofree[o])) : "memory");
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
     const uint32_t warp = threadIdx.x / 32u, lane = threadIdx.x & 31u;
+    const uint32_t nseg = tb.nseg();
 
     if (warp == static_cast<uint32_t>(kReduceWarps)) {
         // ------------------------------------------------------------ loader
         if (lane != 0) return;
-        uint32_t chunk = blockIdx.x;           // < nchunk: the host plans nchunk >= grid
-        uint32_t t = a.cta[2 * chunk], cur = a.cta[2 * chunk + 1], tend = a.cta[2 * chunk + 2];
-        uint32_t next = a.grid < a.nchunk ? a.grid + atomicAdd(a.counter, 1u) : a.nchunk;
+        uint32_t unit = blockIdx.x;            // < nunit: the host plans nunit >= grid
+        uint32_t next = grid < nunit ? grid + atomicAdd(counter, 1u) : nunit;
+        uint32_t t, tend, cur;
+        if constexpr (kInline) {
+            t = unit;
+            tend = unit + 1;
+            cur = 0;
+        } else {
+            t = cta[2 * unit];
+            cur = cta[2 * unit + 1];
+            tend = cta[2 * unit + 2];
+        }
         // the current segment, kept in registers while its tiles are issued
-        uint32_t have = 0xFFFFFFFFu, nt0 = 0, J = 0, vec = 0;
-        uint32_t t0 = 0;
-        uint64_t len = 0;
+        uint32_t have = 0xFFFFFFFFu, nt0 = 0;
+        SegV sg{};
         const void* xp[kMaxBatch];
         bool ok = true;
         uint32_t issued = 0;                   // tiles published to the stages
         for (;; ++issued) {
-            while (t == tend && next < a.nchunk) {   // this chunk is done: take the next one
-                chunk = next;
-                t = a.cta[2 * chunk];
-                cur = a.cta[2 * chunk + 1];
-                tend = a.cta[2 * chunk + 2];
-                next = a.grid + atomicAdd(a.counter, 1u);
+            while (t == tend && next < nunit) {      // this unit is done: take the next one
+                unit = next;
+                if constexpr (kInline) {
+                    t = unit;
+                    tend = unit + 1;
+                } else {
+                    t = cta[2 * unit];
+                    cur = cta[2 * unit + 1];
+                    tend = cta[2 * unit + 2];
+                }
+                next = grid + atomicAdd(counter, 1u);
             }
             const uint32_t s = issued % kGatherStages;
             if (issued >= static_cast<uint32_t>(kGatherStages)) {
@@ -130,36 +183,44 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
                 mbar_arrive(bar);
                 break;
             }
-            if (cur != have) nt0 = cur + 1 < a.nseg ? a.segs[cur + 1].tile0 : 0xFFFFFFFFu;
-            while (t >= nt0) {
-                ++cur;
-                nt0 = cur + 1 < a.nseg ? a.segs[cur + 1].tile0 : 0xFFFFFFFFu;
+            if constexpr (kInline) {
+                if (t >= nt0) {
+                    // the last segment whose first tile is at or before t, in [cur, nseg):
+                    // this CTA's tiles only increase
+                    uint32_t lo = cur, hi = nseg;
+                    while (hi - lo > 1) {
+                        const uint32_t mid = (lo + hi) / 2;
+                        if (tb.tile0(mid) <= t) lo = mid; else hi = mid;
+                    }
+                    cur = lo;
+                    nt0 = cur + 1 < nseg ? tb.tile0(cur + 1) : 0xFFFFFFFFu;
+                }
+            } else {
+                if (cur != have) nt0 = cur + 1 < nseg ? tb.tile0(cur + 1) : 0xFFFFFFFFu;
+                while (t >= nt0) {
+                    ++cur;
+                    nt0 = cur + 1 < nseg ? tb.tile0(cur + 1) : 0xFFFFFFFFu;
+                }
             }
             if (cur != have) {
-                const GathSeg& sg = a.segs[cur];
-                J = sg.J;
-                vec = sg.vec_ok;
-                t0 = sg.tile0;
-                len = sg.len;
-                const GathSrc* src = a.src + sg.src0;
+                sg = tb.seg(cur);
 #pragma unroll
                 for (int jj = 0; jj < kMaxBatch; ++jj)
-                    xp[jj] = jj < static_cast<int>(J) ? src[jj].x : nullptr;
+                    xp[jj] = jj < static_cast<int>(sg.J) ? tb.x(sg, jj, sizeof(Tin)) : nullptr;
                 have = cur;
             }
             meta[s] = make_uint2(t, cur);
-            const uint64_t e0 = static_cast<uint64_t>(t - t0) * T;
-            const uint64_t rem = len - e0;
-            const uint32_t n8 = (rem < T ? static_cast<uint32_t>(rem) : T) / kVec;
+            const TileAt ta = tile_in(sg, cur, t, T);
+            const uint32_t n8 = ta.cnt / kVec;
             ++t;
-            if (vec && n8 > 0) {
+            if (sg.vec_ok && n8 > 0) {
                 const uint32_t xb = n8 * kVec * sizeof(Tin);
-                mbar_expect(bar, J * xb);
+                mbar_expect(bar, sg.J * xb);
                 uint8_t* st = ins + s * IB;
 #pragma unroll
                 for (int jj = 0; jj < kMaxBatch; ++jj) {
-                    if (jj >= static_cast<int>(J)) break;
-                    bulk_load(st + jj * XB, static_cast<const Tin*>(xp[jj]) + e0, xb, bar);
+                    if (jj >= static_cast<int>(sg.J)) break;
+                    bulk_load(st + jj * XB, static_cast<const Tin*>(xp[jj]) + ta.e0, xb, bar);
                 }
             } else {
                 mbar_arrive(bar);
@@ -167,7 +228,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
         }
         if (!ok) {
             // a wait gave up: flag it, and wait (bounded) for the loads still in flight
-            atomicOr(a.err, kErrWaitTimeout);
+            atomicOr(err, kErrWaitTimeout);
             for (uint32_t i = issued >= static_cast<uint32_t>(kGatherStages) ? issued - kGatherStages : 0u;
                  i < issued; ++i)
                 mbar_wait(smem_addr(&full[i % kGatherStages]), (i / kGatherStages) & 1u);
@@ -185,8 +246,8 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
             if (!ok) break;
             const uint2 m = ometa[o];
             if (m.x == kNoTile) break;
-            const TileAt ta = gath_tile(a.segs, m.y, m.x, T);
-            const GathSeg& sg = a.segs[m.y];
+            const SegV sg = tb.seg(m.y);
+            const TileAt ta = tile_in(sg, m.y, m.x, T);
             const uint32_t n8 = (sg.vec_ok && ta.cnt >= static_cast<uint32_t>(kVec)) ? ta.cnt / kVec : 0u;
             if (n8 > 0) {
                 bulk_store(static_cast<Tout*>(sg.out) + ta.e0, outs + o * OB, n8 * kVec * sizeof(Tout));
@@ -195,7 +256,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
             }
             mbar_arrive(smem_addr(&ofree[o]));
         }
-        if (!ok) atomicOr(a.err, kErrWaitTimeout);
+        if (!ok) atomicOr(err, kErrWaitTimeout);
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         return;
     }
@@ -204,13 +265,13 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
     for (uint32_t i = 0;; ++i) {
         const uint32_t s = i % kGatherStages, o = i % kGatherOutBufs;
         if (!mbar_wait(smem_addr(&full[s]), (i / kGatherStages) & 1u)) {
-            atomicOr(a.err, kErrWaitTimeout);
+            atomicOr(err, kErrWaitTimeout);
             break;
         }
         const uint2 m = meta[s];
         if (i >= static_cast<uint32_t>(kGatherOutBufs) &&
             !mbar_wait(smem_addr(&ofree[o]), ((i / kGatherOutBufs) - 1) & 1u)) {
-            atomicOr(a.err, kErrWaitTimeout);
+            atomicOr(err, kErrWaitTimeout);
             break;
         }
         if (m.x == kNoTile) {                  // no more tiles: tell the storer
@@ -219,17 +280,16 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
             if (lane == 0) mbar_arrive(smem_addr(&ofull[o]));
             break;
         }
-        const TileAt ta = gath_tile(a.segs, m.y, m.x, T);
-        const GathSeg sg = a.segs[m.y];
+        const SegV sg = tb.seg(m.y);
+        const TileAt ta = tile_in(sg, m.y, m.x, T);
         const bool bulk = sg.vec_ok && ta.cnt >= static_cast<uint32_t>(kVec);
         const uint32_t n8 = bulk ? ta.cnt / kVec : 0;
         const uint8_t* st = ins + s * IB;
         uint8_t* res = outs + o * OB;
         if (bulk) {
-            const GathSrc* src = a.src + sg.src0;
             float wv[kMaxBatch];
 #pragma unroll
-            for (int j = 0; j < kMaxBatch; ++j) wv[j] = j < static_cast<int>(sg.J) ? src[j].w : 0.0f;
+            for (int j = 0; j < kMaxBatch; ++j) wv[j] = j < static_cast<int>(sg.J) ? tb.w(sg, j) : 0.0f;
             for (uint32_t v = threadIdx.x; v < n8; v += kBlock) {
                 float r[8], rl[8];
                 {
@@ -251,10 +311,10 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
                 smem_store8<Tout>(res, v, r);
             }
             const uint32_t tail = ta.cnt - n8 * kVec;
-            if (threadIdx.x < tail) gath_one<Tin, Tout, kComp>(a, sg, ta.e0 + n8 * kVec + threadIdx.x);
+            if (threadIdx.x < tail) gath_one<Tin, Tout, kComp>(tb, sg, ta.e0 + n8 * kVec + threadIdx.x);
         } else {
             for (uint32_t e = threadIdx.x; e < ta.cnt; e += kBlock)
-                gath_one<Tin, Tout, kComp>(a, sg, ta.e0 + e);
+                gath_one<Tin, Tout, kComp>(tb, sg, ta.e0 + e);
         }
         if (threadIdx.x == 0) ometa[o] = m;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -266,6 +326,56 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
     }
 }
 
+// The barriers of one CTA (full / empty per input stage, ofull / ofree per output buffer),
+// at the end of the stage buffers.
+__device__ __forceinline__ void gather_barriers_init(uint32_t T, uint32_t jmax, uint32_t s_in,
+                                                     uint32_t s_out) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(T) *
+                                                 (kGatherStages * jmax * s_in + kGatherOutBufs * s_out));
+    uint64_t* empty = full + kGatherStages;
+    uint64_t* ofull = empty + kGatherStages;
+    uint64_t* ofree = ofull + kGatherOutBufs;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGatherStages; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s])) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[s])),
+                         "r"(kReduceWarps) : "memory");
+        }
+        for (int o = 0; o < kGatherOutBufs; ++o) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&ofull[o])),
+                         "r"(kReduceWarps) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&ofree[o])) : "memory");
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+}
+
+// Tables in device memory: a plain launch after their upload; units are the planned chunks.
+template <typename Tin, typename Tout, bool kComp>
+__global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const __grid_constant__ GathArgs a) {
+    gather_barriers_init(a.tile, a.jmax, sizeof(Tin), sizeof(Tout));
+    const DevTables tb{&a};
+    gather_body<Tin, Tout, kComp, false>(tb, a.ntiles, a.tile, a.jmax, a.grid, a.nchunk, a.cta, a.counter,
+                                         a.err);
+}
+
+// Tables in the parameters: a programmatic dependent launch (its set-up overlaps the
+// previous kernel's tail; nothing in global memory is touched before that kernel has
+// completed); units are single tiles, counted in p.slots[p.slot], and the other slot is
+// zeroed for the next launch.
+template <typename Tin, typename Tout, bool kComp>
+__global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_inline_kernel(
+    const __grid_constant__ GathInline p) {
+    gather_barriers_init(p.tile, p.jmax, sizeof(Tin), sizeof(Tout));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.slots[p.slot ^ 1u] = 0u;
+    const ParTables tb{&p};
+    gather_body<Tin, Tout, kComp, true>(tb, p.ntiles, p.tile, p.jmax, p.grid, p.ntiles, nullptr,
+                                        p.slots + p.slot, p.err);
+}
+
 // ----------------------------------------------------------------- host side
 template <typename Tin, typename Tout, bool kComp>
 cudaError_t prepare_gather(int* occ) {
@@ -275,8 +385,17 @@ cudaError_t prepare_gather(int* occ) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, reduce_gather_kernel<Tin, Tout, kComp>,
-                                                         kGatherThreads, smem);
+    e = cudaFuncSetAttribute(reduce_gather_inline_kernel<Tin, Tout, kComp>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int occ_inline = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_inline, reduce_gather_inline_kernel<Tin, Tout, kComp>,
+                                                      kGatherThreads, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, reduce_gather_kernel<Tin, Tout, kComp>,
+                                                      kGatherThreads, smem);
+    if (e == cudaSuccess) *occ = std::min(*occ, occ_inline);
+    return e;
 }
 
 template <typename Tin, typename Tout, bool kComp>
@@ -290,6 +409,21 @@ cudaError_t launch_gather_t(const GathArgs& a, cudaStream_t stream) {
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
     return cudaLaunchKernelEx(&cfg, reduce_gather_kernel<Tin, Tout, kComp>, a);
+}
+
+template <typename Tin, typename Tout, bool kComp>
+cudaError_t launch_inline_t(const GathInline& p, cudaStream_t stream) {
+    return launch_dependent(reduce_gather_inline_kernel<Tin, Tout, kComp>, p.grid, kGatherThreads,
+                            gather_smem_bytes(p.tile, p.jmax, sizeof(Tin), sizeof(Tout)), stream, p);
+}
+
+template <bool kComp>
+cudaError_t inline_pick(const GathInline& p, int din, int dout, cudaStream_t stream) {
+    if (din == 0)
+        return dout == 0 ? launch_inline_t<float, float, kComp>(p, stream)
+                         : launch_inline_t<float, uint16_t, kComp>(p, stream);
+    return dout == 0 ? launch_inline_t<uint16_t, float, kComp>(p, stream)
+                     : launch_inline_t<uint16_t, uint16_t, kComp>(p, stream);
 }
 
 template <bool kComp>
@@ -332,6 +466,20 @@ cudaError_t launch_gather_final(const GathArgs& a, int dtype_in, int dtype_out, 
         return cudaErrorInvalidValue;
     const int din = dtype_in == 0 ? 0 : 1, dout = dtype_out == 0 ? 0 : 1;
     return comp ? gather_pick<true>(a, din, dout, stream) : gather_pick<false>(a, din, dout, stream);
+}
+
+cudaError_t launch_gather_inline(const GathInline& p, int dtype_in, int dtype_out, bool comp,
+                                 const LaunchShape& s, cudaStream_t stream) {
+    if (p.nseg == 0 || p.ntiles == 0) return cudaSuccess;
+    uint32_t so = 0, bo = 0, wo = 0;
+    if (p.err == nullptr || p.slots == nullptr || p.slot > 1u || p.jmax == 0 ||
+        p.jmax > static_cast<uint32_t>(kMaxBatch) || p.tile != gather_tile(p.jmax, dtype_in, dtype_out) ||
+        p.grid != gather_grid(p.ntiles, dtype_in, dtype_out, comp, s) || p.grid == 0 ||
+        !gather_inline_layout(p.nseg, p.nsrc, p.nclient, &so, &bo, &wo) || so != p.src_off ||
+        bo != p.base_off || wo != p.w_off)
+        return cudaErrorInvalidValue;
+    const int din = dtype_in == 0 ? 0 : 1, dout = dtype_out == 0 ? 0 : 1;
+    return comp ? inline_pick<true>(p, din, dout, stream) : inline_pick<false>(p, din, dout, stream);
 }
 
 }  // namespace fa

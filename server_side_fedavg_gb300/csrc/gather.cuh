@@ -50,6 +50,59 @@ struct GathArgs {
     uint32_t nchunk;             // chunks of work (gather_chunks, >= grid)
 };
 
+// The same tables in compact form, carried in the launch's own parameters when a round is
+// small enough (gather_inline_layout): no upload before the launch and no table reads
+// from global memory in the kernel.  A reporter is a client (its base pointer and weight
+// in the client tables) and the key's element offset in that client's buffer.
+struct GathSegP {
+    void* out;          // destination of element 0 (dtype_out)
+    Divisor div;        // N_p
+    uint32_t len;       // elements of the key (< 2^32)
+    uint32_t tile0;     // first tile
+    uint16_t src0;      // first reporter in the reporter table
+    uint8_t J;          // reporters (1..16)
+    uint8_t vec_ok;     // 1: the output and every reporter's input are 16-byte aligned
+};
+static_assert(sizeof(GathSegP) == 32, "compact segment");
+
+struct GathSrcP {
+    uint32_t off;       // element offset of the key in the client's buffer (< 2^32)
+    uint32_t client;    // index into the client tables
+};
+
+constexpr uint32_t kGathInlineBlob = 32640;   // bytes of tables in the parameters
+
+struct GathInline {
+    unsigned int* err;          // the caller's device error word
+    uint32_t* slots;            // two device counter words of the caller's context
+    uint32_t slot;              // this launch counts tiles in slots[slot] (0 at launch) and
+                                // zeroes slots[slot ^ 1] for the next launch
+    uint32_t nseg;
+    uint32_t nsrc;
+    uint32_t nclient;
+    uint32_t ntiles;
+    uint32_t tile;              // elements per tile (gather_tile)
+    uint32_t jmax;
+    uint32_t grid;              // CTAs (gather_grid)
+    uint32_t src_off;           // byte offsets in blob: reporters, client bases, client weights
+    uint32_t base_off;          //   (the segments start at 0)
+    uint32_t w_off;
+    uint32_t pad;
+    alignas(16) uint8_t blob[kGathInlineBlob];
+};
+static_assert(sizeof(GathInline) <= 32764, "kernel parameters are limited to 32764 bytes");
+
+// Byte offsets of the reporter, client-base and client-weight tables in GathInline::blob
+// for nseg segments, nsrc reporters and nclient clients; false if they do not fit.
+bool gather_inline_layout(uint32_t nseg, uint32_t nsrc, uint32_t nclient, uint32_t* src_off,
+                          uint32_t* base_off, uint32_t* w_off);
+
+// Launches the subset reduce with its tables in the parameters, as a programmatic
+// dependent of the previous kernel on the stream.  The caller fills every field; the
+// tiles are handed out one by one from slots[slot].
+cudaError_t launch_gather_inline(const GathInline& p, int dtype_in, int dtype_out, bool comp,
+                                 const LaunchShape& s, cudaStream_t stream);
+
 // Round-level subset reduce: out = RNE(sum over the segment's reporters, in order, / N_p)
 // per segment, straight from the reporters' inputs (no running sum); comp: compensated
 // arithmetic (Dot2), the same operation sequence as every other path.  The caller picks

@@ -24,6 +24,19 @@ uint32_t gather_grid(uint32_t ntiles, int dtype_in, int dtype_out, bool comp, co
     return grid_for(ntiles, s.sms, per);
 }
 
+bool gather_inline_layout(uint32_t nseg, uint32_t nsrc, uint32_t nclient, uint32_t* src_off,
+                          uint32_t* base_off, uint32_t* w_off) {
+    const uint64_t so = static_cast<uint64_t>(nseg) * sizeof(GathSegP);
+    const uint64_t bo = so + static_cast<uint64_t>(nsrc) * sizeof(GathSrcP);
+    const uint64_t wo = bo + static_cast<uint64_t>(nclient) * sizeof(void*);
+    const uint64_t end = wo + static_cast<uint64_t>(nclient) * sizeof(float);
+    if (end > kGathInlineBlob || nsrc > 0xFFFFu) return false;
+    *src_off = static_cast<uint32_t>(so);
+    *base_off = static_cast<uint32_t>(bo);
+    *w_off = static_cast<uint32_t>(wo);
+    return true;
+}
+
 uint32_t gather_chunks(uint32_t ntiles, uint32_t grid) {
     uint32_t n = ntiles / 4;
     if (n > kMaxGatherChunks) n = kMaxGatherChunks;

@@ -199,3 +199,43 @@ def test_errors_leave_the_round_empty():
     finally:
         torch.cuda.synchronize()
         fa.fa_close(ctx)
+
+
+def _round_on(ctx, numels, din, dout, ids, weights, bufs, keys):
+    outs = [sentinel(n, dout) for n in numels]
+    fa.fa_reset(ctx)
+    fa.fa_reduce_subsets(ctx, ids, weights, bufs, keys, outs)
+    fa.fa_sync(ctx)
+    return [to_np(o, dout) for o in outs]
+
+
+@pytest.mark.parametrize("flags", [0, fa.FA_COMPENSATED])
+def test_both_table_forms_and_back_to_back_rounds(flags):
+    """A round whose tables fit the launch's parameters (a few keys per client) and one
+    that needs them in device memory (all 1200 keys from every client), alternating on one
+    context: each gives the per-client path's bits, every time.  Back-to-back small rounds
+    hand the tile counter from one launch to the next."""
+    rng = np.random.default_rng(41 + flags)
+    numels = [int(n) for n in rng.integers(1, 3000, 1200)]
+    numels[5] = 9000
+    K = 3
+    _, hosts = _random_round(rng, numels, K, "bf16", p_send=0.0)
+    few = [sorted(rng.choice(len(numels), 40, replace=False).tolist()) for _ in range(K)]
+    every = [list(range(len(numels))) for _ in range(K)]
+    ids = [2, 0, 1]
+    weights = [3.0, 1.0, 7.0]
+    want = {}
+    for name, keys in (("few", few), ("every", every)):
+        want[name], _ = _per_client(numels, "bf16", "bf16", ids, weights, hosts, keys, flags)
+    ctx = fa.fa_open(_layout(numels), "bf16", "bf16", K, flags=flags)
+    try:
+        bufs = {name: [_packed(hosts[j], keys[j]) for j in range(K)]
+                for name, keys in (("few", few), ("every", every))}
+        for name in ("few", "few", "every", "few", "every", "every", "few", "few", "few"):
+            keys = few if name == "few" else every
+            got = _round_on(ctx, numels, "bf16", "bf16", ids, weights, bufs[name], keys)
+            for p in range(len(numels)):
+                assert np.array_equal(got[p], want[name][p]), (name, p)
+    finally:
+        torch.cuda.synchronize()
+        fa.fa_close(ctx)
