@@ -1161,11 +1161,10 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
             gp.nsrc = static_cast<uint32_t>(n_entries);
             gp.nclient = n_clients;
             gp.jmax = jmax;
-            gp.tile = fa::gather_tile(jmax, c->din, c->dout);
+            gp.pad = 0;
             gp.src_off = so;
             gp.base_off = bo;
             gp.w_off = wo;
-            gp.pad = 0;
             auto* gs = reinterpret_cast<fa::GathSegP*>(gp.blob);
             auto* gr = reinterpret_cast<fa::GathSrcP*>(gp.blob + so);
             auto* gb = reinterpret_cast<const void**>(gp.blob + bo);
@@ -1183,7 +1182,8 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
                 bool ok = aligned(g.out);
                 for (uint32_t q = 0; q < g.J && ok; ++q) ok = aligned(src_x[g.src0 + q]);
                 g.vec_ok = ok ? 1u : 0u;
-                tiles += (it.numel + gp.tile - 1) / gp.tile;
+                const uint64_t tile = fa::gather_tile(g.J, c->din);
+                tiles += (it.numel + tile - 1) / tile;
             }
             if (tiles > 0xFFFFFFFFull) {
                 c->broken = true;
@@ -1197,6 +1197,7 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
                 gw[j] = static_cast<float>(weights[j]);
             }
             gp.grid = fa::gather_grid(gp.ntiles, c->din, c->dout, comp, c->shape);
+            gp.unit_tiles = fa::gather_unit_tiles(gp.ntiles, gp.grid);
             cudaError_t ce = fa::launch_gather_inline(gp, c->din, c->dout, comp, c->shape, s);
             if (ce != cudaSuccess) {
                 c->broken = true;
@@ -1254,15 +1255,14 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
     ga.err = c->err_dev;
     ga.nseg = nseg;
     ga.jmax = jmax;
-    ga.tile = fa::gather_tile(jmax, c->din, c->dout);
-    if (!fa::plan_gather_tiles(segs, nseg, ga.tile, &ga.ntiles)) {
+    if (!fa::plan_gather_tiles(segs, nseg, c->din, &ga.ntiles)) {
         c->broken = true;
         return fail(c, FA_ERR_RANGE, "layout too large for one subset reduce");
     }
     ga.grid = fa::gather_grid(ga.ntiles, c->din, c->dout, comp, c->shape);
     ga.nchunk = fa::gather_chunks(ga.ntiles, ga.grid);
     auto* cta = reinterpret_cast<uint32_t*>(c->gath_host + seg_bytes + src_bytes);
-    fa::plan_gather_ctas(segs, nseg, ga.tile, ga.ntiles, c->din, c->dout, ga.nchunk, cta);
+    fa::plan_gather_ctas(segs, nseg, ga.ntiles, c->din, c->dout, ga.nchunk, cta);
     // the chunk counter starts at 0: the word right after the chunk table, uploaded with
     // the tables in one copy
     const size_t counter_off = seg_bytes + src_bytes + 2 * sizeof(uint32_t) * (ga.nchunk + 1);

@@ -53,7 +53,7 @@ __device__ __forceinline__ void global_store8(void* out, uint64_t e, const float
     }
 }
 
-// Segments whose first tiles a finalize CTA keeps in shared memory (16 KB).
+// Segments whose first tiles a searching finalize CTA keeps in shared memory (16 KB).
 constexpr uint32_t kFinSegCache = 4096;
 
 // q = sum / N; delta rounds then add server_lr * q to the base with one rounding (fma).
@@ -84,7 +84,11 @@ __device__ __forceinline__ void fin_one(const FinSeg& sg, uint64_t e, const floa
     store_one<Tout>(sg.out, e, q);
 }
 
-template <typename Tout, bool kApply, bool kComp>
+// kSearch: the layout has many keys per grid stride (small keys), so each CTA keeps the
+// segments' first tiles in shared memory (up to kFinSegCache of them) and finds a tile's
+// segment by binary search; otherwise the table is walked in global memory, one step per
+// segment boundary crossed, which for large keys is rarely more than one step per tile.
+template <typename Tout, bool kApply, bool kComp, bool kSearch>
 __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restrict__ segs,
                                                           uint32_t nseg, uint32_t ntiles,
                                                           const float* __restrict__ acc,
@@ -92,27 +96,36 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
                                                           float lr) {
     constexpr int kVecPerTile = kTile / kVec;
     constexpr int kUnroll = kVecPerTile / kBlock;
-    // each segment's first tile, in shared memory when the table is small enough: a CTA
-    // strides gridDim.x tiles at a time, which can skip many small keys at once, and the
-    // search for the next tile's segment then costs shared-memory reads, not a chain of
-    // dependent global loads
-    __shared__ uint32_t t0s[kFinSegCache];
-    const bool cached = nseg <= kFinSegCache;
-    if (cached) {
-        for (uint32_t i = threadIdx.x; i < nseg; i += kBlock) t0s[i] = segs[i].tile0;
-        __syncthreads();
-    }
-    auto tile0_of = [&](uint32_t i) { return cached ? t0s[i] : segs[i].tile0; };
     uint32_t si = 0;
+    uint32_t next0 = nseg > 1 ? segs[1].tile0 : 0xFFFFFFFFu;   // first tile of segment si + 1
+    [[maybe_unused]] uint32_t* t0s = nullptr;
+    [[maybe_unused]] bool cached = false;
+    if constexpr (kSearch) {
+        __shared__ uint32_t t0_cache[kFinSegCache];
+        t0s = t0_cache;
+        cached = nseg <= kFinSegCache;
+        if (cached) {
+            for (uint32_t i = threadIdx.x; i < nseg; i += kBlock) t0s[i] = segs[i].tile0;
+            __syncthreads();
+        }
+    }
     for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        if (si + 1 < nseg && t >= tile0_of(si + 1)) {
-            // the last segment whose first tile is at or before t, in (si, nseg)
-            uint32_t lo = si + 1, hi = nseg;
-            while (hi - lo > 1) {
-                const uint32_t mid = (lo + hi) / 2;
-                if (tile0_of(mid) <= t) lo = mid; else hi = mid;
+        if constexpr (kSearch) {
+            if (t >= next0) {
+                // the last segment whose first tile is at or before t, in (si, nseg)
+                uint32_t lo = si + 1, hi = nseg;
+                while (hi - lo > 1) {
+                    const uint32_t mid = (lo + hi) / 2;
+                    if ((cached ? t0s[mid] : segs[mid].tile0) <= t) lo = mid; else hi = mid;
+                }
+                si = lo;
+                next0 = si + 1 < nseg ? (cached ? t0s[si + 1] : segs[si + 1].tile0) : 0xFFFFFFFFu;
             }
-            si = lo;
+        } else {
+            while (t >= next0) {
+                ++si;
+                next0 = si + 1 < nseg ? segs[si + 1].tile0 : 0xFFFFFFFFu;
+            }
         }
         const FinSeg sg = segs[si];
         const uint64_t e0 = static_cast<uint64_t>(t - sg.tile0) * kTile;
@@ -172,6 +185,8 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
 template <typename Tout, bool kApply, bool kComp>
 cudaError_t finalize_t(uint32_t grid, const FinSeg* segs, uint32_t nseg, uint32_t ntiles,
                        const float* acc, const float* acc_lo, float lr, cudaStream_t stream) {
+    // many keys per grid stride: search the segment table instead of walking it
+    const bool search = nseg > 1 && static_cast<uint64_t>(ntiles) < static_cast<uint64_t>(nseg) * grid;
     // a plain launch (no programmatic dependency: the kernel reads the sum from its
     // first instruction); the status is this launch's own
     cudaLaunchConfig_t cfg = {};
@@ -181,8 +196,10 @@ cudaError_t finalize_t(uint32_t grid, const FinSeg* segs, uint32_t nseg, uint32_
     cfg.stream = stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, finalize_kernel<Tout, kApply, kComp>, segs, nseg, ntiles, acc,
-                              acc_lo, lr);
+    return search ? cudaLaunchKernelEx(&cfg, finalize_kernel<Tout, kApply, kComp, true>, segs, nseg, ntiles,
+                                       acc, acc_lo, lr)
+                  : cudaLaunchKernelEx(&cfg, finalize_kernel<Tout, kApply, kComp, false>, segs, nseg, ntiles,
+                                       acc, acc_lo, lr);
 }
 
 template <bool kComp>
@@ -203,13 +220,13 @@ cudaError_t prepare_finalize_shapes_t(LaunchShape* s) {
     cudaError_t r = cudaSuccess;
     auto keep = [&r](cudaError_t x) { if (r == cudaSuccess) r = x; };
     keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->fin_ctas_per_sm[c][0][0],
-                                                       finalize_kernel<float, false, kComp>, kBlock, 0));
+                                                       finalize_kernel<float, false, kComp, false>, kBlock, 0));
     keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->fin_ctas_per_sm[c][0][1],
-                                                       finalize_kernel<uint16_t, false, kComp>, kBlock, 0));
+                                                       finalize_kernel<uint16_t, false, kComp, false>, kBlock, 0));
     keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->fin_ctas_per_sm[c][1][0],
-                                                       finalize_kernel<float, true, kComp>, kBlock, 0));
+                                                       finalize_kernel<float, true, kComp, false>, kBlock, 0));
     keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->fin_ctas_per_sm[c][1][1],
-                                                       finalize_kernel<uint16_t, true, kComp>, kBlock, 0));
+                                                       finalize_kernel<uint16_t, true, kComp, false>, kBlock, 0));
     return r;
 }
 

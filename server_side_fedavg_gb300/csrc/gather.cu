@@ -26,6 +26,7 @@ struct SegV {
     uint32_t src0;
     uint32_t tile0;
     uint32_t vec_ok;
+    uint32_t tile;      // elements per tile (gather_tile_for(J, s_in); set by the loader)
 };
 
 // Tables in device memory.
@@ -35,7 +36,7 @@ struct DevTables {
     __device__ __forceinline__ uint32_t tile0(uint32_t i) const { return a->segs[i].tile0; }
     __device__ __forceinline__ SegV seg(uint32_t i) const {
         const GathSeg& g = a->segs[i];
-        return SegV{g.len, g.out, g.div, g.J, g.src0, g.tile0, g.vec_ok};
+        return SegV{g.len, g.out, g.div, g.J, g.src0, g.tile0, g.vec_ok, 0u};
     }
     __device__ __forceinline__ const void* x(const SegV& s, uint32_t j, uint32_t) const {
         return a->src[s.src0 + j].x;
@@ -57,7 +58,7 @@ struct ParTables {
     __device__ __forceinline__ uint32_t tile0(uint32_t i) const { return g(i).tile0; }
     __device__ __forceinline__ SegV seg(uint32_t i) const {
         const GathSegP& s = g(i);
-        return SegV{s.len, s.out, s.div, s.J, s.src0, s.tile0, s.vec_ok};
+        return SegV{s.len, s.out, s.div, s.J, s.src0, s.tile0, s.vec_ok, 0u};
     }
     __device__ __forceinline__ const void* x(const SegV& s, uint32_t j, uint32_t s_in) const {
         const GathSrcP& q = r(s.src0 + j);
@@ -81,72 +82,104 @@ __device__ __forceinline__ void gath_one(const Tab& tb, const SegV& sg, uint64_t
     store_one<Tout>(sg.out, e, quotient_out<kComp, Tout>(r, rl, sg.div));
 }
 
-// Stage metadata: the tile held by an input stage or an output buffer and its segment,
-// or kNoTile once the CTA has no more work.  Written before the barrier that hands the
-// stage or buffer over, read after waiting on it.
+// What the compute warps need about a tile, written to shared memory by the loader
+// (which already holds the tile's segment and reporters in registers) before it hands
+// the stage over, so that the compute warps read no table per tile: t = kNoTile marks
+// the end of the CTA's work.
+struct TileMeta {
+    uint64_t e0;               // first element of the tile in its key
+    void* out;                 // the key's output (element 0)
+    Divisor div;               // N_p
+    uint32_t cnt;              // elements in the tile
+    uint32_t J;                // reporters
+    uint32_t vec;              // 1: bulk copies (aligned and at least kVec elements)
+    uint32_t t;                // tile index, or kNoTile
+    uint32_t si;               // segment
+    uint32_t xb;               // bytes of one reporter's tile in the stage
+    uint32_t pad[3];
+    float w[kMaxBatch];        // the reporters' weights, in order
+};
+static_assert(sizeof(TileMeta) % 16 == 0, "meta slots stay 16-byte aligned");
 constexpr uint32_t kNoTile = 0xFFFFFFFFu;
-constexpr int kGatherThreads = kBlock + 64;   // 8 compute warps, a loader and a storer warp
+// 16 compute warps, then a loader warp.  A tile's reduction is a chain of dependent
+// shared-memory loads and fmas per element (one reporter after another), so the compute
+// warps hide latency by numbers.
+constexpr int kGatherWarps = 16;
+constexpr int kGatherCompute = kGatherWarps * 32;
+constexpr int kGatherThreads = kGatherCompute + 32;
+constexpr uint32_t kMaxInlineSegs = kGathInlineBlob / sizeof(GathSegP);
 
-__host__ __device__ constexpr size_t gather_smem_bytes(uint32_t tile, uint32_t jmax, uint32_t s_in,
-                                                       uint32_t s_out) {
-    return static_cast<size_t>(tile) * (kGatherStages * jmax * s_in + kGatherOutBufs * s_out) +
-           (2 * kGatherStages + 2 * kGatherOutBufs) * sizeof(uint64_t) +
-           (kGatherStages + kGatherOutBufs) * sizeof(uint2);
+// Shared memory of a CTA: the input stages, the barriers (full / empty per stage), the
+// tile metadata (per stage) and, for inline tables, each segment's first tile
+// (nseg_cached entries).
+__host__ __device__ constexpr size_t gather_smem_bytes(uint32_t nseg_cached) {
+    return static_cast<size_t>(kGatherStages) * kGatherStageBytes + 2 * kGatherStages * sizeof(uint64_t) +
+           kGatherStages * sizeof(TileMeta) + nseg_cached * sizeof(uint32_t);
 }
 
-__device__ __forceinline__ TileAt tile_in(const SegV& sg, uint32_t si, uint32_t t, uint32_t T) {
+__device__ __forceinline__ TileAt tile_in(const SegV& sg, uint32_t si, uint32_t t) {
     TileAt r;
     r.si = si;
-    r.e0 = static_cast<uint64_t>(t - sg.tile0) * T;
+    r.e0 = static_cast<uint64_t>(t - sg.tile0) * sg.tile;
     const uint64_t rem = sg.len - r.e0;
-    r.cnt = rem < T ? static_cast<uint32_t>(rem) : T;
+    r.cnt = rem < sg.tile ? static_cast<uint32_t>(rem) : sg.tile;
     return r;
 }
 
-// Three roles per CTA, each waiting only on the barrier of the buffer it needs next:
-//  - the loader (one lane of warp 8) fills input stage s (jmax reporter tiles) with bulk
+// Eight results of dtype Tout (RNE for bf16) to a 16-byte aligned global address.
+template <typename Tout>
+__device__ __forceinline__ void store8_global(void* out, uint64_t e, const float (&q)[8]) {
+    if constexpr (sizeof(Tout) == 2) {
+        st_v4u(static_cast<uint16_t*>(out) + e,
+               make_uint4(pack_bf16(q[0], q[1]), pack_bf16(q[2], q[3]), pack_bf16(q[4], q[5]),
+                          pack_bf16(q[6], q[7])));
+    } else {
+        float* p = static_cast<float*>(out) + e;
+        st_v4f(p, make_float4(q[0], q[1], q[2], q[3]));
+        st_v4f(p + 4, make_float4(q[4], q[5], q[6], q[7]));
+    }
+}
+
+// Two roles per CTA:
+//  - the loader (one lane of warp 16) fills input stage s (jmax reporter tiles) with bulk
 //    loads once the compute warps have released it (empty[s]), arming full[s] with the
-//    byte count;
-//  - the compute warps (0-7) wait for full[s] and for output buffer o to be free
-//    (ofree[o]: its previous tile's store has read it), reduce the tile from stage s into
-//    buffer o, release the stage (empty[s]) and hand the buffer on (ofull[o]);
-//  - the storer (one lane of warp 9) writes buffer o to the output with one bulk store
-//    and frees it once the store has read it.
-// Stores therefore never delay the next loads.  Work is handed out dynamically, so that
-// CTAs that run faster (or start earlier) take more of the round and all finish
-// together: CTA b starts with unit b and then takes unit grid + atomicAdd(counter, 1)
-// until none is left, the loader asking for the next unit as soon as it starts one, so
-// the atomic's latency is hidden.  A unit is a chunk of about equal bytes planned on the
-// host (device tables: nchunk + 1 (first tile, segment) pairs) or a single tile, whose
-// segment the loader finds by a binary search over the parameter tables (inline tables).
+//    byte count and writing the tile's metadata;
+//  - the compute warps (0-15) wait for full[s], reduce the tile from stage s, write the
+//    results straight from registers with 16-byte stores (coalesced across each warp)
+//    and release the stage.
+// Work is handed out dynamically, so that CTAs that run faster (or start earlier) take
+// more of the round and all finish together: CTA b starts with unit b and then takes
+// unit grid + atomicAdd(counter, 1) until none is left; the loader keeps two such
+// requests in flight, so their latency is hidden behind the units before them.  A unit
+// is a chunk of about equal bytes planned on the host (device tables: nchunk + 1 (first
+// tile, segment) pairs) or unit_tiles consecutive tiles, whose first segment the loader
+// finds by a binary search over the segments' first tiles, copied to shared memory at
+// the start (inline tables).  Either way a CTA reads a segment's table entries once per
+// unit or key boundary, not per tile.
 template <typename Tin, typename Tout, bool kComp, bool kInline, typename Tab>
-__device__ __forceinline__ void gather_body(const Tab& tb, uint32_t ntiles, uint32_t T, uint32_t jmax,
-                                            uint32_t grid, uint32_t nunit, const uint32_t* cta,
-                                            uint32_t* counter, unsigned int* err) {
-    const uint32_t XB = T * sizeof(Tin);          // one reporter's input tile
-    const uint32_t IB = jmax * XB;                // one input stage
-    const uint32_t OB = T * sizeof(Tout);         // one output buffer
+__device__ __forceinline__ void gather_body(const Tab& tb, uint32_t grid, uint32_t nunit, uint32_t ntiles,
+                                            uint32_t unit_tiles, const uint32_t* cta, uint32_t* counter,
+                                            unsigned int* err) {
+    constexpr uint32_t IB = kGatherStageBytes;    // one input stage
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* ins = smem;
-    uint8_t* outs = smem + kGatherStages * IB;
-    uint64_t* full = reinterpret_cast<uint64_t*>(outs + kGatherOutBufs * OB);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGatherStages * IB);
     uint64_t* empty = full + kGatherStages;
-    uint64_t* ofull = empty + kGatherStages;
-    uint64_t* ofree = ofull + kGatherOutBufs;
-    uint2* meta = reinterpret_cast<uint2*>(ofree + kGatherOutBufs);
-    uint2* ometa = meta + kGatherStages;
+    TileMeta* meta = reinterpret_cast<TileMeta*>(empty + kGatherStages);
+    const uint32_t* t0s = reinterpret_cast<const uint32_t*>(meta + kGatherStages);
     const uint32_t warp = threadIdx.x / 32u, lane = threadIdx.x & 31u;
     const uint32_t nseg = tb.nseg();
 
-    if (warp == static_cast<uint32_t>(kReduceWarps)) {
+    if (warp == static_cast<uint32_t>(kGatherWarps)) {
         // ------------------------------------------------------------ loader
         if (lane != 0) return;
         uint32_t unit = blockIdx.x;            // < nunit: the host plans nunit >= grid
-        uint32_t next = grid < nunit ? grid + atomicAdd(counter, 1u) : nunit;
+        uint32_t q0 = grid < nunit ? grid + atomicAdd(counter, 1u) : nunit;
+        uint32_t q1 = grid < nunit ? grid + atomicAdd(counter, 1u) : nunit;
         uint32_t t, tend, cur;
         if constexpr (kInline) {
-            t = unit;
-            tend = unit + 1;
+            t = unit < nunit ? unit * unit_tiles : ntiles;
+            tend = t + unit_tiles < ntiles ? t + unit_tiles : ntiles;
             cur = 0;
         } else {
             t = cta[2 * unit];
@@ -157,20 +190,22 @@ __device__ __forceinline__ void gather_body(const Tab& tb, uint32_t ntiles, uint
         uint32_t have = 0xFFFFFFFFu, nt0 = 0;
         SegV sg{};
         const void* xp[kMaxBatch];
+        float wv[kMaxBatch];
         bool ok = true;
         uint32_t issued = 0;                   // tiles published to the stages
         for (;; ++issued) {
-            while (t == tend && next < nunit) {      // this unit is done: take the next one
-                unit = next;
+            while (t == tend && q0 < nunit) {        // this unit is done: take the next one
+                unit = q0;
+                q0 = q1;
+                q1 = grid + atomicAdd(counter, 1u);
                 if constexpr (kInline) {
-                    t = unit;
-                    tend = unit + 1;
+                    t = unit * unit_tiles;
+                    tend = t + unit_tiles < ntiles ? t + unit_tiles : ntiles;
                 } else {
                     t = cta[2 * unit];
                     cur = cta[2 * unit + 1];
                     tend = cta[2 * unit + 2];
                 }
-                next = grid + atomicAdd(counter, 1u);
             }
             const uint32_t s = issued % kGatherStages;
             if (issued >= static_cast<uint32_t>(kGatherStages)) {
@@ -178,8 +213,9 @@ __device__ __forceinline__ void gather_body(const Tab& tb, uint32_t ntiles, uint
                 if (!ok) break;
             }
             const uint32_t bar = smem_addr(&full[s]);
+            TileMeta& m = meta[s];
             if (t == tend) {                   // no work left: tell the compute warps
-                meta[s] = make_uint2(kNoTile, 0u);
+                m.t = kNoTile;
                 mbar_arrive(bar);
                 break;
             }
@@ -190,10 +226,10 @@ __device__ __forceinline__ void gather_body(const Tab& tb, uint32_t ntiles, uint
                     uint32_t lo = cur, hi = nseg;
                     while (hi - lo > 1) {
                         const uint32_t mid = (lo + hi) / 2;
-                        if (tb.tile0(mid) <= t) lo = mid; else hi = mid;
+                        if (t0s[mid] <= t) lo = mid; else hi = mid;
                     }
                     cur = lo;
-                    nt0 = cur + 1 < nseg ? tb.tile0(cur + 1) : 0xFFFFFFFFu;
+                    nt0 = cur + 1 < nseg ? t0s[cur + 1] : 0xFFFFFFFFu;
                 }
             } else {
                 if (cur != have) nt0 = cur + 1 < nseg ? tb.tile0(cur + 1) : 0xFFFFFFFFu;
@@ -204,16 +240,32 @@ __device__ __forceinline__ void gather_body(const Tab& tb, uint32_t ntiles, uint
             }
             if (cur != have) {
                 sg = tb.seg(cur);
+                sg.tile = gather_tile_for(sg.J, sizeof(Tin));
 #pragma unroll
-                for (int jj = 0; jj < kMaxBatch; ++jj)
-                    xp[jj] = jj < static_cast<int>(sg.J) ? tb.x(sg, jj, sizeof(Tin)) : nullptr;
+                for (int jj = 0; jj < kMaxBatch; ++jj) {
+                    const bool in = jj < static_cast<int>(sg.J);
+                    xp[jj] = in ? tb.x(sg, jj, sizeof(Tin)) : nullptr;
+                    wv[jj] = in ? tb.w(sg, jj) : 0.0f;
+                }
                 have = cur;
             }
-            meta[s] = make_uint2(t, cur);
-            const TileAt ta = tile_in(sg, cur, t, T);
+            const TileAt ta = tile_in(sg, cur, t);
+            const uint32_t XB = sg.tile * sizeof(Tin);    // one reporter's tile in the stage
             const uint32_t n8 = ta.cnt / kVec;
+            const bool bulk = sg.vec_ok && n8 > 0;
+            m.e0 = ta.e0;
+            m.out = sg.out;
+            m.div = sg.div;
+            m.cnt = ta.cnt;
+            m.J = sg.J;
+            m.vec = bulk ? 1u : 0u;
+            m.t = t;
+            m.si = cur;
+            m.xb = XB;
+#pragma unroll
+            for (int jj = 0; jj < kMaxBatch; ++jj) m.w[jj] = wv[jj];
             ++t;
-            if (sg.vec_ok && n8 > 0) {
+            if (bulk) {
                 const uint32_t xb = n8 * kVec * sizeof(Tin);
                 mbar_expect(bar, sg.J * xb);
                 uint8_t* st = ins + s * IB;
@@ -236,61 +288,26 @@ __device__ __forceinline__ void gather_body(const Tab& tb, uint32_t ntiles, uint
         return;
     }
 
-    if (warp == static_cast<uint32_t>(kReduceWarps) + 1u) {
-        // ------------------------------------------------------------ storer
-        if (lane != 0) return;
-        bool ok = true;
-        for (uint32_t i = 0;; ++i) {
-            const uint32_t o = i % kGatherOutBufs;
-            ok = mbar_wait(smem_addr(&ofull[o]), (i / kGatherOutBufs) & 1u);
-            if (!ok) break;
-            const uint2 m = ometa[o];
-            if (m.x == kNoTile) break;
-            const SegV sg = tb.seg(m.y);
-            const TileAt ta = tile_in(sg, m.y, m.x, T);
-            const uint32_t n8 = (sg.vec_ok && ta.cnt >= static_cast<uint32_t>(kVec)) ? ta.cnt / kVec : 0u;
-            if (n8 > 0) {
-                bulk_store(static_cast<Tout*>(sg.out) + ta.e0, outs + o * OB, n8 * kVec * sizeof(Tout));
-                bulk_commit();
-                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            }
-            mbar_arrive(smem_addr(&ofree[o]));
-        }
-        if (!ok) atomicOr(err, kErrWaitTimeout);
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        return;
-    }
-
     // ---------------------------------------------------------------- compute warps
     for (uint32_t i = 0;; ++i) {
-        const uint32_t s = i % kGatherStages, o = i % kGatherOutBufs;
+        const uint32_t s = i % kGatherStages;
         if (!mbar_wait(smem_addr(&full[s]), (i / kGatherStages) & 1u)) {
             atomicOr(err, kErrWaitTimeout);
             break;
         }
-        const uint2 m = meta[s];
-        if (i >= static_cast<uint32_t>(kGatherOutBufs) &&
-            !mbar_wait(smem_addr(&ofree[o]), ((i / kGatherOutBufs) - 1) & 1u)) {
-            atomicOr(err, kErrWaitTimeout);
-            break;
-        }
-        if (m.x == kNoTile) {                  // no more tiles: tell the storer
-            if (threadIdx.x == 0) ometa[o] = m;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ofull[o]));
-            break;
-        }
-        const SegV sg = tb.seg(m.y);
-        const TileAt ta = tile_in(sg, m.y, m.x, T);
-        const bool bulk = sg.vec_ok && ta.cnt >= static_cast<uint32_t>(kVec);
-        const uint32_t n8 = bulk ? ta.cnt / kVec : 0;
+        const TileMeta& m = meta[s];
+        if (m.t == kNoTile) break;
+        const uint32_t J = m.J, cnt = m.cnt, XB = m.xb;
+        const uint64_t e0 = m.e0;
         const uint8_t* st = ins + s * IB;
-        uint8_t* res = outs + o * OB;
-        if (bulk) {
+        if (m.vec) {
+            const uint32_t n8 = cnt / kVec;
+            const Divisor div = m.div;
+            void* out = m.out;
             float wv[kMaxBatch];
 #pragma unroll
-            for (int j = 0; j < kMaxBatch; ++j) wv[j] = j < static_cast<int>(sg.J) ? tb.w(sg, j) : 0.0f;
-            for (uint32_t v = threadIdx.x; v < n8; v += kBlock) {
+            for (int j = 0; j < kMaxBatch; ++j) wv[j] = m.w[j];
+            for (uint32_t v = threadIdx.x; v < n8; v += kGatherCompute) {
                 float r[8], rl[8];
                 {
                     float xv[8];
@@ -300,65 +317,58 @@ __device__ __forceinline__ void gather_body(const Tab& tb, uint32_t ntiles, uint
                 }
 #pragma unroll
                 for (int j = 1; j < kMaxBatch; ++j) {
-                    if (j >= static_cast<int>(sg.J)) break;
+                    if (j >= static_cast<int>(J)) break;
                     float xv[8];
                     smem_vec8<Tin>(st + j * XB, v, xv);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) contrib_add<kComp>(wv[j], xv[e], r[e], rl[e]);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) r[e] = quotient_out<kComp, Tout>(r[e], rl[e], sg.div);
-                smem_store8<Tout>(res, v, r);
+                for (int e = 0; e < 8; ++e) r[e] = quotient_out<kComp, Tout>(r[e], rl[e], div);
+                store8_global<Tout>(out, e0 + static_cast<uint64_t>(v) * kVec, r);
             }
-            const uint32_t tail = ta.cnt - n8 * kVec;
-            if (threadIdx.x < tail) gath_one<Tin, Tout, kComp>(tb, sg, ta.e0 + n8 * kVec + threadIdx.x);
+            const uint32_t tail = cnt - n8 * kVec;
+            if (threadIdx.x < tail) {
+                const SegV sg = tb.seg(m.si);
+                gath_one<Tin, Tout, kComp>(tb, sg, e0 + n8 * kVec + threadIdx.x);
+            }
         } else {
-            for (uint32_t e = threadIdx.x; e < ta.cnt; e += kBlock)
-                gath_one<Tin, Tout, kComp>(tb, sg, ta.e0 + e);
+            const SegV sg = tb.seg(m.si);
+            for (uint32_t e = threadIdx.x; e < cnt; e += kGatherCompute)
+                gath_one<Tin, Tout, kComp>(tb, sg, e0 + e);
         }
-        if (threadIdx.x == 0) ometa[o] = m;
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(smem_addr(&empty[s]));
-            mbar_arrive(smem_addr(&ofull[o]));
-        }
+        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     }
 }
 
-// The barriers of one CTA (full / empty per input stage, ofull / ofree per output buffer),
-// at the end of the stage buffers.
-__device__ __forceinline__ void gather_barriers_init(uint32_t T, uint32_t jmax, uint32_t s_in,
-                                                     uint32_t s_out) {
+// The barriers of one CTA and, for inline tables, the segments' first tiles in shared
+// memory (nseg_cached entries read through tb).
+template <typename Tab>
+__device__ __forceinline__ void gather_setup(const Tab& tb, uint32_t nseg_cached) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(T) *
-                                                 (kGatherStages * jmax * s_in + kGatherOutBufs * s_out));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kGatherStages) * kGatherStageBytes);
     uint64_t* empty = full + kGatherStages;
-    uint64_t* ofull = empty + kGatherStages;
-    uint64_t* ofree = ofull + kGatherOutBufs;
+    uint32_t* t0s = reinterpret_cast<uint32_t*>(reinterpret_cast<TileMeta*>(empty + kGatherStages) +
+                                                kGatherStages);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGatherStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s])) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[s])),
-                         "r"(kReduceWarps) : "memory");
-        }
-        for (int o = 0; o < kGatherOutBufs; ++o) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&ofull[o])),
-                         "r"(kReduceWarps) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&ofree[o])) : "memory");
+                         "r"(kGatherWarps) : "memory");
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    for (uint32_t i = threadIdx.x; i < nseg_cached; i += blockDim.x) t0s[i] = tb.tile0(i);
     __syncthreads();
 }
 
 // Tables in device memory: a plain launch after their upload; units are the planned chunks.
 template <typename Tin, typename Tout, bool kComp>
 __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const __grid_constant__ GathArgs a) {
-    gather_barriers_init(a.tile, a.jmax, sizeof(Tin), sizeof(Tout));
     const DevTables tb{&a};
-    gather_body<Tin, Tout, kComp, false>(tb, a.ntiles, a.tile, a.jmax, a.grid, a.nchunk, a.cta, a.counter,
-                                         a.err);
+    gather_setup(tb, 0u);
+    gather_body<Tin, Tout, kComp, false>(tb, a.grid, a.nchunk, a.ntiles, 0u, a.cta, a.counter, a.err);
 }
 
 // Tables in the parameters: a programmatic dependent launch (its set-up overlaps the
@@ -368,19 +378,18 @@ __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const 
 template <typename Tin, typename Tout, bool kComp>
 __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_inline_kernel(
     const __grid_constant__ GathInline p) {
-    gather_barriers_init(p.tile, p.jmax, sizeof(Tin), sizeof(Tout));
+    const ParTables tb{&p};
+    gather_setup(tb, p.nseg);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0) p.slots[p.slot ^ 1u] = 0u;
-    const ParTables tb{&p};
-    gather_body<Tin, Tout, kComp, true>(tb, p.ntiles, p.tile, p.jmax, p.grid, p.ntiles, nullptr,
-                                        p.slots + p.slot, p.err);
+    gather_body<Tin, Tout, kComp, true>(tb, p.grid, (p.ntiles + p.unit_tiles - 1) / p.unit_tiles, p.ntiles,
+                                        p.unit_tiles, nullptr, p.slots + p.slot, p.err);
 }
 
 // ----------------------------------------------------------------- host side
 template <typename Tin, typename Tout, bool kComp>
 cudaError_t prepare_gather(int* occ) {
-    // the largest stage set any tile size picks (gather_tile keeps every one within it)
-    const size_t smem = kGatherSmemBudget + gather_smem_bytes(0, 0, 0, 0);
+    const size_t smem = gather_smem_bytes(kMaxInlineSegs);
     cudaError_t e = cudaFuncSetAttribute(reduce_gather_kernel<Tin, Tout, kComp>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -400,7 +409,7 @@ cudaError_t prepare_gather(int* occ) {
 
 template <typename Tin, typename Tout, bool kComp>
 cudaError_t launch_gather_t(const GathArgs& a, cudaStream_t stream) {
-    const size_t smem = gather_smem_bytes(a.tile, a.jmax, sizeof(Tin), sizeof(Tout));
+    const size_t smem = gather_smem_bytes(0u);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.grid);
     cfg.blockDim = dim3(kGatherThreads);
@@ -414,7 +423,7 @@ cudaError_t launch_gather_t(const GathArgs& a, cudaStream_t stream) {
 template <typename Tin, typename Tout, bool kComp>
 cudaError_t launch_inline_t(const GathInline& p, cudaStream_t stream) {
     return launch_dependent(reduce_gather_inline_kernel<Tin, Tout, kComp>, p.grid, kGatherThreads,
-                            gather_smem_bytes(p.tile, p.jmax, sizeof(Tin), sizeof(Tout)), stream, p);
+                            gather_smem_bytes(p.nseg), stream, p);
 }
 
 template <bool kComp>
@@ -460,7 +469,6 @@ cudaError_t launch_gather_final(const GathArgs& a, int dtype_in, int dtype_out, 
     if (a.nseg == 0 || a.ntiles == 0) return cudaSuccess;
     if (a.err == nullptr || a.segs == nullptr || a.src == nullptr || a.cta == nullptr ||
         a.counter == nullptr || a.jmax == 0 || a.jmax > static_cast<uint32_t>(kMaxBatch) ||
-        a.tile != gather_tile(a.jmax, dtype_in, dtype_out) ||
         a.grid != gather_grid(a.ntiles, dtype_in, dtype_out, comp, s) || a.grid == 0 ||
         a.nchunk < a.grid || a.nchunk > a.ntiles)
         return cudaErrorInvalidValue;
@@ -472,8 +480,9 @@ cudaError_t launch_gather_inline(const GathInline& p, int dtype_in, int dtype_ou
                                  const LaunchShape& s, cudaStream_t stream) {
     if (p.nseg == 0 || p.ntiles == 0) return cudaSuccess;
     uint32_t so = 0, bo = 0, wo = 0;
-    if (p.err == nullptr || p.slots == nullptr || p.slot > 1u || p.jmax == 0 ||
-        p.jmax > static_cast<uint32_t>(kMaxBatch) || p.tile != gather_tile(p.jmax, dtype_in, dtype_out) ||
+    if (p.err == nullptr || p.slots == nullptr || p.slot > 1u || p.jmax == 0 || p.nseg > kMaxInlineSegs ||
+        p.unit_tiles == 0 ||
+        p.jmax > static_cast<uint32_t>(kMaxBatch) ||
         p.grid != gather_grid(p.ntiles, dtype_in, dtype_out, comp, s) || p.grid == 0 ||
         !gather_inline_layout(p.nseg, p.nsrc, p.nclient, &so, &bo, &wo) || so != p.src_off ||
         bo != p.base_off || wo != p.w_off)

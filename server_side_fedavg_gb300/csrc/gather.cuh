@@ -9,11 +9,20 @@
 
 namespace fa {
 
-// kGatherStages input stages (jmax reporter tiles each) and kGatherOutBufs output tiles,
-// kGatherSmemBudget bytes in all (the tile size is chosen to fit; see gather_tile).
+// kGatherStages input stages of kGatherStageBytes each.  A tile of a key with J reporters
+// holds gather_tile(J, dtype_in) elements: the most that J reporter tiles fit in one
+// stage (a multiple of 256), so keys with fewer reporters take longer tiles and a round
+// has as few tiles as its bytes allow.
 constexpr int kGatherStages = 3;
-constexpr int kGatherOutBufs = 2;
-constexpr int kGatherSmemBudget = 221184;
+constexpr int kGatherStageBytes = 73728;
+
+// Elements per tile of a key with J reporters of s_in bytes each (host and device).
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr uint32_t gather_tile_for(uint32_t J, uint32_t s_in) {
+    return (kGatherStageBytes / ((J ? J : 1u) * s_in)) / 256u * 256u;
+}
 
 // Round-level reduce of client key subsets (fa_reduce_subsets): one segment per key to
 // write, each with its own reporters.  Reporter j of segment s is src[s.src0 + j], in the
@@ -44,7 +53,6 @@ struct GathArgs {
     unsigned int* err;           // the caller's device error word
     uint32_t nseg;
     uint32_t ntiles;             // tiles over all segments (plan_gather_tiles)
-    uint32_t tile;               // elements per tile (gather_tile)
     uint32_t jmax;               // largest J over the segments (1..16)
     uint32_t grid;               // CTAs (gather_grid)
     uint32_t nchunk;             // chunks of work (gather_chunks, >= grid)
@@ -81,13 +89,13 @@ struct GathInline {
     uint32_t nsrc;
     uint32_t nclient;
     uint32_t ntiles;
-    uint32_t tile;              // elements per tile (gather_tile)
+    uint32_t pad;
     uint32_t jmax;
     uint32_t grid;              // CTAs (gather_grid)
     uint32_t src_off;           // byte offsets in blob: reporters, client bases, client weights
     uint32_t base_off;          //   (the segments start at 0)
     uint32_t w_off;
-    uint32_t pad;
+    uint32_t unit_tiles;        // tiles per unit of work (gather_unit_tiles)
     alignas(16) uint8_t blob[kGathInlineBlob];
 };
 static_assert(sizeof(GathInline) <= 32764, "kernel parameters are limited to 32764 bytes");
@@ -97,24 +105,31 @@ static_assert(sizeof(GathInline) <= 32764, "kernel parameters are limited to 327
 bool gather_inline_layout(uint32_t nseg, uint32_t nsrc, uint32_t nclient, uint32_t* src_off,
                           uint32_t* base_off, uint32_t* w_off);
 
+// Tiles per unit of work of an inline launch: consecutive tiles, so that a CTA reads a
+// segment's entries from the tables once per unit (or key boundary), not once per tile,
+// while about eight units per CTA keep the hand-out balanced.
+uint32_t gather_unit_tiles(uint32_t ntiles, uint32_t grid);
+
 // Launches the subset reduce with its tables in the parameters, as a programmatic
-// dependent of the previous kernel on the stream.  The caller fills every field; the
-// tiles are handed out one by one from slots[slot].
+// dependent of the previous kernel on the stream.  The caller fills every field; units
+// of unit_tiles consecutive tiles are handed out from slots[slot].
 cudaError_t launch_gather_inline(const GathInline& p, int dtype_in, int dtype_out, bool comp,
                                  const LaunchShape& s, cudaStream_t stream);
 
 // Round-level subset reduce: out = RNE(sum over the segment's reporters, in order, / N_p)
 // per segment, straight from the reporters' inputs (no running sum); comp: compensated
-// arithmetic (Dot2), the same operation sequence as every other path.  The caller picks
-// tile = gather_tile(jmax, ...), numbers the tiles of its host copy of the segment table
-// with plan_gather_tiles, takes grid = gather_grid(...) and nchunk = gather_chunks(...),
-// splits the tiles into chunks with plan_gather_ctas, uploads the three tables and a
-// zero counter word, and launches with a.tile, a.ntiles, a.grid and a.nchunk set.  Each
-// CTA starts with chunk blockIdx.x and takes further chunks from the counter.
-uint32_t gather_tile(uint32_t jmax, int dtype_in, int dtype_out);
-// Sets tile0 of every segment for `tile` elements per tile; false if there would be more
-// than 2^32 - 1 tiles.
-bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t* ntiles);
+// arithmetic (Dot2), the same operation sequence as every other path.  The caller numbers
+// the tiles of its host copy of the segment table with plan_gather_tiles, takes
+// grid = gather_grid(...) and nchunk = gather_chunks(...), splits the tiles into chunks
+// with plan_gather_ctas, uploads the three tables and a zero counter word, and launches
+// with a.ntiles, a.grid and a.nchunk set.  Each CTA starts with chunk blockIdx.x and
+// takes further chunks from the counter.
+// Elements per tile of a key with J reporters (gather_tile_for).
+uint32_t gather_tile(uint32_t J, int dtype_in);
+// Sets tile0 of every segment (each segment's tiles of gather_tile(J, dtype_in)
+// elements, numbered across the segments in order); false if there would be more than
+// 2^32 - 1 tiles.
+bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, int dtype_in, uint32_t* ntiles);
 // CTAs of a subset-reduce launch over ntiles tiles (a persistent grid, at most one
 // resident wave).
 uint32_t gather_grid(uint32_t ntiles, int dtype_in, int dtype_out, bool comp, const LaunchShape& s);
@@ -123,13 +138,13 @@ uint32_t gather_grid(uint32_t ntiles, int dtype_in, int dtype_out, bool comp, co
 constexpr uint32_t kMaxGatherChunks = 65536;
 uint32_t gather_chunks(uint32_t ntiles, uint32_t grid);
 // Splits tiles [0, ntiles) into `grid` contiguous runs (chunks) of about equal HBM bytes
-// (a tile of segment s moves cnt * (J_s * s_in + s_out) bytes), so that keys with more
-// reporters do not weigh more per chunk.  Writes grid + 1 pairs to cta: cta[2b] is chunk
+// (a tile of segment s moves cnt * (J_s * s_in + s_out) bytes, cnt up to that segment's
+// tile size), so that keys with more reporters do not weigh more per chunk.  Writes grid + 1 pairs to cta: cta[2b] is chunk
 // b's first tile (0 for b = 0, ntiles for b = grid, and in between the first tile whose
 // preceding bytes reach b / grid of the total), cta[2b + 1] the last segment whose first
 // tile is at or before it.  Segments numbered by plan_gather_tiles.
-void plan_gather_ctas(const GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t ntiles,
-                      int dtype_in, int dtype_out, uint32_t grid, uint32_t* cta);
+void plan_gather_ctas(const GathSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_in,
+                      int dtype_out, uint32_t grid, uint32_t* cta);
 cudaError_t launch_gather_final(const GathArgs& a, int dtype_in, int dtype_out, bool comp,
                                 const LaunchShape& s, cudaStream_t stream);
 

@@ -6,17 +6,18 @@
 
 namespace fa {
 
-uint32_t gather_tile(uint32_t jmax, int dtype_in, int dtype_out) {
-    // the largest multiple of 256 elements whose input stages (jmax reporter tiles each)
-    // and output buffers fit kGatherSmemBudget
-    const uint32_t eb = kGatherStages * jmax * (dtype_in == 0 ? 4u : 2u) +
-                        kGatherOutBufs * (dtype_out == 0 ? 4u : 2u);
-    const uint32_t t = kGatherSmemBudget / eb / 256 * 256;
-    return t < 256 ? 256 : t;
-}
+uint32_t gather_tile(uint32_t J, int dtype_in) { return gather_tile_for(J, dtype_in == 0 ? 4u : 2u); }
 
-bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t* ntiles) {
-    return number_tiles(segs, nseg, tile, ntiles);
+bool plan_gather_tiles(GathSeg* segs, uint32_t nseg, int dtype_in, uint32_t* ntiles) {
+    uint64_t t = 0;
+    for (uint32_t i = 0; i < nseg; ++i) {
+        const uint64_t tile = gather_tile(segs[i].J, dtype_in);
+        segs[i].tile0 = static_cast<uint32_t>(t);
+        t += (segs[i].len + tile - 1) / tile;
+        if (t > 0xFFFFFFFFull) return false;
+    }
+    *ntiles = static_cast<uint32_t>(t);
+    return true;
 }
 
 uint32_t gather_grid(uint32_t ntiles, int dtype_in, int dtype_out, bool comp, const LaunchShape& s) {
@@ -37,6 +38,11 @@ bool gather_inline_layout(uint32_t nseg, uint32_t nsrc, uint32_t nclient, uint32
     return true;
 }
 
+uint32_t gather_unit_tiles(uint32_t ntiles, uint32_t grid) {
+    const uint64_t per = grid ? ntiles / (8ull * grid) : 1;
+    return per < 1 ? 1u : static_cast<uint32_t>(per);
+}
+
 uint32_t gather_chunks(uint32_t ntiles, uint32_t grid) {
     uint32_t n = ntiles / 4;
     if (n > kMaxGatherChunks) n = kMaxGatherChunks;
@@ -44,8 +50,8 @@ uint32_t gather_chunks(uint32_t ntiles, uint32_t grid) {
     return n < ntiles ? n : ntiles;
 }
 
-void plan_gather_ctas(const GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_t ntiles,
-                      int dtype_in, int dtype_out, uint32_t grid, uint32_t* cta) {
+void plan_gather_ctas(const GathSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_in,
+                      int dtype_out, uint32_t grid, uint32_t* cta) {
     // exact integer arithmetic: boundary b (1..grid-1) is the first tile t whose preceding
     // bytes P(t) satisfy P(t) * grid >= total * b; tiles of one segment cost the same
     // except its last (ragged) one, so each boundary is found by one division
@@ -62,7 +68,7 @@ void plan_gather_ctas(const GathSeg* segs, uint32_t nseg, uint32_t tile, uint32_
         const u128 per = g.J * si + so;                 // bytes per element of this segment
         const u128 end = before + static_cast<u128>(g.len) * per;
         if (nt > 0) {
-            const u128 c = static_cast<u128>(tile) * per;   // bytes of a full tile
+            const u128 c = static_cast<u128>(gather_tile(g.J, dtype_in)) * per;   // bytes of a full tile
             while (b < grid && end * grid > total * b) {
                 const u128 want = total * b, have = before * grid;
                 const u128 k = want > have ? (want - have + c * grid - 1) / (c * grid) : 0;

@@ -8,25 +8,22 @@
 
 extern "C" {
 
-// Segments of lens[i] elements with J[i] reporters each; tiles of gather_tile(jmax, din,
-// dout) elements.  Writes the tile size, the tile count, each segment's first tile and
-// the grid + 1 (first tile, segment) pairs of the CTA split.  Returns 0, or -1 if the
-// tiles do not fit 32 bits.
+// Segments of lens[i] elements with J[i] reporters each, tiles of gather_tile(J[i], din)
+// elements.  Writes each segment's tile size and first tile, the tile count and the
+// grid + 1 (first tile, segment) pairs of the CTA split.  Returns 0, or -1 if the tiles
+// do not fit 32 bits.
 int32_t gp_plan(const uint64_t* lens, const uint32_t* J, uint32_t nseg, int din, int dout,
-                uint32_t grid, uint32_t* tile, uint32_t* ntiles, uint32_t* tile0,
-                uint32_t* cta) {
+                uint32_t grid, uint32_t* tiles, uint32_t* ntiles, uint32_t* tile0, uint32_t* cta) {
     std::vector<fa::GathSeg> segs(nseg);
-    uint32_t jmax = 1;
     for (uint32_t i = 0; i < nseg; ++i) {
         segs[i] = fa::GathSeg{};
         segs[i].len = lens[i];
         segs[i].J = J[i];
-        if (J[i] > jmax) jmax = J[i];
+        tiles[i] = fa::gather_tile(J[i], din);
     }
-    *tile = fa::gather_tile(jmax, din, dout);
-    if (!fa::plan_gather_tiles(segs.data(), nseg, *tile, ntiles)) return -1;
+    if (!fa::plan_gather_tiles(segs.data(), nseg, din, ntiles)) return -1;
     for (uint32_t i = 0; i < nseg; ++i) tile0[i] = segs[i].tile0;
-    fa::plan_gather_ctas(segs.data(), nseg, *tile, *ntiles, din, dout, grid, cta);
+    fa::plan_gather_ctas(segs.data(), nseg, *ntiles, din, dout, grid, cta);
     return 0;
 }
 

@@ -1,6 +1,7 @@
 """Host planning of a subset-reduce launch (the round-level adapter reduce): the tiles
-of every key written are numbered in order and split into chunks -- contiguous runs of
-about equal HBM bytes, each tile of key p moving cnt * (J_p * s_in + s_out) bytes, each
+of every key written are numbered in order (a key with J reporters in tiles of the most
+elements that J reporter tiles fit in one stage) and split into chunks -- contiguous runs
+of about equal HBM bytes, each tile of key p moving cnt * (J_p * s_in + s_out) bytes, each
 chunk told the key its first tile is in -- which the persistent CTAs take one by one.  Checked against a brute-force walk over every tile
 in exact integers, and for the properties the kernel relies on (a monotone split that
 starts at tile 0 and ends at the last tile)."""
@@ -45,10 +46,10 @@ def plan(lens, J, din, dout, grid):
     lens = np.ascontiguousarray(lens, np.uint64)
     J = np.ascontiguousarray(J, np.uint32)
     n = len(lens)
-    tile, ntiles = ctypes.c_uint32(), ctypes.c_uint32()
+    tiles, ntiles = np.zeros(max(1, n), np.uint32), ctypes.c_uint32()
     tile0 = np.zeros(max(1, n), np.uint32)
     pairs = np.zeros(2 * (grid + 1), np.uint32)
-    st = lib().gp_plan(lens.ctypes.data, J.ctypes.data, n, din, dout, grid, ctypes.byref(tile),
+    st = lib().gp_plan(lens.ctypes.data, J.ctypes.data, n, din, dout, grid, tiles.ctypes.data,
                        ctypes.byref(ntiles), tile0.ctypes.data, pairs.ctypes.data)
     assert st == 0
     cta, seg = pairs[0::2], pairs[1::2]
@@ -56,15 +57,24 @@ def plan(lens, J, din, dout, grid):
     # the CTA's first tile (where the kernel's forward walk over the table begins)
     for f, sg in zip(cta, seg):
         assert sg == max(i for i in range(n) if tile0[i] <= f), (f, sg)
-    return tile.value, ntiles.value, tile0[:n], cta
+    return tiles[:n], ntiles.value, tile0[:n], cta
 
 
-def tile_bytes(lens, J, tile, din, dout):
+STAGE_BYTES = 73728
+
+
+def tile_for(j, din):
+    """Elements per tile of a key with j reporters: the most that j reporter tiles fit in
+    one 73,728-byte stage, a multiple of 256."""
+    return STAGE_BYTES // (j * (4 if din == 0 else 2)) // 256 * 256
+
+
+def tile_bytes(lens, J, tiles, din, dout):
     """Bytes of every tile in order (exact integers)."""
     si, so = (4 if din == 0 else 2), (4 if dout == 0 else 2)
     out = []
-    for n, j in zip(lens, J):
-        n = int(n)
+    for n, j, tile in zip(lens, J, tiles):
+        n, tile = int(n), int(tile)
         full, rem = divmod(n, tile)
         out += [tile * (int(j) * si + so)] * full
         if rem:
@@ -98,12 +108,26 @@ CASES = [
 
 @pytest.mark.parametrize("lens,J,din,dout,grid", CASES)
 def test_split_matches_the_brute_force_definition(lens, J, din, dout, grid):
-    tile, ntiles, tile0, cta = plan(lens, J, din, dout, grid)
-    cost = tile_bytes(lens, J, tile, din, dout)
+    tiles, ntiles, tile0, cta = plan(lens, J, din, dout, grid)
+    assert list(tiles) == [tile_for(j, din) for j in J]
+    cost = tile_bytes(lens, J, tiles, din, dout)
     assert ntiles == len(cost)
-    starts = np.cumsum([0] + [-(-int(n) // tile) for n in lens])[:-1]
+    starts = np.cumsum([0] + [-(-int(n) // int(t)) for n, t in zip(lens, tiles)])[:-1]
     assert list(tile0) == list(starts)
     assert list(cta) == brute_split(cost, grid)
+
+
+def test_tile_sizes():
+    # a stage holds J reporter tiles: bf16 in, J = 8 -> 4608 elements (8 x 9,216 B), J = 1
+    # -> 36,864, J = 16 -> 2304; fp32 in, J = 16 -> 1024 (16 x 4,096 B), J = 3 -> 6144
+    tiles, _, _, _ = plan([10, 10, 10], [8, 1, 16], 1, 1, 1)
+    assert list(tiles) == [4608, 36864, 2304]
+    tiles, _, _, _ = plan([10, 10], [16, 3], 0, 0, 1)
+    assert list(tiles) == [1024, 6144]
+    for j in range(1, 17):
+        for din, s in ((0, 4), (1, 2)):
+            t = tile_for(j, din)
+            assert t % 256 == 0 and j * t * s <= STAGE_BYTES < j * (t + 256) * s
 
 
 def test_random_rounds_match_and_balance():
@@ -115,10 +139,10 @@ def test_random_rounds_match_and_balance():
         lens[small] = rng.integers(1, 9, int(small.sum()))
         J = rng.integers(1, 17, n)
         din, dout = int(rng.integers(0, 2)), int(rng.integers(0, 2))
-        tile, ntiles, _, _ = plan(lens, J, din, dout, 1)
+        tiles, ntiles, _, _ = plan(lens, J, din, dout, 1)
         grid = int(min(ntiles, rng.integers(1, 400)))
-        tile, ntiles, _, cta = plan(lens, J, din, dout, grid)
-        cost = tile_bytes(lens, J, tile, din, dout)
+        tiles, ntiles, _, cta = plan(lens, J, din, dout, grid)
+        cost = tile_bytes(lens, J, tiles, din, dout)
         assert list(cta) == brute_split(cost, grid)
         assert cta[0] == 0 and cta[-1] == ntiles and np.all(np.diff(cta.astype(np.int64)) >= 0)
         # every CTA's bytes are within one tile of the even share
@@ -130,10 +154,10 @@ def test_random_rounds_match_and_balance():
 
 def test_more_ctas_than_bytes_need():
     # a single tile and several CTAs: one CTA takes it, the others take nothing
-    tile, ntiles, _, cta = plan([5], [2], 1, 1, 1)
+    tiles, ntiles, _, cta = plan([5], [2], 1, 1, 1)
     assert ntiles == 1 and list(cta) == [0, 1]
-    _, _, _, cta = plan([5, 7], [2, 3], 1, 1, 2)
-    assert list(cta) == brute_split(tile_bytes([5, 7], [2, 3], tile, 1, 1), 2)
+    tiles, _, _, cta = plan([5, 7], [2, 3], 1, 1, 2)
+    assert list(cta) == brute_split(tile_bytes([5, 7], [2, 3], tiles, 1, 1), 2)
 
 
 def test_chunk_count():
