@@ -15,7 +15,9 @@ sum in HBM), fa_finalize (divide by the per-key weight total, RNE to bf16).
          launches skip the sum read) over its CUDA-event-timed duration
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
   resident  the same round when every update is resident, reduced in one pass by
-         fa_reduce_resident (K*s_in + s_out bytes per element), for comparison
+         fa_reduce_resident (K*s_in + s_out bytes per element), for comparison: device
+         time per round (the host's work hidden behind a queued device-side wait) and wall
+         time per round back to back
   compensated  the streamed round in the compensated mode (FA_COMPENSATED: a (hi, lo)
          pair sum, within one bf16 ulp of the exact mean everywhere), its HBM fraction
          on that mode's bytes (s_in + 16 per later client-element)
@@ -159,6 +161,33 @@ def algorithmic_bytes(w):
     acc_later = sum(n * (c - 1) * (si + 8) for n, c in zip(w.numels, cnt) if c > 1)
     fin = sum(n * (4 + so) for n, t in zip(w.numels, tot) if t > 0)
     return acc_first, acc_later, fin
+
+
+def resident_kernel(w):
+    """The kernel fa_reduce_resident runs for this workload: a layout of more than 48 keys
+    from at most 16 clients whose per-key tables fit a launch's 32,640 bytes of table
+    parameters (32 B per key, 8 B per client and key, 12 B per client) takes the one-launch
+    subset-reduce kernel; otherwise the J-client reduce kernel in final mode."""
+    si = "bf16" if w.dtype_in == "bf16" else "f32"
+    so = "bf16" if w.dtype_out == "bf16" else "f32"
+    nk, K = w.n_keys, w.K
+    if K <= 16 and nk > 48 and 32 * nk + 8 * nk * K + 12 * K <= 32640 and max(w.numels) < 2 ** 32:
+        return f"reduce_gather_inline_kernel<{si},{so}>"
+    return f"reduce_bulk_kernel<{si},{so},final>"
+
+
+def subsets_kernel(w):
+    """The kernel fa_reduce_subsets runs for this round: the form with its tables in the
+    launch's parameters when they fit 32,640 bytes (32 B per key written, 8 B per
+    (client, key) entry, 12 B per client), else the one with tables in device memory."""
+    si = "bf16" if w.dtype_in == "bf16" else "f32"
+    so = "bf16" if w.dtype_out == "bf16" else "f32"
+    cnt, tot = reporters(w)
+    nseg = sum(1 for c, t in zip(cnt, tot) if c > 0 and t > 0)
+    nsrc = sum(len(r) for r in w.reports)
+    if 32 * nseg + 8 * nsrc + 12 * w.K <= 32640 and max(w.numels) < 2 ** 32:
+        return f"reduce_gather_inline_kernel<{si},{so}>"
+    return f"reduce_gather_kernel<{si},{so}>"
 
 
 def subset_bytes(w):
@@ -572,9 +601,17 @@ def run_ours(args, world, rank, local, pg):
         ids = list(range(w.K))
         ptrs = [b.data_ptr() for b in bufs]
 
-        def round_resident():
+        def round_resident(e=None):
             fa.fa_reset(ctx)
+            if e is not None:
+                # a short device-side wait ahead of the call, so that the call's host work is
+                # done before the GPU reaches the start event: the events bracket device work
+                with torch.cuda.stream(s):
+                    torch.cuda._sleep(4_000_000)
+                e[0].record(s)
             fa.fa_reduce_resident(ctx, ids, w.weights, ptrs, [out], sh)
+            if e is not None:
+                e[1].record(s)
 
         for _ in range(args.warmup):
             round_resident()
@@ -586,15 +623,22 @@ def run_ours(args, world, rank, local, pg):
             round_resident()
         r1.record(s)
         torch.cuda.synchronize()
-        rms = r0.elapsed_time(r1) / args.steps
+        wall_ms = r0.elapsed_time(r1) / args.steps
+        launches_r = int((fa.fa_get_stats(ctx)["kernel_launches"] - l0) // args.steps)
+        evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for e in evr:
+            round_resident(e)
+        torch.cuda.synchronize()
+        rms = sum(a.elapsed_time(b) for a, b in evr) / len(evr)
         rbytes = w.P * (w.K * si + so)
         resident_line = {"value": round(client_bytes / (rms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                         "ms_per_round": round(rms, 3),
+                         "device_ms_per_round": round(rms, 4), "wall_ms_per_round": round(wall_ms, 4),
+                         "value_wall": round(client_bytes / (wall_ms * 1e-3) / 1e9, 2),
                          "hbm_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1),
                          "hbm_frac": round(rbytes / (rms * 1e-3) / 1e9 / peak, 4),
-                         "bytes_per_round": int(rbytes),
-                         "launches_per_round": int((fa.fa_get_stats(ctx)["kernel_launches"] - l0) // args.steps),
-                         "kernel": f"reduce_bulk_kernel<{w.dtype_in},{w.dtype_out},final>"}
+                         "bytes_per_round": int(rbytes), "launches_per_round": launches_r,
+                         "kernel": resident_kernel(w)}
 
     fa.fa_close(ctx)
     torch.cuda.synchronize()
@@ -709,7 +753,7 @@ def run_subsets(args, w, ctx, bufs, out, s, peak):
             "hbm_gbs": round(b / (dev_ms * 1e-3) / 1e9, 1),
             "hbm_frac": round(b / (dev_ms * 1e-3) / 1e9 / peak, 4),
             "bytes_per_round": int(b), "launches_per_round": int(launches),
-            "kernel": f"reduce_gather_kernel<{w.dtype_in},{w.dtype_out}>"}
+            "kernel": subsets_kernel(w)}
 
 
 def run_compensated(args, w, layout, bufs, out, s, peak):

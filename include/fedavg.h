@@ -274,7 +274,8 @@ fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* con
  * Every client counts as having sent every key.  The result is bit-identical to
  * fa_accumulate of each update (in the same order) followed by fa_finalize; up to 16
  * clients take one pass, more take ceil(K/16) passes (the earlier ones through the
- * running sum).  Needs a round with no contributions yet; closes it (fa_key_total works,
+ * running sum).  A layout of more than 48 keys, small enough for the per-key tables to
+ * travel in a launch's parameters, takes one launch of the subset-reduce kernel.  Needs a round with no contributions yet; closes it (fa_key_total works,
  * fa_finalize then returns FA_ERR_STATE because the outputs are already written).
  * If all weights are 0 nothing is written.
  * Errors: FA_ERR_ARG, FA_ERR_WEIGHT, FA_ERR_STATE, FA_ERR_CUDA. */

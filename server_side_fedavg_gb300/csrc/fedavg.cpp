@@ -713,6 +713,93 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
 
 namespace {
 
+// A one-pass round (fa_reduce_subsets, or fa_reduce_resident with every client sending
+// every key) with its tables in the launch's parameters, when they fit: no upload and no
+// table reads from global memory.  The entries of the key of c->items[i] are
+// [cnt[key], cnt[key + 1]) in the order they apply; entry e is client src_client[e] at
+// element offset src_off[e] of that client's buffer.  Returns false (nothing done) if the
+// round is too large for this form; otherwise launches, with *st the status.
+bool launch_inline_round(fa_ctx* c, void* const* out_ptrs, uint32_t jmax, const std::vector<uint32_t>& cnt,
+                         uint64_t n_entries, const uint32_t* src_client, const uint64_t* src_off,
+                         uint32_t n_clients, const void* const* client_ptrs, const double* weights,
+                         cudaStream_t s, fa_status* st) {
+    const bool flat = (c->flags & FA_FLAT_OUT) != 0;
+    const bool comp = c->acc_lo != nullptr;
+    const uint32_t nseg = static_cast<uint32_t>(c->items.size());
+    auto aligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    uint32_t so = 0, bo = 0, wo = 0;
+    // every key and client offset must fit 32 bits
+    bool small = jmax <= static_cast<uint32_t>(fa::kMaxBatch) &&
+                 fa::gather_inline_layout(nseg, static_cast<uint32_t>(std::min<uint64_t>(n_entries, 0xFFFFFFFFu)),
+                                          n_clients, &so, &bo, &wo);
+    for (uint32_t i = 0; small && i < nseg; ++i) small = c->items[i].numel <= 0xFFFFFFFFull;
+    for (uint64_t e = 0; small && e < n_entries; ++e) small = src_off[e] <= 0xFFFFFFFFull;
+    if (!small) return false;
+    if (!c->gath_inline) c->gath_inline.reset(new fa::GathInline);
+    fa::GathInline& gp = *c->gath_inline;
+    gp.err = c->err_dev;
+    gp.slots = c->gath_slots;
+    gp.slot = c->gath_slot;
+    gp.nseg = nseg;
+    gp.nsrc = static_cast<uint32_t>(n_entries);
+    gp.nclient = n_clients;
+    gp.jmax = jmax;
+    gp.pad = 0;
+    gp.src_off = so;
+    gp.base_off = bo;
+    gp.w_off = wo;
+    auto* gs = reinterpret_cast<fa::GathSegP*>(gp.blob);
+    auto* gr = reinterpret_cast<fa::GathSrcP*>(gp.blob + so);
+    auto* gb = reinterpret_cast<const void**>(gp.blob + bo);
+    auto* gw = reinterpret_cast<float*>(gp.blob + wo);
+    uint64_t tiles = 0;
+    for (uint32_t i = 0; i < nseg; ++i) {
+        const fa::FinItem& it = c->items[i];
+        fa::GathSegP& g = gs[i];
+        char* dst = static_cast<char*>(flat ? out_ptrs[0] : out_ptrs[it.key]);
+        g.out = flat ? dst + it.flat_off * c->s_out : dst;
+        g.div = fa::make_divisor(it.total);
+        g.len = static_cast<uint32_t>(it.numel);
+        g.tile0 = static_cast<uint32_t>(tiles);
+        g.src0 = static_cast<uint16_t>(cnt[it.key]);
+        g.J = static_cast<uint8_t>(cnt[it.key + 1] - cnt[it.key]);
+        bool ok = aligned(g.out);
+        for (uint32_t q = 0; q < g.J && ok; ++q) {
+            const uint64_t e = g.src0 + q;
+            ok = aligned(static_cast<const char*>(client_ptrs[src_client[e]]) + src_off[e] * c->s_in);
+        }
+        g.vec_ok = ok ? 1u : 0u;
+        const uint64_t tile = fa::gather_tile(g.J, c->din);
+        tiles += (it.numel + tile - 1) / tile;
+    }
+    if (tiles > 0xFFFFFFFFull) {
+        c->broken = true;
+        *st = fail(c, FA_ERR_RANGE, "layout too large for one pass");
+        return true;
+    }
+    gp.ntiles = static_cast<uint32_t>(tiles);
+    for (uint64_t e = 0; e < n_entries; ++e)
+        gr[e] = fa::GathSrcP{static_cast<uint32_t>(src_off[e]), src_client[e]};
+    for (uint32_t j = 0; j < n_clients; ++j) {
+        gb[j] = client_ptrs[j];
+        gw[j] = static_cast<float>(weights[j]);
+    }
+    gp.grid = fa::gather_grid(gp.ntiles, c->din, c->dout, comp, c->shape);
+    gp.unit_tiles = fa::gather_unit_tiles(gp.ntiles, gp.grid);
+    cudaError_t ce = fa::launch_gather_inline(gp, c->din, c->dout, comp, c->shape, s);
+    if (ce != cudaSuccess) {
+        c->broken = true;
+        *st = cuda_fail(c, ce, "one-pass round launch");
+        return true;
+    }
+    if (gp.ntiles > 0) {
+        c->gath_slot ^= 1u;   // the kernel zeroed the other counter
+        c->stats.kernel_launches++;
+    }
+    *st = FA_OK;
+    return true;
+}
+
 // Shared driver of fa_finalize and fa_finalize_apply (base_ptrs != NULL).
 fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* out_ptrs,
                         double server_lr, void* stream) {
@@ -925,6 +1012,27 @@ fa_status fa_reduce_resident(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cl
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     fa_status r = chain_in(c, s);
     if (r != FA_OK) return r;
+    if (n_clients <= static_cast<uint32_t>(fa::kMaxBatch) && c->items.size() > static_cast<size_t>(fa::kMaxSegs)) {
+        // more keys than one J-client reduce launch takes: if the layout is small enough, the
+        // round as a one-pass round of every key from every client, its tables in the launch's
+        // parameters -- one launch instead of one per 48 keys (the same operations in the same
+        // order)
+        const uint32_t nk = c->ledger.n_keys();
+        std::vector<uint32_t> cnt(nk + 1);
+        for (uint32_t p = 0; p <= nk; ++p) cnt[p] = p * n_clients;
+        const uint64_t n_entries = static_cast<uint64_t>(nk) * n_clients;
+        std::vector<uint32_t> src_client(n_entries);
+        std::vector<uint64_t> src_off(n_entries);
+        for (uint32_t p = 0; p < nk; ++p)
+            for (uint32_t j = 0; j < n_clients; ++j) {
+                src_client[cnt[p] + j] = j;
+                src_off[cnt[p] + j] = c->ledger.flat_off(p);
+            }
+        fa_status st = FA_OK;
+        if (launch_inline_round(c, out_ptrs, n_clients, cnt, n_entries, src_client.data(), src_off.data(),
+                                n_clients, flat_ptrs, weights, s, &st))
+            return st == FA_OK ? chain_out(c, s) : st;
+    }
     const uint32_t K = n_clients;
     const uint32_t last = K - (K - 1) / fa::kMaxBatch * fa::kMaxBatch;   // 1..16 clients in the last pass
     const uint32_t head = K - last;                                       // earlier passes write the sum
@@ -1138,75 +1246,11 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
     }
     const uint32_t nseg = static_cast<uint32_t>(c->items.size());
     const bool comp = c->acc_lo != nullptr;
-    auto out_of = [&](const fa::FinItem& it) {
-        char* dst = static_cast<char*>(flat ? out_ptrs[0] : out_ptrs[it.key]);
-        return flat ? dst + it.flat_off * c->s_out : dst;
-    };
-    auto aligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     {
-        // a small round: the tables travel in the launch's parameters (no upload, no table
-        // reads from global memory), when every key and client offset fits 32 bits
-        uint32_t so = 0, bo = 0, wo = 0;
-        bool small = fa::gather_inline_layout(nseg, static_cast<uint32_t>(std::min<uint64_t>(n_entries, 0xFFFFFFFFu)),
-                                              n_clients, &so, &bo, &wo);
-        for (uint32_t i = 0; small && i < nseg; ++i) small = c->items[i].numel <= 0xFFFFFFFFull;
-        for (uint64_t e2 = 0; small && e2 < n_entries; ++e2) small = src_off[e2] <= 0xFFFFFFFFull;
-        if (small) {
-            if (!c->gath_inline) c->gath_inline.reset(new fa::GathInline);
-            fa::GathInline& gp = *c->gath_inline;
-            gp.err = c->err_dev;
-            gp.slots = c->gath_slots;
-            gp.slot = c->gath_slot;
-            gp.nseg = nseg;
-            gp.nsrc = static_cast<uint32_t>(n_entries);
-            gp.nclient = n_clients;
-            gp.jmax = jmax;
-            gp.pad = 0;
-            gp.src_off = so;
-            gp.base_off = bo;
-            gp.w_off = wo;
-            auto* gs = reinterpret_cast<fa::GathSegP*>(gp.blob);
-            auto* gr = reinterpret_cast<fa::GathSrcP*>(gp.blob + so);
-            auto* gb = reinterpret_cast<const void**>(gp.blob + bo);
-            auto* gw = reinterpret_cast<float*>(gp.blob + wo);
-            uint64_t tiles = 0;
-            for (uint32_t i = 0; i < nseg; ++i) {
-                const fa::FinItem& it = c->items[i];
-                fa::GathSegP& g = gs[i];
-                g.out = out_of(it);
-                g.div = fa::make_divisor(it.total);
-                g.len = static_cast<uint32_t>(it.numel);
-                g.tile0 = static_cast<uint32_t>(tiles);
-                g.src0 = static_cast<uint16_t>(cnt[it.key]);
-                g.J = static_cast<uint8_t>(cnt[it.key + 1] - cnt[it.key]);
-                bool ok = aligned(g.out);
-                for (uint32_t q = 0; q < g.J && ok; ++q) ok = aligned(src_x[g.src0 + q]);
-                g.vec_ok = ok ? 1u : 0u;
-                const uint64_t tile = fa::gather_tile(g.J, c->din);
-                tiles += (it.numel + tile - 1) / tile;
-            }
-            if (tiles > 0xFFFFFFFFull) {
-                c->broken = true;
-                return fail(c, FA_ERR_RANGE, "layout too large for one subset reduce");
-            }
-            gp.ntiles = static_cast<uint32_t>(tiles);
-            for (uint64_t e2 = 0; e2 < n_entries; ++e2)
-                gr[e2] = fa::GathSrcP{static_cast<uint32_t>(src_off[e2]), src_client[e2]};
-            for (uint32_t j = 0; j < n_clients; ++j) {
-                gb[j] = client_ptrs[j];
-                gw[j] = static_cast<float>(weights[j]);
-            }
-            gp.grid = fa::gather_grid(gp.ntiles, c->din, c->dout, comp, c->shape);
-            gp.unit_tiles = fa::gather_unit_tiles(gp.ntiles, gp.grid);
-            cudaError_t ce = fa::launch_gather_inline(gp, c->din, c->dout, comp, c->shape, s);
-            if (ce != cudaSuccess) {
-                c->broken = true;
-                return cuda_fail(c, ce, "subset reduce launch");
-            }
-            if (gp.ntiles > 0) c->gath_slot ^= 1u;   // the kernel zeroed the other counter
-            c->stats.kernel_launches++;
-            return chain_out(c, s);
-        }
+        fa_status st = FA_OK;
+        if (launch_inline_round(c, out_ptrs, jmax, cnt, n_entries, src_client.data(), src_off.data(),
+                                n_clients, client_ptrs, weights, s, &st))
+            return st == FA_OK ? chain_out(c, s) : st;
     }
     // segment table (one entry per key to write) and source table in device memory
     const size_t seg_bytes = (sizeof(fa::GathSeg) * nseg + 15) / 16 * 16;
