@@ -176,6 +176,16 @@ def resident_kernel(w):
     return f"reduce_bulk_kernel<{si},{so},final>"
 
 
+def fused_bytes(w):
+    """Per round, streaming path with the last client's chunks through fa_accumulate_final
+    (every client sends every key): the first client s_in + 4, the middle ones s_in + 8,
+    the last s_in + 4 + s_out (read x and the sum, write the output; no finalize) bytes per
+    element."""
+    si = 2 if w.dtype_in == "bf16" else 4
+    so = 2 if w.dtype_out == "bf16" else 4
+    return w.P * (si + 4), w.P * (w.K - 2) * (si + 8), w.P * (si + 4 + so)
+
+
 def subsets_kernel(w):
     """The kernel fa_reduce_subsets runs for this round: the form with its tables in the
     launch's parameters when they fit 32,640 bytes (32 B per key written, 8 B per
@@ -512,7 +522,13 @@ def run_ours(args, world, rank, local, pg):
 
     nchunk = -(-w.P // (w.chunk_elems or w.P))
 
-    def step(evs=None):
+    # the last client's chunks go through fa_accumulate_final (its kernels write the
+    # aggregate; fa_finalize then has nothing left to write) unless --no-fused, or when
+    # clients send key subsets (then fa_accumulate_keys and fa_finalize)
+    fused = not part and not args.no_fused and w.K >= 2
+    out_arr = fa.out_array([out])
+
+    def step(evs=None, final=fused):
         # evs: (start, after the accumulate launches, after finalize) on the launching stream
         fa.fa_reset(ctx)
         if evs is not None:
@@ -524,9 +540,14 @@ def run_ours(args, world, rank, local, pg):
                 continue
             base = bufs[k % resident].data_ptr()
             P, ce = w.P, w.chunk_elems or w.P
+            last = final and k == w.K - 1
             for c0 in range(0, P, ce):
-                fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base + c0 * si,
-                                 min(ce, P - c0), sh)
+                if last:
+                    fa.fa_accumulate_final(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base + c0 * si,
+                                           min(ce, P - c0), out_arr, sh)
+                else:
+                    fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base + c0 * si,
+                                     min(ce, P - c0), sh)
         if evs is not None:
             evs[1].record(s)
         fa.fa_finalize(ctx, [out], sh)
@@ -562,19 +583,47 @@ def run_ours(args, world, rank, local, pg):
 
     # kernel times: events bracket each step's run of accumulate launches (one launch
     # per call here) and its finalize launch, on the stream they are launched on
-    acc_first_b, acc_later_b, fin_b = algorithmic_bytes(w)
     acc_ms = 0.0
     fin_ms = 0.0
     for evs in ev_sets:
         acc_ms += evs[0].elapsed_time(evs[1])
         fin_ms += evs[1].elapsed_time(evs[2])
+    if fused:
+        b0, b1, b2 = fused_bytes(w)
+        acc_bytes = b0 + b1 + b2
+        step_bytes = acc_bytes
+    else:
+        acc_first_b, acc_later_b, fin_b = algorithmic_bytes(w)
+        acc_bytes = acc_first_b + acc_later_b
+        step_bytes = acc_bytes + fin_b
     acc_launch_ms = acc_ms / (args.steps * n_calls)
-    acc_bytes_per_launch = (acc_first_b + acc_later_b) / n_calls
+    acc_bytes_per_launch = acc_bytes / n_calls
     achieved = acc_bytes_per_launch / (acc_launch_ms * 1e-3) / 1e9
-    fin_gbs = fin_b / (fin_ms / args.steps * 1e-3) / 1e9
-    step_bytes = acc_first_b + acc_later_b + fin_b
     ms_per_step = ms_total / args.steps
     value = world * client_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # ---- the same round with every client through fa_accumulate and then fa_finalize:
+    # the finalize kernel's rate, and the sum a delta round's finalize reads below
+    unfused_line = None
+    ev_u = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for _ in range(2 if fused else 0):
+        step(final=False)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if fused:
+        u0.record(s)
+        for i in range(args.steps):
+            step(ev_u[i], final=False)
+        u1.record(s)
+        torch.cuda.synchronize()
+        ums = max_over_ranks(pg, u0.elapsed_time(u1)) / args.steps
+        ufin = sum(e[1].elapsed_time(e[2]) for e in ev_u) / args.steps
+        _, _, fin_b = algorithmic_bytes(w)
+        fin_gbs = fin_b / (ufin * 1e-3) / 1e9
+        unfused_line = {"value": round(world * client_bytes / (ums * 1e-3) / 1e9, 2), "unit": "GB/s",
+                        "ms_per_step": round(ums, 3), "finalize_ms": round(ufin, 3),
+                        "calls": "every client through fa_accumulate, then fa_finalize"}
+    else:
+        fin_gbs = fin_b / (fin_ms / args.steps * 1e-3) / 1e9
 
     # ---- a delta round's finalize: the same aggregate applied in place to a base model
     # (fa_finalize_apply, server_lr 0.5): reads the sum and the base, writes the output
@@ -680,6 +729,8 @@ def run_ours(args, world, rank, local, pg):
                    "l2": "inputs (client updates, running sum) far larger than L2; no flush",
                    "hbm_frac_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4),
                    "finalize_gbs": round(fin_gbs, 1),
+                   "last_client": ("fa_accumulate_final (its kernels write the aggregate)" if fused
+                                   else "fa_accumulate, then fa_finalize"),
                    "wall_s": round(wall, 3)},
         "roofline": {"bound": "hbm", "kernel": f"accumulate_bulk_kernel<{w.dtype_in}>",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -688,6 +739,7 @@ def run_ours(args, world, rank, local, pg):
                      "launch_ms": round(acc_launch_ms, 4),
                      "traffic": profiled_traffic(acc_bytes_per_launch)},
         "gpu_launches": int(launches),
+        "unfused": unfused_line,
         "resident": resident_line,
         "subsets": subsets_line,
         "compensated": comp_line,
@@ -937,6 +989,10 @@ def run_e2e(args, w, layout, s, pg, world, hb):
                      ring_slots=args.ring_slots, slot_bytes=args.slot_mb << 20)
     sh = s.cuda_stream
     link = h2d_peak(pool[0], s)
+    # the last client through fa_accumulate_final: its kernels read its chunks in place and
+    # write the aggregate into the pinned output (not for staged chunks or a pageable output)
+    fused = (not part and not args.stage_host and not args.no_fused and out_pinned and w.K >= 2)
+    out_arr = fa.out_array([out])
 
     def step(evs=None):
         # evs: (start, after the accumulate calls, after finalize) on the stream
@@ -955,8 +1011,12 @@ def run_e2e(args, w, layout, s, pg, world, hb):
                 continue
             for c0 in range(0, w.P, ce):
                 n = min(ce, w.P - c0)
-                fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0,
-                                 pool[i % pool_n].data_ptr(), n, sh)
+                if fused and k == w.K - 1:
+                    fa.fa_accumulate_final(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0,
+                                           pool[i % pool_n].data_ptr(), n, out_arr, sh)
+                else:
+                    fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0,
+                                     pool[i % pool_n].data_ptr(), n, sh)
                 i += 1
         if evs is not None:
             evs[1].record(s)
@@ -992,6 +1052,8 @@ def run_e2e(args, w, layout, s, pg, world, hb):
     # copy)
     a_first, a_later, a_fin = algorithmic_bytes(w)
     hbm = a_first // (si + 4) * 4 + a_later // (si + 8) * 8 + a_fin // (4 + so) * 4
+    if fused:   # the last client reads the sum and writes no sum; no finalize reads it
+        hbm = w.P * 4 + w.P * (w.K - 2) * 8 + w.P * 4
     if args.stage_host:
         hbm += w.client_bytes() * 2
     if args.stage_host or not out_pinned:
@@ -1009,10 +1071,13 @@ def run_e2e(args, w, layout, s, pg, world, hb):
             "host_pool": (f"{w.K} pinned buffers, one per client, its reported keys packed" if part
                           else f"{pool_n} distinct pinned chunks of {ce * si >> 20} MiB, reused"),
             "output": (("pinned host buffer, " + ("copied from a device buffer" if args.stage_host
-                                                  else "written in place by the finalize kernel"))
+                                                  else "written in place by the last client's kernels"
+                                                  if fused else "written in place by the finalize kernel"))
                        if out_pinned else "pageable host buffer (pinned budget too small)"),
             "ingest": (f"staging ring: {args.ring_slots or 4} device slots of {args.slot_mb or 64} MiB"
-                       if args.stage_host else "pinned chunks read in place by the accumulate kernel")}
+                       if args.stage_host else "pinned chunks read in place by the accumulate kernel"),
+            "last_client": ("fa_accumulate_final: its kernels write the aggregate into the pinned output"
+                            if fused else "fa_accumulate, then fa_finalize")}
 
 
 def run_hierarchical(args, world, rank, local, pg):
@@ -1115,6 +1180,8 @@ def main(argv=None):
     ap.add_argument("--ref-elems", type=int, default=64 << 20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-resident", action="store_true")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="send the last client through fa_accumulate too (no fa_accumulate_final)")
     ap.add_argument("--no-compensated", action="store_true",
                     help="skip the round in the compensated mode (FA_COMPENSATED)")
     ap.add_argument("--ring-slots", type=int, default=0, help="e2e staging slots (0 = library default)")

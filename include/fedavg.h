@@ -227,6 +227,33 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
                              const int64_t* keys, const uint64_t* offsets,
                              const void* const* chunk_ptrs, const uint64_t* lens, void* stream);
 
+/* The LAST contribution to a range, fused with the finalize of that range ([Clara]
+ * "Server-side workflow": once the last update of the round is in, the aggregate
+ * replaces the global model; here it is written while that update is read).  As
+ * fa_accumulate for this chunk, then for every element i of the range, key p,
+ *     out[p][i] = round_to_dtype_out( (sum[p][i] + n_k * x[i]) / N_p )
+ * with the same operations, in the same order, as fa_accumulate followed by fa_finalize
+ * (bit-identical), written straight from the kernel: the running sum of the range is
+ * not stored, so the last client costs s_in + 4 + s_out bytes per element instead of
+ * s_in + 8 plus the finalize's 4 + s_out.
+ *   key, offset_elems, chunk_ptr, len_elems, stream   as fa_accumulate; the chunk is read
+ *                  in place: this GPU's memory, managed memory, or host memory the device
+ *                  addresses (FA_ERR_ARG for a staged chunk: use fa_accumulate there)
+ *   out_ptrs       as fa_finalize (n_keys pointers, or one flat pointer with
+ *                  FA_FLAT_OUT); the range's outputs must be in this GPU's memory, managed
+ *                  memory, or pinned host memory the device addresses (written in place)
+ * N_p is the key's total over its senders so far, this client included.  Every OTHER
+ * client that sent a key of the range must already have sent all of it
+ * (FA_ERR_INCOMPLETE).  From this call on the key takes no new sender, and the range
+ * takes no further contribution (FA_ERR_STATE); fa_finalize later writes the rest of the
+ * layout and leaves this range as written.  A key none of whose senders has weight
+ * (N_p == 0) is not written.  Ownership and errors otherwise as fa_accumulate.
+ * Errors: FA_ERR_ARG, FA_ERR_RANGE, FA_ERR_WEIGHT, FA_ERR_INCOMPLETE, FA_ERR_STATE,
+ * FA_ERR_CUDA, FA_ERR_TIMEOUT. */
+fa_status fa_accumulate_final(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64_t key,
+                              uint64_t offset_elems, const void* chunk_ptr, uint64_t len_elems,
+                              void* const* out_ptrs, void* stream);
+
 /* Write the aggregate: for every key with N_p > 0,
  *     out[p][i] = round_to_dtype_out( sum[p][i] / N_p )      (RNE)
  * where the quotient is one IEEE fp32 division when N_p is exact in fp32 (every integer

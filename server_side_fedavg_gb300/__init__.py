@@ -88,6 +88,7 @@ def lib():
                                           u64, ctypes.POINTER(vp), u64, vp]
         L.fa_accumulate_keys.argtypes = [vp, u32, f64, u32, ctypes.POINTER(i64), ctypes.POINTER(u64),
                                          ctypes.POINTER(vp), ctypes.POINTER(u64), vp]
+        L.fa_accumulate_final.argtypes = [vp, u32, f64, i64, u64, vp, u64, ctypes.POINTER(vp), vp]
         L.fa_finalize.argtypes = [vp, ctypes.POINTER(vp), vp]
         L.fa_reduce_resident.argtypes = [vp, u32, ctypes.POINTER(u32), ctypes.POINTER(f64),
                                          ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
@@ -111,7 +112,8 @@ def lib():
         L.fa_strerror.restype = ctypes.c_char_p
         L.fa_last_error.argtypes = [vp]
         L.fa_last_error.restype = ctypes.c_char_p
-        for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_accumulate_keys", "fa_finalize",
+        for name in ("fa_open", "fa_accumulate", "fa_accumulate_batch", "fa_accumulate_keys",
+                     "fa_accumulate_final", "fa_finalize",
                      "fa_finalize_apply", "fa_reduce_resident", "fa_reduce_subsets", "fa_reset",
                      "fa_close", "fa_key_total", "fa_sync", "fa_get_stats"):
             getattr(L, name).restype = i32
@@ -175,6 +177,19 @@ def fa_open(layout, dtype_in, dtype_out, max_clients, ring_slots=0, slot_bytes=0
 def fa_accumulate(ctx, client_id, weight_nk, key, offset_elems, chunk, len_elems, stream=None):
     _check(lib().fa_accumulate(ctx, client_id, float(weight_nk), key, offset_elems, _ptr(chunk),
                                len_elems, _stream(stream)), ctx)
+
+
+def out_array(outs):
+    """A C array of output pointers (per-key outputs, None allowed, or one flat output)."""
+    return (ctypes.c_void_p * max(len(outs), 1))(*[_ptr(o) for o in outs])
+
+
+def fa_accumulate_final(ctx, client_id, weight_nk, key, offset_elems, chunk, len_elems, outs,
+                        stream=None):
+    """outs: as for fa_finalize, or an array made by out_array (reused across calls)."""
+    ps = outs if isinstance(outs, ctypes.Array) else out_array(outs)
+    _check(lib().fa_accumulate_final(ctx, client_id, float(weight_nk), key, offset_elems, _ptr(chunk),
+                                     len_elems, ps, _stream(stream)), ctx)
 
 
 def _same_length(**seqs):

@@ -15,10 +15,15 @@ namespace fa {
 
 namespace {
 
+constexpr int kFinalThreads = 1024;   // threads of a final-form streaming CTA (see bulk_threads)
+
 // ----------------------------------------------------------------- streaming accumulate
 // One element through global memory (ragged tails, unaligned segments).
-template <typename Tin, bool kComp>
-__device__ __forceinline__ void acc_one(const Tin* x, float w, float* s, float* sl, bool first) {
+// kFinal: the element's last contribution -- the quotient is written to out[0] (dtype
+// Tout) instead of the sum.
+template <typename Tin, bool kComp, bool kFinal, typename Tout>
+__device__ __forceinline__ void acc_one(const Tin* x, float w, float* s, float* sl, bool first,
+                                        void* out, const Divisor& d) {
     const float xv = load_one<Tin>(x);
     float hi, lo = 0.0f;
     if (first) {
@@ -28,8 +33,12 @@ __device__ __forceinline__ void acc_one(const Tin* x, float w, float* s, float* 
         if constexpr (kComp) lo = *sl;
         contrib_add<kComp>(w, xv, hi, lo);
     }
-    *s = hi;
-    if constexpr (kComp) *sl = lo;
+    if constexpr (kFinal) {
+        store_one<Tout>(out, 0, quotient_out<kComp, Tout>(hi, lo, d));
+    } else {
+        *s = hi;
+        if constexpr (kComp) *sl = lo;
+    }
 }
 
 template <bool kComp>
@@ -46,9 +55,18 @@ constexpr size_t bulk_smem_bytes() {
 
 // Stage = input tile (T x Tin) + sum tile (T x fp32) [+ lo tile (T x fp32), compensated
 // mode]: 48 KB for bf16 and 64 KB for fp32 input (T = 8192), 60 / 72 KB compensated
-// (T = 6144); one CTA per SM.
-template <typename Tin, bool kComp>
-__global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid_constant__ AccArgs a) {
+// (T = 6144); one CTA per SM.  kFinal (the elements' last contribution): the quotient
+// is rounded to Tout into the sum tile's space and stored to the segment's output; the
+// sum is not written back.
+// Threads of a streaming-accumulate CTA: the plain form moves data and does one fma per
+// element (8 warps keep the copies going); the final form also divides every element, a
+// chain of dependent instructions that needs more warps to hide.
+template <bool kFinal>
+__host__ __device__ constexpr int bulk_threads() { return kFinal ? kFinalThreads : kBlock; }
+
+template <typename Tin, bool kComp, bool kFinal, typename Tout>
+__global__ void __launch_bounds__(bulk_threads<kFinal>(), 1) accumulate_bulk_kernel(const __grid_constant__ AccArgs a) {
+    constexpr uint32_t NT = bulk_threads<kFinal>();
     constexpr uint32_t T = bulk_tile<kComp>();
     constexpr uint32_t XB = T * sizeof(Tin);
     constexpr uint32_t SB = T * sizeof(float);
@@ -107,10 +125,10 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
         const bool bulk = ((a.vec_ok >> ta.si) & 1ull) && ta.cnt >= static_cast<uint32_t>(kVec);
         const uint32_t n8 = bulk ? ta.cnt / kVec : 0;
         if (ok && bulk) {
-            const uint8_t* xt = xs + s * XB;
+            uint8_t* xt = xs + s * XB;
             uint8_t* st = ss + s * SB;
             uint8_t* lt = ss + (kStages + s) * SB;
-            for (uint32_t v = threadIdx.x; v < n8; v += kBlock) {
+            for (uint32_t v = threadIdx.x; v < n8; v += NT) {
                 float xv[8], hi[8], lo[8];
                 smem_vec8<Tin>(xt, v, xv);
                 if (first) {
@@ -122,25 +140,43 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
 #pragma unroll
                     for (int e = 0; e < 8; ++e) contrib_add<kComp>(w, xv[e], hi[e], lo[e]);
                 }
-                smem_st8f(st, v, hi);
-                if constexpr (kComp) smem_st8f(lt, v, lo);
+                if constexpr (kFinal) {
+                    // the results take this thread's own vector slot: of the sum tile for
+                    // fp32 out, of the input tile for bf16 out (bf16 in: the same 16 bytes)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) hi[e] = quotient_out<kComp, Tout>(hi[e], lo[e], sg.div);
+                    smem_store8<Tout>(sizeof(Tout) == 4 ? st : xt, v, hi);
+                } else {
+                    smem_st8f(st, v, hi);
+                    if constexpr (kComp) smem_st8f(lt, v, lo);
+                }
             }
             const uint32_t tail = ta.cnt - n8 * kVec;
             if (threadIdx.x < tail) {
                 const uint32_t e = n8 * kVec + threadIdx.x;
-                acc_one<Tin, kComp>(xg + e, w, g0 + e, kComp ? l0 + e : nullptr, first);
+                acc_one<Tin, kComp, kFinal, Tout>(xg + e, w, g0 + e, kComp ? l0 + e : nullptr, first,
+                                                  kFinal ? static_cast<Tout*>(sg.out) + ta.e0 + e : nullptr,
+                                                  sg.div);
             }
         } else if (ok) {
-            for (uint32_t e = threadIdx.x; e < ta.cnt; e += kBlock)
-                acc_one<Tin, kComp>(xg + e, w, g0 + e, kComp ? l0 + e : nullptr, first);
+            for (uint32_t e = threadIdx.x; e < ta.cnt; e += NT)
+                acc_one<Tin, kComp, kFinal, Tout>(xg + e, w, g0 + e, kComp ? l0 + e : nullptr, first,
+                                                  kFinal ? static_cast<Tout*>(sg.out) + ta.e0 + e : nullptr,
+                                                  sg.div);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (!__syncthreads_and(ok)) break;
         consumed = i + 1;
         if (threadIdx.x == 0) {
             if (n8 > 0) {
-                bulk_store(g0, ss + s * SB, n8 * kVec * 4u);
-                if constexpr (kComp) bulk_store(l0, ss + (kStages + s) * SB, n8 * kVec * 4u);
+                if constexpr (kFinal) {
+                    static_assert(sizeof(Tout) == 4 || sizeof(Tin) == 2, "bf16 results need bf16 input slots");
+                    bulk_store(static_cast<Tout*>(sg.out) + ta.e0, sizeof(Tout) == 4 ? ss + s * SB : xs + s * XB,
+                               n8 * kVec * static_cast<uint32_t>(sizeof(Tout)));
+                } else {
+                    bulk_store(g0, ss + s * SB, n8 * kVec * 4u);
+                    if constexpr (kComp) bulk_store(l0, ss + (kStages + s) * SB, n8 * kVec * 4u);
+                }
             }
             bulk_commit();
             // refill the stage drained one iteration ago once its store has read it
@@ -162,7 +198,9 @@ __global__ void __launch_bounds__(kBlock, 1) accumulate_bulk_kernel(const __grid
 // in HBM is not the limit and no shared-memory staging is needed.  Tiles of
 // kDirectTile elements, one 8-element vector per thread; many CTAs per SM keep enough
 // loads in flight to cover the link's latency.
-template <typename Tin, bool kComp>
+// kFinal: the elements' last contribution; the quotient (dtype Tout) goes to the
+// segment's output and the sum is not stored.
+template <typename Tin, bool kComp, bool kFinal, typename Tout>
 __global__ void __launch_bounds__(kBlock) accumulate_direct_kernel(const __grid_constant__ AccArgs a) {
     static_assert(kDirectTile == kBlock * kVec, "one vector per thread per tile");
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -189,8 +227,14 @@ __global__ void __launch_bounds__(kBlock) accumulate_direct_kernel(const __grid_
 #pragma unroll
                 for (int e = 0; e < 8; ++e) contrib_add<kComp>(w, xv[e], hi[e], lo[e]);
             }
-            st8f(gp, hi);
-            if constexpr (kComp) st8f(gl + threadIdx.x * kVec, lo);
+            if constexpr (kFinal) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) hi[e] = quotient_out<kComp, Tout>(hi[e], lo[e], sg.div);
+                store8_global<Tout>(sg.out, ta.e0 + threadIdx.x * kVec, hi);
+            } else {
+                st8f(gp, hi);
+                if constexpr (kComp) st8f(gl + threadIdx.x * kVec, lo);
+            }
         }
         for (uint32_t e = n8 * kVec + threadIdx.x; e < ta.cnt; e += kBlock) {
             const float xv = load_plain<Tin>(xt + e);
@@ -202,37 +246,65 @@ __global__ void __launch_bounds__(kBlock) accumulate_direct_kernel(const __grid_
                 if constexpr (kComp) lo = gl[e];
                 contrib_add<kComp>(w, xv, hi, lo);
             }
-            g[e] = hi;
-            if constexpr (kComp) gl[e] = lo;
+            if constexpr (kFinal) {
+                store_one<Tout>(sg.out, ta.e0 + e, quotient_out<kComp, Tout>(hi, lo, sg.div));
+            } else {
+                g[e] = hi;
+                if constexpr (kComp) gl[e] = lo;
+            }
         }
     }
 }
 
 // ----------------------------------------------------------------- host side
-template <typename Tin, bool kComp>
+template <typename Tin, bool kComp, bool kFinal = false, typename Tout = float>
 cudaError_t launch_stream_t(AccArgs a, int per_sm, int sms, cudaStream_t stream) {
     if (!number_tiles(a.seg, a.nseg, bulk_tile<kComp>(), &a.ntiles)) return cudaErrorInvalidValue;
     if (a.ntiles == 0) return cudaSuccess;
-    return launch_dependent(accumulate_bulk_kernel<Tin, kComp>, grid_for(a.ntiles, sms, per_sm), kBlock,
-                            bulk_smem_bytes<Tin, kComp>(), stream, a);
+    return launch_dependent(accumulate_bulk_kernel<Tin, kComp, kFinal, Tout>, grid_for(a.ntiles, sms, per_sm),
+                            bulk_threads<kFinal>(), bulk_smem_bytes<Tin, kComp>(), stream, a);
 }
 
-template <typename Tin, bool kComp>
+template <typename Tin, bool kComp, bool kFinal = false, typename Tout = float>
 cudaError_t launch_direct_t(AccArgs a, int per_sm, int sms, cudaStream_t stream) {
     if (!number_tiles(a.seg, a.nseg, kDirectTile, &a.ntiles)) return cudaErrorInvalidValue;
     if (a.ntiles == 0) return cudaSuccess;
-    return launch_dependent(accumulate_direct_kernel<Tin, kComp>, grid_for(a.ntiles, sms, per_sm), kBlock,
-                            0, stream, a);
+    return launch_dependent(accumulate_direct_kernel<Tin, kComp, kFinal, Tout>, grid_for(a.ntiles, sms, per_sm),
+                            kBlock, 0, stream, a);
 }
 
-template <typename Tin, bool kComp>
-cudaError_t prepare_stream(int* occ) {
-    cudaError_t e = cudaFuncSetAttribute(accumulate_bulk_kernel<Tin, kComp>,
+template <typename Tin, bool kComp, bool kFinal, typename Tout>
+cudaError_t prepare_stream_one(int* occ) {
+    cudaError_t e = cudaFuncSetAttribute(accumulate_bulk_kernel<Tin, kComp, kFinal, Tout>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bulk_smem_bytes<Tin, kComp>()));
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, accumulate_bulk_kernel<Tin, kComp>, kBlock,
-                                                         bulk_smem_bytes<Tin, kComp>());
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, accumulate_bulk_kernel<Tin, kComp, kFinal, Tout>,
+                                                         bulk_threads<kFinal>(), bulk_smem_bytes<Tin, kComp>());
+}
+
+// The streaming kernel and its final variants (the same shared memory): the occupancy of
+// all of them.  Final variants exist for the dtype pairs whose result fits the stage in
+// place (see fused_final_bulk).
+template <typename Tin, bool kComp>
+cudaError_t prepare_stream(int* occ) {
+    int o1 = 0, o2 = 0;
+    cudaError_t e = prepare_stream_one<Tin, kComp, false, float>(occ);
+    if (e == cudaSuccess) e = prepare_stream_one<Tin, kComp, true, float>(&o1);
+    o2 = o1;
+    if constexpr (sizeof(Tin) == 2) {
+        if (e == cudaSuccess) e = prepare_stream_one<Tin, kComp, true, uint16_t>(&o2);
+    }
+    if (e == cudaSuccess) *occ = std::min(*occ, std::min(o1, o2));
+    return e;
+}
+
+// The direct kernel's CTAs per SM (its final variants launch the same grid: a CTA that
+// does not fit waits for a slot, which the grid-stride loop allows).
+template <typename Tin, bool kComp>
+cudaError_t direct_occupancy(int* occ) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, accumulate_direct_kernel<Tin, kComp, false, float>,
+                                                         kBlock, 0);
 }
 
 template <bool kComp>
@@ -242,10 +314,8 @@ cudaError_t prepare_accumulate_shapes(LaunchShape* s) {
     auto keep = [&r](cudaError_t x) { if (r == cudaSuccess) r = x; };
     keep(prepare_stream<float, kComp>(&s->bulk_ctas_per_sm[c][0]));
     keep(prepare_stream<uint16_t, kComp>(&s->bulk_ctas_per_sm[c][1]));
-    keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->direct_ctas_per_sm[c][0],
-                                                       accumulate_direct_kernel<float, kComp>, kBlock, 0));
-    keep(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&s->direct_ctas_per_sm[c][1],
-                                                       accumulate_direct_kernel<uint16_t, kComp>, kBlock, 0));
+    keep(direct_occupancy<float, kComp>(&s->direct_ctas_per_sm[c][0]));
+    keep(direct_occupancy<uint16_t, kComp>(&s->direct_ctas_per_sm[c][1]));
     return r;
 }
 
@@ -254,6 +324,30 @@ cudaError_t accumulate_t(const AccArgs& a, int in, const LaunchShape& s, cudaStr
     const int c = kComp ? 1 : 0;
     return in == 0 ? launch_stream_t<float, kComp>(a, s.bulk_ctas_per_sm[c][0], s.sms, stream)
                    : launch_stream_t<uint16_t, kComp>(a, s.bulk_ctas_per_sm[c][1], s.sms, stream);
+}
+
+// The bulk kernel writes a tile's results into its own shared-memory vector slots before
+// storing them: in the sum tile (fp32 out: 32 B per 8 elements, as the sum) or in the
+// input tile (bf16 in and out: 16 B, as the input).  fp32 in with bf16 out fits neither
+// slot for slot, so it runs the direct kernel (plain loads from device memory).
+bool fused_final_bulk(int din, int dout) { return dout == 0 || din == 1; }
+
+template <bool kComp>
+cudaError_t final_t(const AccArgs& a, int in, int out, bool direct, const LaunchShape& s,
+                    cudaStream_t stream) {
+    const int c = kComp ? 1 : 0;
+    if (direct || !fused_final_bulk(in, out)) {
+        const int per = s.direct_ctas_per_sm[c][in];
+        if (in == 0)
+            return out == 0 ? launch_direct_t<float, kComp, true, float>(a, per, s.sms, stream)
+                            : launch_direct_t<float, kComp, true, uint16_t>(a, per, s.sms, stream);
+        return out == 0 ? launch_direct_t<uint16_t, kComp, true, float>(a, per, s.sms, stream)
+                        : launch_direct_t<uint16_t, kComp, true, uint16_t>(a, per, s.sms, stream);
+    }
+    const int per = s.bulk_ctas_per_sm[c][in];
+    if (in == 0) return launch_stream_t<float, kComp, true, float>(a, per, s.sms, stream);
+    return out == 0 ? launch_stream_t<uint16_t, kComp, true, float>(a, per, s.sms, stream)
+                    : launch_stream_t<uint16_t, kComp, true, uint16_t>(a, per, s.sms, stream);
 }
 
 }  // namespace
@@ -270,6 +364,14 @@ cudaError_t query_launch_shape(LaunchShape* s) {
     if (e == cudaSuccess) e = prepare_gather_shapes(s);
     if (e == cudaSuccess) e = prepare_finalize_shapes(s);
     return e;
+}
+
+cudaError_t launch_accumulate_final(const AccArgs& a, int dtype_in, int dtype_out, bool direct,
+                                    const LaunchShape& s, cudaStream_t stream) {
+    if (a.nseg == 0 || a.nseg > static_cast<uint32_t>(kMaxSegs) || a.J != 1 || a.err == nullptr)
+        return cudaErrorInvalidValue;
+    const int in = dtype_in == 0 ? 0 : 1, out = dtype_out == 0 ? 0 : 1;
+    return a.acc_lo ? final_t<true>(a, in, out, direct, s, stream) : final_t<false>(a, in, out, direct, s, stream);
 }
 
 cudaError_t launch_accumulate_direct(const AccArgs& a, int dtype_in, const LaunchShape& s,

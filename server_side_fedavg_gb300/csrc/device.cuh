@@ -135,6 +135,20 @@ __device__ __forceinline__ void store_one(void* out, uint64_t e, float q) {
         static_cast<float*>(out)[e] = q;
 }
 
+// Eight results of dtype Tout (RNE for bf16) to a 16-byte aligned global address.
+template <typename Tout>
+__device__ __forceinline__ void store8_global(void* out, uint64_t e, const float (&q)[8]) {
+    if constexpr (sizeof(Tout) == 2) {
+        st_v4u(static_cast<uint16_t*>(out) + e,
+               make_uint4(pack_bf16(q[0], q[1]), pack_bf16(q[2], q[3]), pack_bf16(q[4], q[5]),
+                          pack_bf16(q[6], q[7])));
+    } else {
+        float* p = static_cast<float*>(out) + e;
+        st_v4f(p, make_float4(q[0], q[1], q[2], q[3]));
+        st_v4f(p + 4, make_float4(q[4], q[5], q[6], q[7]));
+    }
+}
+
 // ----------------------------------------------------------------- arithmetic
 // The first contribution to an element and every later one.  Plain mode: a rounded
 // product, then one fused multiply-add per client.  Compensated mode: the Dot2 step of

@@ -80,6 +80,7 @@ struct fa_ctx {
 
     fa::FinSeg* fin_dev = nullptr;
     fa::FinSeg* fin_host = nullptr;
+    size_t fin_cap = 0;           // entries of both (n_keys; more once final contributions split keys)
     cudaEvent_t fin_ev = nullptr;
     bool fin_pending = false;
 
@@ -282,9 +283,17 @@ fa_status ensure_ring(fa_ctx* c, bool need_host) {
 // [c0, c0 + n), reading inputs xs[0..J) whose element 0 is chunk element c0 -- or, for
 // one client's several chunks (J = 1, fa_accumulate_keys), xs[i] is chunk i and each
 // piece reads the chunk it was cut from.
+// A final contribution (fa_accumulate_final) passes fin: each piece's N_p and the outputs
+// (n_keys pointers, or one flat pointer with FA_FLAT_OUT); its launches then write the
+// pieces' outputs instead of the sum.
+struct FinalOut {
+    const std::vector<double>* totals;
+    void* const* outs;
+};
+
 fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_t c0,
                         uint64_t n, const void* const* xs, const float* ws, uint32_t J,
-                        cudaStream_t s, bool direct = false) {
+                        cudaStream_t s, bool direct = false, const FinalOut* fin = nullptr) {
     // launches of up to 16 clients (one at a time for the direct kernel, which takes one);
     // after the first launch the sum is started everywhere
     uint32_t done = 0;
@@ -304,17 +313,21 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
         a.J = jb;
         auto flush = [&]() -> fa_status {
             if (a.nseg == 0) return FA_OK;
-            FA_CUDA(c, direct ? fa::launch_accumulate_direct(a, c->din, c->shape, s)
-                              : fa::launch_accumulate(a, c->din, c->shape, s));
+            FA_CUDA(c, fin ? fa::launch_accumulate_final(a, c->din, c->dout, direct, c->shape, s)
+                           : direct ? fa::launch_accumulate_direct(a, c->din, c->shape, s)
+                                    : fa::launch_accumulate(a, c->din, c->shape, s));
             c->stats.kernel_launches++;
             a.nseg = 0;
             a.vec_ok = 0;
             return FA_OK;
         };
-        for (const auto& p : pieces) {
+        const bool flat = (c->flags & FA_FLAT_OUT) != 0;
+        for (size_t pi = 0; pi < pieces.size(); ++pi) {
+            const auto& p = pieces[pi];
             uint64_t b = std::max(p.chunk_off, c0);
             uint64_t e = std::min(p.chunk_off + p.len, c0 + n);
             if (b >= e) continue;
+            if (fin && (*fin->totals)[pi] == 0.0) continue;   // N_p == 0: nothing to write
             if (a.nseg == static_cast<uint32_t>(fa::kMaxSegs)) {
                 fa_status st = flush();
                 if (st != FA_OK) return st;
@@ -327,6 +340,15 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
             g.len = e - b;
             g.first = (p.first && done == 0) ? 1u : 0u;
             bool ok = (reinterpret_cast<uintptr_t>(c->acc + g.acc_idx) & 15u) == 0;
+            if (fin) {
+                // the output element of acc_idx: its key's output at the same offset in the key
+                const uint64_t koff = g.acc_idx - c->ledger.acc_off(p.key);
+                char* dst = static_cast<char*>(flat ? fin->outs[0] : fin->outs[p.key]);
+                dst += (flat ? c->ledger.flat_off(p.key) + koff : koff) * c->s_out;
+                g.out = dst;
+                g.div = fa::make_divisor((*fin->totals)[pi]);
+                ok = ok && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+            }
             for (uint32_t j = 0; j < jb && ok; ++j) {
                 const void* base = jb == 1 ? g.x : a.x[j];
                 uintptr_t xa = reinterpret_cast<uintptr_t>(base) + g.x_off * c->s_in;
@@ -348,9 +370,9 @@ fa_status launch_pieces(fa_ctx* c, const std::vector<fa::Piece>& pieces, uint64_
 // for fa_accumulate_keys one client's several chunks (J = 1).  A pageable source is
 // waited for before returning, so the caller may reuse it at once.
 fa_status launch_in_place(fa_ctx* c, const void* const* ptrs, const float* ws, uint32_t J,
-                          cudaStream_t s, bool host, bool pageable) {
+                          cudaStream_t s, bool host, bool pageable, const FinalOut* fin = nullptr) {
     fa_status r = chain_in(c, s);
-    if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, UINT64_MAX, ptrs, ws, J, s, host);
+    if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, UINT64_MAX, ptrs, ws, J, s, host, fin);
     if (r == FA_OK && pageable) {
         cudaError_t ce = cudaEventRecord(c->read_ev, s);
         if (ce != cudaSuccess) r = cuda_fail(c, ce, "pageable read");
@@ -362,7 +384,7 @@ fa_status launch_in_place(fa_ctx* c, const void* const* ptrs, const float* ws, u
 
 fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const double* weights,
                           int64_t key, uint64_t offset, const void* const* ptrs, uint64_t len,
-                          cudaStream_t s, bool batch) {
+                          cudaStream_t s, bool batch, void* const* final_outs = nullptr) {
     if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
     if (len > 0) {
         for (uint32_t j = 0; j < J; ++j)
@@ -396,15 +418,24 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
                     "fa_accumulate_batch reads its chunks in place: all in this GPU's memory, or all "
                     "in managed memory or host memory the device addresses");
     const bool direct = !all_device && all_in_place;
+    if (final_outs && len > 0 && !all_device && !all_in_place)
+        return fail(c, FA_ERR_ARG,
+                    "fa_accumulate_final reads its chunk in place: this GPU's memory, managed memory, or "
+                    "host memory the device addresses (not staged)");
     if (len > 0 && kind != Mem::kDevice && !direct) {
         // staging first: a failed allocation must not leave the round half-recorded
         fa_status rr = ensure_ring(c, kind == Mem::kPageable);
         if (rr != FA_OK) return rr;
     }
     std::string e;
-    int32_t st = c->ledger.plan_accumulate(ids, weights, J, key, offset, len, &c->pieces, &e);
+    std::vector<double> totals;
+    int32_t st = final_outs ? c->ledger.plan_accumulate_final(ids[0], weights[0], key, offset, len, &c->pieces,
+                                                             &totals, &e)
+                            : c->ledger.plan_accumulate(ids, weights, J, key, offset, len, &c->pieces, &e);
     if (st != fa::kOk) return fail(c, st, e);
     if (len == 0) return FA_OK;
+    const FinalOut fo{&totals, final_outs};
+    const FinalOut* fin = final_outs ? &fo : nullptr;
 
     std::vector<float> wv(J);
     for (uint32_t j = 0; j < J; ++j) wv[j] = static_cast<float>(weights[j]);
@@ -413,12 +444,12 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
     fa_status r = FA_OK;
     if (kind == Mem::kDevice) {
         r = chain_in(c, s);
-        if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, J, s);
+        if (r == FA_OK) r = launch_pieces(c, c->pieces, 0, len, ptrs, wp, J, s, false, fin);
         if (r == FA_OK) r = chain_out(c, s);
     } else if (direct) {
         // host memory read by the kernel over the host link, ordered on `s` (a batch: one
         // direct launch per client, in batch order)
-        r = launch_in_place(c, ptrs, wp, J, s, true, any_pageable);
+        r = launch_in_place(c, ptrs, wp, J, s, true, any_pageable, fin);
         if (r == FA_OK) c->stats.h2d_bytes += static_cast<uint64_t>(host_chunks) * len * c->s_in;
     } else {
         // host memory: through the staging ring, slot-sized pieces
@@ -613,6 +644,7 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
     if (ce == cudaSuccess) ce = cudaMemset(c->gath_slots, 0, 2 * sizeof(uint32_t));
     if (ce == cudaSuccess) ce = cudaMalloc(&c->fin_dev, sizeof(fa::FinSeg) * n_keys);
     if (ce == cudaSuccess) ce = cudaHostAlloc(&c->fin_host, sizeof(fa::FinSeg) * n_keys, cudaHostAllocDefault);
+    if (ce == cudaSuccess) c->fin_cap = n_keys;
     if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&c->err_stream, cudaStreamNonBlocking);
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->err_ev, cudaEventDisableTiming);
     if (ce == cudaSuccess)
@@ -637,6 +669,53 @@ fa_status fa_accumulate(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64
     const void* ptrs[1] = {chunk_ptr};
     return accumulate_impl(ctx, 1, &client_id, &weight_nk, key, offset_elems, ptrs, len_elems,
                            static_cast<cudaStream_t>(stream), false);
+}
+
+fa_status fa_accumulate_final(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64_t key,
+                              uint64_t offset_elems, const void* chunk_ptr, uint64_t len_elems,
+                              void* const* out_ptrs, void* stream) {
+    Range range("fa_accumulate_final");
+    if (!ctx) return FA_ERR_ARG;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    DeviceGuard dg(ctx->device);
+    fa_ctx* c = ctx;
+    c->err.clear();
+    if (out_ptrs == nullptr) return fail(c, FA_ERR_ARG, "out_ptrs is NULL");
+    // the outputs this range writes: this GPU's memory, managed memory, or pinned host
+    // memory the device addresses (written in place over the host link)
+    const bool flat = (c->flags & FA_FLAT_OUT) != 0;
+    uint64_t host_bytes = 0;
+    if (len_elems > 0) {
+        const uint32_t nk = c->ledger.n_keys();
+        uint32_t p0 = 0, p1 = 0;   // keys [p0, p1] whose outputs are written
+        if (key >= 0 && key < static_cast<int64_t>(nk)) {
+            p0 = p1 = static_cast<uint32_t>(key);
+        } else if (key == FA_KEY_FLAT && offset_elems < c->ledger.total_elems()) {
+            uint32_t lo = 0, hi = nk;   // the last key starting at or before the offset
+            while (hi - lo > 1) {
+                const uint32_t mid = (lo + hi) / 2;
+                if (c->ledger.flat_off(mid) <= offset_elems) lo = mid; else hi = mid;
+            }
+            p0 = p1 = lo;
+            const uint64_t end = offset_elems + std::min(len_elems, c->ledger.total_elems() - offset_elems);
+            while (p1 + 1 < nk && c->ledger.flat_off(p1 + 1) < end) ++p1;
+        }   // else the range check below refuses the call
+        for (uint32_t p = p0; p <= (flat ? p0 : p1); ++p) {
+            void* dst = flat ? out_ptrs[0] : out_ptrs[p];
+            bool other = false, in_place = false;
+            const Mem m = dst ? classify(dst, c->device, &other, &in_place) : Mem::kPageable;
+            if (dst == nullptr || other || !(m == Mem::kDevice || m == Mem::kManaged || (m == Mem::kPinned && in_place)))
+                return fail(c, FA_ERR_ARG,
+                            "fa_accumulate_final writes its outputs in place: this GPU's memory, managed "
+                            "memory, or pinned host memory the device addresses");
+            if (m == Mem::kPinned) host_bytes = len_elems * c->s_out;
+        }
+    }
+    const void* ptrs[1] = {chunk_ptr};
+    fa_status r = accumulate_impl(c, 1, &client_id, &weight_nk, key, offset_elems, ptrs, len_elems,
+                                  static_cast<cudaStream_t>(stream), false, out_ptrs);
+    if (r == FA_OK) c->stats.d2h_bytes += host_bytes;
+    return r;
 }
 
 fa_status fa_accumulate_batch(fa_ctx* ctx, uint32_t n_clients, const uint32_t* client_ids,
@@ -871,11 +950,29 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
         if (r != FA_OK) return r;
         c->fin_pending = false;
     }
+    if (c->items.size() > c->fin_cap) {
+        // final contributions split some keys into several ranges to write
+        const size_t cap = c->items.size() * 2;
+        fa::FinSeg* dev = nullptr;
+        fa::FinSeg* host = nullptr;
+        cudaError_t ce = cudaMalloc(&dev, sizeof(fa::FinSeg) * cap);
+        if (ce == cudaSuccess) ce = cudaHostAlloc(&host, sizeof(fa::FinSeg) * cap, cudaHostAllocDefault);
+        if (ce != cudaSuccess) {
+            if (dev) cudaFree(dev);
+            cudaGetLastError();
+            return fail(c, ce == cudaErrorMemoryAllocation ? FA_ERR_NOMEM : FA_ERR_CUDA, "finalize table");
+        }
+        cudaFree(c->fin_dev);
+        cudaFreeHost(c->fin_host);
+        c->fin_dev = dev;
+        c->fin_host = host;
+        c->fin_cap = cap;
+    }
     uint32_t ntiles = 0;
     for (size_t i = 0; i < c->items.size(); ++i) {
         const auto& it = c->items[i];
         char* dst = static_cast<char*>(flat ? out_ptrs[0] : out_ptrs[it.key]);
-        if (flat) dst += it.flat_off * c->s_out;
+        dst += (flat ? it.flat_off : it.koff) * c->s_out;
         if (kind[i] != Mem::kDevice)
             dst = static_cast<char*>(c->out_stage) + it.flat_off * c->s_out;
         fa::FinSeg& g = c->fin_host[i];
@@ -885,7 +982,7 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
         g.base = nullptr;
         if (apply) {
             const char* b = static_cast<const char*>(flat ? base_ptrs[0] : base_ptrs[it.key]);
-            g.base = flat ? b + it.flat_off * c->s_out : b;
+            g.base = b + (flat ? it.flat_off : it.koff) * c->s_out;
         }
         g.div = fa::make_divisor(it.total);
         g.tile0 = ntiles;
@@ -931,7 +1028,8 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
             } else {
                 const char* src = static_cast<const char*>(c->out_stage) + it.flat_off * c->s_out;
                 uint64_t bytes = it.numel * c->s_out;
-                FA_CUDA(c, cudaMemcpyAsync(out_ptrs[it.key], src, bytes, cudaMemcpyDeviceToHost, s));
+                FA_CUDA(c, cudaMemcpyAsync(static_cast<char*>(out_ptrs[it.key]) + it.koff * c->s_out, src,
+                                           bytes, cudaMemcpyDeviceToHost, s));
                 c->stats.d2h_bytes += bytes;
                 ++i;
             }

@@ -40,19 +40,6 @@ struct LoadBase<uint16_t> {
     }
 };
 
-template <typename Tout>
-__device__ __forceinline__ void global_store8(void* out, uint64_t e, const float (&q)[8]) {
-    if constexpr (sizeof(Tout) == 2) {
-        st_v4u(static_cast<uint16_t*>(out) + e,
-               make_uint4(pack_bf16(q[0], q[1]), pack_bf16(q[2], q[3]), pack_bf16(q[4], q[5]),
-                          pack_bf16(q[6], q[7])));
-    } else {
-        float* p = static_cast<float*>(out) + e;
-        st_v4f(p, make_float4(q[0], q[1], q[2], q[3]));
-        st_v4f(p + 4, make_float4(q[4], q[5], q[6], q[7]));
-    }
-}
-
 // Segments whose first tiles a searching finalize CTA keeps in shared memory (16 KB).
 constexpr uint32_t kFinSegCache = 4096;
 
@@ -72,7 +59,7 @@ __device__ __forceinline__ void fin_vec(const FinSeg& sg, uint64_t e, const floa
 #pragma unroll
         for (int i = 0; i < 8; ++i) q[i] = __fmaf_rn(lr, q[i], b[i]);
     }
-    global_store8<Tout>(sg.out, e, q);
+    store8_global<Tout>(sg.out, e, q);
 }
 
 template <typename Tout, bool kApply, bool kComp>
@@ -161,7 +148,7 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
 #pragma unroll
                         for (int i = 0; i < 8; ++i) q[i] = __fmaf_rn(lr, q[i], b[u][i]);
                     }
-                    global_store8<Tout>(sg.out, e0 + v * kVec, q);
+                    store8_global<Tout>(sg.out, e0 + v * kVec, q);
                 }
             } else {
                 const uint32_t nv = cnt / kVec;

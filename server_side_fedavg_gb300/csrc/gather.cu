@@ -126,20 +126,6 @@ __device__ __forceinline__ TileAt tile_in(const SegV& sg, uint32_t si, uint32_t 
     return r;
 }
 
-// Eight results of dtype Tout (RNE for bf16) to a 16-byte aligned global address.
-template <typename Tout>
-__device__ __forceinline__ void store8_global(void* out, uint64_t e, const float (&q)[8]) {
-    if constexpr (sizeof(Tout) == 2) {
-        st_v4u(static_cast<uint16_t*>(out) + e,
-               make_uint4(pack_bf16(q[0], q[1]), pack_bf16(q[2], q[3]), pack_bf16(q[4], q[5]),
-                          pack_bf16(q[6], q[7])));
-    } else {
-        float* p = static_cast<float*>(out) + e;
-        st_v4f(p, make_float4(q[0], q[1], q[2], q[3]));
-        st_v4f(p + 4, make_float4(q[4], q[5], q[6], q[7]));
-    }
-}
-
 // Two roles per CTA:
 //  - the loader (one lane of warp 16) fills input stage s (jmax reporter tiles) with bulk
 //    loads once the compute warps have released it (empty[s]), arming full[s] with the

@@ -64,6 +64,9 @@ struct AccSeg {
     uint64_t len;       // elements (>= 1)
     uint32_t first;     // 1: the first client of the launch starts the sum here
     uint32_t tile0;     // first tile of this segment (set by launch_accumulate)
+    void* out;          // final launches: destination of the segment's element 0 (dtype_out)
+    Divisor div;        // final launches: N_p
+    uint32_t pad;
 };
 
 struct AccArgs {
@@ -149,6 +152,14 @@ cudaError_t launch_reduce_sum(const AccArgs& a, int dtype_in, const LaunchShape&
 // Returns cudaErrorInvalidValue if the arguments are out of range.
 cudaError_t launch_accumulate(const AccArgs& a, int dtype_in, const LaunchShape& s,
                               cudaStream_t stream);
+
+// The last contribution to its elements (fa_accumulate_final), a.J == 1: the same
+// operations as launch_accumulate, then out = RNE((sum) / N_p) per segment (AccSeg::out,
+// AccSeg::div) written straight from the kernel; the running sum is not stored.  vec_ok
+// bit s also requires the segment's output to be 16-byte aligned.  direct: the input is
+// read in place by plain loads (as launch_accumulate_direct).
+cudaError_t launch_accumulate_final(const AccArgs& a, int dtype_in, int dtype_out, bool direct,
+                                    const LaunchShape& s, cudaStream_t stream);
 
 // One client (a.J == 1) with the input read in place by plain loads, no bulk copies:
 // for inputs in host memory the device can address (pinned memory read over the

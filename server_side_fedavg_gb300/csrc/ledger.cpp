@@ -56,6 +56,8 @@ int32_t Ledger::init(const uint64_t* numels, uint32_t n_keys, uint32_t max_clien
     has_weight_.assign(max_clients, 0);
     recv_.assign(static_cast<size_t>(max_clients) * n_keys, 0);
     started_.assign(n_keys, {});
+    written_.assign(n_keys, {});
+    frozen_.assign(n_keys, 0);
     closed_ = false;
     return kOk;
 }
@@ -71,7 +73,31 @@ void Ledger::reset() {
     std::fill(has_weight_.begin(), has_weight_.end(), 0);
     std::fill(recv_.begin(), recv_.end(), 0);
     for (auto& s : started_) s.clear();
+    for (auto& s : written_) s.clear();
+    std::fill(frozen_.begin(), frozen_.end(), 0);
     closed_ = false;
+}
+
+int32_t Ledger::check_frozen(uint32_t c, const std::vector<Span>& spans, size_t from, size_t to,
+                             std::string* err) const {
+    const uint32_t nk = n_keys();
+    for (size_t i = from; i < to; ++i) {
+        const Span& s = spans[i];
+        if (!frozen_[s.p]) continue;
+        if (recv_[static_cast<size_t>(c) * nk + s.p] == 0) {
+            *err = fmt("key %llu already has a final contribution: client %llu cannot start sending it",
+                       s.p, c);
+            return kErrState;
+        }
+        for (const auto& w : written_[s.p]) {
+            if (w.first < s.koff + s.n && s.koff < w.second) {
+                *err = fmt("elements [%llu, %llu) of key %llu were already written by a final contribution",
+                           w.first, w.second, s.p);
+                return kErrState;
+            }
+        }
+    }
+    return kOk;
 }
 
 void Ledger::split_and_mark(uint32_t p, uint64_t a, uint64_t b,
@@ -220,6 +246,8 @@ int32_t Ledger::plan_accumulate(const uint32_t* clients, const double* weights, 
                 return kErrRange;
             }
         }
+        st = check_frozen(c, spans, 0, spans.size(), err);
+        if (st != kOk) return st;
     }
     // commit
     for (uint32_t j = 0; j < J; ++j) {
@@ -278,6 +306,8 @@ int32_t Ledger::plan_accumulate_keys(uint32_t client, double weight, uint32_t n,
             return kErrRange;
         }
     }
+    st = check_frozen(client, spans, 0, spans.size(), err);
+    if (st != kOk) return st;
     // commit
     if (spans.empty()) return kOk;
     weight_[client] = weight;
@@ -317,6 +347,11 @@ int32_t Ledger::record_whole_keys(uint32_t client, double weight, uint32_t n, co
             st = kErrRange;
             break;
         }
+        if (frozen_[static_cast<size_t>(k)]) {
+            *err = fmt("key %llu already has a final contribution", static_cast<unsigned long long>(k));
+            st = kErrState;
+            break;
+        }
         row[k] = numel_[static_cast<size_t>(k)];
     }
     if (st != kOk) {
@@ -326,6 +361,67 @@ int32_t Ledger::record_whole_keys(uint32_t client, double weight, uint32_t n, co
     if (n > 0) {
         weight_[client] = weight;
         has_weight_[client] = 1;
+    }
+    return kOk;
+}
+
+int32_t Ledger::plan_accumulate_final(uint32_t client, double weight, int64_t key, uint64_t offset,
+                                      uint64_t len, std::vector<Piece>* out, std::vector<double>* totals,
+                                      std::string* err) {
+    out->clear();
+    totals->clear();
+    if (closed_) {
+        *err = "round already finalized: call fa_reset before accumulating again";
+        return kErrState;
+    }
+    int32_t st = check_client(client, weight, err);
+    if (st != kOk) return st;
+    std::vector<Span> spans;
+    st = chunk_spans(key, offset, len, &spans, err);
+    if (st != kOk || len == 0) return st;
+    const uint32_t nk = n_keys();
+    for (const auto& s : spans) {
+        const uint64_t have = recv_[static_cast<size_t>(client) * nk + s.p];
+        if (s.n > numel_[s.p] - have) {
+            *err = fmt("client %llu would send more than numel (%llu) elements of key %llu",
+                       client, numel_[s.p], s.p);
+            return kErrRange;
+        }
+        for (uint32_t c = 0; c < max_clients_; ++c) {
+            if (c == client) continue;
+            const uint64_t h = recv_[static_cast<size_t>(c) * nk + s.p];
+            if (h != 0 && h != numel_[s.p]) {
+                *err = fmt("a final contribution to key %llu needs every other sender's whole key: "
+                           "client %llu has sent %llu of %llu elements",
+                           s.p, c, h, numel_[s.p]);
+                return kErrIncomplete;
+            }
+        }
+    }
+    st = check_frozen(client, spans, 0, spans.size(), err);
+    if (st != kOk) return st;
+    // commit
+    weight_[client] = weight;
+    has_weight_[client] = 1;
+    for (const auto& s : spans) recv_[static_cast<size_t>(client) * nk + s.p] += s.n;
+    emit_pieces(spans, 0, spans.size(), 0, out);
+    for (const auto& s : spans) {
+        frozen_[s.p] = 1;
+        // add [koff, koff + n) to the written ranges (disjoint from them, checked above)
+        auto& w = written_[s.p];
+        w.emplace_back(s.koff, s.koff + s.n);
+        std::sort(w.begin(), w.end());
+        std::vector<std::pair<uint64_t, uint64_t>> merged;
+        for (const auto& r : w) {
+            if (!merged.empty() && merged.back().second == r.first) merged.back().second = r.second;
+            else merged.push_back(r);
+        }
+        w.swap(merged);
+    }
+    for (const Piece& pc : *out) {
+        double total = 0.0;
+        key_total(pc.key, &total, nullptr);
+        totals->push_back(total);
     }
     return kOk;
 }
@@ -348,7 +444,15 @@ int32_t Ledger::plan_finalize(std::vector<FinItem>* out, std::string* err) const
         uint32_t reporters = 0;
         key_total(p, &total, &reporters);
         if (reporters == 0 || total == 0.0) continue;
-        out->push_back({p, acc_off_[p], flat_off_[p], numel_[p], total, reporters});
+        // the key less the ranges final contributions wrote
+        uint64_t a = 0;
+        for (const auto& w : written_[p]) {
+            if (w.first > a)
+                out->push_back({p, acc_off_[p] + a, flat_off_[p] + a, w.first - a, total, reporters, a});
+            a = w.second;
+        }
+        if (a < numel_[p])
+            out->push_back({p, acc_off_[p] + a, flat_off_[p] + a, numel_[p] - a, total, reporters, a});
     }
     return kOk;
 }

@@ -47,14 +47,16 @@ struct Piece {
     bool first;           // no earlier contribution to these elements this round
 };
 
-// One key to write at finalize.
+// One range of a key to write at finalize: the whole key, or the part of it that no final
+// contribution has written yet.
 struct FinItem {
     uint32_t key;
     uint64_t acc_idx;     // start in the padded running sum
     uint64_t flat_off;    // start in the flat (unpadded) layout
-    uint64_t numel;
+    uint64_t numel;       // elements of the range
     double total;         // N_p
     uint32_t reporters;   // |S_p|
+    uint64_t koff = 0;    // start of the range within the key
 };
 
 class Ledger {
@@ -86,7 +88,19 @@ public:
     int32_t record_whole_keys(uint32_t client, double weight, uint32_t n, const int64_t* keys,
                               std::string* err);
 
-    // Check completeness and list the keys to write (N_p > 0).  Changes nothing.
+    // Validate and record ONE client's last contribution to a range (fa_accumulate_final):
+    // as plan_accumulate with J = 1, and for every key the range touches, every OTHER
+    // sender of that key has already sent all of it (else kErrIncomplete), so the key's
+    // weight total is final.  On success `out` holds the pieces and `totals` each piece's
+    // N_p (this client included); the keys touched are frozen (no new sender from now on)
+    // and the range is marked written (no further contribution to it; plan_finalize
+    // leaves it out).  All or nothing: on error nothing changes.
+    int32_t plan_accumulate_final(uint32_t client, double weight, int64_t key, uint64_t offset,
+                                  uint64_t len, std::vector<Piece>* out, std::vector<double>* totals,
+                                  std::string* err);
+
+    // Check completeness and list the ranges to write: every key with N_p > 0, less what
+    // final contributions have already written.  Changes nothing.
     int32_t plan_finalize(std::vector<FinItem>* out, std::string* err) const;
 
     // Close the round: accumulation is refused until reset().
@@ -125,6 +139,10 @@ private:
     // mark all of [a, b) started.
     void split_and_mark(uint32_t p, uint64_t a, uint64_t b,
                         std::vector<std::pair<uint64_t, bool>>* runs_end_first);
+    // Spans that a contribution of client c may not make: a new sender of a frozen key, or
+    // a range a final contribution has written.  kOk or kErrState (with *err).
+    int32_t check_frozen(uint32_t c, const std::vector<Span>& spans, size_t from, size_t to,
+                         std::string* err) const;
 
     std::vector<uint64_t> numel_, flat_off_, acc_off_;
     uint64_t total_ = 0, padded_ = 0;
@@ -133,6 +151,9 @@ private:
     std::vector<uint8_t> has_weight_;   // per client
     std::vector<uint64_t> recv_;        // [client * n_keys + key]
     std::vector<std::vector<std::pair<uint64_t, uint64_t>>> started_;  // per key, sorted disjoint
+    std::vector<std::vector<std::pair<uint64_t, uint64_t>>> written_;  // per key: ranges a final
+                                                                       // contribution wrote
+    std::vector<uint8_t> frozen_;       // per key: its senders are final
     bool closed_ = false;
 };
 

@@ -38,6 +38,10 @@ def lib():
         L.lg_reset.argtypes = [vp]
         L.lg_key_total.argtypes = [vp, u32, ctypes.POINTER(f64), ctypes.POINTER(u32)]
         L.lg_key_total.restype = i32
+        L.lg_accumulate_final.argtypes = [vp, u32, f64, i64, u64, u64, vp, vp, u32, ctypes.POINTER(u32)]
+        L.lg_accumulate_final.restype = i32
+        L.lg_finalize_ranges.argtypes = [vp, vp, vp, u32, ctypes.POINTER(u32)]
+        L.lg_finalize_ranges.restype = i32
         L.lg_acc_off.argtypes = [vp, u32]
         L.lg_acc_off.restype = u64
         L.lg_padded.argtypes = [vp]
@@ -96,6 +100,25 @@ class Ledger:
         st = lib().lg_finalize(self.h, rows, tot, 4096, ctypes.byref(n))
         items = [tuple(rows[5 * i:5 * i + 5]) + (tot[i],) for i in range(min(n.value, 4096))]
         return st, items
+
+    def accumulate_final(self, client, weight, key, offset, length):
+        """Returns (status, pieces as in accumulate, each piece's N_p)."""
+        rows = (ctypes.c_uint64 * (5 * 4096))()
+        tot = (ctypes.c_double * 4096)()
+        n = ctypes.c_uint32()
+        st = lib().lg_accumulate_final(self.h, client, weight, key, offset, length, rows, tot, 4096,
+                                       ctypes.byref(n))
+        m = min(n.value, 4096)
+        return st, [tuple(rows[5 * i:5 * i + 5]) for i in range(m)], [tot[i] for i in range(m)]
+
+    def finalize_ranges(self):
+        """The ranges fa_finalize would write, without closing the round: (status,
+        [(key, koff, acc_idx, flat_off, numel, reporters, total)])."""
+        rows = (ctypes.c_uint64 * (6 * 4096))()
+        tot = (ctypes.c_double * 4096)()
+        n = ctypes.c_uint32()
+        st = lib().lg_finalize_ranges(self.h, rows, tot, 4096, ctypes.byref(n))
+        return st, [tuple(rows[6 * i:6 * i + 6]) + (tot[i],) for i in range(min(n.value, 4096))]
 
     def reset(self):
         lib().lg_reset(self.h)

@@ -97,6 +97,47 @@ int32_t lg_finalize(void* p, uint64_t* rows, double* totals, uint32_t max_rows, 
     return st;
 }
 
+// one client's final contribution; pieces out as lg_accumulate, plus each piece's N_p
+int32_t lg_accumulate_final(void* p, uint32_t client, double weight, int64_t key, uint64_t offset,
+                            uint64_t len, uint64_t* rows, double* totals, uint32_t max_rows,
+                            uint32_t* n_rows) {
+    auto* h = static_cast<Handle*>(p);
+    std::vector<double> tot;
+    int32_t st = h->lg.plan_accumulate_final(client, weight, key, offset, len, &h->pieces, &tot, &h->err);
+    *n_rows = static_cast<uint32_t>(h->pieces.size());
+    for (uint32_t i = 0; i < *n_rows && i < max_rows; ++i) {
+        const auto& q = h->pieces[i];
+        uint64_t* r = rows + 5 * i;
+        r[0] = q.key;
+        r[1] = q.chunk_off;
+        r[2] = q.acc_idx;
+        r[3] = q.len;
+        r[4] = q.first ? 1 : 0;
+        totals[i] = tot[i];
+    }
+    return st;
+}
+
+// ranges to write (without closing the round): rows of (key, koff, acc_idx, flat_off, numel,
+// reporters) and totals
+int32_t lg_finalize_ranges(void* p, uint64_t* rows, double* totals, uint32_t max_rows, uint32_t* n_rows) {
+    auto* h = static_cast<Handle*>(p);
+    int32_t st = h->lg.plan_finalize(&h->items, &h->err);
+    *n_rows = static_cast<uint32_t>(h->items.size());
+    for (uint32_t i = 0; i < *n_rows && i < max_rows; ++i) {
+        const auto& q = h->items[i];
+        uint64_t* r = rows + 6 * i;
+        r[0] = q.key;
+        r[1] = q.koff;
+        r[2] = q.acc_idx;
+        r[3] = q.flat_off;
+        r[4] = q.numel;
+        r[5] = q.reporters;
+        totals[i] = q.total;
+    }
+    return st;
+}
+
 void lg_reset(void* p) { static_cast<Handle*>(p)->lg.reset(); }
 
 int32_t lg_key_total(void* p, uint32_t key, double* total, uint32_t* reporters) {

@@ -357,3 +357,84 @@ def test_whole_keys_errors_record_nothing():
     st, _ = lg.finalize()
     assert st == 0
     assert lg.whole_keys(2, 1.0, [0]) == -6             # closed
+
+
+# ------------------------------------------------------------------ final contributions
+# fa_accumulate_final: the last contribution to a range, fused with its finalize.  N_p is
+# final once every other sender of the key has sent all of it; the key then takes no new
+# sender, the range no further contribution, and fa_finalize writes only the rest.
+
+def test_final_contribution_totals_and_written_ranges():
+    lg = Ledger([10, 6], 3)
+    assert lg.accumulate([0], [2.0], 0, 0, 10)[0] == OK
+    st, pieces, totals = lg.accumulate_final(1, 3.0, 0, 0, 4)
+    assert st == OK and pieces == [(0, 0, 0, 4, 0)] and totals == [5.0]
+    # the rest of key 0 through a plain call, key 1 untouched by any final call
+    assert lg.accumulate([1], [3.0], 0, 4, 6)[0] == OK
+    assert lg.accumulate([2], [1.0], 1, 0, 6)[0] == OK
+    st, items = lg.finalize_ranges()
+    assert st == OK
+    assert items == [(0, 4, 4, 4, 6, 2, 5.0), (1, 0, 32, 10, 6, 1, 1.0)]
+    # everything written by final calls: nothing left for fa_finalize
+    lg.reset()
+    lg.accumulate([0], [2.0], 0, 0, 10)
+    st, _, totals = lg.accumulate_final(1, 3.0, 0, 0, 10)
+    assert st == OK and totals == [5.0]
+    assert lg.finalize_ranges() == (OK, [])
+
+
+def test_final_needs_every_other_sender_complete():
+    lg = Ledger([10], 3)
+    assert lg.accumulate([0], [2.0], 0, 0, 6)[0] == OK
+    st, pieces, _ = lg.accumulate_final(1, 3.0, 0, 0, 10)
+    assert st == INCOMPLETE and pieces == []
+    assert lg.key_total(0) == (OK, 2.0, 1)               # nothing recorded
+    assert lg.accumulate([1], [3.0], 0, 0, 10)[0] == OK  # the key is not frozen
+    assert lg.accumulate([0], [2.0], 0, 6, 4)[0] == OK
+    assert lg.finalize_ranges()[1] == [(0, 0, 0, 0, 10, 2, 5.0)]
+
+
+def test_frozen_key_refuses_new_senders_and_written_ranges():
+    lg = Ledger([8, 8], 4)
+    lg.accumulate([0], [1.0], 0, 0, 8)
+    assert lg.accumulate_final(1, 2.0, 0, 2, 3)[0] == OK            # [2, 5) written
+    assert lg.accumulate([2], [4.0], 0, 0, 8)[0] == STATE            # new sender of a frozen key
+    assert lg.accumulate_keys(2, 4.0, [(0, 0, 1)])[0] == STATE
+    assert lg.whole_keys(2, 4.0, [0]) == STATE
+    assert lg.accumulate([1], [2.0], 0, 4, 2)[0] == STATE            # overlaps [2, 5)
+    assert lg.accumulate_final(1, 2.0, 0, 0, 3)[0] == STATE
+    # all or nothing: a keys call with one bad chunk records none of them
+    assert lg.accumulate_keys(1, 2.0, [(0, 0, 2), (0, 4, 1)])[0] == STATE
+    assert lg.key_total(0) == (OK, 3.0, 2)
+    assert lg.accumulate([1], [2.0], 0, 0, 2)[0] == OK               # outside the written range
+    assert lg.accumulate_final(1, 2.0, 0, 5, 3)[0] == OK
+    assert lg.accumulate([2], [4.0], 1, 0, 8)[0] == OK               # key 1 is not frozen
+    st, items = lg.finalize_ranges()
+    assert st == OK and items == [(0, 0, 0, 0, 2, 2, 3.0), (1, 0, 32, 8, 8, 1, 4.0)]
+    lg.reset()                                                        # a new round forgets it all
+    assert lg.accumulate([2], [4.0], 0, 0, 8)[0] == OK
+
+
+def test_final_flat_chunk_across_keys_and_sole_sender():
+    lg = Ledger([5, 7, 3], 2)
+    lg.accumulate([0], [2.0], 1, 0, 7)
+    # client 1: a flat chunk over the end of key 0, all of key 1, the start of key 2;
+    # keys 0 and 2 have no other sender (first contribution, N_p = 6), key 1 has client 0
+    st, pieces, totals = lg.accumulate_final(1, 6.0, -1, 3, 10)
+    assert st == OK
+    assert pieces == [(0, 0, 3, 2, 1), (1, 2, 32, 7, 0), (2, 9, 64, 1, 1)]
+    assert totals == [6.0, 8.0, 6.0]
+    st, items = lg.finalize_ranges()
+    assert st == INCOMPLETE                                           # client 1 owes the rest of keys 0, 2
+    assert lg.accumulate([1], [6.0], -1, 0, 3)[0] == OK
+    assert lg.accumulate([1], [6.0], 2, 1, 2)[0] == OK
+    st, items = lg.finalize_ranges()
+    assert st == OK and items == [(0, 0, 0, 0, 3, 1, 6.0), (2, 1, 65, 13, 2, 1, 6.0)]
+
+
+def test_final_zero_weight_key_reports_a_zero_total():
+    lg = Ledger([4], 2)
+    lg.accumulate([0], [0.0], 0, 0, 4)
+    st, _, totals = lg.accumulate_final(1, 0.0, 0, 0, 4)
+    assert st == OK and totals == [0.0]
+    assert lg.finalize_ranges() == (OK, [])
