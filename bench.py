@@ -57,22 +57,28 @@ def _peaks():
 
 
 # --------------------------------------------------------------------------- round drivers
-def stream_client(fa, ctx, w, k, base_ptr, stream):
-    """Client k's whole update (flat layout at base_ptr, device or host) in chunk_elems pieces."""
+def stream_client(fa, ctx, w, k, base_ptr, stream, outs=None):
+    """Client k's whole update (flat layout at base_ptr, device or host) in chunk_elems
+    pieces; through fa_accumulate_final into `outs` (an fa.out_array) when given."""
     P, ce = w.P, w.chunk_elems or w.P
     es = 2 if w.dtype_in == "bf16" else 4
     calls = 0
     for c0 in range(0, P, ce):
         n = min(ce, P - c0)
-        fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base_ptr + c0 * es, n, stream)
+        if outs is not None:
+            fa.fa_accumulate_final(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base_ptr + c0 * es, n, outs,
+                                   stream)
+        else:
+            fa.fa_accumulate(ctx, k, w.weights[k], fa.FA_KEY_FLAT, c0, base_ptr + c0 * es, n, stream)
         calls += 1
     return calls
 
 
-def run_streamed_round(w, resident=False, flags=0):
+def run_streamed_round(w, resident=False, flags=0, fused=False):
     """One full round on the device, inputs from the device generator, streamed
     client by client exactly as the bench does; returns the flat bf16 output.
-    `flags` adds fa_opts flags (FA_COMPENSATED for the compensated mode)."""
+    `flags` adds fa_opts flags (FA_COMPENSATED for the compensated mode); `fused` sends the
+    last client through fa_accumulate_final, as the bench's timed round does."""
     import torch
 
     import server_side_fedavg_gb300 as fa
@@ -89,15 +95,16 @@ def run_streamed_round(w, resident=False, flags=0):
                 synth.client_fill_device(w, k, 0, w.P, bufs[k].data_ptr(), s.cuda_stream)
         else:
             buf = torch.empty(w.P, dtype=tdt, device="cuda")
+        out = torch.empty(w.P, dtype=torch.int16 if w.dtype_out == "bf16" else torch.float32,
+                          device="cuda")
+        outs = fa.out_array([out])
         for k in range(w.K):
             if resident:
                 ptr = bufs[k].data_ptr()
             else:
                 synth.client_fill_device(w, k, 0, w.P, buf.data_ptr(), s.cuda_stream)
                 ptr = buf.data_ptr()
-            stream_client(fa, ctx, w, k, ptr, s.cuda_stream)
-        out = torch.empty(w.P, dtype=torch.int16 if w.dtype_out == "bf16" else torch.float32,
-                          device="cuda")
+            stream_client(fa, ctx, w, k, ptr, s.cuda_stream, outs if fused and k == w.K - 1 else None)
         fa.fa_finalize(ctx, [out], s.cuda_stream)
         fa.fa_sync(ctx)
         torch.cuda.synchronize()
@@ -732,7 +739,9 @@ def run_ours(args, world, rank, local, pg):
                    "last_client": ("fa_accumulate_final (its kernels write the aggregate)" if fused
                                    else "fa_accumulate, then fa_finalize"),
                    "wall_s": round(wall, 3)},
-        "roofline": {"bound": "hbm", "kernel": f"accumulate_bulk_kernel<{w.dtype_in}>",
+        "roofline": {"bound": "hbm",
+                     "kernel": (f"accumulate_bulk_kernel<{w.dtype_in}> (the last client's launches in the "
+                                f"final form)" if fused else f"accumulate_bulk_kernel<{w.dtype_in}>"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": int(acc_bytes_per_launch),

@@ -216,19 +216,22 @@ def _check_sampled(got, xs, w, what, strict=False):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,flags", [("vlm2b", 0), ("llama7b", 0), ("llama7b", fa.FA_COMPENSATED)])
-def test_full_size_streamed_every_element(name, flags):
+@pytest.mark.parametrize("name,flags,fused", [("vlm2b", 0, False), ("llama7b", 0, False), ("llama7b", 0, True),
+                                              ("llama7b", fa.FA_COMPENSATED, False)])
+def test_full_size_streamed_every_element(name, flags, fused):
     """The full-size round streamed exactly as bench.py streams it (flat chunks of 64 / 256
     MiB, clients in id order), compared with the oracle on EVERY element, key by key.
-    Default mode: the bf16 rule with the fp32-sum escape; compensated mode
-    (FA_COMPENSATED): the plain rule, no escape."""
+    `fused`: the last client through fa_accumulate_final, the bench's timed round; else
+    every client through fa_accumulate, then fa_finalize.  Default mode: the bf16 rule
+    with the fp32-sum escape; compensated mode (FA_COMPENSATED): the plain rule, no
+    escape."""
     import bench
     from tests.full_compare import compare_every_element
     w = W.make(name)
     free, _ = torch.cuda.mem_get_info()
     need = w.P * 2 * 2 + w.P * 4 * (2 if flags else 1) + (8 << 30)
     assert free > need, f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}"
-    out = bench.run_streamed_round(w, flags=flags)
+    out = bench.run_streamed_round(w, flags=flags, fused=fused)
     got = out.cpu().numpy().view(np.uint16)
     del out
     torch.cuda.empty_cache()
