@@ -723,7 +723,8 @@ def run_ours(args, world, rank, local, pg):
             a2.e2e_steps = args.e2e_staged_steps
             st = run_e2e(a2, w, layout, s, pg, world, hb)
             e2e["staged"] = {k: st[k] for k in ("value", "ms_per_step", "accumulate_ms", "finalize_ms",
-                                                 "link_frac", "accumulate_link_frac", "ingest", "output")}
+                                                 "host_call_ms", "host_cpu_ms", "link_frac",
+                                                 "accumulate_link_frac", "ingest", "output")}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -1003,12 +1004,15 @@ def run_e2e(args, w, layout, s, pg, world, hb):
     fused = (not part and not args.stage_host and not args.no_fused and out_pinned and w.K >= 2)
     out_arr = fa.out_array([out])
 
+    host = {"wall": 0.0, "cpu": 0.0}   # the calling thread's time in the accumulate calls
+
     def step(evs=None):
         # evs: (start, after the accumulate calls, after finalize) on the stream
         fa.fa_reset(ctx)
         if evs is not None:
             evs[0].record(s)
         i = 0
+        hw0, hc0 = time.perf_counter(), time.thread_time()
         for k in range(w.K):
             if part:
                 ks, os_, ps, ls = key_args[k]
@@ -1028,6 +1032,8 @@ def run_e2e(args, w, layout, s, pg, world, hb):
                                      pool[i % pool_n].data_ptr(), n, sh)
                 i += 1
         if evs is not None:
+            host["wall"] += time.perf_counter() - hw0
+            host["cpu"] += time.thread_time() - hc0
             evs[1].record(s)
         fa.fa_finalize(ctx, [out], sh)
         if evs is not None:
@@ -1072,6 +1078,8 @@ def run_e2e(args, w, layout, s, pg, world, hb):
             "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
             "ms_per_step": round(dt / args.e2e_steps * 1e3, 2),
             "accumulate_ms": round(acc_ms, 3), "finalize_ms": round(fin_ms, 3),
+            "host_call_ms": round(host["wall"] * 1e3 / args.e2e_steps, 1),
+            "host_cpu_ms": round(host["cpu"] * 1e3 / args.e2e_steps, 1),
             "h2d_peak_gbs": round(link, 1),
             "link_frac": round(h2d * args.e2e_steps / dt / 1e9 / link, 3),
             "accumulate_link_frac": round(h2d / (acc_ms * 1e-3) / 1e9 / link, 3),
