@@ -247,7 +247,10 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
  * (FA_ERR_INCOMPLETE).  From this call on the key takes no new sender, and the range
  * takes no further contribution (FA_ERR_STATE); fa_finalize later writes the rest of the
  * layout and leaves this range as written.  A key none of whose senders has weight
- * (N_p == 0) is not written.  Ownership and errors otherwise as fa_accumulate.
+ * (N_p == 0) is not written.  The outputs hold plain means, so a round with a final
+ * contribution ends in fa_finalize, not fa_finalize_apply (FA_ERR_STATE there): a delta
+ * round sends its last client through fa_accumulate.  Ownership and errors otherwise as
+ * fa_accumulate.
  * Errors: FA_ERR_ARG, FA_ERR_RANGE, FA_ERR_WEIGHT, FA_ERR_INCOMPLETE, FA_ERR_STATE,
  * FA_ERR_CUDA, FA_ERR_TIMEOUT. */
 fa_status fa_accumulate_final(fa_ctx* ctx, uint32_t client_id, double weight_nk, int64_t key,
@@ -284,7 +287,9 @@ fa_status fa_finalize(fa_ctx* ctx, void* const* out_ptrs, void* stream);
  * refused); out may equal base (in place).
  * Keys with N_p == 0 are not written (out keeps its contents; in place, the model is
  * unchanged).  Otherwise as fa_finalize (closes the round, non-destructive, may repeat).
- * Errors: as fa_finalize; FA_ERR_ARG for host memory or a non-finite server_lr. */
+ * Errors: as fa_finalize; FA_ERR_ARG for host memory or a non-finite server_lr;
+ * FA_ERR_STATE, changing nothing, after an fa_accumulate_final this round (the ranges it
+ * wrote hold plain means). */
 fa_status fa_finalize_apply(fa_ctx* ctx, const void* const* base_ptrs, void* const* out_ptrs,
                             double server_lr, void* stream);
 

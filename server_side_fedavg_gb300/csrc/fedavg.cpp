@@ -887,6 +887,10 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
         return fail(c, FA_ERR_STATE, "this round was reduced by fa_reduce_resident: its outputs are already written");
     if (c->broken) return fail(c, FA_ERR_CUDA, "an earlier CUDA failure left this round inconsistent: call fa_reset");
     if (out_ptrs == nullptr) return fail(c, FA_ERR_ARG, "out_ptrs is NULL");
+    if (apply && c->ledger.has_final())
+        return fail(c, FA_ERR_STATE,
+                    "fa_finalize_apply: fa_accumulate_final wrote plain means this round; a delta round "
+                    "sends its last client through fa_accumulate");
     const bool flat = (c->flags & FA_FLAT_OUT) != 0;
     std::string e;
     {

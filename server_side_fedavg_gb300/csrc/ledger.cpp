@@ -68,6 +68,12 @@ bool Ledger::has_contributions() const {
     return false;
 }
 
+bool Ledger::has_final() const {
+    for (const auto& w : written_)
+        if (!w.empty()) return true;
+    return false;
+}
+
 void Ledger::reset() {
     std::fill(weight_.begin(), weight_.end(), 0.0);
     std::fill(has_weight_.begin(), has_weight_.end(), 0);

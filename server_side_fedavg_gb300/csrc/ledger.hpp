@@ -120,6 +120,8 @@ public:
     bool closed() const { return closed_; }
     // True once any client has sent any element this round.
     bool has_contributions() const;
+    // True once a final contribution (plan_accumulate_final) has written a range this round.
+    bool has_final() const;
 
 private:
     // One run of a chunk inside one key.

@@ -42,6 +42,8 @@ def lib():
         L.lg_accumulate_final.restype = i32
         L.lg_finalize_ranges.argtypes = [vp, vp, vp, u32, ctypes.POINTER(u32)]
         L.lg_finalize_ranges.restype = i32
+        L.lg_has_final.argtypes = [vp]
+        L.lg_has_final.restype = i32
         L.lg_acc_off.argtypes = [vp, u32]
         L.lg_acc_off.restype = u64
         L.lg_padded.argtypes = [vp]
@@ -119,6 +121,10 @@ class Ledger:
         n = ctypes.c_uint32()
         st = lib().lg_finalize_ranges(self.h, rows, tot, 4096, ctypes.byref(n))
         return st, [tuple(rows[6 * i:6 * i + 6]) + (tot[i],) for i in range(min(n.value, 4096))]
+
+    def has_final(self):
+        """Whether a final contribution has written a range this round."""
+        return bool(lib().lg_has_final(self.h))
 
     def reset(self):
         lib().lg_reset(self.h)

@@ -118,6 +118,9 @@ int32_t lg_accumulate_final(void* p, uint32_t client, double weight, int64_t key
     return st;
 }
 
+// whether a final contribution has written a range this round
+int32_t lg_has_final(void* p) { return static_cast<Handle*>(p)->lg.has_final() ? 1 : 0; }
+
 // ranges to write (without closing the round): rows of (key, koff, acc_idx, flat_off, numel,
 // reporters) and totals
 int32_t lg_finalize_ranges(void* p, uint64_t* rows, double* totals, uint32_t max_rows, uint32_t* n_rows) {

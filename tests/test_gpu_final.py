@@ -219,6 +219,12 @@ def test_refusals_leave_the_round_unchanged():
             fa.fa_accumulate(ctx, 2, 4.0, 0, 0, d[2][0], 64)
         assert e.value.status == fa.FA_ERR_STATE
         fa.fa_accumulate(ctx, 2, 4.0, 1, 0, d[2][1], 64)                         # key 1 is open
+        base = [sentinel(n, "bf16") for n in numels]
+        with pytest.raises(fa.FedAvgError) as e:                                 # plain means
+            fa.fa_finalize_apply(ctx, base, outs, 0.5)
+        assert e.value.status == fa.FA_ERR_STATE
+        torch.cuda.synchronize()
+        assert np.all(to_np(outs[1], "bf16") == 0x7FBF)                          # nothing written
         fa.fa_finalize(ctx, outs)
         fa.fa_sync(ctx)
         want0, _, _ = oracle.fedavg_key([1.0, 2.0], [True, True], [xs[0][0], xs[1][0]], "bf16", "bf16")

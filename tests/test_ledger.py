@@ -367,8 +367,10 @@ def test_whole_keys_errors_record_nothing():
 def test_final_contribution_totals_and_written_ranges():
     lg = Ledger([10, 6], 3)
     assert lg.accumulate([0], [2.0], 0, 0, 10)[0] == OK
+    assert not lg.has_final()
     st, pieces, totals = lg.accumulate_final(1, 3.0, 0, 0, 4)
     assert st == OK and pieces == [(0, 0, 0, 4, 0)] and totals == [5.0]
+    assert lg.has_final()
     # the rest of key 0 through a plain call, key 1 untouched by any final call
     assert lg.accumulate([1], [3.0], 0, 4, 6)[0] == OK
     assert lg.accumulate([2], [1.0], 1, 0, 6)[0] == OK
@@ -377,6 +379,7 @@ def test_final_contribution_totals_and_written_ranges():
     assert items == [(0, 4, 4, 4, 6, 2, 5.0), (1, 0, 32, 10, 6, 1, 1.0)]
     # everything written by final calls: nothing left for fa_finalize
     lg.reset()
+    assert not lg.has_final()
     lg.accumulate([0], [2.0], 0, 0, 10)
     st, _, totals = lg.accumulate_final(1, 3.0, 0, 0, 10)
     assert st == OK and totals == [5.0]
@@ -389,6 +392,7 @@ def test_final_needs_every_other_sender_complete():
     st, pieces, _ = lg.accumulate_final(1, 3.0, 0, 0, 10)
     assert st == INCOMPLETE and pieces == []
     assert lg.key_total(0) == (OK, 2.0, 1)               # nothing recorded
+    assert not lg.has_final()
     assert lg.accumulate([1], [3.0], 0, 0, 10)[0] == OK  # the key is not frozen
     assert lg.accumulate([0], [2.0], 0, 6, 4)[0] == OK
     assert lg.finalize_ranges()[1] == [(0, 0, 0, 0, 10, 2, 5.0)]
