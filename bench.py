@@ -44,6 +44,9 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 METRIC = "client-update GB/s aggregated (1×GB300) and % of HBM peak; oracle host GB/s"
+# rounds of at most this many client bytes are also timed captured into a CUDA graph and
+# replayed (the small, launch-bound models; a 7B round is bound by HBM, not by its calls)
+GRAPH_MAX_BYTES = 4 << 30
 DEFAULT_WORKLOAD = "llama7b"
 
 
@@ -535,9 +538,10 @@ def run_ours(args, world, rank, local, pg):
     fused = not part and not args.no_fused and w.K >= 2
     out_arr = fa.out_array([out])
 
-    def step(evs=None, final=fused):
+    def step(evs=None, final=fused, sh=sh, reset=True):
         # evs: (start, after the accumulate launches, after finalize) on the launching stream
-        fa.fa_reset(ctx)
+        if reset:
+            fa.fa_reset(ctx)
         if evs is not None:
             evs[0].record(s)
         for k in range(w.K):
@@ -632,6 +636,16 @@ def run_ours(args, world, rank, local, pg):
     else:
         fin_gbs = fin_b / (fin_ms / args.steps * 1e-3) / 1e9
 
+    # ---- a launch-bound round (a small model) captured once into a CUDA graph and replayed:
+    # the host's calls leave the round, one graph launch remains
+    graph_line = None
+    if not args.no_graph and client_bytes <= GRAPH_MAX_BYTES:
+        graph_line = graph_replay(fa, ctx, lambda gsh: step(sh=gsh, reset=False), max(20, args.steps))
+        graph_line["calls_wall_ms_per_round"] = round(wall / args.steps * 1e3, 4)
+        graph_line["value"] = round(world * client_bytes / (graph_line["wall_ms_per_round"] * 1e-3) / 1e9, 2)
+        graph_line["unit"] = "GB/s"
+        step(final=False)   # the delta-round finalize below reads this round's sum
+
     # ---- a delta round's finalize: the same aggregate applied in place to a base model
     # (fa_finalize_apply, server_lr 0.5): reads the sum and the base, writes the output
     for _ in range(2):
@@ -688,12 +702,17 @@ def run_ours(args, world, rank, local, pg):
         torch.cuda.synchronize()
         rms = sum(a.elapsed_time(b) for a, b in evr) / len(evr)
         rbytes = w.P * (w.K * si + so)
+        rgraph = None
+        if not args.no_graph and client_bytes <= GRAPH_MAX_BYTES:
+            rgraph = graph_replay(fa, ctx, lambda sh: fa.fa_reduce_resident(ctx, ids, w.weights, ptrs, [out], sh),
+                                  max(20, args.steps))
         resident_line = {"value": round(client_bytes / (rms * 1e-3) / 1e9, 2), "unit": "GB/s",
                          "device_ms_per_round": round(rms, 4), "wall_ms_per_round": round(wall_ms, 4),
                          "value_wall": round(client_bytes / (wall_ms * 1e-3) / 1e9, 2),
                          "hbm_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1),
                          "hbm_frac": round(rbytes / (rms * 1e-3) / 1e9 / peak, 4),
                          "bytes_per_round": int(rbytes), "launches_per_round": launches_r,
+                         "graph": rgraph,
                          "kernel": resident_kernel(w)}
 
     fa.fa_close(ctx)
@@ -750,6 +769,7 @@ def run_ours(args, world, rank, local, pg):
                      "traffic": profiled_traffic(acc_bytes_per_launch)},
         "gpu_launches": int(launches),
         "unfused": unfused_line,
+        "graph": graph_line,
         "resident": resident_line,
         "subsets": subsets_line,
         "compensated": comp_line,
@@ -763,6 +783,36 @@ def run_ours(args, world, rank, local, pg):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def graph_replay(fa, ctx, calls, reps):
+    """A round captured once into a CUDA graph and replayed `reps` times back to back on
+    the current stream: wall and device (CUDA events) ms per replayed round.  calls(stream)
+    issues the round's library calls on the capturing stream; fa_reset runs before the
+    capture (it waits for the context's work) and after it, leaving the context as it was."""
+    import torch
+
+    fa.fa_reset(ctx)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    cs = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        g.replay()
+    e1.record(cs)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) / reps
+    dev = e0.elapsed_time(e1) / reps
+    del g
+    fa.fa_reset(ctx)
+    return {"wall_ms_per_round": round(wall * 1e3, 4), "device_ms_per_round": round(dev, 4)}
 
 
 def run_subsets(args, w, ctx, bufs, out, s, peak):
@@ -809,12 +859,16 @@ def run_subsets(args, w, ctx, bufs, out, s, peak):
     dev_ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
     b = subset_bytes(w)
     cb = w.client_bytes()
+    graph = None if args.no_graph else graph_replay(
+        fa, ctx, lambda sh: fa.fa_reduce_subsets(ctx, ids, w.weights, ptrs, table, [out], sh),
+        max(20, args.steps))
     return {"value": round(cb / (dev_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "device_ms_per_round": round(dev_ms, 4), "wall_ms_per_round": round(wall * 1e3, 4),
             "value_wall": round(cb / wall / 1e9, 2),
             "hbm_gbs": round(b / (dev_ms * 1e-3) / 1e9, 1),
             "hbm_frac": round(b / (dev_ms * 1e-3) / 1e9 / peak, 4),
             "bytes_per_round": int(b), "launches_per_round": int(launches),
+            "graph": graph,
             "kernel": subsets_kernel(w)}
 
 
@@ -1197,6 +1251,8 @@ def main(argv=None):
     ap.add_argument("--ref-elems", type=int, default=64 << 20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-resident", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the rounds captured into a CUDA graph and replayed")
     ap.add_argument("--no-fused", action="store_true",
                     help="send the last client through fa_accumulate too (no fa_accumulate_final)")
     ap.add_argument("--no-compensated", action="store_true",

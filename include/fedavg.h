@@ -45,6 +45,21 @@
  *    chained across streams with events, so contributions apply in call
  *    order and two streams never race on the running sum.
  *  - Sizes and offsets are in ELEMENTS of the input dtype.
+ *  - CUDA graphs: a round whose calls are issued on a stream that is capturing
+ *    (cudaStreamBeginCapture) is recorded into the graph and replays as it ran:
+ *    the same kernels on the same buffers with the same weights, over whatever
+ *    the client buffers hold at replay.  Captured calls issue only kernels whose
+ *    tables ride in their own parameters (a finalize of at most 600 ranges, a
+ *    one-pass round whose tables fit a launch) and copies between fixed
+ *    buffers; a call that needs the host while the round runs -- a staged or
+ *    pageable chunk, a pageable output, a staged output before the context's
+ *    first finalize, a one-pass round too large for its parameters (that round
+ *    is then to be reset) -- returns FA_ERR_STATE and issues nothing, so the
+ *    capture goes on.  Call fa_reset
+ *    (which waits for the context's work) before the capture, not inside it;
+ *    the context's host bookkeeping is that of the captured round, so the
+ *    context serves the graph: replays are ordered by the stream they are
+ *    launched on, and fa_reset comes before any further direct call.
  */
 #ifndef FEDAVG_H
 #define FEDAVG_H

@@ -78,7 +78,9 @@ struct fa_ctx {
     std::vector<uint8_t> slot_used;
     uint32_t next_slot = 0;
 
-    fa::FinSeg* fin_dev = nullptr;
+    std::unique_ptr<fa::FinArgs> fin_args;   // a finalize launch's parameters (its table
+                                             // inline up to kFinInlineSegs ranges)
+    fa::FinSeg* fin_dev = nullptr;           // larger tables: uploaded from fin_host
     fa::FinSeg* fin_host = nullptr;
     size_t fin_cap = 0;           // entries of both (n_keys; more once final contributions split keys)
     cudaEvent_t fin_ev = nullptr;
@@ -92,8 +94,8 @@ struct fa_ctx {
     bool gath_pending = false;
     // ... or, for a small round, its tables in the launch's parameters
     std::unique_ptr<fa::GathInline> gath_inline;
-    uint32_t* gath_slots = nullptr;   // two tile counters; the kernel zeroes the unused one
-    uint32_t gath_slot = 0;           // the counter the next inline launch uses
+    uint32_t* gath_counter = nullptr;   // an inline subset reduce's two counter words (0 between
+                                        // launches: each launch leaves them so)
     void* out_stage = nullptr;
 
     unsigned int* err_dev = nullptr;     // this context's device error word (kernels OR bits in)
@@ -212,12 +214,22 @@ Mem classify(const void* p, int device, bool* other_device, bool* in_place = nul
     }
 }
 
+// Whether `s` is capturing into a CUDA graph.  A captured call issues only work a graph
+// replays as it ran -- kernels whose tables ride in their parameters, copies between fixed
+// buffers -- and refuses (FA_ERR_STATE) what needs the host while the round runs: staged
+// chunks, pageable memory, table uploads, allocations.  Captured work is ordered by the
+// stream it is replayed on, not by the context's chain of calls.
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(s, &st) == cudaSuccess && st != cudaStreamCaptureStatusNone;
+}
+
 // Make `s` wait for everything queued on the context so far.  Work on the same
 // stream as the last record is already ordered after it (stream ids are unique
 // for the life of the context, unlike handles), so the wait is only issued when
 // the stream changes -- a cross-stream wait costs a full launch latency.
 fa_status chain_in(fa_ctx* c, cudaStream_t s) {
-    if (!c->chain_valid) return FA_OK;
+    if (!c->chain_valid || capturing(s)) return FA_OK;
     unsigned long long id = 0;
     FA_CUDA(c, cudaStreamGetId(s, &id));
     if (id != c->chain_stream_id) FA_CUDA(c, cudaStreamWaitEvent(s, c->chain, 0));
@@ -225,6 +237,10 @@ fa_status chain_in(fa_ctx* c, cudaStream_t s) {
 }
 
 fa_status chain_out(fa_ctx* c, cudaStream_t s) {
+    if (capturing(s)) {
+        c->chain_valid = false;   // nothing of the capture has run: later calls need not wait
+        return FA_OK;
+    }
     FA_CUDA(c, cudaEventRecord(c->chain, s));
     FA_CUDA(c, cudaStreamGetId(s, &c->chain_stream_id));
     c->chain_valid = true;
@@ -418,6 +434,10 @@ fa_status accumulate_impl(fa_ctx* c, uint32_t J, const uint32_t* ids, const doub
                     "fa_accumulate_batch reads its chunks in place: all in this GPU's memory, or all "
                     "in managed memory or host memory the device addresses");
     const bool direct = !all_device && all_in_place;
+    if (len > 0 && (any_pageable || (!all_device && !direct)) && capturing(s))
+        return fail(c, FA_ERR_STATE,
+                    "a captured call reads its chunks in place from this GPU's memory, managed memory or "
+                    "pinned host memory (staged and pageable chunks need the host during the round)");
     if (final_outs && len > 0 && !all_device && !all_in_place)
         return fail(c, FA_ERR_ARG,
                     "fa_accumulate_final reads its chunk in place: this GPU's memory, managed memory, or "
@@ -526,7 +546,7 @@ void free_ctx(fa_ctx* c) {
     if (c->gath_host) cudaFreeHost(c->gath_host);
     if (c->gath_dev) cudaFree(c->gath_dev);
     if (c->gath_ev) cudaEventDestroy(c->gath_ev);
-    if (c->gath_slots) cudaFree(c->gath_slots);
+    if (c->gath_counter) cudaFree(c->gath_counter);
     if (c->out_stage) cudaFree(c->out_stage);
     if (c->err_ev) cudaEventDestroy(c->err_ev);
     if (c->err_stream) cudaStreamDestroy(c->err_stream);
@@ -640,8 +660,10 @@ fa_status fa_open(const fa_key* layout, uint32_t n_keys, fa_dtype dtype_in, fa_d
     }
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->fin_ev, cudaEventDisableTiming);
     if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->gath_ev, cudaEventDisableTiming);
-    if (ce == cudaSuccess) ce = cudaMalloc(reinterpret_cast<void**>(&c->gath_slots), 2 * sizeof(uint32_t));
-    if (ce == cudaSuccess) ce = cudaMemset(c->gath_slots, 0, 2 * sizeof(uint32_t));
+    if (ce == cudaSuccess) ce = cudaMalloc(reinterpret_cast<void**>(&c->gath_counter), 2 * sizeof(uint32_t));
+    if (ce == cudaSuccess) ce = cudaMemset(c->gath_counter, 0, 2 * sizeof(uint32_t));
+    if (ce == cudaSuccess) c->fin_args.reset(new (std::nothrow) fa::FinArgs);
+    if (ce == cudaSuccess && !c->fin_args) ce = cudaErrorMemoryAllocation;
     if (ce == cudaSuccess) ce = cudaMalloc(&c->fin_dev, sizeof(fa::FinSeg) * n_keys);
     if (ce == cudaSuccess) ce = cudaHostAlloc(&c->fin_host, sizeof(fa::FinSeg) * n_keys, cudaHostAllocDefault);
     if (ce == cudaSuccess) c->fin_cap = n_keys;
@@ -770,6 +792,8 @@ fa_status fa_accumulate_keys(fa_ctx* ctx, uint32_t client_id, double weight_nk, 
                     "fa_accumulate_keys reads its chunks in place: all in this GPU's memory, or all "
                     "in managed memory or host memory the device addresses; send others through "
                     "fa_accumulate");
+    if (any && pageable && !all_device && capturing(static_cast<cudaStream_t>(stream)))
+        return fail(c, FA_ERR_STATE, "a captured call reads no pageable chunk (its read needs the host)");
     std::string e;
     int32_t st = c->ledger.plan_accumulate_keys(client_id, weight_nk, n_chunks, keys, offsets, lens,
                                                 &c->pieces, &e);
@@ -817,8 +841,8 @@ bool launch_inline_round(fa_ctx* c, void* const* out_ptrs, uint32_t jmax, const 
     if (!c->gath_inline) c->gath_inline.reset(new fa::GathInline);
     fa::GathInline& gp = *c->gath_inline;
     gp.err = c->err_dev;
-    gp.slots = c->gath_slots;
-    gp.slot = c->gath_slot;
+    gp.counter = c->gath_counter;
+    gp.pad0 = 0;
     gp.nseg = nseg;
     gp.nsrc = static_cast<uint32_t>(n_entries);
     gp.nclient = n_clients;
@@ -871,10 +895,7 @@ bool launch_inline_round(fa_ctx* c, void* const* out_ptrs, uint32_t jmax, const 
         *st = cuda_fail(c, ce, "one-pass round launch");
         return true;
     }
-    if (gp.ntiles > 0) {
-        c->gath_slot ^= 1u;   // the kernel zeroed the other counter
-        c->stats.kernel_launches++;
-    }
+    if (gp.ntiles > 0) c->stats.kernel_launches++;
     *st = FA_OK;
     return true;
 }
@@ -947,14 +968,24 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
         any_host = any_host || kind[i] != Mem::kDevice;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (capturing(s)) {
+        bool pageable_out = false;
+        for (size_t i = 0; i < c->items.size(); ++i) pageable_out = pageable_out || kind[i] == Mem::kPageable;
+        if (c->items.size() > fa::kFinInlineSegs || pageable_out || (any_host && c->out_stage == nullptr))
+            return fail(c, FA_ERR_STATE,
+                        "a captured finalize writes at most 600 ranges, into this GPU's memory or pinned "
+                        "host memory (a staged output needs its device buffer from an earlier finalize)");
+    }
     if (any_host && c->out_stage == nullptr)
         FA_CUDA(c, cudaMalloc(&c->out_stage, c->ledger.total_elems() * c->s_out));
-    if (c->fin_pending) {
+    // the table rides in the launch's parameters when it fits, else it is uploaded
+    const bool inline_tab = c->items.size() <= fa::kFinInlineSegs;
+    if (!inline_tab && c->fin_pending) {
         fa_status r = wait_event(c, c->fin_ev, "finalize table reuse");
         if (r != FA_OK) return r;
         c->fin_pending = false;
     }
-    if (c->items.size() > c->fin_cap) {
+    if (!inline_tab && c->items.size() > c->fin_cap) {
         // final contributions split some keys into several ranges to write
         const size_t cap = c->items.size() * 2;
         fa::FinSeg* dev = nullptr;
@@ -979,7 +1010,7 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
         dst += (flat ? it.flat_off : it.koff) * c->s_out;
         if (kind[i] != Mem::kDevice)
             dst = static_cast<char*>(c->out_stage) + it.flat_off * c->s_out;
-        fa::FinSeg& g = c->fin_host[i];
+        fa::FinSeg& g = inline_tab ? c->fin_args->seg[i] : c->fin_host[i];
         g.acc_idx = it.acc_idx;
         g.len = it.numel;
         g.out = dst;
@@ -1000,13 +1031,20 @@ fa_status finalize_impl(fa_ctx* c, const void* const* base_ptrs, void* const* ou
     fa_status r = chain_in(c, s);
     if (r != FA_OK) return r;
     if (nseg > 0) {
-        FA_CUDA(c, cudaMemcpyAsync(c->fin_dev, c->fin_host, sizeof(fa::FinSeg) * nseg,
-                                   cudaMemcpyHostToDevice, s));
-        FA_CUDA(c, cudaEventRecord(c->fin_ev, s));
-        c->fin_pending = true;
-        FA_CUDA(c, fa::launch_finalize(c->fin_dev, nseg, ntiles, c->dout, c->acc, c->acc_lo, apply,
-                                       static_cast<float>(server_lr), written_in_place > 0,
-                                       c->shape, s));
+        fa::FinArgs& fa_args = *c->fin_args;
+        fa_args.segs = inline_tab ? nullptr : c->fin_dev;
+        fa_args.acc = c->acc;
+        fa_args.acc_lo = c->acc_lo;
+        fa_args.nseg = nseg;
+        fa_args.ntiles = ntiles;
+        if (!inline_tab) {
+            FA_CUDA(c, cudaMemcpyAsync(c->fin_dev, c->fin_host, sizeof(fa::FinSeg) * nseg,
+                                       cudaMemcpyHostToDevice, s));
+            FA_CUDA(c, cudaEventRecord(c->fin_ev, s));
+            c->fin_pending = true;
+        }
+        FA_CUDA(c, fa::launch_finalize(fa_args, c->dout, apply, static_cast<float>(server_lr),
+                                       written_in_place > 0, c->shape, s));
         c->stats.kernel_launches++;
         c->stats.d2h_bytes += written_in_place;
         // host outputs: copy the staged keys back, merging neighbours in the flat layout
@@ -1353,6 +1391,12 @@ fa_status fa_reduce_subsets(fa_ctx* ctx, uint32_t n_clients, const uint32_t* cli
         if (launch_inline_round(c, out_ptrs, jmax, cnt, n_entries, src_client.data(), src_off.data(),
                                 n_clients, client_ptrs, weights, s, &st))
             return st == FA_OK ? chain_out(c, s) : st;
+    }
+    if (capturing(s)) {
+        c->broken = true;   // the round is recorded but cannot be captured: fa_reset
+        return fail(c, FA_ERR_STATE,
+                    "a captured fa_reduce_subsets carries its tables in the launch's parameters: this round "
+                    "is too large for that (call fa_reset)");
     }
     // segment table (one entry per key to write) and source table in device memory
     const size_t seg_bytes = (sizeof(fa::GathSeg) * nseg + 15) / 16 * 16;

@@ -76,11 +76,11 @@ __device__ __forceinline__ void fin_one(const FinSeg& sg, uint64_t e, const floa
 // segment by binary search; otherwise the table is walked in global memory, one step per
 // segment boundary crossed, which for large keys is rarely more than one step per tile.
 template <typename Tout, bool kApply, bool kComp, bool kSearch>
-__global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restrict__ segs,
-                                                          uint32_t nseg, uint32_t ntiles,
-                                                          const float* __restrict__ acc,
-                                                          const float* __restrict__ acc_lo,
-                                                          float lr) {
+__global__ void __launch_bounds__(kBlock) finalize_kernel(const __grid_constant__ FinArgs a, float lr) {
+    const FinSeg* segs = a.segs ? a.segs : a.seg;   // device memory or these parameters
+    const uint32_t nseg = a.nseg, ntiles = a.ntiles;
+    const float* __restrict__ acc = a.acc;
+    const float* __restrict__ acc_lo = a.acc_lo;
     constexpr int kVecPerTile = kTile / kVec;
     constexpr int kUnroll = kVecPerTile / kBlock;
     uint32_t si = 0;
@@ -170,10 +170,9 @@ __global__ void __launch_bounds__(kBlock) finalize_kernel(const FinSeg* __restri
 
 // ----------------------------------------------------------------- host side
 template <typename Tout, bool kApply, bool kComp>
-cudaError_t finalize_t(uint32_t grid, const FinSeg* segs, uint32_t nseg, uint32_t ntiles,
-                       const float* acc, const float* acc_lo, float lr, cudaStream_t stream) {
+cudaError_t finalize_t(uint32_t grid, const FinArgs& a, float lr, cudaStream_t stream) {
     // many keys per grid stride: search the segment table instead of walking it
-    const bool search = nseg > 1 && static_cast<uint64_t>(ntiles) < static_cast<uint64_t>(nseg) * grid;
+    const bool search = a.nseg > 1 && static_cast<uint64_t>(a.ntiles) < static_cast<uint64_t>(a.nseg) * grid;
     // a plain launch (no programmatic dependency: the kernel reads the sum from its
     // first instruction); the status is this launch's own
     cudaLaunchConfig_t cfg = {};
@@ -183,22 +182,19 @@ cudaError_t finalize_t(uint32_t grid, const FinSeg* segs, uint32_t nseg, uint32_
     cfg.stream = stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return search ? cudaLaunchKernelEx(&cfg, finalize_kernel<Tout, kApply, kComp, true>, segs, nseg, ntiles,
-                                       acc, acc_lo, lr)
-                  : cudaLaunchKernelEx(&cfg, finalize_kernel<Tout, kApply, kComp, false>, segs, nseg, ntiles,
-                                       acc, acc_lo, lr);
+    return search ? cudaLaunchKernelEx(&cfg, finalize_kernel<Tout, kApply, kComp, true>, a, lr)
+                  : cudaLaunchKernelEx(&cfg, finalize_kernel<Tout, kApply, kComp, false>, a, lr);
 }
 
 template <bool kComp>
-cudaError_t finalize_pick(uint32_t grid, int dtype_out, bool apply, const FinSeg* segs,
-                          uint32_t nseg, uint32_t ntiles, const float* acc, const float* acc_lo,
-                          float lr, cudaStream_t stream) {
+cudaError_t finalize_pick(uint32_t grid, int dtype_out, bool apply, const FinArgs& a, float lr,
+                          cudaStream_t stream) {
     if (dtype_out == 0) {
-        return apply ? finalize_t<float, true, kComp>(grid, segs, nseg, ntiles, acc, acc_lo, lr, stream)
-                     : finalize_t<float, false, kComp>(grid, segs, nseg, ntiles, acc, acc_lo, lr, stream);
+        return apply ? finalize_t<float, true, kComp>(grid, a, lr, stream)
+                     : finalize_t<float, false, kComp>(grid, a, lr, stream);
     }
-    return apply ? finalize_t<uint16_t, true, kComp>(grid, segs, nseg, ntiles, acc, acc_lo, lr, stream)
-                 : finalize_t<uint16_t, false, kComp>(grid, segs, nseg, ntiles, acc, acc_lo, lr, stream);
+    return apply ? finalize_t<uint16_t, true, kComp>(grid, a, lr, stream)
+                 : finalize_t<uint16_t, false, kComp>(grid, a, lr, stream);
 }
 
 template <bool kComp>
@@ -233,15 +229,15 @@ cudaError_t prepare_finalize_shapes(LaunchShape* s) {
     return e;
 }
 
-cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_out,
-                            const float* acc, const float* acc_lo, bool apply, float server_lr,
-                            bool host_out, const LaunchShape& s, cudaStream_t stream) {
-    if (ntiles == 0 || nseg == 0) return cudaSuccess;
-    const int c = acc_lo ? 1 : 0;
+cudaError_t launch_finalize(const FinArgs& a, int dtype_out, bool apply, float server_lr, bool host_out,
+                            const LaunchShape& s, cudaStream_t stream) {
+    if (a.ntiles == 0 || a.nseg == 0) return cudaSuccess;
+    if (a.segs == nullptr && a.nseg > kFinInlineSegs) return cudaErrorInvalidValue;
+    const int c = a.acc_lo ? 1 : 0;
     const int occ = s.fin_ctas_per_sm[c][apply ? 1 : 0][dtype_out == 0 ? 0 : 1];
-    const uint32_t grid = grid_for(ntiles, s.sms, host_out ? occ : std::min(occ, kFinCtasPerSm));
-    return c ? finalize_pick<true>(grid, dtype_out, apply, segs, nseg, ntiles, acc, acc_lo, server_lr, stream)
-             : finalize_pick<false>(grid, dtype_out, apply, segs, nseg, ntiles, acc, acc_lo, server_lr, stream);
+    const uint32_t grid = grid_for(a.ntiles, s.sms, host_out ? occ : std::min(occ, kFinCtasPerSm));
+    return c ? finalize_pick<true>(grid, dtype_out, apply, a, server_lr, stream)
+             : finalize_pick<false>(grid, dtype_out, apply, a, server_lr, stream);
 }
 
 }  // namespace fa

@@ -145,7 +145,7 @@ __device__ __forceinline__ TileAt tile_in(const SegV& sg, uint32_t si, uint32_t 
 template <typename Tin, typename Tout, bool kComp, bool kInline, typename Tab>
 __device__ __forceinline__ void gather_body(const Tab& tb, uint32_t grid, uint32_t nunit, uint32_t ntiles,
                                             uint32_t unit_tiles, const uint32_t* cta, uint32_t* counter,
-                                            unsigned int* err) {
+                                            uint32_t* done, unsigned int* err) {
     constexpr uint32_t IB = kGatherStageBytes;    // one input stage
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* ins = smem;
@@ -271,6 +271,16 @@ __device__ __forceinline__ void gather_body(const Tab& tb, uint32_t grid, uint32
                  i < issued; ++i)
                 mbar_wait(smem_addr(&full[i % kGatherStages]), (i / kGatherStages) & 1u);
         }
+        if (done != nullptr) {
+            // this CTA takes no more units; the last CTA to get here leaves the counter and
+            // this word at 0 for the next launch (the fence orders each CTA's last hand-out
+            // before its count, so the last one sees every hand-out done)
+            __threadfence();
+            if (atomicAdd(done, 1u) == grid - 1u) {
+                atomicExch(counter, 0u);
+                atomicExch(done, 0u);
+            }
+        }
         return;
     }
 
@@ -354,22 +364,21 @@ template <typename Tin, typename Tout, bool kComp>
 __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_kernel(const __grid_constant__ GathArgs a) {
     const DevTables tb{&a};
     gather_setup(tb, 0u);
-    gather_body<Tin, Tout, kComp, false>(tb, a.grid, a.nchunk, a.ntiles, 0u, a.cta, a.counter, a.err);
+    gather_body<Tin, Tout, kComp, false>(tb, a.grid, a.nchunk, a.ntiles, 0u, a.cta, a.counter, nullptr, a.err);
 }
 
 // Tables in the parameters: a programmatic dependent launch (its set-up overlaps the
 // previous kernel's tail; nothing in global memory is touched before that kernel has
-// completed); units are single tiles, counted in p.slots[p.slot], and the other slot is
-// zeroed for the next launch.
+// completed); units of unit_tiles tiles are counted in p.counter[0], and the launch leaves
+// both counter words at 0 (so a captured launch replays as it ran).
 template <typename Tin, typename Tout, bool kComp>
 __global__ void __launch_bounds__(kGatherThreads, 1) reduce_gather_inline_kernel(
     const __grid_constant__ GathInline p) {
     const ParTables tb{&p};
     gather_setup(tb, p.nseg);
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (blockIdx.x == 0 && threadIdx.x == 0) p.slots[p.slot ^ 1u] = 0u;
     gather_body<Tin, Tout, kComp, true>(tb, p.grid, (p.ntiles + p.unit_tiles - 1) / p.unit_tiles, p.ntiles,
-                                        p.unit_tiles, nullptr, p.slots + p.slot, p.err);
+                                        p.unit_tiles, nullptr, p.counter, p.counter + 1, p.err);
 }
 
 // ----------------------------------------------------------------- host side
@@ -466,7 +475,7 @@ cudaError_t launch_gather_inline(const GathInline& p, int dtype_in, int dtype_ou
                                  const LaunchShape& s, cudaStream_t stream) {
     if (p.nseg == 0 || p.ntiles == 0) return cudaSuccess;
     uint32_t so = 0, bo = 0, wo = 0;
-    if (p.err == nullptr || p.slots == nullptr || p.slot > 1u || p.jmax == 0 || p.nseg > kMaxInlineSegs ||
+    if (p.err == nullptr || p.counter == nullptr || p.jmax == 0 || p.nseg > kMaxInlineSegs ||
         p.unit_tiles == 0 ||
         p.jmax > static_cast<uint32_t>(kMaxBatch) ||
         p.grid != gather_grid(p.ntiles, dtype_in, dtype_out, comp, s) || p.grid == 0 ||

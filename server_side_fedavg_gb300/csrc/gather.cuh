@@ -82,9 +82,9 @@ constexpr uint32_t kGathInlineBlob = 32640;   // bytes of tables in the paramete
 
 struct GathInline {
     unsigned int* err;          // the caller's device error word
-    uint32_t* slots;            // two device counter words of the caller's context
-    uint32_t slot;              // this launch counts tiles in slots[slot] (0 at launch) and
-                                // zeroes slots[slot ^ 1] for the next launch
+    uint32_t* counter;          // two device words of the caller's context, 0 at launch: units
+                                // handed out, CTAs done; the launch leaves both at 0
+    uint32_t pad0;
     uint32_t nseg;
     uint32_t nsrc;
     uint32_t nclient;
@@ -112,7 +112,7 @@ uint32_t gather_unit_tiles(uint32_t ntiles, uint32_t grid);
 
 // Launches the subset reduce with its tables in the parameters, as a programmatic
 // dependent of the previous kernel on the stream.  The caller fills every field; units
-// of unit_tiles consecutive tiles are handed out from slots[slot].
+// of unit_tiles consecutive tiles are handed out from counter[0].
 cudaError_t launch_gather_inline(const GathInline& p, int dtype_in, int dtype_out, bool comp,
                                  const LaunchShape& s, cudaStream_t stream);
 

@@ -118,6 +118,21 @@ struct FinSeg {
     uint32_t tile0;     // first tile of this segment
 };
 
+// Segments a finalize launch carries in its own parameters (48 B each, inside the 32,764
+// bytes a launch takes): no table upload before the launch, and a launch captured into a
+// CUDA graph replays from its own copy of the table.
+constexpr uint32_t kFinInlineSegs = 600;
+
+struct FinArgs {
+    const FinSeg* segs;   // the segment table in device memory, or nullptr: seg[0..nseg)
+    const float* acc;     // running sum (compensated mode: its hi part)
+    const float* acc_lo;  // compensated mode: the lo part, else nullptr
+    uint32_t nseg;
+    uint32_t ntiles;
+    FinSeg seg[kFinInlineSegs];
+};
+static_assert(sizeof(FinArgs) <= 32764, "kernel parameters are limited to 32764 bytes");
+
 struct LaunchShape {
     int sms = 0;
     int bulk_ctas_per_sm[2][2] = {};       // [compensated][dtype_in], streaming kernel
@@ -173,15 +188,15 @@ cudaError_t launch_accumulate_direct(const AccArgs& a, int dtype_in, const Launc
 cudaError_t launch_reduce_final(const RedArgs& a, int dtype_in, int dtype_out,
                                 const LaunchShape& s, cudaStream_t stream);
 
-// segs: device array of nseg FinSeg sorted by tile0.
+// a.segs: device array of a.nseg FinSeg sorted by tile0, or nullptr with the table in
+// a.seg (a.nseg <= kFinInlineSegs).
 //   apply == false: out = RNE(sum / N)
 //   apply == true:  out = RNE(fma(server_lr, sum / N, base))   (delta rounds)
 // acc_lo: compensated mode (sum = acc + acc_lo), else nullptr.
 // host_out: some outputs are host memory written in place over the host link; the grid
 // then runs at full occupancy (more stores in flight for the link) instead of
 // kFinCtasPerSm, the HBM-bound optimum.
-cudaError_t launch_finalize(const FinSeg* segs, uint32_t nseg, uint32_t ntiles, int dtype_out,
-                            const float* acc, const float* acc_lo, bool apply, float server_lr,
-                            bool host_out, const LaunchShape& s, cudaStream_t stream);
+cudaError_t launch_finalize(const FinArgs& a, int dtype_out, bool apply, float server_lr, bool host_out,
+                            const LaunchShape& s, cudaStream_t stream);
 
 }  // namespace fa

@@ -6,16 +6,15 @@
 //
 // Its device state lives in fixed arrays of this library's device image, which
 // every GPU that loads the library keeps until the process exits: the fp32
-// running sum (FA_NOALLOC_MAX_ELEMS floats, 16 MiB), the finalize kernel's
-// one-entry segment table, and an error word of its own (read and cleared by
-// fa_aggregate_noalloc_status).  Host code cannot use
+// running sum (FA_NOALLOC_MAX_ELEMS floats, 16 MiB) and an error word of its own
+// (read and cleared by fa_aggregate_noalloc_status); the finalize kernel's one-entry
+// segment table travels in its launch's parameters.  Host code cannot use
 // these names as device addresses: on the first call on each device the entry
 // point looks the addresses up with cudaGetSymbolAddress (with that device
 // current) and caches them; that first call should therefore come before any
 // stream capture.  All calls share the arrays and they keep the last call's
 // contents: the first client's launch overwrites every element of the sum it
-// uses and each call writes its segment entry before the finalize reads it (no
-// clearing is needed), and calls that overlap on the GPU race on them.
+// uses (no clearing is needed), and calls that overlap on the GPU race on it.
 #include <fedavg.h>
 
 #include <cuda_runtime.h>
@@ -31,7 +30,6 @@
 namespace {
 
 __device__ __align__(256) float g_noalloc_sum[FA_NOALLOC_MAX_ELEMS];
-__device__ __align__(16) fa::FinSeg g_noalloc_fin;
 __device__ unsigned int g_noalloc_error;
 
 constexpr int kMaxDevices = 64;
@@ -39,7 +37,6 @@ constexpr int kMaxDevices = 64;
 struct DeviceSetup {
     bool ready = false;
     float* sum = nullptr;            // device address of g_noalloc_sum on this device
-    fa::FinSeg* fin = nullptr;       // ... of g_noalloc_fin
     unsigned int* err = nullptr;     // ... of g_noalloc_error
     fa::LaunchShape shape;
 };
@@ -53,15 +50,12 @@ cudaError_t setup_for(int dev, DeviceSetup** out) {
     DeviceSetup& d = g_setup[dev];
     if (!d.ready) {
         void* sum = nullptr;
-        void* fin = nullptr;
         void* err = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&sum, g_noalloc_sum);
-        if (e == cudaSuccess) e = cudaGetSymbolAddress(&fin, g_noalloc_fin);
         if (e == cudaSuccess) e = cudaGetSymbolAddress(&err, g_noalloc_error);
         if (e == cudaSuccess) e = fa::query_launch_shape(&d.shape);
         if (e != cudaSuccess) return e;
         d.sum = static_cast<float*>(sum);
-        d.fin = static_cast<fa::FinSeg*>(fin);
         d.err = static_cast<unsigned int*>(err);
         d.ready = true;
     }
@@ -69,9 +63,6 @@ cudaError_t setup_for(int dev, DeviceSetup** out) {
     return cudaSuccess;
 }
 
-// Writes the finalize kernel's one-entry segment table, on the stream, from the kernel's
-// own parameters (no host buffer and no copy).
-__global__ void set_noalloc_segment(const __grid_constant__ fa::FinSeg seg) { g_noalloc_fin = seg; }
 
 // Memory of device `dev`; managed memory only where plain stores touch it (the output):
 // inputs are read with bulk copies, which are kept off pages that may sit on the host.
@@ -142,9 +133,15 @@ extern "C" fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weig
         if (fa::launch_accumulate(a, din, d->shape, s) != cudaSuccess) return FA_ERR_CUDA;
         done += jb;
     }
-    // the finalize step: the library's tiled finalize kernel over a one-entry segment
-    // table in the fixed array, written on `s` just before it
-    fa::FinSeg seg;
+    // the finalize step: the library's tiled finalize kernel, its one-entry segment table
+    // in the launch's parameters
+    static thread_local fa::FinArgs fin;
+    fin.segs = nullptr;
+    fin.acc = d->sum;
+    fin.acc_lo = nullptr;
+    fin.nseg = 1;
+    fin.ntiles = static_cast<uint32_t>((numel + fa::kTile - 1) / fa::kTile);
+    fa::FinSeg& seg = fin.seg[0];
     std::memset(&seg, 0, sizeof seg);
     seg.acc_idx = 0;
     seg.len = numel;
@@ -152,15 +149,7 @@ extern "C" fa_status fa_aggregate_noalloc(uint32_t n_clients, const double* weig
     seg.base = nullptr;
     seg.div = fa::make_divisor(total);
     seg.tile0 = 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(1);
-    cfg.stream = s;
-    if (cudaLaunchKernelEx(&cfg, set_noalloc_segment, seg) != cudaSuccess) return FA_ERR_CUDA;
-    const uint64_t ntiles = (numel + fa::kTile - 1) / fa::kTile;
-    const cudaError_t fe = fa::launch_finalize(d->fin, 1, static_cast<uint32_t>(ntiles),
-                                               dtype_out == FA_F32 ? 0 : 1, d->sum, nullptr, false,
-                                               1.0f, false, d->shape, s);
+    const cudaError_t fe = fa::launch_finalize(fin, dtype_out == FA_F32 ? 0 : 1, false, 1.0f, false, d->shape, s);
     return fe == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
