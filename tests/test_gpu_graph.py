@@ -254,6 +254,48 @@ def test_captured_delta_round_replays():
         fa.fa_close(ctx)
 
 
+def test_captured_batch_round_replays():
+    """fa_accumulate_batch captured: 6 resident clients in one pass per key, then finalize."""
+    rng = np.random.default_rng(51)
+    K = 6
+    weights = [float(x) for x in rng.integers(1, 1000, K)]
+    P = sum(NUMELS)
+    bufs = _bufs(K, P, "bf16")
+    offs = np.cumsum([0] + NUMELS)
+    ctx = fa.fa_open(_layout(NUMELS), "bf16", "bf16", K)
+    try:
+        outs = [sentinel(n, "bf16") for n in NUMELS]
+
+        def rnd(s):
+            for p, n in enumerate(NUMELS):
+                fa.fa_accumulate_batch(ctx, list(range(K)), weights, p, 0,
+                                       [b.data_ptr() + 2 * int(offs[p]) for b in bufs], n, s)
+            fa.fa_finalize(ctx, outs, s)
+
+        _fill(rng, bufs, "bf16")
+        s0 = torch.cuda.Stream()
+        with torch.cuda.stream(s0):
+            rnd(s0)
+        torch.cuda.synchronize()
+        fa.fa_reset(ctx)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            rnd(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        for r in range(3):
+            _fill(rng, bufs, "bf16")
+            for o in outs:
+                o.fill_(0x7FBF)
+            g.replay()
+            torch.cuda.synchronize()
+            want = _direct(NUMELS, "bf16", "bf16", bufs, weights)
+            for p in range(len(NUMELS)):
+                assert np.array_equal(to_np(outs[p], "bf16"), want[p]), (r, p)
+    finally:
+        torch.cuda.synchronize()
+        fa.fa_close(ctx)
+
+
 def test_calls_that_need_the_host_refuse_capture():
     """Inside a capture: a staged chunk, a pageable chunk and a pageable output are refused
     with FA_ERR_STATE and issue nothing, so the capture still ends and replays the calls
