@@ -442,3 +442,99 @@ def test_final_zero_weight_key_reports_a_zero_total():
     st, _, totals = lg.accumulate_final(1, 0.0, 0, 0, 4)
     assert st == OK and totals == [0.0]
     assert lg.finalize_ranges() == (OK, [])
+
+
+def test_random_final_contributions_against_model():
+    """Random plain and final contributions (per key and flat) against a per-element model
+    of the rules: a final chunk needs every other sender of its keys complete, then those
+    keys take no new sender and its range no further contribution; totals count every
+    sender; finalize writes each key less the ranges final chunks wrote."""
+    rng = random.Random(23)
+    for trial in range(40):
+        numels = [rng.randint(1, 24) for _ in range(rng.randint(1, 5))]
+        K = rng.randint(2, 5)
+        lg = Ledger(numels, K)
+        offs = np.cumsum([0] + numels)
+        nk = len(numels)
+        started = [np.zeros(n, bool) for n in numels]
+        written = [np.zeros(n, bool) for n in numels]
+        frozen = [False] * nk
+        recv = np.zeros((K, nk), np.int64)
+        weight = {}
+        for _ in range(50):
+            c = rng.randrange(K)
+            w = weight.get(c, float(rng.randint(0, 9)))
+            if rng.random() < 0.4:
+                key = -1
+                off = rng.randint(0, int(offs[-1]))
+                ln = rng.randint(0, int(offs[-1]) - off)
+            else:
+                key = rng.randrange(nk)
+                off = rng.randint(0, numels[key])
+                ln = rng.randint(0, numels[key] - off)
+            final = rng.random() < 0.3
+            spans = _spans(numels, offs, key, off, ln)
+            want = OK
+            for (p, koff, n, _) in spans:
+                if recv[c, p] + n > numels[p]:
+                    want = RANGE
+                    break
+                if final and any(0 < recv[o, p] < numels[p] for o in range(K) if o != c):
+                    want = INCOMPLETE
+                    break
+            if want == OK:
+                for (p, koff, n, _) in spans:
+                    if frozen[p] and (recv[c, p] == 0 or written[p][koff:koff + n].any()):
+                        want = STATE
+                        break
+            if final:
+                st, pieces, totals = lg.accumulate_final(c, w, key, off, ln)
+            else:
+                st, pieces = lg.accumulate([c], [w], key, off, ln)
+            assert st == want, (trial, final, key, off, ln, st, want)
+            if st != OK or ln == 0:
+                assert pieces == []
+                continue
+            weight[c] = w
+            for (p, _, n, _) in spans:
+                recv[c, p] += n
+            got = {}
+            for (p, coff, acc, n, first) in pieces:
+                for i in range(n):
+                    got[(p, acc - lg.acc_off(p) + i)] = (first, coff + i)
+            for (p, koff, n, coff) in spans:
+                for i in range(n):
+                    f, ci = got.pop((p, koff + i))
+                    assert ci == coff + i
+                    assert f == (0 if started[p][koff + i] else 1)
+                    started[p][koff + i] = True
+            assert not got
+            if final:
+                for (p, koff, n, _) in spans:
+                    frozen[p] = True
+                    written[p][koff:koff + n] = True
+                for (p, _, _, _, _), tot in zip(pieces, totals):
+                    assert tot == sum(weight[k] for k in range(K) if recv[k, p] > 0)
+        assert lg.has_final() == any(wr.any() for wr in written)
+        st, items = lg.finalize_ranges()
+        complete = all(recv[k, p] in (0, numels[p]) for k in range(K) for p in range(nk))
+        assert st == (OK if complete else INCOMPLETE)
+        if not complete:
+            continue
+        want_items = []
+        for p in range(nk):
+            rep = [k for k in range(K) if recv[k, p] > 0]
+            total = sum(weight[k] for k in rep)
+            if not rep or total == 0.0:
+                continue
+            a = 0
+            while a < numels[p]:
+                if written[p][a]:
+                    a += 1
+                    continue
+                b = a
+                while b < numels[p] and not written[p][b]:
+                    b += 1
+                want_items.append((p, a, lg.acc_off(p) + a, int(offs[p]) + a, b - a, len(rep), total))
+                a = b
+        assert items == want_items, trial
