@@ -115,7 +115,16 @@ def test_random_rounds_more_seeds(seed):
     _random_rounds(*pairs[seed % 4], seed)
 
 
-def _random_rounds(din, dout, seed):
+@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32"), ("f32", "bf16")])
+def test_random_rounds_with_final_contributions(din, dout):
+    """As test_random_rounds, and for each key one client that sends it in per-key chunks
+    sends them last, through fa_accumulate_final: those chunks' outputs come from the
+    accumulate kernels, the rest of the layout from fa_finalize."""
+    _random_rounds(din, dout, {"bf16bf16": 31, "f32f32": 32, "bf16f32": 33, "f32bf16": 34}[din + dout],
+                   final=True)
+
+
+def _random_rounds(din, dout, seed, final=False):
     rng_py = random.Random(seed)
     rng = np.random.default_rng(seed)
     numels = [rng_py.choice(SIZES) for _ in range(9)]
@@ -135,6 +144,20 @@ def _random_rounds(din, dout, seed):
                 p, ks, ranges = batch
                 ops += [("batch", p, ks, a, b) for a, b in ranges]
             rng_py.shuffle(ops)
+            if final:
+                # per key, one client's per-key chunks move to the end as final contributions
+                last = []
+                for p in range(len(numels)):
+                    cands = sorted({op[1] for op in ops if op[0] == "one" and op[2] == p})
+                    if not cands:
+                        continue
+                    k = rng_py.choice(cands)
+                    mine = [op for op in ops if op[0] == "one" and op[1] == k and op[2] == p]
+                    ops = [op for op in ops if op not in mine]
+                    last += [("final",) + op[1:] for op in mine]
+                rng_py.shuffle(last)
+                ops += last
+            outs = [sentinel(n, dout) for n in numels]
             keep = []
             for op in ops:
                 if op[0] == "batch":
@@ -155,11 +178,17 @@ def _random_rounds(din, dout, seed):
                         assert e.status == fa.FA_ERR_ARG and kind == "pageable", e
                         ptrs = [_put(data[k][g:g + (b - a)], "device", keep) for (_, _, a, b, g) in mine]
                         fa.fa_accumulate_keys(ctx, k, weights[k], args[0], args[1], ptrs, args[3], s)
+                elif op[0] == "final":
+                    # read in place: device memory, or pinned memory where the context does
+                    # not stage it
+                    _, k, key, a, b, g = op
+                    kind = "device" if seed % 2 else rng_py.choice(["device", "pinned"])
+                    ptr = _put(data[k][g:g + (b - a)], kind, keep)
+                    fa.fa_accumulate_final(ctx, k, weights[k], key, a, ptr, b - a, outs, s)
                 else:
                     _, k, key, a, b, g = op
                     ptr = _put(data[k][g:g + (b - a)], rng_py.choice(KINDS), keep)
                     fa.fa_accumulate(ctx, k, weights[k], key, a, ptr, b - a, s)
-            outs = [sentinel(n, dout) for n in numels]
             fa.fa_finalize(ctx, outs, s)
             fa.fa_sync(ctx)
             torch.cuda.synchronize()
