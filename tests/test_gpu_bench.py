@@ -60,6 +60,11 @@ def test_bench_line_has_the_contract():
     assert d["gpu_launches"] >= 2 * w.K
     assert d["unfused"]["value"] > 0 and d["config"]["last_client"].startswith("fa_accumulate_final")
     assert d["resident"]["value"] > 0 and d["resident"]["launches_per_round"] >= 1
+    # a small model's rounds, captured into CUDA graphs and replayed
+    g = d["graph"]
+    assert g["wall_ms_per_round"] > 0 and g["device_ms_per_round"] > 0 and g["calls_wall_ms_per_round"] > 0
+    assert abs(g["value"] - client / (g["wall_ms_per_round"] * 1e-3) / 1e9) <= 0.05 * g["value"]
+    assert d["resident"]["graph"]["wall_ms_per_round"] > 0
     assert d["delta_apply"]["gbs"] > 0 and d["delta_apply"]["bytes"] == w.P * (4 + 2 * so)
     cp = d["compensated"]
     assert cp["value"] > 0 and cp["bytes_per_round"] == w.P * (si + 8 + (w.K - 1) * (si + 16) + 8 + so)
