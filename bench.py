@@ -539,12 +539,15 @@ def run_ours(args, world, rank, local, pg):
     out_arr = fa.out_array([out])
 
     def step(evs=None, final=fused, sh=sh, reset=True):
-        # evs: (start, after the accumulate launches, after finalize) on the launching stream
+        # evs: (start, after the accumulate launches, after finalize, after clients 0..K-2)
+        # on the launching stream
         if reset:
             fa.fa_reset(ctx)
         if evs is not None:
             evs[0].record(s)
         for k in range(w.K):
+            if evs is not None and k == w.K - 1:
+                evs[3].record(s)
             if part:
                 ks, os_, ps, ls = key_args[k]
                 fa.fa_accumulate_keys(ctx, k, w.weights[k], ks, os_, ps, ls, sh)
@@ -572,7 +575,7 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize()
 
     n_calls = w.K * nchunk          # accumulate launches per round (flat chunks)
-    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = fa.fa_get_stats(ctx)["kernel_launches"]
     clocks = ClockSampler(local)
@@ -596,13 +599,26 @@ def run_ours(args, world, rank, local, pg):
     # per call here) and its finalize launch, on the stream they are launched on
     acc_ms = 0.0
     fin_ms = 0.0
+    last_ms = 0.0          # the last client's launches (the final form in a fused round)
     for evs in ev_sets:
         acc_ms += evs[0].elapsed_time(evs[1])
         fin_ms += evs[1].elapsed_time(evs[2])
+        last_ms += evs[3].elapsed_time(evs[1])
+    final_form = None
     if fused:
         b0, b1, b2 = fused_bytes(w)
-        acc_bytes = b0 + b1 + b2
-        step_bytes = acc_bytes
+        step_bytes = b0 + b1 + b2
+        # the dominant launches are the plain form's (clients 0..K-2); the last client's
+        # final-form launches are reported beside them
+        acc_bytes = b0 + b1
+        acc_ms -= last_ms
+        n_calls = (w.K - 1) * nchunk
+        fl = nchunk
+        f_launch_ms = last_ms / (args.steps * fl)
+        f_ach = b2 / fl / (f_launch_ms * 1e-3) / 1e9
+        final_form = {"kernel": f"accumulate_bulk_kernel<{w.dtype_in}, final, {w.dtype_out}>",
+                      "achieved": round(f_ach, 1), "frac": round(f_ach / peak, 4),
+                      "bytes_per_launch": int(b2 / fl), "launch_ms": round(f_launch_ms, 4)}
     else:
         acc_first_b, acc_later_b, fin_b = algorithmic_bytes(w)
         acc_bytes = acc_first_b + acc_later_b
@@ -616,7 +632,7 @@ def run_ours(args, world, rank, local, pg):
     # ---- the same round with every client through fa_accumulate and then fa_finalize:
     # the finalize kernel's rate, and the sum a delta round's finalize reads below
     unfused_line = None
-    ev_u = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev_u = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for _ in range(2 if fused else 0):
         step(final=False)
     u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -760,13 +776,15 @@ def run_ours(args, world, rank, local, pg):
                                    else "fa_accumulate, then fa_finalize"),
                    "wall_s": round(wall, 3)},
         "roofline": {"bound": "hbm",
-                     "kernel": (f"accumulate_bulk_kernel<{w.dtype_in}> (the last client's launches in the "
-                                f"final form)" if fused else f"accumulate_bulk_kernel<{w.dtype_in}>"),
+                     "kernel": (f"accumulate_bulk_kernel<{w.dtype_in}> (clients 0..{w.K - 2}; the last "
+                                f"client's final form in final_form)" if fused
+                                else f"accumulate_bulk_kernel<{w.dtype_in}>"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": int(acc_bytes_per_launch),
                      "launch_ms": round(acc_launch_ms, 4),
-                     "traffic": profiled_traffic(acc_bytes_per_launch)},
+                     "traffic": profiled_traffic(acc_bytes_per_launch),
+                     "final_form": final_form},
         "gpu_launches": int(launches),
         "unfused": unfused_line,
         "graph": graph_line,
