@@ -75,7 +75,9 @@ def test_argument_errors_need_no_device(lib):
     assert lib.fa_sync(None) == fa.FA_ERR_ARG
     assert lib.fa_reset(None) == fa.FA_ERR_ARG
     assert lib.fa_accumulate(None, 0, 1.0, 0, 0, None, 0, None) == fa.FA_ERR_ARG
+    assert lib.fa_accumulate_final(None, 0, 1.0, 0, 0, None, 0, None, None) == fa.FA_ERR_ARG
     assert lib.fa_finalize(None, None, None) == fa.FA_ERR_ARG
+    assert lib.fa_finalize_apply(None, None, None, 1.0, None) == fa.FA_ERR_ARG
     assert fa.fa_last_error(None) == ""
 
 
