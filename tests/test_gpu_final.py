@@ -246,3 +246,49 @@ def test_full_round_of_a_workload_through_final_calls():
     assert gtot == rtot
     for p in range(w.n_keys):
         assert np.array_equal(got[p], ref[p]), p
+
+
+@pytest.mark.slow
+def test_last_quotient_is_correctly_rounded_for_every_fp32_sum():
+    """The division in the final form, checked exhaustively: for every fp32 bit pattern s as
+    the sum before the division (zeros, subnormals, infinities and NaN included) and
+    divisors N_p exact in fp32 (powers of two, odd and even integers up to 2^24 - 1, exact
+    non-integers), the output is the correctly rounded quotient: the fp64 quotient rounded to
+    fp32 (rounding a 53-bit quotient to 24 bits gives the correctly rounded 24-bit quotient).
+    Client 0 (weight N_p - 1) sends zeros and client 1 (weight 1) sends s through
+    fa_accumulate_final, so its sum is fma(1, s, +0) = s (for s = -0 that is +0, whose
+    quotient is +0)."""
+    n = 1 << 32
+    free, _ = torch.cuda.mem_get_info()
+    assert free > 4 * n * 4 + (8 << 30), f"needs about 72 GB free, have {free / 1e9:.0f}"
+    S = 1 << 28
+    x1 = torch.empty(n, dtype=torch.int32, device="cuda")
+    for a in range(0, n, S):
+        v = torch.arange(a, a + S, dtype=torch.int64, device="cuda")
+        x1[a:a + S] = torch.where(v >= 1 << 31, v - (1 << 32), v).to(torch.int32)
+    del v
+    x0 = torch.zeros(n, dtype=torch.float32, device="cuda")
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    xs = x1.view(torch.float32)
+    neg0 = torch.tensor([0x80000000 - (1 << 32)], dtype=torch.int32, device="cuda")
+    ctx = fa.fa_open([("s", n)], "f32", "f32", 2)
+    try:
+        for d in (1.0, 2.0, 3.0, 7.0, 10.0, 1000.0, 4095.0, 12345.0, 65537.0, 1048575.0, 16777215.0,
+                  1.5, 1.75):
+            fa.fa_reset(ctx)
+            fa.fa_accumulate(ctx, 0, d - 1.0, 0, 0, x0, n)
+            fa.fa_accumulate_final(ctx, 1, 1.0, 0, 0, x1, n, [out])
+            fa.fa_sync(ctx)
+            torch.cuda.synchronize()
+            total, _ = fa.fa_key_total(ctx, 0)
+            for a in range(0, n, S):
+                s = xs[a:a + S]
+                want = (s.double() / total).float()
+                want = torch.where(x1[a:a + S] == neg0, torch.zeros_like(want), want)
+                got = out[a:a + S]
+                same = (got.view(torch.int32) == want.view(torch.int32)) | (torch.isnan(got) & torch.isnan(want))
+                bad = int((~same).sum())
+                assert bad == 0, (d, a, bad)
+    finally:
+        torch.cuda.synchronize()
+        fa.fa_close(ctx)
