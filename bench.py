@@ -722,6 +722,7 @@ def run_ours(args, world, rank, local, pg):
         if not args.no_graph and client_bytes <= GRAPH_MAX_BYTES:
             rgraph = graph_replay(fa, ctx, lambda sh: fa.fa_reduce_resident(ctx, ids, w.weights, ptrs, [out], sh),
                                   max(20, args.steps))
+            rgraph["hbm_frac"] = round(rbytes / (rgraph["device_ms_per_round"] * 1e-3) / 1e9 / peak, 4)
         resident_line = {"value": round(client_bytes / (rms * 1e-3) / 1e9, 2), "unit": "GB/s",
                          "device_ms_per_round": round(rms, 4), "wall_ms_per_round": round(wall_ms, 4),
                          "value_wall": round(client_bytes / (wall_ms * 1e-3) / 1e9, 2),
@@ -880,6 +881,8 @@ def run_subsets(args, w, ctx, bufs, out, s, peak):
     graph = None if args.no_graph else graph_replay(
         fa, ctx, lambda sh: fa.fa_reduce_subsets(ctx, ids, w.weights, ptrs, table, [out], sh),
         max(20, args.steps))
+    if graph is not None:
+        graph["hbm_frac"] = round(b / (graph["device_ms_per_round"] * 1e-3) / 1e9 / peak, 4)
     return {"value": round(cb / (dev_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "device_ms_per_round": round(dev_ms, 4), "wall_ms_per_round": round(wall * 1e3, 4),
             "value_wall": round(cb / wall / 1e9, 2),
