@@ -63,7 +63,7 @@ def _direct(numels, din, dout, bufs, weights, final=False, flags=0):
         fa.fa_close(ctx)
 
 
-@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32")])
+@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32"), ("f32", "bf16")])
 @pytest.mark.parametrize("final", [False, True])
 @pytest.mark.parametrize("flags", [0, fa.FA_COMPENSATED])
 def test_captured_streamed_round_replays_bit_identical(din, dout, final, flags):
