@@ -17,6 +17,46 @@ namespace {
 
 constexpr int kFinalThreads = 1024;   // threads of a final-form streaming CTA (see bulk_threads)
 
+// ----------------------------------------------------------------- the last quotient
+// Whether a segment's divisor admits quotient8's division-free path: N_p exact in fp32 (no
+// lo part) and within [2^-20, 2^60].
+__device__ __forceinline__ bool fast_divisor(const Divisor& d) {
+    return d.lo == 0.0f && d.hi >= 0x1p-20f && d.hi <= 0x1p60f && d.rcp > 0.0f;
+}
+
+// The quotients of one 8-element vector of a final contribution: the bits of quotient_out.
+// When the divisor admits it and every sum has 2^-60 <= |s| < 2^61 -- one test for the
+// vector, so the common path has no branch per element -- they take no division:
+// Markstein's correction of a reciprocal (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990).
+// With y = d.rcp = RN(1/d) (rounded once, on the host), q = RN(s*y) is within two ulps of
+// s/d; one step q <- RN(q + RN(s - q*d)*y), its remainder from an fma, leaves q within an
+// ulp; the remainder of such a q is exact, so a second step gives s/d + (s/d - q)(d*y - 1)
+// before its one rounding, nearer to s/d than s/d is to any rounding midpoint (a quotient of
+// two floats with 24-bit significands lies at least ulp/2^25 from one, and |d*y - 1| <
+// 2^-24): the result is RN(s/d).  Nothing underflows or overflows in those ranges.  Any
+// other vector (zeros, subnormals, infinities, NaN, larger sums), divisor or the
+// compensated mode takes quotient_out.
+template <bool kComp, typename Tout>
+__device__ __forceinline__ void quotient8(float (&hi)[8], const float (&lo)[8], const Divisor& d, bool fast) {
+    if constexpr (!kComp) {
+        bool in = fast;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) in &= ((__float_as_uint(hi[e]) >> 23) & 0xFFu) - 67u < 121u;
+        if (in) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float q = __fmul_rn(hi[e], d.rcp);
+                q = __fmaf_rn(__fmaf_rn(-q, d.hi, hi[e]), d.rcp, q);
+                hi[e] = __fmaf_rn(__fmaf_rn(-q, d.hi, hi[e]), d.rcp, q);
+            }
+            return;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hi[e] = quotient_out<kComp, Tout>(hi[e], lo[e], d);
+}
+
 // ----------------------------------------------------------------- streaming accumulate
 // One element through global memory (ragged tails, unaligned segments).
 // kFinal: the element's last contribution -- the quotient is written to out[0] (dtype
@@ -124,6 +164,7 @@ __global__ void __launch_bounds__(bulk_threads<kFinal>(), 1) accumulate_bulk_ker
         float* l0 = kComp ? a.acc_lo + sg.acc_idx + ta.e0 : nullptr;
         const bool bulk = ((a.vec_ok >> ta.si) & 1ull) && ta.cnt >= static_cast<uint32_t>(kVec);
         const uint32_t n8 = bulk ? ta.cnt / kVec : 0;
+        [[maybe_unused]] const bool fast = kFinal && fast_divisor(sg.div);
         if (ok && bulk) {
             uint8_t* xt = xs + s * XB;
             uint8_t* st = ss + s * SB;
@@ -143,8 +184,7 @@ __global__ void __launch_bounds__(bulk_threads<kFinal>(), 1) accumulate_bulk_ker
                 if constexpr (kFinal) {
                     // the results take this thread's own vector slot: of the sum tile for
                     // fp32 out, of the input tile for bf16 out (bf16 in: the same 16 bytes)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) hi[e] = quotient_out<kComp, Tout>(hi[e], lo[e], sg.div);
+                    quotient8<kComp, Tout>(hi, lo, sg.div, fast);
                     smem_store8<Tout>(sizeof(Tout) == 4 ? st : xt, v, hi);
                 } else {
                     smem_st8f(st, v, hi);
